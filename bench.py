@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Throughput of the sm_103a TN GEMM: TFLOP/s = 2MNK / t on one GB300.
+
+One step = one call of the C ABI on one rotating input set of the workload
+(default sq_8192: FP16, M = N = K = 8192, N(0,1) inputs, 4 rotating sets of
+256 MiB each, larger than L2, so no L2 flush is needed between steps).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+Prints ONE JSON line on rank 0.  Under torchrun (N > 1) every rank runs its
+own replica on its own GPU (the GEMM does not shard across GPUs here), times
+are max-reduced, and `value` sums all ranks' FLOPs ("scaling": "weak").
+--impl reference times the CPU oracle (fp64 triple loop) on a bounded sample
+of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "TFLOP/s (2MNK/t) FP16 TN GEMM 8192³ on 1 GB300; % of dense tensor peak"
+NOMINAL_PEAK = {"f16": 2250.0, "e4m3": 4500.0}          # dense TFLOP/s per GPU
+KERNEL_NAME = {"f16": "tn_gemm_kernel<KindF16>", "e4m3": "tn_gemm_kernel<KindE4M3>"}
+KERNEL_SOURCES = ["dense_gemm_tn_gb300/csrc/tn_gemm_kernel.cuh", "dense_gemm_tn_gb300/csrc/sm103_ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"bf16_burst": d.get("bf16_tflops"), "bf16_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d.get("hbm_gbs"), "src": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "src": "fallback"}
+
+
+def measured_traffic(workload: str):
+    """dram read+write bytes per launch from the committed ncu summary, if it
+    was taken on the current kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_sha") != kernel_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, pw = [], [], []
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                pw.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        loaded = [s for s, p in zip(sm, pw) if p > 300.0] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(pw)}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample(w: synth.Workload, A, B, sa, sb, target_s: float):
+    """Times the oracle on a random sample of the workload's outputs (full K
+    each); the sample grows until one run takes about `target_s` seconds.
+    Returns (TFLOP/s, cores, description)."""
+    import oracle
+    rng = np.random.default_rng(12345)
+    count = 256
+    while True:
+        mi = rng.integers(0, w.M, count)
+        ni = rng.integers(0, w.N, count)
+        t0 = time.perf_counter()
+        if w.dtype == "e4m3":
+            oracle.gemm_f8e4m3_tn_at(w.M, w.N, w.K, A, w.K, B, w.K, sa, sb, mi, ni)
+        else:
+            oracle.gemm_f16_tn_at(w.M, w.N, w.K, A, w.K, B, w.K, mi, ni)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or count >= w.M * w.N:
+            break
+        count = int(min(w.M * w.N, count * max(2.0, 1.2 * target_s / max(dt, 1e-4))))
+    tflops = 2.0 * count * w.K / dt / 1e12
+    desc = f"{count} random outputs of {w.name} (full K={w.K} each), {dt:.1f} s"
+    return tflops, oracle.num_threads(), desc
+
+
+def host_inputs(w: synth.Workload, sets: int):
+    out = []
+    for i in range(sets):
+        A, B, sa, sb = synth.make_inputs(w, i)
+        out.append((A, B, sa, sb))
+    return out
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, w: synth.Workload, rank: int) -> None:
+    if rank != 0:
+        return
+    import oracle
+    A, B, sa, sb = synth.make_inputs(w, 0)
+    cores = oracle.num_threads()
+    # one step = a sample of outputs sized to about 0.5 s of host work
+    rng = np.random.default_rng(7)
+    count = 256
+    while True:
+        mi, ni = rng.integers(0, w.M, count), rng.integers(0, w.N, count)
+        t0 = time.perf_counter()
+        (oracle.gemm_f8e4m3_tn_at if w.dtype == "e4m3" else oracle.gemm_f16_tn_at)(
+            *((w.M, w.N, w.K, A, w.K, B, w.K) + ((sa, sb) if w.dtype == "e4m3" else ()) + (mi, ni)))
+        dt = time.perf_counter() - t0
+        if dt > 0.5 or count >= w.M * w.N:
+            break
+        count *= 2
+    fn = oracle.gemm_f8e4m3_tn_at if w.dtype == "e4m3" else oracle.gemm_f16_tn_at
+    extra = (sa, sb) if w.dtype == "e4m3" else ()
+    samples = [(rng.integers(0, w.M, count), rng.integers(0, w.N, count)) for _ in range(4)]
+    for i in range(args.warmup):
+        mi, ni = samples[i % 4]
+        fn(*((w.M, w.N, w.K, A, w.K, B, w.K) + extra + (mi, ni)))
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        mi, ni = samples[i % 4]
+        fn(*((w.M, w.N, w.K, A, w.K, B, w.K) + extra + (mi, ni)))
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = 2.0 * count * w.K / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{w.name}: M={w.M} N={w.N} K={w.K}, {count} sampled outputs per step",
+                   "M": w.M, "N": w.N, "K": w.K},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{count} random outputs per step, full K"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) -> None:
+    import torch
+
+    import dense_gemm_tn_gb300 as g
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    sets = w.rotating
+    host = host_inputs(w, sets)
+    is_f8 = w.dtype == "e4m3"
+    esz = 1 if is_f8 else 2
+    dA, dB, scales = [], [], []
+    for A, B, sa, sb in host:
+        if is_f8:
+            dA.append(torch.from_numpy(A).to(dev))
+            dB.append(torch.from_numpy(B).to(dev))
+        else:
+            dA.append(torch.from_numpy(A.view(np.int16)).to(dev))
+            dB.append(torch.from_numpy(B.view(np.int16)).to(dev))
+        scales.append((sa, sb))
+    C = torch.empty((w.N, w.M), dtype=torch.bfloat16 if is_f8 else torch.float16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = int(stream.cuda_stream)
+    M, N, K = w.M, w.N, w.K
+
+    def step(i):
+        j = i % sets
+        if is_f8:
+            g.lib.gemm_f8e4m3_tn(M, N, K, dA[j].data_ptr(), K, dB[j].data_ptr(), K, C.data_ptr(), M,
+                                 scales[j][0], scales[j][1], sh)
+        else:
+            g.lib.gemm_f16_tn(M, N, K, dA[j].data_ptr(), K, dB[j].data_ptr(), K, C.data_ptr(), M, sh)
+
+    # validate once before timing (sampled against the oracle happens in the tests)
+    step(0)
+    g.gemm_poll_device_status(sh)
+
+    clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    clocks.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        step(i)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    g.gemm_poll_device_status(sh)
+    per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flop = 2.0 * M * N * K
+    value = world * flop * args.steps / (total_ms * 1e-3) / 1e12
+    kernel_ms = statistics.mean(per_launch_ms)
+
+    # ---- end to end: pinned host inputs -> device -> GEMM -> pinned host output
+    e2e_steps = max(3, min(args.steps, 50))
+    hsets = min(sets, 2)
+    hA = [torch.from_numpy(host[j][0].view(np.int16) if not is_f8 else host[j][0]).pin_memory()
+          for j in range(hsets)]
+    hB = [torch.from_numpy(host[j][1].view(np.int16) if not is_f8 else host[j][1]).pin_memory()
+          for j in range(hsets)]
+    hC = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
+    eA, eB = torch.empty_like(dA[0]), torch.empty_like(dB[0])
+
+    def e2e_step(i):
+        j = i % hsets
+        eA.copy_(hA[j], non_blocking=True)
+        eB.copy_(hB[j], non_blocking=True)
+        sa, sb = scales[j]
+        if is_f8:
+            g.lib.gemm_f8e4m3_tn(M, N, K, eA.data_ptr(), K, eB.data_ptr(), K, C.data_ptr(), M, sa, sb, sh)
+        else:
+            g.lib.gemm_f16_tn(M, N, K, eA.data_ptr(), K, eB.data_ptr(), K, C.data_ptr(), M, sh)
+        hC.copy_(C, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    g.gemm_poll_device_status(sh)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = (M * K + N * K) * esz
+    d2h = M * N * 2
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    peaks = load_peaks()
+    ratio = 2.0 if is_f8 else 1.0      # nominal fp8 / bf16 dense ratio (4.5 / 2.25 PF)
+    peak = peaks["bf16_sustained"] * ratio
+    achieved = flop / (kernel_ms * 1e-3) / 1e12
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        tf, cores, desc = oracle_sample(w, *host[0], target_s=args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": f"{w.name}: {w.dtype} TN GEMM M={M} N={N} K={K}, {w.values} inputs, "
+                               f"{sets} rotating input set(s)",
+                   "M": M, "N": N, "K": K, "accumulate": "f32",
+                   "l2": f"inputs larger than L2: {sets} rotating sets of {(M + N) * K * esz >> 20} MiB"
+                         if sets > 1 else "single input set",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_dense_peak": 100.0 * value / world / NOMINAL_PEAK[w.dtype],
+        "e2e": {"value": world * flop / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "peak_src": f"{peaks['src']} bf16 sustained" + (" x2 (nominal fp8/bf16)" if is_f8 else
+                                                                      " (fp16 = bf16 rate)"),
+                     "kernel": KERNEL_NAME[w.dtype], "kernel_ms": kernel_ms,
+                     "traffic": measured_traffic(w.name)},
+        "cpu_baseline": cpu,
+        "clocks": clk,
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="sq_8192", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+    else:
+        run_ours(args, w, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

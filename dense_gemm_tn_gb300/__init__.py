@@ -1,0 +1,177 @@
+"""Python binding of libdense_gemm_tn.so (the C ABI in include/tn_gemm.h).
+
+Argument marshalling only: every step of the GEMM runs in the library's CUDA
+kernels.  There is no CPU or PyTorch fallback -- importing this package
+without the built library raises ImportError.
+
+The same names as the C ABI:
+
+    gemm_f16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream=None)
+    gemm_f8e4m3_tn(M, N, K, A, lda, B, ldb, C, ldc, scale_a, scale_b, stream=None)
+    gemm_poll_device_status(stream=None)
+
+A, B and C are device pointers given as ints or as CUDA torch tensors (their
+data_ptr() is passed; the tensor's shape is NOT consulted).  `stream` is an
+int handle, a torch.cuda.Stream, or None for torch's current stream.  A
+status other than GEMM_OK raises GemmError.
+
+Convenience wrappers over torch tensors in TN storage:
+    f16_tn(A (M,K) fp16, Bt (N,K) fp16, C=None) -> C^T as an (N, M) fp16 tensor
+    f8e4m3_tn(A (M,K) uint8/float8_e4m3fn, Bt (N,K), scale_a, scale_b, C=None) -> (N, M) bf16
+The (N, M) row-major result IS the column-major M x N matrix C with ldc = M.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_ARG = 1
+GEMM_ERR_UNSUPPORTED = 2
+GEMM_ERR_CUDA = 3
+GEMM_ERR_TIMEOUT = 4
+
+LIB_PATH = _build.LIB
+
+#: C symbols the header declares (checked by the test suite).
+EXPORTS = (
+    "gemm_f16_tn", "gemm_f8e4m3_tn", "gemm_status_string", "gemm_last_error",
+    "gemm_poll_device_status", "gemm_release_workspace", "gemm_tile_coord",
+    "gemm_set_wait_limit_ns", "gemm_debug_inject_stall", "gemm_build_info",
+)
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        self.status = status
+        super().__init__(f"{status_string(status)}: {detail}" if detail else status_string(status))
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+            "(nvcc for sm_103a); there is no fallback path")
+    lib = ctypes.CDLL(LIB_PATH)
+    i64, vp, st = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    lib.gemm_f16_tn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp]
+    lib.gemm_f16_tn.restype = st
+    lib.gemm_f8e4m3_tn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64,
+                                   ctypes.c_float, ctypes.c_float, vp]
+    lib.gemm_f8e4m3_tn.restype = st
+    lib.gemm_status_string.argtypes = [st]
+    lib.gemm_status_string.restype = ctypes.c_char_p
+    lib.gemm_last_error.argtypes = []
+    lib.gemm_last_error.restype = ctypes.c_char_p
+    lib.gemm_poll_device_status.argtypes = [vp]
+    lib.gemm_poll_device_status.restype = st
+    lib.gemm_release_workspace.argtypes = []
+    lib.gemm_release_workspace.restype = None
+    lib.gemm_tile_coord.argtypes = [i64, i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    lib.gemm_tile_coord.restype = ctypes.c_int
+    lib.gemm_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+    lib.gemm_set_wait_limit_ns.restype = None
+    lib.gemm_debug_inject_stall.argtypes = [ctypes.c_int]
+    lib.gemm_debug_inject_stall.restype = None
+    lib.gemm_build_info.argtypes = []
+    lib.gemm_build_info.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = _load()
+lib = _lib
+
+
+def status_string(status: int) -> str:
+    return _lib.gemm_status_string(int(status)).decode()
+
+
+def last_error() -> str:
+    return _lib.gemm_last_error().decode()
+
+
+def build_info() -> str:
+    return _lib.gemm_build_info().decode()
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _check(status: int) -> int:
+    if status != GEMM_OK:
+        raise GemmError(status, last_error())
+    return status
+
+
+def gemm_f16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
+    return _check(_lib.gemm_f16_tn(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _stream(stream)))
+
+
+def gemm_f8e4m3_tn(M, N, K, A, lda, B, ldb, C, ldc, scale_a, scale_b, stream=None) -> int:
+    return _check(_lib.gemm_f8e4m3_tn(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
+                                      float(scale_a), float(scale_b), _stream(stream)))
+
+
+def gemm_poll_device_status(stream=None) -> int:
+    return _check(_lib.gemm_poll_device_status(_stream(stream)))
+
+
+def gemm_release_workspace() -> None:
+    _lib.gemm_release_workspace()
+
+
+def gemm_tile_coord(tiles_m, tiles_n, group, tile_id):
+    tm, tn = ctypes.c_int64(), ctypes.c_int64()
+    rc = _lib.gemm_tile_coord(tiles_m, tiles_n, group, tile_id, ctypes.byref(tm), ctypes.byref(tn))
+    if rc != 0:
+        raise ValueError("gemm_tile_coord: argument out of range")
+    return tm.value, tn.value
+
+
+def gemm_set_wait_limit_ns(limit_ns: int) -> None:
+    _lib.gemm_set_wait_limit_ns(int(limit_ns))
+
+
+def gemm_debug_inject_stall(enable: bool) -> None:
+    _lib.gemm_debug_inject_stall(1 if enable else 0)
+
+
+# ---------------------------------------------------------------- torch helpers
+def f16_tn(A, Bt, C=None, stream=None):
+    """C^T (N, M) = Bt (N, K) @ A (M, K)^T, i.e. column-major C = A x B."""
+    import torch
+    M, K = A.shape
+    N = Bt.shape[0]
+    if C is None:
+        C = torch.empty((N, M), dtype=torch.float16, device=A.device)
+    gemm_f16_tn(M, N, K, A, A.stride(0) if M > 0 else max(K, 1), Bt,
+                Bt.stride(0) if N > 0 else max(K, 1), C, C.stride(0) if N > 0 else max(M, 1), stream)
+    return C
+
+
+def f8e4m3_tn(A, Bt, scale_a, scale_b, C=None, stream=None):
+    import torch
+    M, K = A.shape
+    N = Bt.shape[0]
+    if C is None:
+        C = torch.empty((N, M), dtype=torch.bfloat16, device=A.device)
+    gemm_f8e4m3_tn(M, N, K, A, A.stride(0) if M > 0 else max(K, 1), Bt,
+                   Bt.stride(0) if N > 0 else max(K, 1), C, C.stride(0) if N > 0 else max(M, 1),
+                   scale_a, scale_b, stream)
+    return C

@@ -1,0 +1,337 @@
+// tn_gemm.cu -- host side of the C ABI declared in include/tn_gemm.h:
+// argument validation, per-device state, TMA tensor-map encoding, the
+// repack path for operands TMA cannot address, and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "tn_gemm.h"
+#include "tn_gemm_kernel.cuh"
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 256;   // TMA coordinates are signed 32-bit
+constexpr int kMaxDevices = 64;
+constexpr int kGroupM = 8;                               // tile rows per raster group
+
+thread_local char t_last_error[512] = "";
+
+gemm_status_t fail(gemm_status_t s, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0, major = 0, minor = 0;
+    bool smem_attr_f16 = false, smem_attr_f8 = false;
+    void *workspace = nullptr;
+    size_t workspace_bytes = 0;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_inject_stall{0};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Current device's state, initialised on first use (caller holds no lock).
+gemm_status_t device_state(DeviceState **out, int *dev_out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(GEMM_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState &d = g_devices[dev];
+    if (!d.ready) {
+        if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return fail(GEMM_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        d.ready = true;
+    }
+    if (d.major != 10 || d.minor != 3)
+        return fail(GEMM_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                    d.major, d.minor);
+    *out = &d;
+    if (dev_out) *dev_out = dev;
+    return GEMM_OK;
+}
+
+gemm_status_t ensure_workspace(DeviceState &d, size_t bytes)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (d.workspace_bytes >= bytes) return GEMM_OK;
+    if (d.workspace) {
+        cudaFree(d.workspace);   // synchronises the device: earlier users are done
+        d.workspace = nullptr;
+        d.workspace_bytes = 0;
+    }
+    const size_t rounded = (bytes + (size_t(2) << 20) - 1) & ~((size_t(2) << 20) - 1);
+    cudaError_t e = cudaMalloc(&d.workspace, rounded);
+    if (e != cudaSuccess) {
+        d.workspace = nullptr;
+        return fail(GEMM_ERR_CUDA, "cudaMalloc(%zu) for the repack workspace: %s", rounded, cudaGetErrorString(e));
+    }
+    d.workspace_bytes = rounded;
+    return GEMM_OK;
+}
+
+gemm_status_t encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, uint64_t inner,
+                        uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                        const char *what)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t elem_strides[2] = {1, 1};
+    CUresult r = fn(map, type, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+    return GEMM_OK;
+}
+
+int launch_grid(int64_t work, int cap)
+{
+    int64_t g = (work + 255) / 256;
+    if (g > cap) g = cap;
+    return g < 1 ? 1 : static_cast<int>(g);
+}
+
+template <class Kind>
+gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                       const void *B, int64_t ldb, void *C, int64_t ldc, float scale, cudaStream_t stream)
+{
+    constexpr int64_t esz = Kind::kElemBytes;
+    const int64_t kmin = K > 1 ? K : 1;
+    if (M < 0 || N < 0 || K < 0)
+        return fail(GEMM_ERR_INVALID_ARG, "%s: negative size (M=%lld N=%lld K=%lld)", name, (long long)M,
+                    (long long)N, (long long)K);
+    if (lda < kmin) return fail(GEMM_ERR_INVALID_ARG, "%s: lda=%lld < max(1,K)", name, (long long)lda);
+    if (ldb < kmin) return fail(GEMM_ERR_INVALID_ARG, "%s: ldb=%lld < max(1,K)", name, (long long)ldb);
+    if (ldc < (M > 1 ? M : 1)) return fail(GEMM_ERR_INVALID_ARG, "%s: ldc=%lld < max(1,M)", name, (long long)ldc);
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim || lda > kMaxDim || ldb > kMaxDim || ldc > kMaxDim)
+        return fail(GEMM_ERR_UNSUPPORTED, "%s: a size or leading dimension exceeds 2^31-256", name);
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C) return fail(GEMM_ERR_INVALID_ARG, "%s: C is NULL", name);
+    if (reinterpret_cast<uintptr_t>(C) % 2) return fail(GEMM_ERR_INVALID_ARG, "%s: C is not 2-byte aligned", name);
+    if (K > 0) {
+        if (!A || !B) return fail(GEMM_ERR_INVALID_ARG, "%s: A or B is NULL", name);
+        if (reinterpret_cast<uintptr_t>(A) % esz || reinterpret_cast<uintptr_t>(B) % esz)
+            return fail(GEMM_ERR_INVALID_ARG, "%s: A or B is not aligned to its element size", name);
+    }
+    const int64_t tiles_m = (M + tn::kBlockM - 1) / tn::kBlockM;
+    const int64_t tiles_n = (N + tn::kBlockN - 1) / tn::kBlockN;
+    if (tiles_m * tiles_n > INT32_MAX) return fail(GEMM_ERR_UNSUPPORTED, "%s: too many output tiles", name);
+
+    DeviceState *dev = nullptr;
+    gemm_status_t st = device_state(&dev, nullptr);
+    if (st != GEMM_OK) return st;
+
+    if (K == 0) {
+        tn::zero_fill_kernel<<<launch_grid(M * N, dev->sms * 8), 256, 0, stream>>>(static_cast<uint16_t *>(C), ldc,
+                                                                                 M, N);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: zero fill launch: %s", name, cudaGetErrorString(e));
+        return GEMM_OK;
+    }
+
+    // The TMA reads an operand in place only when its base, its row stride and
+    // its row length K are all multiples of 16 bytes (a row that ends inside a
+    // 16-byte unit is not clipped element by element).  Other operands are
+    // first copied to a workspace with a padded stride and zero-filled pad,
+    // and the padded length becomes the tensor's inner dimension.
+    const void *a_use = A, *b_use = B;
+    int64_t lda_use = lda, ldb_use = ldb, ka = K, kb = K;
+    const bool k_aligned = (K * esz) % 16 == 0;
+    const bool repack_a = !k_aligned || (lda * esz) % 16 != 0 || reinterpret_cast<uintptr_t>(A) % 16 != 0;
+    const bool repack_b = !k_aligned || (ldb * esz) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0;
+    if (repack_a || repack_b) {
+        const int64_t ldp = (K + (16 / esz) - 1) / (16 / esz) * (16 / esz);
+        const size_t bytes_a = repack_a ? ((size_t(M) * ldp * esz + 255) & ~size_t(255)) : 0;
+        const size_t bytes_b = repack_b ? ((size_t(N) * ldp * esz + 255) & ~size_t(255)) : 0;
+        if ((st = ensure_workspace(*dev, bytes_a + bytes_b)) != GEMM_OK) return st;
+        uint8_t *ws = static_cast<uint8_t *>(dev->workspace);
+        using T = typename std::conditional<esz == 2, uint16_t, uint8_t>::type;
+        if (repack_a) {
+            tn::repack_rows_kernel<T><<<launch_grid(M * ldp, dev->sms * 8), 256, 0, stream>>>(
+                static_cast<const T *>(A), lda, reinterpret_cast<T *>(ws), ldp, M, K);
+            a_use = ws;
+            lda_use = ka = ldp;
+        }
+        if (repack_b) {
+            tn::repack_rows_kernel<T><<<launch_grid(N * ldp, dev->sms * 8), 256, 0, stream>>>(
+                static_cast<const T *>(B), ldb, reinterpret_cast<T *>(ws + bytes_a), ldp, N, K);
+            b_use = ws + bytes_a;
+            ldb_use = kb = ldp;
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: repack launch: %s", name, cudaGetErrorString(e));
+    }
+
+    tn::KernelParams prm;
+    memset(&prm, 0, sizeof(prm));
+    const CUtensorMapDataType in_type = Kind::kF8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType out_type = Kind::kF8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint32_t box_k = tn::kBlockKBytes / esz;
+    if ((st = encode_2d(&prm.tmap_a, in_type, a_use, ka, M, lda_use * esz, box_k, tn::kBlockM, "A")) != GEMM_OK)
+        return st;
+    if ((st = encode_2d(&prm.tmap_b, in_type, b_use, kb, N, ldb_use * esz, box_k, tn::kBlockN, "B")) != GEMM_OK)
+        return st;
+    // TMA stores cover rows m < M rounded down to 8 (16 bytes); the kernel
+    // writes the ragged rest, or all of C when C's base or stride is unaligned.
+    const int64_t m_tma = M & ~int64_t(7);
+    const bool tma_c = (ldc * 2) % 16 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0 && m_tma > 0;
+    if (tma_c &&
+        (st = encode_2d(&prm.tmap_c, out_type, C, m_tma, N, ldc * 2, tn::kEpiBoxM, tn::kEpiBoxN, "C")) != GEMM_OK)
+        return st;
+    prm.m_tma = tma_c ? static_cast<int32_t>(m_tma) : 0;
+    prm.c_ptr = C;
+    prm.ldc = ldc;
+    prm.M = static_cast<int32_t>(M);
+    prm.N = static_cast<int32_t>(N);
+    prm.K = static_cast<int32_t>(K);
+    prm.tiles_m = static_cast<int32_t>(tiles_m);
+    prm.tiles_n = static_cast<int32_t>(tiles_n);
+    prm.num_tiles = static_cast<int32_t>(tiles_m * tiles_n);
+    prm.num_kb = static_cast<int32_t>((K * esz + tn::kBlockKBytes - 1) / tn::kBlockKBytes);
+    prm.group = kGroupM;
+    prm.scale = scale;
+    prm.flags = (tma_c ? tn::kFlagTmaStore : 0u) | (g_inject_stall.load() ? tn::kFlagInjectStall : 0u);
+    prm.wait_limit_ns = g_wait_limit_ns.load();
+
+    auto kernel = tn::tn_gemm_kernel<Kind>;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        bool &attr = Kind::kF8 ? dev->smem_attr_f8 : dev->smem_attr_f16;
+        if (!attr) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tn::kSmemBytes);
+            if (e != cudaSuccess)
+                return fail(GEMM_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", name, cudaGetErrorString(e));
+            attr = true;
+        }
+    }
+    const int grid = static_cast<int>(prm.num_tiles < dev->sms ? prm.num_tiles : dev->sms);
+    kernel<<<grid, tn::kThreads, tn::kSmemBytes, stream>>>(prm);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_f16_tn(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+                          void *C, int64_t ldc, void *stream)
+{
+    t_last_error[0] = '\0';
+    return run_gemm<tn::KindF16>("gemm_f16_tn", M, N, K, A, lda, B, ldb, C, ldc, 1.0f,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_f8e4m3_tn(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                             int64_t ldb, void *C, int64_t ldc, float scale_a, float scale_b, void *stream)
+{
+    t_last_error[0] = '\0';
+    return run_gemm<tn::KindE4M3>("gemm_f8e4m3_tn", M, N, K, A, lda, B, ldb, C, ldc, scale_a * scale_b,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+const char *gemm_status_string(gemm_status_t s)
+{
+    switch (s) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT";
+    }
+    return "GEMM_ERR_UNKNOWN";
+}
+
+const char *gemm_last_error(void) { return t_last_error; }
+
+gemm_status_t gemm_poll_device_status(void *stream)
+{
+    t_last_error[0] = '\0';
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaStreamSynchronize: %s", cudaGetErrorString(e));
+    int v = 0;
+    e = cudaMemcpyFromSymbol(&v, tn::g_tn_status, sizeof(int));
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "reading the status word: %s", cudaGetErrorString(e));
+    if (v != 0) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(tn::g_tn_status, &zero, sizeof(int));
+        return fail(GEMM_ERR_TIMEOUT, "a kernel's bounded wait ran out (site %d)", v >> 8);
+    }
+    return GEMM_OK;
+}
+
+void gemm_release_workspace(void)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState &d = g_devices[dev];
+    if (d.workspace) cudaFree(d.workspace);
+    d.workspace = nullptr;
+    d.workspace_bytes = 0;
+}
+
+int gemm_tile_coord(int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t id, int64_t *tile_m, int64_t *tile_n)
+{
+    if (tiles_m <= 0 || tiles_n <= 0 || group <= 0 || id < 0 || id >= tiles_m * tiles_n || !tile_m || !tile_n)
+        return -1;
+    tn::tile_coord(id, tiles_m, tiles_n, group, *tile_m, *tile_n);
+    return 0;
+}
+
+void gemm_set_wait_limit_ns(uint64_t limit_ns) { g_wait_limit_ns.store(limit_ns ? limit_ns : 2000000000ull); }
+
+void gemm_debug_inject_stall(int enable) { g_inject_stall.store(enable ? 1 : 0); }
+
+const char *gemm_build_info(void)
+{
+    static char info[256];
+    snprintf(info, sizeof(info),
+             "dense_gemm_tn sm_103a: tile %dx%d (m x n), K block %d B, %d stages, TMEM %u cols, smem %d B, "
+             "group %d",
+             tn::kBlockM, tn::kBlockN, tn::kBlockKBytes, tn::kStages, tn::kTmemCols, tn::kSmemBytes, kGroupM);
+    return info;
+}
+
+}  // extern "C"

@@ -1,0 +1,425 @@
+// tn_gemm_kernel.cuh -- the persistent, warp-specialised sm_103a TN GEMM.
+//
+// C = A x B with A row-major M x K, B column-major K x N (both K-contiguous)
+// and C column-major with leading dimension ldc: the TN storage of the AMD
+// ROCm blog "FP16 GEMM optimization on AMD RDNA 3 and RDNA 4" (section "What
+// we compute"); the sum is the definition of hello-gpu ch.11 "GEMM-Like",
+// section 11.1.  Accumulation is FP32 in tensor memory.
+//
+// Orientation.  C column-major is C^T row-major: row n of C^T (= column n of
+// C) is contiguous in m.  The kernel therefore computes C^T = B^T A^T: the
+// tensor core's first operand ("lanes") is a 128-row tile of B's columns, its
+// second operand ("columns") a 256-row tile of A's rows.  TMEM lane i then
+// holds one output column n and 256 consecutive m values, so every epilogue
+// thread owns a contiguous run of C.
+//
+// The blog's RDNA design problems and their Blackwell re-solutions:
+//   LDS padding / XOR permutation (its Step 3)   -> TMA 128-byte swizzle that
+//       the tcgen05 shared-memory descriptor reads natively;
+//   buffer-descriptor OOB-zero loads (Step 4)    -> TMA out-of-bounds zero
+//       fill on loads, clipping on the TMA store, so M, N, K need not divide
+//       the tile (hello-gpu ch.11, section 11.4);
+//   double buffer + staged commit (Steps 2, 8)   -> a kStages-deep shared
+//       memory ring with full/empty mbarriers;
+//   deeper K slices (Step 5)                     -> 128-byte K blocks (64 fp16
+//       or 128 e4m3 values) per stage, 4 MMAs per stage;
+//   block reordering for cache reuse (Step 6)    -> persistent CTAs walking a
+//       grouped raster (tile_coord below);
+//   prefetch / WMMA interleave (Step 7)          -> warp specialisation: a TMA
+//       producer warp, a single-thread MMA issuer, 4 epilogue warps, and a
+//       double-buffered TMEM accumulator so the epilogue of tile i overlaps
+//       the main loop of tile i+1.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "sm103_ptx.cuh"
+
+namespace tn {
+
+// ------------------------------------------------------------------ config
+constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
+constexpr int kBlockN = 128;                // C columns per tile = MMA M (TMEM lanes)
+constexpr int kBlockM = 256;                // C rows per tile    = MMA N (TMEM columns)
+constexpr int kBlockKBytes = 128;           // bytes of K per stage and row (one swizzle span)
+constexpr int kStages = 4;
+constexpr int kTileBBytes = kBlockN * kBlockKBytes;         // 16 KiB
+constexpr int kTileABytes = kBlockM * kBlockKBytes;         // 32 KiB
+constexpr int kStageBytes = kTileABytes + kTileBBytes;      // 48 KiB
+constexpr int kMmaKBytes = 32;              // K bytes per tcgen05.mma (16 fp16 / 32 e4m3)
+constexpr int kEpiWarps = 4;
+constexpr int kEpiBoxM = 64;                // m values per TMA store box (128 B of 16-bit C)
+constexpr int kEpiBoxN = 32;                // n rows per box = one warp's TMEM lane quarter
+constexpr int kEpiBufBytes = kEpiBoxN * kEpiBoxM * 2;       // 4 KiB
+constexpr int kEpiBufs = 2;                 // per epilogue warp (ping-pong)
+constexpr uint32_t kAccCols = kBlockM;      // FP32 accumulator columns per buffer
+constexpr uint32_t kTmemCols = 2 * kAccCols;  // double-buffered accumulator = 512 columns
+
+constexpr int kSmemRing = kStages * kStageBytes;
+constexpr int kSmemEpi = kEpiWarps * kEpiBufs * kEpiBufBytes;
+constexpr int kNumBarriers = 2 * kStages + 2 + 2 + 1;
+constexpr int kSmemCtl = kNumBarriers * 8 + 16;
+constexpr int kSmemBytes = 1024 /* alignment slack */ + kSmemRing + kSmemEpi + kSmemCtl;
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB shared memory of one CTA");
+
+constexpr uint32_t kFlagTmaStore = 1u;      // C rows m < m_tma are written with TMA stores
+constexpr uint32_t kFlagInjectStall = 2u;   // test hook: MMA warp waits on a barrier nobody arrives on
+
+// Status word of the current device; set (never cleared) by a kernel whose
+// bounded wait ran out: 4 (timeout) | site << 8.
+__device__ int g_tn_status;
+
+enum WaitSite : int { kSiteEmpty = 1, kSiteFull = 2, kSiteAccEmpty = 3, kSiteAccFull = 4, kSiteStall = 5 };
+
+struct KernelParams {
+    CUtensorMap tmap_a;      // A: dims {K, M}, box {kBlockKBytes / esz, kBlockM}, 128B swizzle
+    CUtensorMap tmap_b;      // B: dims {K, N}, box {kBlockKBytes / esz, kBlockN}, 128B swizzle
+    CUtensorMap tmap_c;      // C: dims {M, N}, box {kEpiBoxM, kEpiBoxN}, 128B swizzle (TMA-store mode)
+    void *c_ptr;             // C base (direct stores)
+    int64_t ldc;
+    int32_t M, N, K;
+    int32_t m_tma;           // rows m < m_tma are written by TMA stores (a multiple of 8, or 0)
+    int32_t tiles_m, tiles_n, num_tiles, num_kb, group;
+    float scale;             // epilogue multiplier (F8: scale_a * scale_b)
+    uint32_t flags;
+    uint64_t wait_limit_ns;
+};
+
+// ------------------------------------------------------------------ scheduler
+// Grouped raster: `group` tile rows (m) form a tall region; consecutive ids
+// walk down the region's rows for one tile column (n), then the next column.
+// The last region is short when tiles_m % group != 0.  This is the GROUP_M
+// mapping of hello-gpu ch.11 section 11.3.4 and the grouped block order of
+// the ROCm blog's Step 6.
+__host__ __device__ __forceinline__ void tile_coord(int64_t id, int64_t tiles_m, int64_t tiles_n, int64_t group,
+                                                    int64_t &tm, int64_t &tn)
+{
+    const int64_t per_group = group * tiles_n;
+    const int64_t g = id / per_group;
+    const int64_t first_m = g * group;
+    const int64_t rows = (tiles_m - first_m) < group ? (tiles_m - first_m) : group;
+    const int64_t in_group = id - g * per_group;
+    tm = first_m + in_group % rows;
+    tn = in_group / rows;
+}
+
+// ------------------------------------------------------------------ waits
+// Every wait is bounded: after `limit` ns the waiting thread raises the
+// CTA's abort flag and the device status word, and returns false; the other
+// roles see the flag and leave their loops.  drain() waits for copies already
+// in flight and ignores the flag (those copies always land).
+struct Waiter {
+    volatile uint32_t *abort_flag;
+    uint64_t limit;
+
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, int site) const
+    {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        const uint64_t t0 = ptx::globaltimer();
+        while (true) {
+            if (ptx::mbar_try_wait(bar, parity)) return true;
+            if (*abort_flag) return false;
+            if (ptx::globaltimer() - t0 > limit) {
+                *abort_flag = 1u;
+                atomicCAS(&g_tn_status, 0, 4 | (site << 8));
+                return false;
+            }
+        }
+    }
+
+    __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const
+    {
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(bar, parity)) {
+            if (ptx::globaltimer() - t0 > limit) {
+                atomicCAS(&g_tn_status, 0, 4 | (kSiteFull << 8));
+                return false;
+            }
+        }
+        return true;
+    }
+};
+
+// ------------------------------------------------------------------ kinds
+struct KindF16 {
+    static constexpr bool kF8 = false;
+    static constexpr int kElemBytes = 2;
+    static constexpr uint32_t kIdesc = ptx::idesc_f32acc(kBlockN, kBlockM, 0 /*F16*/, 0 /*F16*/);
+    __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc)
+    {
+        ptx::mma_f16(d, a, b, kIdesc, acc);
+    }
+    __device__ static uint32_t pack(float lo, float hi, float) { return ptx::pack_f16x2(lo, hi); }
+};
+
+struct KindE4M3 {
+    static constexpr bool kF8 = true;
+    static constexpr int kElemBytes = 1;
+    static constexpr uint32_t kIdesc = ptx::idesc_f32acc(kBlockN, kBlockM, 0 /*E4M3*/, 0 /*E4M3*/);
+    __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc)
+    {
+        ptx::mma_f8(d, a, b, kIdesc, acc);
+    }
+    // acc * (scale_a * scale_b) in FP32, one RNE rounding to bf16.
+    __device__ static uint32_t pack(float lo, float hi, float s) { return ptx::pack_bf16x2(lo * s, hi * s); }
+};
+
+// ------------------------------------------------------------------ kernel
+template <class Kind>
+__global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_constant__ KernelParams p)
+{
+    constexpr int kBlockKElems = kBlockKBytes / Kind::kElemBytes;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_ring = ptx::smem_addr(smem);
+    const uint32_t s_epi = s_ring + kSmemRing;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmemRing + kSmemEpi);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + kNumBarriers);
+    volatile uint32_t *abort_flag = tmem_holder + 1;
+
+    const uint32_t bar0 = ptx::smem_addr(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto accfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+    auto accempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(accfull_bar(b), 1);
+            ptx::mbar_init(accempty_bar(b), kEpiWarps);
+        }
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0u;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (threadIdx.x == 32) {
+        ptx::prefetch_tensormap(&p.tmap_a);
+        ptx::prefetch_tensormap(&p.tmap_b);
+        if (p.flags & kFlagTmaStore) ptx::prefetch_tensormap(&p.tmap_c);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), kTmemCols);
+        ptx::tmem_relinquish_alloc_permit();
+    }
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const Waiter w{abort_flag, p.wait_limit_ns};
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0, issued_parity = 0;   // per stage: a load was issued / its phase parity
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                int64_t tm, tn;
+                tile_coord(tile, p.tiles_m, p.tiles_n, p.group, tm, tn);
+                const int32_t m0 = static_cast<int32_t>(tm * kBlockM);
+                const int32_t n0 = static_cast<int32_t>(tn * kBlockN);
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!w.wait(empty_bar(stage), phase ^ 1u, kSiteEmpty)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t s_b = s_ring + stage * kStageBytes;
+                    const uint32_t s_a = s_b + kTileBBytes;
+                    ptx::mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+                    ptx::tma_load_2d(s_b, &p.tmap_b, full_bar(stage), kb * kBlockKElems, n0);
+                    ptx::tma_load_2d(s_a, &p.tmap_a, full_bar(stage), kb * kBlockKElems, m0);
+                    issued |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Let every issued load land before the CTA can exit.
+            for (int s = 0; s < kStages; ++s)
+                if (issued & (1u << s)) w.drain(full_bar(s), (issued_parity >> s) & 1u);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true, issued_any = false;
+            if (p.flags & kFlagInjectStall) ok = w.wait(drain_bar, 0u, kSiteStall);   // never completes
+            for (int64_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+                if (!w.wait(accempty_bar(acc), acc_phase ^ 1u, kSiteAccEmpty)) break;
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + acc * kAccCols;
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!w.wait(full_bar(stage), phase, kSiteFull)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    const uint32_t s_b = s_ring + stage * kStageBytes;
+                    const uint32_t s_a = s_b + kTileBBytes;
+                    const uint64_t desc_b = ptx::desc_kmajor_sw128(s_b);
+                    const uint64_t desc_a = ptx::desc_kmajor_sw128(s_a);
+#pragma unroll
+                    for (int j = 0; j < kBlockKBytes / kMmaKBytes; ++j) {
+                        // +32 bytes along K inside the 128-byte swizzle span = +2 in the address field
+                        Kind::mma(d_tmem, desc_b + 2u * j, desc_a + 2u * j, (kb | j) != 0 ? 1u : 0u);
+                    }
+                    issued_any = true;
+                    ptx::mma_commit(empty_bar(stage));   // frees the stage once these MMAs have read it
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(accfull_bar(acc));       // accumulator complete
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            // All MMAs this thread issued must finish before TMEM is freed.
+            if (issued_any) {
+                ptx::mma_commit(drain_bar);
+                w.drain(drain_bar, 0u);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31 are this warp's
+        const int ew = warp - 2;
+        const bool tma_store = (p.flags & kFlagTmaStore) != 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        uint32_t chunk_ctr = 0;
+        for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+            int64_t tm, tn;
+            tile_coord(tile, p.tiles_m, p.tiles_n, p.group, tm, tn);
+            bool ok = w.wait(accfull_bar(acc), acc_phase, kSiteAccFull);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            __syncwarp();
+            ptx::tc_fence_after_sync();
+            const int32_t m0 = static_cast<int32_t>(tm * kBlockM);
+            const int32_t nw = static_cast<int32_t>(tn * kBlockN) + 32 * quarter;   // this warp's first column
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + acc * kAccCols;
+#pragma unroll 1
+            for (int c = 0; c < kBlockM / kEpiBoxM; ++c) {
+                uint32_t r0[32], r1[32];
+                ptx::tmem_ld_32x32b_x32(t_row + c * kEpiBoxM, r0);
+                ptx::tmem_ld_32x32b_x32(t_row + c * kEpiBoxM + 32, r1);
+                ptx::tmem_ld_wait(r0);
+                ptx::reg_dependency(r1);
+                if (c == kBlockM / kEpiBoxM - 1) {
+                    // last read of this accumulator: hand it back to the MMA warp
+                    ptx::tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(accempty_bar(acc));
+                }
+                uint32_t packed[32];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    packed[j] = Kind::pack(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]), p.scale);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    packed[16 + j] =
+                        Kind::pack(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]), p.scale);
+                const int32_t mc = m0 + c * kEpiBoxM;
+                if (tma_store && mc < p.m_tma) {
+                    const uint32_t buf = s_epi + (ew * kEpiBufs + (chunk_ctr & 1u)) * kEpiBufBytes;
+                    if (lane == 0) ptx::bulk_wait_group_read<kEpiBufs - 1>();   // buffer's previous store has read it
+                    __syncwarp();
+                    // row = lane (one output column n), 8 chunks of 16 B, 128-byte swizzle
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t addr = buf + lane * 128 + ((j ^ (lane & 7)) << 4);
+                        ptx::st_shared_v4(addr, packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                                          packed[4 * j + 3]);
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&p.tmap_c, buf, mc, nw);   // clipped at m_tma and N
+                        ptx::bulk_commit_group();
+                    }
+                    ++chunk_ctr;
+                }
+                if (mc + kEpiBoxM > p.m_tma) {
+                    // Direct stores with bounds: rows m_tma <= m < M (the ragged tail TMA cannot
+                    // clip at element granularity, or all of C when C is not TMA-addressable).
+                    const int64_t n = nw + lane;
+                    const int32_t lo = mc > p.m_tma ? mc : p.m_tma;
+                    if (n < p.N) {
+                        uint16_t *col = static_cast<uint16_t *>(p.c_ptr) + n * p.ldc;
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int32_t m = mc + 2 * j;
+                            if (m >= lo && m < p.M) col[m] = static_cast<uint16_t>(packed[j] & 0xFFFFu);
+                            if (m + 1 >= lo && m + 1 < p.M) col[m + 1] = static_cast<uint16_t>(packed[j] >> 16);
+                        }
+                    }
+                }
+            }
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+        if (lane == 0) ptx::bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ helpers
+// Copies a rows x K operand with row stride ld_src (elements) into a buffer
+// with row stride ld_dst >= K (a multiple of 16 bytes), zero-filling the pad.
+template <typename T>
+__global__ void repack_rows_kernel(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst, int64_t ld_dst,
+                                   int64_t rows, int64_t K)
+{
+    const int64_t total = rows * ld_dst;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / ld_dst;
+        const int64_t k = i - r * ld_dst;
+        dst[i] = k < K ? src[r * ld_src + k] : T(0);
+    }
+}
+
+// C[m + n*ldc] = +0 for m < M, n < N (the K == 0 case).
+__global__ void zero_fill_kernel(uint16_t *__restrict__ c, int64_t ldc, int64_t M, int64_t N)
+{
+    const int64_t total = M * N;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t n = i / M;
+        c[(i - n * M) + n * ldc] = 0;
+    }
+}
+
+}  // namespace tn

@@ -1,0 +1,139 @@
+/*
+ * tn_gemm.h -- C ABI of the GB300 (sm_103a) dense TN GEMM library
+ *              (libdense_gemm_tn.so).
+ *
+ * The operation, for every 0 <= m < M and 0 <= n < N:
+ *
+ *     C[m,n] = sum_{k=0}^{K-1} A[m,k] * B[k,n]
+ *
+ * is the plain matrix product of hello-gpu ch.11 "GEMM-Like", section 11.1
+ * (no alpha, no beta: C is overwritten), in the "TN" storage of the AMD ROCm
+ * blog "FP16 GEMM optimization on AMD RDNA 3 and RDNA 4", section "What we
+ * compute":
+ *
+ *   A  row-major M x K:     element (m,k) at A[m*lda + k],  lda >= max(1,K)
+ *   B  column-major K x N:  element (k,n) at B[k + n*ldb],  ldb >= max(1,K)
+ *   C  column-major M x N:  element (m,n) at C[m + n*ldc],  ldc >= max(1,M)
+ *
+ * so A and B are both contiguous along K.  (A PyTorch caller holds B as an
+ * (N, K) row-major tensor and C as an (N, M) row-major tensor.)  Products
+ * are accumulated in FP32 on the tensor cores and rounded once to the output
+ * type with round-to-nearest-even.  M, N and K need not be multiples of any
+ * tile size (the same section requires non-divisible shapes to work).
+ *
+ * Conventions shared by every entry point below:
+ *   - Pointers A, B, C are DEVICE pointers (or managed memory) on the
+ *     current CUDA device.  The caller owns all of them; the library keeps
+ *     no reference after the call returns.
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *     default stream.  Calls are asynchronous: they return after enqueueing
+ *     work; errors found inside a kernel (a bounded wait that ran out) are
+ *     reported later by gemm_poll_device_status().
+ *   - M == 0 or N == 0: nothing is launched, GEMM_OK.  K == 0: C is filled
+ *     with +0.
+ *   - C must not overlap A or B (undefined result).
+ *   - Operands whose row stride (ld * element size) or base address is not
+ *     a multiple of 16 bytes are first copied into a library-owned, lazily
+ *     grown device workspace (one per device) with a padded stride.  Calls
+ *     that take this path must not run concurrently on different streams.
+ *   - Thread safety: every entry point may be called from several host
+ *     threads; the per-device state is guarded internally.
+ */
+#ifndef DENSE_GEMM_TN_H
+#define DENSE_GEMM_TN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1,   /* negative size, ld too small, NULL or misaligned pointer */
+    GEMM_ERR_UNSUPPORTED = 2,   /* device is not sm_103, or a size beyond 2^31 - 256 */
+    GEMM_ERR_CUDA = 3,          /* a CUDA runtime / driver call failed (see gemm_last_error) */
+    GEMM_ERR_TIMEOUT = 4        /* a kernel's bounded wait ran out (reported by poll) */
+} gemm_status_t;
+
+/*
+ * FP16 TN GEMM.  A, B: IEEE binary16 (__half); C: binary16.
+ * Errors: GEMM_ERR_INVALID_ARG for M, N or K < 0, lda/ldb < max(1,K),
+ * ldc < max(1,M), a NULL pointer with work to do, or a pointer not 2-byte
+ * aligned; GEMM_ERR_UNSUPPORTED off sm_103; GEMM_ERR_CUDA on a failed launch.
+ */
+gemm_status_t gemm_f16_tn(int64_t M, int64_t N, int64_t K,
+                          const void *A, int64_t lda,
+                          const void *B, int64_t ldb,
+                          void *C, int64_t ldc,
+                          void *stream);
+
+/*
+ * FP8 TN GEMM.  A, B: OCP E4M3 ("e4m3fn") codes, one byte each; C: bfloat16.
+ * scale_a and scale_b are per-tensor DEQUANTISATION factors: the FP32
+ * accumulator is multiplied by (scale_a * scale_b) in FP32 and rounded once
+ * to bfloat16, i.e. C[m,n] = bf16(acc[m,n] * scale_a * scale_b).  (The FP8
+ * variant with per-tensor scales and bf16 output has no printed counterpart
+ * on the pages; the blog above announces the FP8 port as its part 2.)
+ * Errors as for gemm_f16_tn (pointers need 1-byte alignment, C 2-byte).
+ */
+gemm_status_t gemm_f8e4m3_tn(int64_t M, int64_t N, int64_t K,
+                             const void *A, int64_t lda,
+                             const void *B, int64_t ldb,
+                             void *C, int64_t ldc,
+                             float scale_a, float scale_b,
+                             void *stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *gemm_status_string(gemm_status_t status);
+
+/* Detail of the last error returned on the calling host thread (static,
+ * thread-local storage; "" when none). */
+const char *gemm_last_error(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word.  Returns GEMM_ERR_TIMEOUT if a kernel gave up on a bounded wait since
+ * the last poll (its C is then incomplete), GEMM_ERR_CUDA if the stream
+ * reported an error, GEMM_OK otherwise.
+ */
+gemm_status_t gemm_poll_device_status(void *stream);
+
+/* Frees the current device's repack workspace (synchronises the device). */
+void gemm_release_workspace(void);
+
+/*
+ * Output-tile order of the persistent scheduler, exported so the host can
+ * check it.  Tile `id` of a tiles_m x tiles_n grid maps to (*tile_m, *tile_n)
+ * by the grouped raster of hello-gpu ch.11 section 11.3.4 (GROUP_M) and of the
+ * ROCm blog's "Step 6" (blocks grouped into tall regions of `group` tile rows,
+ * the last group short): consecutive ids walk down `group` rows of one tile
+ * column before moving to the next column.  Returns 0, or -1 if an argument
+ * is out of range.
+ */
+int gemm_tile_coord(int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t id,
+                    int64_t *tile_m, int64_t *tile_n);
+
+/*
+ * Limit, in nanoseconds, of every device-side wait of kernels launched after
+ * this call on any device (default 2e9).  0 restores the default.  A wait that
+ * exceeds it makes the kernel record GEMM_ERR_TIMEOUT, drain its in-flight
+ * copies, free its tensor memory and return.
+ */
+void gemm_set_wait_limit_ns(uint64_t limit_ns);
+
+/*
+ * Test hook: while `enable` is non-zero, launched GEMM kernels make their MMA
+ * warp wait first on a barrier nothing arrives on, so the bounded wait runs
+ * out and the kernel exits through its timeout path (no fault, no hang).
+ */
+void gemm_debug_inject_stall(int enable);
+
+/* Tile configuration and build string, e.g. for logs (static storage). */
+const char *gemm_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DENSE_GEMM_TN_H */

@@ -1,0 +1,119 @@
+"""CPU-side checks of the C ABI: the library loads and exports every function
+include/tn_gemm.h declares, host-side argument validation, the scheduler's
+tile order, and the no-GPU failure mode.  No kernel runs here."""
+import os
+import re
+
+import pytest
+
+from tests.conftest import GOLDEN, ROOT
+
+g = pytest.importorskip("dense_gemm_tn_gb300", reason="library not built")
+
+HEADER = os.path.join(ROOT, "include", "tn_gemm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    names = declared_functions()
+    assert "gemm_f16_tn" in names and "gemm_f8e4m3_tn" in names
+    for n in names:
+        assert hasattr(g.lib, n), n
+    assert sorted(g.EXPORTS) == names
+
+
+def test_status_strings():
+    assert g.status_string(0) == "GEMM_OK"
+    assert g.status_string(4) == "GEMM_ERR_TIMEOUT"
+    assert g.status_string(99) == "GEMM_ERR_UNKNOWN"
+    assert "sm_103a" in g.build_info()
+
+
+BAD_ARGS = [
+    dict(M=-1), dict(N=-1), dict(K=-1),
+    dict(lda=3), dict(ldb=3), dict(ldc=7),
+    dict(C=0), dict(A=0), dict(B=0), dict(C=0x1001),
+]
+
+
+@pytest.mark.parametrize("bad", BAD_ARGS)
+def test_invalid_arguments_rejected_before_any_cuda_call(bad):
+    args = dict(M=8, N=8, K=4, A=0x1000, lda=4, B=0x2000, ldb=4, C=0x3000, ldc=8)
+    args.update(bad)
+    st = g.lib.gemm_f16_tn(args["M"], args["N"], args["K"], args["A"], args["lda"], args["B"],
+                           args["ldb"], args["C"], args["ldc"], None)
+    assert st == g.GEMM_ERR_INVALID_ARG
+    assert g.last_error() != ""
+    st8 = g.lib.gemm_f8e4m3_tn(args["M"], args["N"], args["K"], args["A"], args["lda"], args["B"],
+                               args["ldb"], args["C"], args["ldc"], 1.0, 1.0, None)
+    assert st8 == g.GEMM_ERR_INVALID_ARG
+
+
+def test_misaligned_f16_operand_rejected():
+    assert g.lib.gemm_f16_tn(8, 8, 4, 0x1001, 4, 0x2000, 4, 0x3000, 8, None) == g.GEMM_ERR_INVALID_ARG
+    # one-byte alignment is enough for e4m3 operands: this passes validation
+    # and then fails only for lack of a device (or runs on a GPU machine; not here)
+
+
+def test_oversized_dimensions_unsupported():
+    assert g.lib.gemm_f16_tn(1 << 31, 8, 4, 0x1000, 4, 0x2000, 4, 0x3000, 1 << 31, None) == \
+        g.GEMM_ERR_UNSUPPORTED
+
+
+def test_empty_output_is_noop_without_device():
+    assert g.lib.gemm_f16_tn(0, 8, 4, None, 4, None, 4, None, 1, None) == g.GEMM_OK
+    assert g.lib.gemm_f16_tn(8, 0, 4, None, 4, None, 4, None, 8, None) == g.GEMM_OK
+
+
+def test_no_device_reports_cuda_error():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = g.lib.gemm_f16_tn(8, 8, 4, 0x1000, 4, 0x2000, 4, 0x3000, 8, None)
+    assert st == g.GEMM_ERR_CUDA
+
+
+# ------------------------------------------------------------------ scheduler
+def test_tile_order_matches_hand_mapping():
+    """hello-gpu ch.11 section 11.3.4: 4 x 3 output blocks, GROUP_M = 1 and 2."""
+    import json
+    with open(os.path.join(GOLDEN, "group_m_mapping.json")) as f:
+        gold = json.load(f)
+    tm, tn = gold["tiles_m"], gold["tiles_n"]
+    assert [list(g.gemm_tile_coord(tm, tn, 1, i)) for i in range(4)] == gold["group_1_first"]
+    assert [list(g.gemm_tile_coord(tm, tn, 2, i)) for i in range(4)] == gold["group_2_first"]
+
+
+def rocm_blog_step6(block, tiles_m, tiles_n, group):
+    """The grouped block order as the ROCm blog's Step 6 states it (rows of
+    tiles are grouped by `group`, the last group short)."""
+    index_n = block % tiles_n
+    index_m = block // tiles_n
+    group_rows = group if index_m < tiles_m - tiles_m % group else tiles_m % group
+    grp = index_m // group
+    local = index_n + (index_m % group) * tiles_n
+    return local % group_rows + grp * group, local // group_rows
+
+
+@pytest.mark.parametrize("tiles_m,tiles_n,group", [(4, 3, 2), (32, 64, 8), (12, 97, 8), (13, 7, 8),
+                                                   (1, 5, 8), (9, 1, 4), (24, 49, 8), (8, 8, 8)])
+def test_tile_order_matches_step6_and_covers_grid(tiles_m, tiles_n, group):
+    seen = set()
+    for i in range(tiles_m * tiles_n):
+        t = g.gemm_tile_coord(tiles_m, tiles_n, group, i)
+        assert t == rocm_blog_step6(i, tiles_m, tiles_n, group)
+        assert 0 <= t[0] < tiles_m and 0 <= t[1] < tiles_n
+        seen.add(t)
+    assert len(seen) == tiles_m * tiles_n
+
+
+def test_tile_coord_rejects_out_of_range():
+    with pytest.raises(ValueError):
+        g.gemm_tile_coord(4, 3, 2, 12)
+    with pytest.raises(ValueError):
+        g.gemm_tile_coord(0, 3, 2, 0)

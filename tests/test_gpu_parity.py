@@ -1,0 +1,213 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bit-exact on +-1 inputs (every partial sum is an integer below 2^24, so FP32
+accumulation is exact in any order and both sides round the same integer
+once); within |C - C_ref| <= 2^-10 |C_ref| + 2^-12 sum_k|a b| for FP16 and
+2^-7 |C_ref| + 2^-8 sum_k|a b| for FP8 with bf16 output on Gaussian inputs.
+Every output buffer is NaN-poisoned and fenced by canary bands.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_helpers import (F8_TOL, F16_TOL, assert_tol, bf16_values, check_f8_full,
+                               check_f16_full, f16_values, run_f8, run_f16, sample_positions,
+                               to_dev_u8, to_dev_u16, GuardedC)
+
+pytestmark = pytest.mark.gpu
+
+EDGE_SHAPES = [(1, 1, 1), (3, 5, 7), (15, 17, 19), (17, 19, 23), (31, 33, 29)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import dense_gemm_tn_gb300 as g
+    return g
+
+
+def f16(vals):
+    return np.asarray(vals, np.float64).astype(np.float16).view(np.uint16)
+
+
+# ---------------------------------------------------------------- page values
+def test_worked_example():
+    """hello-gpu ch.11 section 11.1: [[1,2,3],[4,5,6]] x [[1,0],[2,1],[0,2]]."""
+    A = f16([1, 2, 3, 4, 5, 6])
+    B = f16([1, 2, 0, 0, 1, 2])
+    got = run_f16(2, 2, 3, A, 3, B, 3)
+    assert f16_values(got).T.tolist() == [[5, 8], [14, 17]]
+
+
+@pytest.mark.parametrize("M,N,K", EDGE_SHAPES)
+def test_edge_shapes_gaussian(M, N, K):
+    A = synth.gauss_fp16(M * K, 1000 + K)
+    B = synth.gauss_fp16(N * K, 2000 + K)
+    check_f16_full(M, N, K, A, B, what=f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", EDGE_SHAPES)
+def test_edge_shapes_pm1_exact(M, N, K):
+    A = synth.sign_fp16(M * K, 3000 + K)
+    B = synth.sign_fp16(N * K, 4000 + K)
+    check_f16_full(M, N, K, A, B, exact=True, what=f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", EDGE_SHAPES)
+def test_edge_shapes_e4m3(M, N, K):
+    A, sa = synth.gauss_e4m3(M * K, 5000 + K)
+    B, sb = synth.gauss_e4m3(N * K, 6000 + K)
+    check_f8_full(M, N, K, A, B, sa, sb, what=f"e4m3 {M}x{N}x{K}")
+
+
+# ---------------------------------------------------------------- tile boundaries
+BOUNDARY = [(255, 127, 64), (256, 128, 64), (257, 129, 65), (511, 383, 63), (513, 257, 200),
+            (128, 640, 1), (300, 200, 136), (1000, 300, 1000), (64, 64, 8)]
+
+
+@pytest.mark.parametrize("M,N,K", BOUNDARY)
+def test_tile_boundaries_pm1_exact(M, N, K):
+    A = synth.sign_fp16(M * K, 7 + M)
+    B = synth.sign_fp16(N * K, 8 + N)
+    check_f16_full(M, N, K, A, B, exact=True, what=f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", BOUNDARY)
+def test_tile_boundaries_gaussian(M, N, K):
+    A = synth.gauss_fp16(M * K, 9 + M)
+    B = synth.gauss_fp16(N * K, 10 + N)
+    check_f16_full(M, N, K, A, B, what=f"{M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(257, 129, 130), (300, 200, 256), (513, 384, 1000)])
+def test_tile_boundaries_e4m3(M, N, K):
+    A, sa = synth.gauss_e4m3(M * K, 11 + M)
+    B, sb = synth.gauss_e4m3(N * K, 12 + N)
+    check_f8_full(M, N, K, A, B, sa, sb, what=f"e4m3 {M}x{N}x{K}")
+
+
+# ---------------------------------------------------------------- layouts
+@pytest.mark.parametrize("lda,ldb,ldc,c_off", [
+    (136, 136, 304, 0),     # padded, all 16-byte aligned: TMA everywhere
+    (141, 137, 303, 0),     # odd strides: repack A and B, direct C stores
+    (136, 136, 300, 1),     # C base off 16-byte alignment: direct C stores
+    (144, 144, 312, 0),     # K, lda, ldb, ldc aligned, M ragged: TMA stores + direct tail
+])
+def test_leading_dimensions(lda, ldb, ldc, c_off):
+    M, N, K = 300, 200, 130
+    A = synth.gauss_fp16(M * K, 21)
+    B = synth.gauss_fp16(N * K, 22)
+    check_f16_full(M, N, K, A, B, lda=lda, ldb=ldb, ldc=ldc, c_offset=c_off, what="ld")
+
+
+@pytest.mark.parametrize("M,ldc", [(5, 8), (13, 16), (8, 8), (70, 72)])
+def test_small_m_with_aligned_ldc(M, ldc):
+    N, K = 40, 64
+    A = synth.sign_fp16(M * K, 27)
+    B = synth.sign_fp16(N * K, 28)
+    check_f16_full(M, N, K, A, B, exact=True, ldc=ldc, what=f"M={M} ldc={ldc}")
+
+
+def test_unaligned_operand_bases():
+    M, N, K = 200, 150, 64
+    A = synth.gauss_fp16(M * K, 23)
+    B = synth.gauss_fp16(N * K, 24)
+    check_f16_full(M, N, K, A, B, a_offset=3, b_offset=5, what="offset bases")
+    A8, sa = synth.gauss_e4m3(M * K, 25)
+    B8, sb = synth.gauss_e4m3(N * K, 26)
+    check_f8_full(M, N, K, A8, B8, sa, sb, a_offset=7, b_offset=1, what="e4m3 offset bases")
+
+
+def test_k_zero_writes_zeros_and_empty_is_noop():
+    import dense_gemm_tn_gb300 as g
+    got = run_f16(5, 3, 0, np.zeros(1, np.uint16), 1, np.zeros(1, np.uint16), 1)
+    assert np.all(got == 0)
+    C = GuardedC(4, 1, 4)
+    g.gemm_f16_tn(0, 1, 8, 0, 8, 0, 8, C.ptr, 4)
+    g.gemm_f16_tn(4, 0, 8, 0, 8, 0, 8, C.ptr, 4)
+    torch.cuda.synchronize()
+    assert np.all(C.host() == 0x7E00)           # untouched
+
+
+def test_identity_returns_b_exactly():
+    K, N = 192, 160
+    Bc = synth.gauss_fp16(N * K, 31)
+    A = f16(np.eye(K).reshape(-1))
+    got = run_f16(K, N, K, A, K, Bc, K)
+    assert np.array_equal(got, Bc.reshape(N, K))
+
+
+def test_all_ones_closed_form():
+    """C == fp16_rne(K): 4097 rounds to 4096 (the wide workload's K)."""
+    M, N, K = 260, 130, 4097
+    got = run_f16(M, N, K, f16(np.ones(M * K)), K, f16(np.ones(N * K)), K)
+    assert np.all(f16_values(got) == 4096.0)
+
+
+def test_deterministic_and_side_stream():
+    M, N, K = 700, 500, 300
+    A = synth.gauss_fp16(M * K, 41)
+    B = synth.gauss_fp16(N * K, 42)
+    s = torch.cuda.Stream()
+    g1 = run_f16(M, N, K, A, K, B, K, stream=s)
+    g2 = run_f16(M, N, K, A, K, B, K)
+    assert np.array_equal(g1, g2)
+
+
+# ---------------------------------------------------------------- the five workloads
+def test_workload_pm1_512_exact():
+    w = synth.WORKLOADS["pm1_512"]
+    A, B, _, _ = synth.make_inputs(w)
+    check_f16_full(w.M, w.N, w.K, A, B, exact=True, what=w.name)
+
+
+def test_workload_qk_1024():
+    w = synth.WORKLOADS["qk_1024"]
+    A, B, _, _ = synth.make_inputs(w)
+    check_f16_full(w.M, w.N, w.K, A, B, what=w.name)
+
+
+def _sampled_f16(w, A, B, got, exact, count=20000):
+    mi, ni = sample_positions(w.M, w.N, count, seed=w.seed_a)
+    c, s, _ = oracle.gemm_f16_tn_at(w.M, w.N, w.K, A, w.K, B, w.K, mi, ni)
+    g = got[ni, mi]
+    if exact:
+        assert np.array_equal(g, c), f"{w.name}: {np.sum(g != c)} sampled outputs differ"
+    else:
+        assert_tol(f16_values(g), f16_values(c), s, F16_TOL, w.name)
+
+
+@pytest.mark.parametrize("name", ["wide_pm1", "wide_gauss"])
+def test_workload_wide(name):
+    w = synth.WORKLOADS[name]
+    A, B, _, _ = synth.make_inputs(w)
+    got = run_f16(w.M, w.N, w.K, A, w.K, B, w.K)
+    _sampled_f16(w, A, B, got, exact=(w.values == "pm1"))
+    vals = f16_values(got)
+    assert not np.isnan(vals).any()
+    if w.values == "pm1":
+        # at every output: an integer of K's parity with |C| <= K (|C| < 2048 here)
+        assert np.all(np.abs(vals) <= w.K) and np.all(vals == np.round(vals))
+        small = np.abs(vals) < 2048
+        assert np.all((vals[small].astype(np.int64) - w.K) % 2 == 0)
+
+
+def test_workload_sq_8192_sampled():
+    w = synth.WORKLOADS["sq_8192"]
+    A, B, _, _ = synth.make_inputs(w, 0)
+    got = run_f16(w.M, w.N, w.K, A, w.K, B, w.K)
+    _sampled_f16(w, A, B, got, exact=False, count=8000)
+    assert not np.isnan(f16_values(got)).any()
+
+
+def test_workload_e4m3_8192_sampled():
+    w = synth.WORKLOADS["e4m3_8192"]
+    A, B, sa, sb = synth.make_inputs(w, 0)
+    got = run_f8(w.M, w.N, w.K, A, w.K, B, w.K, sa, sb)
+    mi, ni = sample_positions(w.M, w.N, 8000, seed=w.seed_a)
+    c, s, _ = oracle.gemm_f8e4m3_tn_at(w.M, w.N, w.K, A, w.K, B, w.K, sa, sb, mi, ni)
+    assert_tol(bf16_values(got[ni, mi]), bf16_values(c), s, F8_TOL, w.name)
+    assert not np.isnan(bf16_values(got)).any()
