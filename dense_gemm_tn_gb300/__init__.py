@@ -40,6 +40,7 @@ EXPORTS = (
     "gemm_f16_tn", "gemm_f8e4m3_tn", "gemm_status_string", "gemm_last_error",
     "gemm_poll_device_status", "gemm_release_workspace", "gemm_tile_coord",
     "gemm_set_wait_limit_ns", "gemm_debug_inject_stall", "gemm_build_info",
+    "gemm_f16_tn_noalloc",
 )
 
 
@@ -61,6 +62,8 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f8e4m3_tn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64,
                                    ctypes.c_float, ctypes.c_float, vp]
     lib.gemm_f8e4m3_tn.restype = st
+    lib.gemm_f16_tn_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp]
+    lib.gemm_f16_tn_noalloc.restype = st
     lib.gemm_status_string.argtypes = [st]
     lib.gemm_status_string.restype = ctypes.c_char_p
     lib.gemm_last_error.argtypes = []
@@ -126,6 +129,15 @@ def gemm_f16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
 def gemm_f8e4m3_tn(M, N, K, A, lda, B, ldb, C, ldc, scale_a, scale_b, stream=None) -> int:
     return _check(_lib.gemm_f8e4m3_tn(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
                                       float(scale_a), float(scale_b), _stream(stream)))
+
+
+def gemm_f16_tn_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
+    """gemm_f16_tn for callers that cannot let the library allocate device
+    memory (their own memory pool or budget, or no implicit synchronisation
+    allowed): operand copies go to a fixed 32 MiB array in the library's
+    device image instead of a cudaMalloc'd workspace."""
+    return _check(_lib.gemm_f16_tn_noalloc(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
+                                           _stream(stream)))
 
 
 def gemm_poll_device_status(stream=None) -> int:

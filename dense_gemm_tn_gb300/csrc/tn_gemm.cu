@@ -335,3 +335,100 @@ const char *gemm_build_info(void)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gemm_f16_tn_noalloc: the FP16 entry point for callers that must not have the
+// library allocate device memory.  Where gemm_f16_tn would grow its repack
+// workspace with cudaMalloc, this variant copies the operand(s) into a fixed
+// array that is part of the library's device image.  Once repacked, the
+// operands are 16-byte aligned with a padded K (zero filled), so the ordinary
+// FP16 path runs on them without touching its own workspace.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB on every device that loads the library
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch per device (host code cannot use the
+// symbol itself: on the host it names a stand-in, not device memory).
+void *g_noalloc_scratch_ptr[kMaxDevices] = {};
+
+gemm_status_t noalloc_scratch(void **out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return fail(GEMM_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_noalloc_scratch_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(GEMM_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+        g_noalloc_scratch_ptr[dev] = p;
+    }
+    *out = g_noalloc_scratch_ptr[dev];
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" gemm_status_t gemm_f16_tn_noalloc(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
+                                             const void *B, int64_t ldb, void *C, int64_t ldc, void *stream)
+{
+    t_last_error[0] = '\0';
+    const char *name = "gemm_f16_tn_noalloc";
+    constexpr int64_t esz = 2;
+    const int64_t kmin = K > 1 ? K : 1;
+    // Arguments the ordinary path would reject are handed to it unchanged so
+    // the caller sees the same status and message; nothing is copied for them.
+    const bool plain = M <= 0 || N <= 0 || K <= 0 || lda < kmin || ldb < kmin || ldc < (M > 1 ? M : 1) ||
+                       M > kMaxDim || N > kMaxDim || K > kMaxDim || lda > kMaxDim || ldb > kMaxDim ||
+                       ldc > kMaxDim || !A || !B || !C || reinterpret_cast<uintptr_t>(A) % esz ||
+                       reinterpret_cast<uintptr_t>(B) % esz;
+    if (plain) return gemm_f16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream);
+
+    const bool k_aligned = (K * esz) % 16 == 0;
+    const bool repack_a = !k_aligned || (lda * esz) % 16 != 0 || reinterpret_cast<uintptr_t>(A) % 16 != 0;
+    const bool repack_b = !k_aligned || (ldb * esz) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0;
+    if (!repack_a && !repack_b) return gemm_f16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream);
+
+    const int64_t ldp = (K + 7) / 8 * 8;
+    const size_t bytes_a = repack_a ? ((size_t(M) * ldp * esz + 255) & ~size_t(255)) : 0;
+    const size_t bytes_b = repack_b ? ((size_t(N) * ldp * esz + 255) & ~size_t(255)) : 0;
+    if (bytes_a + bytes_b > kNoAllocScratchBytes)
+        return fail(GEMM_ERR_INVALID_ARG,
+                    "%s: the repacked operands need %zu bytes, more than the fixed %zu-byte scratch array", name,
+                    bytes_a + bytes_b, kNoAllocScratchBytes);
+
+    DeviceState *dev = nullptr;
+    gemm_status_t st = device_state(&dev, nullptr);
+    if (st != GEMM_OK) return st;
+    void *scratch = nullptr;
+    if ((st = noalloc_scratch(&scratch)) != GEMM_OK) return st;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(scratch);
+    const void *a_use = A, *b_use = B;
+    int64_t lda_use = lda, ldb_use = ldb;
+    if (repack_a) {
+        tn::repack_rows_kernel<uint16_t><<<launch_grid(M * ldp, dev->sms * 8), 256, 0, s>>>(
+            static_cast<const uint16_t *>(A), lda, reinterpret_cast<uint16_t *>(ws), ldp, M, K);
+        a_use = ws;
+        lda_use = ldp;
+    }
+    if (repack_b) {
+        tn::repack_rows_kernel<uint16_t><<<launch_grid(N * ldp, dev->sms * 8), 256, 0, s>>>(
+            static_cast<const uint16_t *>(B), ldb, reinterpret_cast<uint16_t *>(ws + bytes_a), ldp, N, K);
+        b_use = ws + bytes_a;
+        ldb_use = ldp;
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: repack launch: %s", name, cudaGetErrorString(e));
+    // When K is not a multiple of 8 both operands were repacked with zeros in
+    // columns K..ldp-1; those extra products are +0 and leave every sum as is.
+    const int64_t k_use = k_aligned ? K : ldp;
+    st = gemm_f16_tn(M, N, k_use, a_use, lda_use, b_use, ldb_use, C, ldc, stream);
+    if (st != GEMM_OK) return st;
+    return GEMM_OK;
+}

@@ -84,6 +84,38 @@ gemm_status_t gemm_f8e4m3_tn(int64_t M, int64_t N, int64_t K,
                              float scale_a, float scale_b,
                              void *stream);
 
+/*
+ * gemm_f16_tn without any device allocation by the library.
+ *
+ * The paper has no counterpart to this entry point; it exists for callers
+ * that cannot let a library call cudaMalloc: programs that hand out all
+ * device memory from their own pool or fixed budget, and latency-critical
+ * paths where the implicit device synchronisation of cudaMalloc / cudaFree
+ * is not acceptable.  Arguments, layouts and results are those of
+ * gemm_f16_tn; the caller still passes (and owns) A, B and C.
+ *
+ * Where gemm_f16_tn would copy an operand into its lazily grown workspace
+ * (base, row stride or K not a multiple of 16 bytes), this call copies it
+ * into a fixed 32 MiB array that is part of the library's device image
+ * instead (every GPU that loads the library holds it until the process
+ * exits).  If the padded copies need more than 32 MiB
+ * (2 * roundup(K, 8) * (rows of each operand that needs the copy), each
+ * operand rounded up to 256 bytes), the call returns GEMM_ERR_INVALID_ARG
+ * and launches nothing.  Aligned operands need no copy and no scratch.
+ *
+ * The array is shared by every call on a device and keeps the last call's
+ * contents (each call overwrites all of the part it reads).  Calls that
+ * overlap on the GPU -- on different streams, without ordering -- race on it.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ */
+gemm_status_t gemm_f16_tn_noalloc(int64_t M, int64_t N, int64_t K,
+                                  const void *A, int64_t lda,
+                                  const void *B, int64_t ldb,
+                                  void *C, int64_t ldc,
+                                  void *stream);
+
 /* Human-readable name of a status code (static storage). */
 const char *gemm_status_string(gemm_status_t status);
 
