@@ -37,7 +37,7 @@ METRIC = "TFLOP/s (2MNK/t) FP16 TN GEMM 8192³ on 1 GB300; % of dense tensor pea
 NOMINAL_PEAK = {"f16": 2250.0, "e4m3": 4500.0}          # dense TFLOP/s per GPU
 KERNEL_NAME = {"f16": "tn_gemm_kernel<KindF16>", "e4m3": "tn_gemm_kernel<KindE4M3>"}
 KERNEL_SOURCES = ["dense_gemm_tn_gb300/csrc/tn_gemm_kernel.cuh", "dense_gemm_tn_gb300/csrc/sm103_ptx.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+PROFILES_DIR = os.path.join(ROOT, "profiles")
 
 
 def kernel_sha() -> str:
@@ -59,16 +59,20 @@ def load_peaks() -> dict:
 
 
 def measured_traffic(workload: str):
-    """dram read+write bytes per launch from the committed ncu summary, if it
-    was taken on the current kernel source."""
-    if not os.path.exists(TRAFFIC_FILE):
-        return None
-    with open(TRAFFIC_FILE) as f:
-        d = json.load(f)
-    e = d.get(workload)
-    if not e or e.get("kernel_sha") != kernel_sha():
-        return None
-    return e.get("dram_bytes_per_launch")
+    """dram read+write bytes per launch, from the `traffic-record:` line of a
+    committed ncu summary under profiles/, if it was taken on the current
+    kernel source (else None)."""
+    import glob
+    import re
+    pat = re.compile(r"^traffic-record: workload=(\S+) kernel_sha=(\S+) dram_bytes_per_launch=(\d+)")
+    sha = kernel_sha()
+    for path in sorted(glob.glob(os.path.join(PROFILES_DIR, "*.md"))):
+        with open(path) as f:
+            for line in f:
+                m = pat.match(line.strip())
+                if m and m.group(1) == workload and m.group(2) == sha:
+                    return int(m.group(3))
+    return None
 
 
 # ---------------------------------------------------------------- clocks
@@ -223,7 +227,7 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    sets = w.rotating
+    sets = w.rotating if args.sets is None else max(1, args.sets)
     host = host_inputs(w, sets)
     is_f8 = w.dtype == "e4m3"
     esz = 1 if is_f8 else 2
@@ -372,6 +376,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--sets", type=int, default=None,
+                    help="input sets to rotate (default: the workload's; 1 for small profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
