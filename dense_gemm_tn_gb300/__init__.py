@@ -40,7 +40,7 @@ EXPORTS = (
     "gemm_f16_tn", "gemm_f8e4m3_tn", "gemm_status_string", "gemm_last_error",
     "gemm_poll_device_status", "gemm_release_workspace", "gemm_tile_coord",
     "gemm_set_wait_limit_ns", "gemm_debug_inject_stall", "gemm_build_info",
-    "gemm_f16_tn_noalloc",
+    "gemm_f16_tn_noalloc", "gemm_debug_force_cta_group", "gemm_debug_last_launch",
 )
 
 
@@ -78,6 +78,10 @@ def _load() -> ctypes.CDLL:
     lib.gemm_set_wait_limit_ns.restype = None
     lib.gemm_debug_inject_stall.argtypes = [ctypes.c_int]
     lib.gemm_debug_inject_stall.restype = None
+    lib.gemm_debug_force_cta_group.argtypes = [ctypes.c_int]
+    lib.gemm_debug_force_cta_group.restype = ctypes.c_int
+    lib.gemm_debug_last_launch.argtypes = []
+    lib.gemm_debug_last_launch.restype = ctypes.c_char_p
     lib.gemm_build_info.argtypes = []
     lib.gemm_build_info.restype = ctypes.c_char_p
     return lib
@@ -93,6 +97,10 @@ def status_string(status: int) -> str:
 
 def last_error() -> str:
     return _lib.gemm_last_error().decode()
+
+
+def last_launch() -> str:
+    return _lib.gemm_debug_last_launch().decode()
 
 
 def build_info() -> str:
@@ -162,6 +170,11 @@ def gemm_set_wait_limit_ns(limit_ns: int) -> None:
 
 def gemm_debug_inject_stall(enable: bool) -> None:
     _lib.gemm_debug_inject_stall(1 if enable else 0)
+
+
+def gemm_debug_force_cta_group(group: int) -> None:
+    if _lib.gemm_debug_force_cta_group(int(group)) != 0:
+        raise ValueError("cta group must be 0 (automatic), 1 or 2")
 
 
 # ---------------------------------------------------------------- torch helpers

@@ -34,7 +34,8 @@ gemm_status_t fail(gemm_status_t s, const char *fmt, ...)
 struct DeviceState {
     bool ready = false;
     int sms = 0, major = 0, minor = 0;
-    bool smem_attr_f16 = false, smem_attr_f8 = false;
+    bool smem_attr[2][3] = {};        // [kind: f16, e4m3][cta group]
+    int max_clusters[2][3] = {};      // co-resident clusters of the kernel (0 = not queried yet)
     void *workspace = nullptr;
     size_t workspace_bytes = 0;
 };
@@ -43,6 +44,8 @@ std::mutex g_mutex;
 DeviceState g_devices[kMaxDevices];
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
+std::atomic<int> g_force_cta_group{0};
+thread_local char t_last_launch[160] = "";
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -131,6 +134,55 @@ int launch_grid(int64_t work, int cap)
     return g < 1 ? 1 : static_cast<int>(g);
 }
 
+// Launches the persistent kernel: one CTA (or one 2-CTA cluster) per
+// co-resident slot, each walking the tile raster with a stride of the grid.
+template <class Kind, int G>
+gemm_status_t launch(const char *name, const tn::KernelParams &prm, DeviceState &dev, cudaStream_t stream)
+{
+    using Cfg = tn::TileCfg<G>;
+    auto kernel = tn::tn_gemm_kernel<Kind, G>;
+    const int ki = Kind::kF8 ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(tn::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int slots;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!dev.smem_attr[ki][G]) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+            if (e != cudaSuccess)
+                return fail(GEMM_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", name, cudaGetErrorString(e));
+            dev.smem_attr[ki][G] = true;
+        }
+        if (dev.max_clusters[ki][G] == 0) {
+            int n = 0;
+            cfg.gridDim = dim3(G * (dev.sms / G), 1, 1);
+            cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+            if (e != cudaSuccess || n <= 0) {
+                cudaGetLastError();
+                n = dev.sms / G;     // fall back to one slot per SM (pair)
+            }
+            dev.max_clusters[ki][G] = n;
+        }
+        slots = dev.max_clusters[ki][G];
+    }
+    const int clusters = prm.num_tiles < slots ? prm.num_tiles : slots;
+    cfg.gridDim = dim3(G * clusters, 1, 1);
+    snprintf(t_last_launch, sizeof(t_last_launch), "%s: cta_group=%d grid=%d clusters=%d slots=%d tiles=%d",
+             name, G, G * clusters, clusters, slots, prm.num_tiles);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));
+    return GEMM_OK;
+}
+
 template <class Kind>
 gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
                        const void *B, int64_t ldb, void *C, int64_t ldc, float scale, cudaStream_t stream)
@@ -153,8 +205,12 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         if (reinterpret_cast<uintptr_t>(A) % esz || reinterpret_cast<uintptr_t>(B) % esz)
             return fail(GEMM_ERR_INVALID_ARG, "%s: A or B is not aligned to its element size", name);
     }
-    const int64_t tiles_m = (M + tn::kBlockM - 1) / tn::kBlockM;
-    const int64_t tiles_n = (N + tn::kBlockN - 1) / tn::kBlockN;
+    // 2-CTA pairs (256 x 256 tiles) unless the problem has at most one
+    // 128-column slab of n, where the pair's second half would be idle.
+    int cta_group = N > 128 ? 2 : 1;
+    if (const int forced = g_force_cta_group.load()) cta_group = forced;
+    const int64_t tiles_m = (M + tn::kTileM - 1) / tn::kTileM;
+    const int64_t tiles_n = (N + 128 * cta_group - 1) / (128 * cta_group);
     if (tiles_m * tiles_n > INT32_MAX) return fail(GEMM_ERR_UNSUPPORTED, "%s: too many output tiles", name);
 
     DeviceState *dev = nullptr;
@@ -207,9 +263,10 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     const CUtensorMapDataType in_type = Kind::kF8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const CUtensorMapDataType out_type = Kind::kF8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     const uint32_t box_k = tn::kBlockKBytes / esz;
-    if ((st = encode_2d(&prm.tmap_a, in_type, a_use, ka, M, lda_use * esz, box_k, tn::kBlockM, "A")) != GEMM_OK)
+    const uint32_t rows_a = static_cast<uint32_t>(tn::kTileM / cta_group);
+    if ((st = encode_2d(&prm.tmap_a, in_type, a_use, ka, M, lda_use * esz, box_k, rows_a, "A")) != GEMM_OK)
         return st;
-    if ((st = encode_2d(&prm.tmap_b, in_type, b_use, kb, N, ldb_use * esz, box_k, tn::kBlockN, "B")) != GEMM_OK)
+    if ((st = encode_2d(&prm.tmap_b, in_type, b_use, kb, N, ldb_use * esz, box_k, 128, "B")) != GEMM_OK)
         return st;
     // TMA stores cover rows m < M rounded down to 8 (16 bytes); the kernel
     // writes the ragged rest, or all of C when C's base or stride is unaligned.
@@ -233,22 +290,7 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     prm.flags = (tma_c ? tn::kFlagTmaStore : 0u) | (g_inject_stall.load() ? tn::kFlagInjectStall : 0u);
     prm.wait_limit_ns = g_wait_limit_ns.load();
 
-    auto kernel = tn::tn_gemm_kernel<Kind>;
-    {
-        std::lock_guard<std::mutex> lock(g_mutex);
-        bool &attr = Kind::kF8 ? dev->smem_attr_f8 : dev->smem_attr_f16;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tn::kSmemBytes);
-            if (e != cudaSuccess)
-                return fail(GEMM_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", name, cudaGetErrorString(e));
-            attr = true;
-        }
-    }
-    const int grid = static_cast<int>(prm.num_tiles < dev->sms ? prm.num_tiles : dev->sms);
-    kernel<<<grid, tn::kThreads, tn::kSmemBytes, stream>>>(prm);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));
-    return GEMM_OK;
+    return cta_group == 2 ? launch<Kind, 2>(name, prm, *dev, stream) : launch<Kind, 1>(name, prm, *dev, stream);
 }
 
 }  // namespace
@@ -324,13 +366,23 @@ void gemm_set_wait_limit_ns(uint64_t limit_ns) { g_wait_limit_ns.store(limit_ns 
 
 void gemm_debug_inject_stall(int enable) { g_inject_stall.store(enable ? 1 : 0); }
 
+int gemm_debug_force_cta_group(int group)
+{
+    if (group < 0 || group > 2) return -1;
+    g_force_cta_group.store(group);
+    return 0;
+}
+
+const char *gemm_debug_last_launch(void) { return t_last_launch; }
+
 const char *gemm_build_info(void)
 {
-    static char info[256];
+    static char info[320];
     snprintf(info, sizeof(info),
-             "dense_gemm_tn sm_103a: tile %dx%d (m x n), K block %d B, %d stages, TMEM %u cols, smem %d B, "
-             "group %d",
-             tn::kBlockM, tn::kBlockN, tn::kBlockKBytes, tn::kStages, tn::kTmemCols, tn::kSmemBytes, kGroupM);
+             "dense_gemm_tn sm_103a: 2-CTA tile 256x256 (%d stages, %d B smem), 1-CTA tile 128x256 (%d stages, "
+             "%d B smem); K block %d B; TMEM %u cols; raster group %d",
+             tn::TileCfg<2>::kStages, tn::TileCfg<2>::kSmemBytes, tn::TileCfg<1>::kStages,
+             tn::TileCfg<1>::kSmemBytes, tn::kBlockKBytes, tn::kTmemCols, kGroupM);
     return info;
 }
 

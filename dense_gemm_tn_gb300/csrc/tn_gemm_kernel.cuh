@@ -39,43 +39,55 @@
 namespace tn {
 
 // ------------------------------------------------------------------ config
-constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 epilogue
-constexpr int kBlockN = 128;                // C columns per tile = MMA M (TMEM lanes)
-constexpr int kBlockM = 256;                // C rows per tile    = MMA N (TMEM columns)
+constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA/TMEM (or relay), warps 2-5 epilogue
 constexpr int kBlockKBytes = 128;           // bytes of K per stage and row (one swizzle span)
-constexpr int kStages = 4;
-constexpr int kTileBBytes = kBlockN * kBlockKBytes;         // 16 KiB
-constexpr int kTileABytes = kBlockM * kBlockKBytes;         // 32 KiB
-constexpr int kStageBytes = kTileABytes + kTileBBytes;      // 48 KiB
 constexpr int kMmaKBytes = 32;              // K bytes per tcgen05.mma (16 fp16 / 32 e4m3)
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBoxM = 64;                // m values per TMA store box (128 B of 16-bit C)
 constexpr int kEpiBoxN = 32;                // n rows per box = one warp's TMEM lane quarter
 constexpr int kEpiBufBytes = kEpiBoxN * kEpiBoxM * 2;       // 4 KiB
 constexpr int kEpiBufs = 2;                 // per epilogue warp (ping-pong)
-constexpr uint32_t kAccCols = kBlockM;      // FP32 accumulator columns per buffer
-constexpr uint32_t kTmemCols = 2 * kAccCols;  // double-buffered accumulator = 512 columns
-
-constexpr int kSmemRing = kStages * kStageBytes;
 constexpr int kSmemEpi = kEpiWarps * kEpiBufs * kEpiBufBytes;
-constexpr int kNumBarriers = 2 * kStages + 2 + 2 + 1;
-constexpr int kSmemCtl = kNumBarriers * 8 + 16;
-constexpr int kSmemBytes = 1024 /* alignment slack */ + kSmemRing + kSmemEpi + kSmemCtl;
-static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB shared memory of one CTA");
+constexpr int kTileM = 256;                 // C rows m per tile = MMA N = TMEM columns per accumulator
+constexpr uint32_t kAccCols = kTileM;
+constexpr uint32_t kTmemCols = 2 * kAccCols;  // double-buffered accumulator = all 512 columns
+
+// kGroup = 1: one CTA computes a 128 (n) x 256 (m) tile with M128 MMAs.
+// kGroup = 2: a 2-CTA cluster computes a 256 (n) x 256 (m) tile with M256
+// MMAs issued by the even CTA; each CTA holds 128 rows of each operand tile
+// per stage and the accumulator rows of its own 128 columns n.
+template <int kGroup>
+struct TileCfg {
+    static constexpr int kTileN = 128 * kGroup;            // C columns n per tile = MMA M
+    static constexpr int kRowsB = 128;                      // B rows (columns n) per CTA and stage
+    static constexpr int kRowsA = kTileM / kGroup;          // A rows (m) per CTA and stage
+    static constexpr int kStages = kGroup == 2 ? 6 : 4;
+    static constexpr int kTileBBytes = kRowsB * kBlockKBytes;
+    static constexpr int kTileABytes = kRowsA * kBlockKBytes;
+    static constexpr int kStageBytes = kTileBBytes + kTileABytes;
+    static constexpr int kSmemRing = kStages * kStageBytes;
+    // loaded[S], peer_ready[S], empty[S], accfull[2], accempty[2], drain
+    static constexpr int kNumBarriers = 3 * kStages + 5;
+    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kSmemRing + kSmemEpi + kNumBarriers * 8 + 16;
+    static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB shared memory of one CTA");
+};
 
 constexpr uint32_t kFlagTmaStore = 1u;      // C rows m < m_tma are written with TMA stores
-constexpr uint32_t kFlagInjectStall = 2u;   // test hook: MMA warp waits on a barrier nobody arrives on
+constexpr uint32_t kFlagInjectStall = 2u;   // test hook: MMA thread waits on a barrier nobody arrives on
 
 // Status word of the current device; set (never cleared) by a kernel whose
 // bounded wait ran out: 4 (timeout) | site << 8.
 __device__ int g_tn_status;
 
-enum WaitSite : int { kSiteEmpty = 1, kSiteFull = 2, kSiteAccEmpty = 3, kSiteAccFull = 4, kSiteStall = 5 };
+enum WaitSite : int {
+    kSiteEmpty = 1, kSiteLoaded = 2, kSiteAccEmpty = 3, kSiteAccFull = 4, kSiteStall = 5, kSitePeer = 6,
+    kSiteDrain = 7
+};
 
 struct KernelParams {
-    CUtensorMap tmap_a;      // A: dims {K, M}, box {kBlockKBytes / esz, kBlockM}, 128B swizzle
-    CUtensorMap tmap_b;      // B: dims {K, N}, box {kBlockKBytes / esz, kBlockN}, 128B swizzle
-    CUtensorMap tmap_c;      // C: dims {M, N}, box {kEpiBoxM, kEpiBoxN}, 128B swizzle (TMA-store mode)
+    CUtensorMap tmap_a;      // A: dims {K', M}, box {kBlockKBytes / esz, kRowsA}, 128B swizzle
+    CUtensorMap tmap_b;      // B: dims {K', N}, box {kBlockKBytes / esz, 128}, 128B swizzle
+    CUtensorMap tmap_c;      // C: dims {m_tma, N}, box {kEpiBoxM, kEpiBoxN}, 128B swizzle
     void *c_ptr;             // C base (direct stores)
     int64_t ldc;
     int32_t M, N, K;
@@ -105,13 +117,22 @@ __host__ __device__ __forceinline__ void tile_coord(int64_t id, int64_t tiles_m,
 }
 
 // ------------------------------------------------------------------ waits
-// Every wait is bounded: after `limit` ns the waiting thread raises the
-// CTA's abort flag and the device status word, and returns false; the other
-// roles see the flag and leave their loops.  drain() waits for copies already
-// in flight and ignores the flag (those copies always land).
+// Every wait is bounded: after `limit` ns the waiting thread raises the abort
+// flag of its CTA (and of the peer CTA of a pair) and the device status word,
+// and returns false; the other roles see the flag and leave their loops.
+// drain() waits for copies already in flight and ignores the flag (those
+// copies always land).
 struct Waiter {
     volatile uint32_t *abort_flag;
+    uint32_t peer_abort;     // shared::cluster address of the peer CTA's flag, 0 without a peer
     uint64_t limit;
+
+    __device__ __forceinline__ void raise(int site) const
+    {
+        *abort_flag = 1u;
+        if (peer_abort) ptx::st_shared_cluster_u32(peer_abort, 1u);
+        atomicCAS(&g_tn_status, 0, 4 | (site << 8));
+    }
 
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, int site) const
     {
@@ -121,8 +142,7 @@ struct Waiter {
             if (ptx::mbar_try_wait(bar, parity)) return true;
             if (*abort_flag) return false;
             if (ptx::globaltimer() - t0 > limit) {
-                *abort_flag = 1u;
-                atomicCAS(&g_tn_status, 0, 4 | (site << 8));
+                raise(site);
                 return false;
             }
         }
@@ -133,7 +153,7 @@ struct Waiter {
         const uint64_t t0 = ptx::globaltimer();
         while (!ptx::mbar_try_wait(bar, parity)) {
             if (ptx::globaltimer() - t0 > limit) {
-                atomicCAS(&g_tn_status, 0, 4 | (kSiteFull << 8));
+                atomicCAS(&g_tn_status, 0, 4 | (kSiteDrain << 8));
                 return false;
             }
         }
@@ -145,10 +165,11 @@ struct Waiter {
 struct KindF16 {
     static constexpr bool kF8 = false;
     static constexpr int kElemBytes = 2;
-    static constexpr uint32_t kIdesc = ptx::idesc_f32acc(kBlockN, kBlockM, 0 /*F16*/, 0 /*F16*/);
-    __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc)
+    static constexpr uint32_t kFmt = 0;      // F16 (kind::f16)
+    template <int kGroup>
+    __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
     {
-        ptx::mma_f16(d, a, b, kIdesc, acc);
+        ptx::mma_f16<kGroup>(d, a, b, idesc, acc);
     }
     __device__ static uint32_t pack(float lo, float hi, float) { return ptx::pack_f16x2(lo, hi); }
 };
@@ -156,47 +177,57 @@ struct KindF16 {
 struct KindE4M3 {
     static constexpr bool kF8 = true;
     static constexpr int kElemBytes = 1;
-    static constexpr uint32_t kIdesc = ptx::idesc_f32acc(kBlockN, kBlockM, 0 /*E4M3*/, 0 /*E4M3*/);
-    __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t acc)
+    static constexpr uint32_t kFmt = 0;      // E4M3 (kind::f8f6f4)
+    template <int kGroup>
+    __device__ static void mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
     {
-        ptx::mma_f8(d, a, b, kIdesc, acc);
+        ptx::mma_f8<kGroup>(d, a, b, idesc, acc);
     }
     // acc * (scale_a * scale_b) in FP32, one RNE rounding to bf16.
     __device__ static uint32_t pack(float lo, float hi, float s) { return ptx::pack_bf16x2(lo * s, hi * s); }
 };
 
 // ------------------------------------------------------------------ kernel
-template <class Kind>
+template <class Kind, int kGroup>
 __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_constant__ KernelParams p)
 {
+    using Cfg = TileCfg<kGroup>;
+    constexpr int kStages = Cfg::kStages;
     constexpr int kBlockKElems = kBlockKBytes / Kind::kElemBytes;
+    constexpr uint32_t kIdesc = ptx::idesc_f32acc(Cfg::kTileN, kTileM, Kind::kFmt, Kind::kFmt);
+    constexpr uint16_t kPairMask = 0x3;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_ring = ptx::smem_addr(smem);
-    const uint32_t s_epi = s_ring + kSmemRing;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmemRing + kSmemEpi);
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + kNumBarriers);
+    const uint32_t s_epi = s_ring + Cfg::kSmemRing;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kSmemRing + kSmemEpi);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + Cfg::kNumBarriers);
     volatile uint32_t *abort_flag = tmem_holder + 1;
 
     const uint32_t bar0 = ptx::smem_addr(bars);
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-    auto accfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-    auto accempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    auto loaded_bar = [&](int s) { return bar0 + 8u * s; };                  // own TMA bytes landed
+    auto peer_bar = [&](int s) { return bar0 + 8u * (kStages + s); };         // (even CTA) peer's bytes landed
+    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * kStages + s); };    // MMAs done reading the stage
+    auto accfull_bar = [&](int b) { return bar0 + 8u * (3 * kStages + b); };
+    auto accempty_bar = [&](int b) { return bar0 + 8u * (3 * kStages + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (3 * kStages + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = kGroup == 2 ? ptx::cluster_ctarank() : 0u;
+    const int64_t cluster_id = blockIdx.x / kGroup;
+    const int64_t num_clusters = gridDim.x / kGroup;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(loaded_bar(s), 1);
+            ptx::mbar_init(peer_bar(s), 1);
             ptx::mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accfull_bar(b), 1);
-            ptx::mbar_init(accempty_bar(b), kEpiWarps);
+            ptx::mbar_init(accempty_bar(b), kEpiWarps * kGroup);
         }
         ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0u;
@@ -209,38 +240,43 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         if (p.flags & kFlagTmaStore) ptx::prefetch_tensormap(&p.tmap_c);
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), kTmemCols);
-        ptx::tmem_relinquish_alloc_permit();
+        ptx::tmem_alloc<kGroup>(ptx::smem_addr(tmem_holder), kTmemCols);
+        ptx::tmem_relinquish_alloc_permit<kGroup>();
     }
     ptx::tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (kGroup == 2)
+        ptx::cluster_sync();     // peer barriers initialised before any remote arrive
+    else
+        __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
 
-    const Waiter w{abort_flag, p.wait_limit_ns};
+    const Waiter w{abort_flag,
+                   kGroup == 2 ? ptx::mapa_shared(ptx::smem_addr(const_cast<uint32_t *>(abort_flag)), rank ^ 1u) : 0u,
+                   p.wait_limit_ns};
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer (every CTA)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, issued_parity = 0;   // per stage: a load was issued / its phase parity
             bool ok = true;
-            for (int64_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            for (int64_t tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
                 int64_t tm, tn;
                 tile_coord(tile, p.tiles_m, p.tiles_n, p.group, tm, tn);
-                const int32_t m0 = static_cast<int32_t>(tm * kBlockM);
-                const int32_t n0 = static_cast<int32_t>(tn * kBlockN);
+                const int32_t m0 = static_cast<int32_t>(tm * kTileM + rank * Cfg::kRowsA);
+                const int32_t n0 = static_cast<int32_t>(tn * Cfg::kTileN + rank * Cfg::kRowsB);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!w.wait(empty_bar(stage), phase ^ 1u, kSiteEmpty)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t s_b = s_ring + stage * kStageBytes;
-                    const uint32_t s_a = s_b + kTileBBytes;
-                    ptx::mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
-                    ptx::tma_load_2d(s_b, &p.tmap_b, full_bar(stage), kb * kBlockKElems, n0);
-                    ptx::tma_load_2d(s_a, &p.tmap_a, full_bar(stage), kb * kBlockKElems, m0);
+                    const uint32_t s_b = s_ring + stage * Cfg::kStageBytes;
+                    const uint32_t s_a = s_b + Cfg::kTileBBytes;
+                    ptx::mbar_arrive_expect_tx(loaded_bar(stage), Cfg::kStageBytes);
+                    ptx::tma_load_2d(s_b, &p.tmap_b, loaded_bar(stage), kb * kBlockKElems, n0);
+                    ptx::tma_load_2d(s_a, &p.tmap_a, loaded_bar(stage), kb * kBlockKElems, m0);
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) {
@@ -251,45 +287,47 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             }
             // Let every issued load land before the CTA can exit.
             for (int s = 0; s < kStages; ++s)
-                if (issued & (1u << s)) w.drain(full_bar(s), (issued_parity >> s) & 1u);
+                if (issued & (1u << s)) w.drain(loaded_bar(s), (issued_parity >> s) & 1u);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------ MMA issuer (even CTA)
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued_any = false;
             if (p.flags & kFlagInjectStall) ok = w.wait(drain_bar, 0u, kSiteStall);   // never completes
-            for (int64_t tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+            for (int64_t tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
                 if (!w.wait(accempty_bar(acc), acc_phase ^ 1u, kSiteAccEmpty)) break;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * kAccCols;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!w.wait(full_bar(stage), phase, kSiteFull)) {
+                    if (!w.wait(loaded_bar(stage), phase, kSiteLoaded) ||
+                        (kGroup == 2 && !w.wait(peer_bar(stage), phase, kSitePeer))) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    const uint32_t s_b = s_ring + stage * kStageBytes;
-                    const uint32_t s_a = s_b + kTileBBytes;
+                    const uint32_t s_b = s_ring + stage * Cfg::kStageBytes;
+                    const uint32_t s_a = s_b + Cfg::kTileBBytes;
                     const uint64_t desc_b = ptx::desc_kmajor_sw128(s_b);
                     const uint64_t desc_a = ptx::desc_kmajor_sw128(s_a);
 #pragma unroll
                     for (int j = 0; j < kBlockKBytes / kMmaKBytes; ++j) {
                         // +32 bytes along K inside the 128-byte swizzle span = +2 in the address field
-                        Kind::mma(d_tmem, desc_b + 2u * j, desc_a + 2u * j, (kb | j) != 0 ? 1u : 0u);
+                        Kind::template mma<kGroup>(d_tmem, desc_b + 2u * j, desc_a + 2u * j, kIdesc,
+                                                   (kb | j) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
-                    ptx::mma_commit(empty_bar(stage));   // frees the stage once these MMAs have read it
+                    ptx::mma_commit<kGroup>(empty_bar(stage), kPairMask);   // stage free in both CTAs
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                ptx::mma_commit(accfull_bar(acc));       // accumulator complete
+                ptx::mma_commit<kGroup>(accfull_bar(acc), kPairMask);       // accumulator complete
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -297,19 +335,40 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             }
             // All MMAs this thread issued must finish before TMEM is freed.
             if (issued_any) {
-                ptx::mma_commit(drain_bar);
+                ptx::mma_commit<kGroup>(drain_bar, 0x1);
                 w.drain(drain_bar, 0u);
+            }
+        } else if (kGroup == 2 && lane == 0) {
+            // ------------------------------------------------ relay (odd CTA)
+            // Tells the even CTA's MMA thread, stage by stage, that this CTA's
+            // operand halves have landed (its own TMA signals its own barrier,
+            // so each CTA can wait for its own copies on every path).
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int64_t tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
+                for (int kb = 0; kb < p.num_kb; ++kb) {
+                    if (!w.wait(loaded_bar(stage), phase, kSiteLoaded)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_remote(ptx::mapa_shared(peer_bar(stage), 0u));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
             }
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
+        // ------------------------------------------------ epilogue (warps 2..5, every CTA)
         const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31 are this warp's
         const int ew = warp - 2;
         const bool tma_store = (p.flags & kFlagTmaStore) != 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t chunk_ctr = 0;
-        for (int64_t tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+        for (int64_t tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
             int64_t tm, tn;
             tile_coord(tile, p.tiles_m, p.tiles_n, p.group, tm, tn);
             bool ok = w.wait(accfull_bar(acc), acc_phase, kSiteAccFull);
@@ -317,21 +376,27 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             if (!ok) break;
             __syncwarp();
             ptx::tc_fence_after_sync();
-            const int32_t m0 = static_cast<int32_t>(tm * kBlockM);
-            const int32_t nw = static_cast<int32_t>(tn * kBlockN) + 32 * quarter;   // this warp's first column
+            const int32_t m0 = static_cast<int32_t>(tm * kTileM);
+            // this warp's first output column
+            const int32_t nw = static_cast<int32_t>(tn * Cfg::kTileN + rank * Cfg::kRowsB) + 32 * quarter;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + acc * kAccCols;
 #pragma unroll 1
-            for (int c = 0; c < kBlockM / kEpiBoxM; ++c) {
+            for (int c = 0; c < kTileM / kEpiBoxM; ++c) {
                 uint32_t r0[32], r1[32];
                 ptx::tmem_ld_32x32b_x32(t_row + c * kEpiBoxM, r0);
                 ptx::tmem_ld_32x32b_x32(t_row + c * kEpiBoxM + 32, r1);
                 ptx::tmem_ld_wait(r0);
                 ptx::reg_dependency(r1);
-                if (c == kBlockM / kEpiBoxM - 1) {
-                    // last read of this accumulator: hand it back to the MMA warp
+                if (c == kTileM / kEpiBoxM - 1) {
+                    // last read of this accumulator: hand it back to the MMA thread
                     ptx::tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(accempty_bar(acc));
+                    if (lane == 0) {
+                        if constexpr (kGroup == 2)
+                            ptx::mbar_arrive_remote(ptx::mapa_shared(accempty_bar(acc), 0u));
+                        else
+                            ptx::mbar_arrive(accempty_bar(acc));
+                    }
                 }
                 uint32_t packed[32];
 #pragma unroll
@@ -386,12 +451,16 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         __syncwarp();
     }
 
+    __syncwarp();                // .aligned barriers below need converged warps
     ptx::tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (kGroup == 2)
+        ptx::cluster_sync();     // no CTA leaves while its peer may still touch its shared memory
+    else
+        __syncthreads();
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after_sync();
-        ptx::tmem_dealloc(tmem_base, kTmemCols);
+        ptx::tmem_dealloc<kGroup>(tmem_base, kTmemCols);
     }
 }
 

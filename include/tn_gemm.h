@@ -161,6 +161,18 @@ void gemm_set_wait_limit_ns(uint64_t limit_ns);
  */
 void gemm_debug_inject_stall(int enable);
 
+/*
+ * Test hook: 0 (default) lets the library choose the tile shape per call
+ * (2-CTA 256 x 256 tiles when N > 128, else 1-CTA 128 x 256 tiles); 1 or 2
+ * forces that CTA group for later calls.  Returns 0, or -1 for other values.
+ */
+int gemm_debug_force_cta_group(int group);
+
+/* Description of the last GEMM kernel launch on the calling host thread
+ * (tile shape, grid, co-resident cluster slots), for logs and tests
+ * (thread-local storage; "" before the first launch). */
+const char *gemm_debug_last_launch(void);
+
 /* Tile configuration and build string, e.g. for logs (static storage). */
 const char *gemm_build_info(void);
 

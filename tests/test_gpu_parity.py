@@ -211,3 +211,33 @@ def test_workload_e4m3_8192_sampled():
     c, s, _ = oracle.gemm_f8e4m3_tn_at(w.M, w.N, w.K, A, w.K, B, w.K, sa, sb, mi, ni)
     assert_tol(bf16_values(got[ni, mi]), bf16_values(c), s, F8_TOL, w.name)
     assert not np.isnan(bf16_values(got)).any()
+
+
+# ---------------------------------------------------------------- both tile shapes
+@pytest.fixture
+def force_group():
+    import dense_gemm_tn_gb300 as g
+    yield g.gemm_debug_force_cta_group
+    g.gemm_debug_force_cta_group(0)
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (31, 33, 29), (257, 129, 65), (300, 200, 136), (513, 640, 520),
+                                   (1000, 300, 1000), (64, 600, 64)])
+def test_forced_cta_group_pm1_exact(force_group, cta_group, M, N, K):
+    force_group(cta_group)
+    A = synth.sign_fp16(M * K, 50 + M)
+    B = synth.sign_fp16(N * K, 60 + N)
+    check_f16_full(M, N, K, A, B, exact=True, what=f"group {cta_group} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("M,N,K", [(300, 200, 136), (513, 640, 520), (200, 1030, 4096)])
+def test_forced_cta_group_gaussian(force_group, cta_group, M, N, K):
+    force_group(cta_group)
+    A = synth.gauss_fp16(M * K, 70 + M)
+    B = synth.gauss_fp16(N * K, 80 + N)
+    check_f16_full(M, N, K, A, B, what=f"group {cta_group} {M}x{N}x{K}")
+    A8, sa = synth.gauss_e4m3(M * K, 90 + M)
+    B8, sb = synth.gauss_e4m3(N * K, 91 + N)
+    check_f8_full(M, N, K, A8, B8, sa, sb, what=f"e4m3 group {cta_group} {M}x{N}x{K}")

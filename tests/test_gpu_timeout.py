@@ -12,10 +12,12 @@ from tests.gpu_helpers import check_f16_full, to_dev_u16, GuardedC
 pytestmark = pytest.mark.gpu
 
 
-def test_stalled_wait_reports_timeout_and_context_survives():
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_stalled_wait_reports_timeout_and_context_survives(cta_group):
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     import dense_gemm_tn_gb300 as g
+    g.gemm_debug_force_cta_group(cta_group)
     M, N, K = 256, 256, 256
     A = synth.gauss_fp16(M * K, 1)
     B = synth.gauss_fp16(N * K, 2)
@@ -31,6 +33,7 @@ def test_stalled_wait_reports_timeout_and_context_survives():
     finally:
         g.gemm_debug_inject_stall(False)
         g.gemm_set_wait_limit_ns(0)
+        g.gemm_debug_force_cta_group(0)
     C.host()                                   # canaries intact
     # the status word was cleared and the next call computes correctly
     g.gemm_poll_device_status()
