@@ -168,8 +168,9 @@ def gemm_set_wait_limit_ns(limit_ns: int) -> None:
     _lib.gemm_set_wait_limit_ns(int(limit_ns))
 
 
-def gemm_debug_inject_stall(enable: bool) -> None:
-    _lib.gemm_debug_inject_stall(1 if enable else 0)
+def gemm_debug_inject_stall(mode) -> None:
+    """0 off; 1 stall the MMA thread; 2 / 3 stall the even / odd CTA's producer."""
+    _lib.gemm_debug_inject_stall(int(mode))
 
 
 def gemm_debug_force_cta_group(group: int) -> None:

@@ -127,6 +127,17 @@ gemm_status_t encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *
     return GEMM_OK;
 }
 
+// gemm_debug_inject_stall modes -> kernel flags.
+uint32_t stall_flags(int mode)
+{
+    switch (mode) {
+    case 1: return tn::kFlagStallMma;
+    case 2: return tn::kFlagStallProducer0;
+    case 3: return tn::kFlagStallProducer1;
+    default: return 0u;
+    }
+}
+
 int launch_grid(int64_t work, int cap)
 {
     int64_t g = (work + 255) / 256;
@@ -287,7 +298,7 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     prm.num_kb = static_cast<int32_t>((K * esz + tn::kBlockKBytes - 1) / tn::kBlockKBytes);
     prm.group = kGroupM;
     prm.scale = scale;
-    prm.flags = (tma_c ? tn::kFlagTmaStore : 0u) | (g_inject_stall.load() ? tn::kFlagInjectStall : 0u);
+    prm.flags = (tma_c ? tn::kFlagTmaStore : 0u) | stall_flags(g_inject_stall.load());
     prm.wait_limit_ns = g_wait_limit_ns.load();
 
     return cta_group == 2 ? launch<Kind, 2>(name, prm, *dev, stream) : launch<Kind, 1>(name, prm, *dev, stream);
@@ -364,7 +375,7 @@ int gemm_tile_coord(int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t id,
 
 void gemm_set_wait_limit_ns(uint64_t limit_ns) { g_wait_limit_ns.store(limit_ns ? limit_ns : 2000000000ull); }
 
-void gemm_debug_inject_stall(int enable) { g_inject_stall.store(enable ? 1 : 0); }
+void gemm_debug_inject_stall(int mode) { g_inject_stall.store(mode >= 0 && mode <= 3 ? mode : 1); }
 
 int gemm_debug_force_cta_group(int group)
 {

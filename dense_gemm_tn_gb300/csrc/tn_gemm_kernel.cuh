@@ -39,7 +39,7 @@
 namespace tn {
 
 // ------------------------------------------------------------------ config
-constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA/TMEM (or relay), warps 2-5 epilogue
+constexpr int kThreads = 192;               // warp 0 TMA, warp 1 TMEM + MMA (even CTA), warps 2-5 epilogue
 constexpr int kBlockKBytes = 128;           // bytes of K per stage and row (one swizzle span)
 constexpr int kMmaKBytes = 32;              // K bytes per tcgen05.mma (16 fp16 / 32 e4m3)
 constexpr int kEpiWarps = 4;
@@ -66,22 +66,26 @@ struct TileCfg {
     static constexpr int kTileABytes = kRowsA * kBlockKBytes;
     static constexpr int kStageBytes = kTileBBytes + kTileABytes;
     static constexpr int kSmemRing = kStages * kStageBytes;
-    // loaded[S], peer_ready[S], empty[S], accfull[2], accempty[2], drain
-    static constexpr int kNumBarriers = 3 * kStages + 5;
+    // loaded[S], empty[S], accfull[2], accempty[2], drain, never
+    static constexpr int kNumBarriers = 2 * kStages + 6;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kSmemRing + kSmemEpi + kNumBarriers * 8 + 16;
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB shared memory of one CTA");
 };
 
 constexpr uint32_t kFlagTmaStore = 1u;      // C rows m < m_tma are written with TMA stores
-constexpr uint32_t kFlagInjectStall = 2u;   // test hook: MMA thread waits on a barrier nobody arrives on
+// Test hooks: the named thread first waits on a barrier nobody arrives on, so
+// its bounded wait runs out and the kernel leaves through its abort path.
+constexpr uint32_t kFlagStallMma = 2u;          // the MMA thread
+constexpr uint32_t kFlagStallProducer0 = 4u;    // the producer of the (even) CTA 0 of a pair, or the only CTA
+constexpr uint32_t kFlagStallProducer1 = 8u;    // the producer of the odd CTA of a pair
 
 // Status word of the current device; set (never cleared) by a kernel whose
 // bounded wait ran out: 4 (timeout) | site << 8.
 __device__ int g_tn_status;
 
 enum WaitSite : int {
-    kSiteEmpty = 1, kSiteLoaded = 2, kSiteAccEmpty = 3, kSiteAccFull = 4, kSiteStall = 5, kSitePeer = 6,
-    kSiteDrain = 7
+    kSiteEmpty = 1, kSiteLoaded = 2, kSiteAccEmpty = 3, kSiteAccFull = 4, kSiteStall = 5, kSitePeerDone = 6,
+    kSiteDrain = 7, kSiteReconcile = 8
 };
 
 struct KernelParams {
@@ -187,6 +191,49 @@ struct KindE4M3 {
     __device__ static uint32_t pack(float lo, float hi, float s) { return ptx::pack_bf16x2(lo * s, hi * s); }
 };
 
+// ------------------------------------------------------------------ pair drain
+// Run by CTA 0's producer of a pair once it issues no more loads, so that no
+// load of either CTA is still in flight when the pair leaves.  Loads go round
+// the stages in order, and a stage can only be refilled after its previous
+// fill completed (which needs both halves), so per stage the two producers
+// are at most one fill apart.  Where only one of them issued the last fill,
+// CTA 0 settles the other half's account (cancels its bytes, or adds the
+// arrival and bytes it owed) so the phase can complete on the bytes really in
+// flight, then waits for it.  On the normal path both counts are equal and
+// every wait returns at once.
+template <int kStages, int kStageBytes, class LoadedBar>
+__device__ __forceinline__ void drain_pair_loads(const Waiter &w, LoadedBar loaded_bar, uint32_t n_own,
+                                                 uint32_t count_addr, uint32_t done_addr)
+{
+    const uint32_t peer_done = ptx::mapa_shared(done_addr, 1u);
+    const uint32_t peer_count = ptx::mapa_shared(count_addr, 1u);
+    const uint64_t t0 = ptx::globaltimer();
+    bool peer_stopped = true;
+    while (ptx::ld_acquire_cluster_u32(peer_done) == 0u) {
+        if (ptx::globaltimer() - t0 > w.limit) {
+            atomicCAS(&g_tn_status, 0, 4 | (kSitePeerDone << 8));
+            peer_stopped = false;
+            break;
+        }
+    }
+    const uint32_t n_peer = peer_stopped ? ptx::ld_relaxed_cluster_u32(peer_count) : n_own;
+    for (int s = 0; s < kStages; ++s) {
+        const uint32_t own = n_own / kStages + (static_cast<uint32_t>(s) < n_own % kStages ? 1u : 0u);
+        const uint32_t peer = n_peer / kStages + (static_cast<uint32_t>(s) < n_peer % kStages ? 1u : 0u);
+        const uint32_t last = own > peer ? own : peer;
+        if (last == 0) continue;
+        if (own > peer + 1 || peer > own + 1) {     // cannot happen; never guess
+            atomicCAS(&g_tn_status, 0, 4 | (kSiteReconcile << 8));
+            continue;
+        }
+        if (own > peer)
+            ptx::mbar_complete_tx(loaded_bar(s), kStageBytes);          // the peer's half will not come
+        else if (peer > own)
+            ptx::mbar_arrive_expect_tx(loaded_bar(s), kStageBytes);     // arm for the peer's half alone
+        w.drain(loaded_bar(s), (last - 1) & 1u);
+    }
+}
+
 // ------------------------------------------------------------------ kernel
 template <class Kind, int kGroup>
 __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_constant__ KernelParams p)
@@ -204,14 +251,17 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Cfg::kSmemRing + kSmemEpi);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + Cfg::kNumBarriers);
     volatile uint32_t *abort_flag = tmem_holder + 1;
+    volatile uint32_t *issued_count = tmem_holder + 2;    // k-block loads this CTA's producer issued
+    volatile uint32_t *producer_done = tmem_holder + 3;   // set once this CTA's producer issues no more
 
     const uint32_t bar0 = ptx::smem_addr(bars);
-    auto loaded_bar = [&](int s) { return bar0 + 8u * s; };                  // own TMA bytes landed
-    auto peer_bar = [&](int s) { return bar0 + 8u * (kStages + s); };         // (even CTA) peer's bytes landed
-    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * kStages + s); };    // MMAs done reading the stage
-    auto accfull_bar = [&](int b) { return bar0 + 8u * (3 * kStages + b); };
-    auto accempty_bar = [&](int b) { return bar0 + 8u * (3 * kStages + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (3 * kStages + 4);
+    // loaded[s]: the stage's bytes (of both CTAs of a pair) have landed; used in CTA 0 only
+    auto loaded_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };        // MMAs done reading the stage
+    auto accfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+    auto accempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+    const uint32_t never_bar = bar0 + 8u * (2 * kStages + 5);                 // nothing ever arrives
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -222,7 +272,6 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(loaded_bar(s), 1);
-            ptx::mbar_init(peer_bar(s), 1);
             ptx::mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -230,7 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             ptx::mbar_init(accempty_bar(b), kEpiWarps * kGroup);
         }
         ptx::mbar_init(drain_bar, 1);
+        ptx::mbar_init(never_bar, 1);
         *abort_flag = 0u;
+        *issued_count = 0u;
+        *producer_done = 0u;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
     }
@@ -257,11 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (every CTA)
+        // 1-CTA: loads complete on the CTA's own loaded[s].  2-CTA: both CTAs'
+        // loads complete on CTA 0's loaded[s], which CTA 0's producer arms with
+        // the bytes of both halves; the MMA thread waits on that one barrier.
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued = 0, issued_parity = 0;   // per stage: a load was issued / its phase parity
+            uint32_t n_issued = 0;
             bool ok = true;
+            const uint32_t stall = rank == 0 ? kFlagStallProducer0 : kFlagStallProducer1;
+            if (p.flags & stall) ok = w.wait(never_bar, 0u, kSiteStall);
             for (int64_t tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
                 int64_t tm, tn;
                 tile_coord(tile, p.tiles_m, p.tiles_n, p.group, tm, tn);
@@ -274,20 +331,38 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     }
                     const uint32_t s_b = s_ring + stage * Cfg::kStageBytes;
                     const uint32_t s_a = s_b + Cfg::kTileBBytes;
-                    ptx::mbar_arrive_expect_tx(loaded_bar(stage), Cfg::kStageBytes);
-                    ptx::tma_load_2d(s_b, &p.tmap_b, loaded_bar(stage), kb * kBlockKElems, n0);
-                    ptx::tma_load_2d(s_a, &p.tmap_a, loaded_bar(stage), kb * kBlockKElems, m0);
-                    issued |= 1u << stage;
-                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if constexpr (kGroup == 2) {
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(loaded_bar(stage), 2 * Cfg::kStageBytes);
+                        const uint32_t lb = ptx::mapa_shared(loaded_bar(stage), 0u);
+                        ptx::tma_load_2d_pair(s_b, &p.tmap_b, lb, kb * kBlockKElems, n0);
+                        ptx::tma_load_2d_pair(s_a, &p.tmap_a, lb, kb * kBlockKElems, m0);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(loaded_bar(stage), Cfg::kStageBytes);
+                        ptx::tma_load_2d(s_b, &p.tmap_b, loaded_bar(stage), kb * kBlockKElems, n0);
+                        ptx::tma_load_2d(s_a, &p.tmap_a, loaded_bar(stage), kb * kBlockKElems, m0);
+                    }
+                    *issued_count = ++n_issued;
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            // Let every issued load land before the CTA can exit.
-            for (int s = 0; s < kStages; ++s)
-                if (issued & (1u << s)) w.drain(loaded_bar(s), (issued_parity >> s) & 1u);
+            if constexpr (kGroup == 2) {
+                if (rank == 1) {
+                    // publish the final count (release: the count store is ordered before it)
+                    ptx::st_release_cluster_u32(ptx::mapa_shared(ptx::smem_addr(const_cast<uint32_t *>(producer_done)), 1u), 1u);
+                } else {
+                    drain_pair_loads<kStages, Cfg::kStageBytes>(w, loaded_bar, n_issued, ptx::smem_addr(const_cast<uint32_t *>(issued_count)),
+                                     ptx::smem_addr(const_cast<uint32_t *>(producer_done)));
+                }
+            } else {
+                // Let every issued load land before the CTA can exit.
+                for (int s = 0; s < kStages; ++s) {
+                    const uint32_t passes = n_issued / kStages + (static_cast<uint32_t>(s) < n_issued % kStages ? 1u : 0u);
+                    if (passes) w.drain(loaded_bar(s), (passes - 1) & 1u);
+                }
+            }
         }
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
@@ -297,14 +372,13 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued_any = false;
-            if (p.flags & kFlagInjectStall) ok = w.wait(drain_bar, 0u, kSiteStall);   // never completes
+            if (p.flags & kFlagStallMma) ok = w.wait(never_bar, 0u, kSiteStall);
             for (int64_t tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
                 if (!w.wait(accempty_bar(acc), acc_phase ^ 1u, kSiteAccEmpty)) break;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * kAccCols;
                 for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!w.wait(loaded_bar(stage), phase, kSiteLoaded) ||
-                        (kGroup == 2 && !w.wait(peer_bar(stage), phase, kSitePeer))) {
+                    if (!w.wait(loaded_bar(stage), phase, kSiteLoaded)) {
                         ok = false;
                         break;
                     }
@@ -337,27 +411,6 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             if (issued_any) {
                 ptx::mma_commit<kGroup>(drain_bar, 0x1);
                 w.drain(drain_bar, 0u);
-            }
-        } else if (kGroup == 2 && lane == 0) {
-            // ------------------------------------------------ relay (odd CTA)
-            // Tells the even CTA's MMA thread, stage by stage, that this CTA's
-            // operand halves have landed (its own TMA signals its own barrier,
-            // so each CTA can wait for its own copies on every path).
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int64_t tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
-                for (int kb = 0; kb < p.num_kb; ++kb) {
-                    if (!w.wait(loaded_bar(stage), phase, kSiteLoaded)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::mbar_arrive_remote(ptx::mapa_shared(peer_bar(stage), 0u));
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
             }
         }
     } else {

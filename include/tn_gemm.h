@@ -155,11 +155,15 @@ int gemm_tile_coord(int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t id,
 void gemm_set_wait_limit_ns(uint64_t limit_ns);
 
 /*
- * Test hook: while `enable` is non-zero, launched GEMM kernels make their MMA
- * warp wait first on a barrier nothing arrives on, so the bounded wait runs
- * out and the kernel exits through its timeout path (no fault, no hang).
+ * Test hook: while `mode` is non-zero, launched GEMM kernels make one thread
+ * wait first on a barrier nothing arrives on, so its bounded wait runs out and
+ * the kernel leaves through its timeout path (no fault, no hang):
+ *   1  the MMA-issuing thread;
+ *   2  the TMA producer of the even CTA of each pair (or of each CTA);
+ *   3  the TMA producer of the odd CTA of each pair.
+ * 0 turns the hook off.
  */
-void gemm_debug_inject_stall(int enable);
+void gemm_debug_inject_stall(int mode);
 
 /*
  * Test hook: 0 (default) lets the library choose the tile shape per call
