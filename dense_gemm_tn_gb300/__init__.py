@@ -126,7 +126,10 @@ def _stream(stream) -> int | None:
 
 def _check(status: int) -> int:
     if status != GEMM_OK:
-        raise GemmError(status, last_error())
+        detail = last_error()
+        if status == GEMM_ERR_CUDA and last_launch():
+            detail += f" (last launch: {last_launch()})"
+        raise GemmError(status, detail)
     return status
 
 

@@ -34,8 +34,9 @@ gemm_status_t fail(gemm_status_t s, const char *fmt, ...)
 struct DeviceState {
     bool ready = false;
     int sms = 0, major = 0, minor = 0;
-    bool smem_attr[2][3] = {};        // [kind: f16, e4m3][cta group]
-    int max_clusters[2][3] = {};      // co-resident clusters of the kernel (0 = not queried yet)
+    // per kernel, indexed [kind: f16, e4m3][CTAs per cluster: 1, 2 or 4]
+    bool smem_attr[2][5] = {};
+    int max_clusters[2][5] = {};      // co-resident clusters (0 = not queried yet)
     void *workspace = nullptr;
     size_t workspace_bytes = 0;
 };
@@ -138,6 +139,19 @@ uint32_t stall_flags(int mode)
     }
 }
 
+// Launches repack_rows_kernel: ld_dst is a multiple of 16 bytes.
+template <typename T>
+void launch_repack(const T *src, int64_t ld_src, T *dst, int64_t ld_dst, int64_t rows, int64_t K,
+                   cudaStream_t stream)
+{
+    constexpr int64_t kVec = 16 / sizeof(T);
+    const int64_t chunks = ld_dst / kVec;
+    const int64_t rows_y = rows < 65535 ? rows : 65535;
+    const dim3 grid(static_cast<unsigned>((chunks + 127) / 128), static_cast<unsigned>(rows_y),
+                    static_cast<unsigned>((rows + rows_y - 1) / rows_y));
+    tn::repack_rows_kernel<T><<<grid, 128, 0, stream>>>(src, ld_src, dst, ld_dst, rows, K);
+}
+
 int launch_grid(int64_t work, int cap)
 {
     int64_t g = (work + 255) / 256;
@@ -147,16 +161,18 @@ int launch_grid(int64_t work, int cap)
 
 // Launches the persistent kernel: one CTA (or one 2-CTA cluster) per
 // co-resident slot, each walking the tile raster with a stride of the grid.
-template <class Kind, int G>
-gemm_status_t launch(const char *name, const tn::KernelParams &prm, DeviceState &dev, cudaStream_t stream)
+template <class Kind, int G, int P>
+gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, cudaStream_t stream)
 {
-    using Cfg = tn::TileCfg<G>;
-    auto kernel = tn::tn_gemm_kernel<Kind, G>;
+    using Cfg = tn::TileCfg<G, P>;
+    constexpr int kCtas = G * P;
+    static_assert(kCtas == 1 || kCtas == 2 || kCtas == 4, "cluster shape outside the per-device caches");
+    auto kernel = tn::tn_gemm_kernel<Kind, G, P>;
     const int ki = Kind::kF8 ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = G;
+    attr[0].val.clusterDim.x = kCtas;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(tn::kThreads, 1, 1);
@@ -167,28 +183,39 @@ gemm_status_t launch(const char *name, const tn::KernelParams &prm, DeviceState 
     int slots;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
-        if (!dev.smem_attr[ki][G]) {
+        if (!dev.smem_attr[ki][kCtas]) {
             cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
             if (e != cudaSuccess)
                 return fail(GEMM_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", name, cudaGetErrorString(e));
-            dev.smem_attr[ki][G] = true;
+            dev.smem_attr[ki][kCtas] = true;
         }
-        if (dev.max_clusters[ki][G] == 0) {
+        if (dev.max_clusters[ki][kCtas] == 0) {
             int n = 0;
-            cfg.gridDim = dim3(G * (dev.sms / G), 1, 1);
+            cfg.gridDim = dim3(kCtas * (dev.sms / kCtas), 1, 1);
             cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
             if (e != cudaSuccess || n <= 0) {
                 cudaGetLastError();
-                n = dev.sms / G;     // fall back to one slot per SM (pair)
+                n = dev.sms / kCtas;     // fall back to one slot per group of SMs
             }
-            dev.max_clusters[ki][G] = n;
+            dev.max_clusters[ki][kCtas] = n;
         }
-        slots = dev.max_clusters[ki][G];
+        slots = dev.max_clusters[ki][kCtas];
     }
     const int clusters = prm.num_tiles < slots ? prm.num_tiles : slots;
-    cfg.gridDim = dim3(G * clusters, 1, 1);
-    snprintf(t_last_launch, sizeof(t_last_launch), "%s: cta_group=%d grid=%d clusters=%d slots=%d tiles=%d",
-             name, G, G * clusters, clusters, slots, prm.num_tiles);
+    cfg.gridDim = dim3(kCtas * clusters, 1, 1);
+    // A last wave that fills at most half of the clusters is run as twice as
+    // many half-width units, so every cluster finishes at about the same time.
+    const int waves = prm.num_tiles / clusters, rem = prm.num_tiles % clusters;
+    if (waves >= 1 && rem > 0 && 2 * rem <= clusters) {
+        prm.tail_start = waves * clusters;
+        prm.num_units = prm.tail_start + 2 * rem;
+    } else {
+        prm.tail_start = prm.num_tiles;
+        prm.num_units = prm.num_tiles;
+    }
+    snprintf(t_last_launch, sizeof(t_last_launch),
+             "%s: ctas_per_cluster=%d grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d", name, kCtas,
+             kCtas * clusters, clusters, slots, prm.num_tiles, prm.num_units, prm.tail_start);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));
     return GEMM_OK;
@@ -216,14 +243,6 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         if (reinterpret_cast<uintptr_t>(A) % esz || reinterpret_cast<uintptr_t>(B) % esz)
             return fail(GEMM_ERR_INVALID_ARG, "%s: A or B is not aligned to its element size", name);
     }
-    // 2-CTA pairs (256 x 256 tiles) unless the problem has at most one
-    // 128-column slab of n, where the pair's second half would be idle.
-    int cta_group = N > 128 ? 2 : 1;
-    if (const int forced = g_force_cta_group.load()) cta_group = forced;
-    const int64_t tiles_m = (M + tn::kTileM - 1) / tn::kTileM;
-    const int64_t tiles_n = (N + 128 * cta_group - 1) / (128 * cta_group);
-    if (tiles_m * tiles_n > INT32_MAX) return fail(GEMM_ERR_UNSUPPORTED, "%s: too many output tiles", name);
-
     DeviceState *dev = nullptr;
     gemm_status_t st = device_state(&dev, nullptr);
     if (st != GEMM_OK) return st;
@@ -235,6 +254,30 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: zero fill launch: %s", name, cudaGetErrorString(e));
         return GEMM_OK;
     }
+
+    // Cluster shape.  One CTA per 128 x 256 tile when N <= 128 (a pair's
+    // second half would idle); else a CTA pair per 256 x 256 tile.  Two pairs
+    // sharing their B rows by multicast (4 CTAs, 512 x 256 units) cut the
+    // operand bytes per SM by a quarter but fit on fewer SMs (144 of a
+    // GB300's 152); measured, they win only when the pair grid's last wave is
+    // a partial wave too full to split into half units, and there are enough
+    // 4-CTA units to fill the GPU.
+    const int64_t m_tiles = (M + tn::kTileM - 1) / tn::kTileM;
+    int ctas = N > 128 ? 2 : 1;
+    if (ctas == 2 && m_tiles >= 2) {
+        const int64_t pair_tiles = m_tiles * ((N + 255) / 256);
+        const int64_t pair_slots = dev->sms / 2;
+        const int64_t rem = pair_tiles % pair_slots;
+        const int64_t quad_units = ((m_tiles + 1) / 2) * ((N + 255) / 256);
+        if (pair_tiles > pair_slots && 2 * rem > pair_slots && quad_units >= dev->sms / 4) ctas = 4;
+    }
+    if (const int forced = g_force_cta_group.load()) ctas = forced;
+    const int cta_group = ctas >= 2 ? 2 : 1;
+    const int pairs = ctas == 4 ? 2 : 1;
+    const int64_t tiles_m = (m_tiles + pairs - 1) / pairs;
+    const int64_t tiles_n = (N + 128 * cta_group - 1) / (128 * cta_group);
+    if (tiles_m * tiles_n > INT32_MAX) return fail(GEMM_ERR_UNSUPPORTED, "%s: too many output tiles", name);
+
 
     // The TMA reads an operand in place only when its base, its row stride and
     // its row length K are all multiples of 16 bytes (a row that ends inside a
@@ -254,14 +297,12 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         uint8_t *ws = static_cast<uint8_t *>(dev->workspace);
         using T = typename std::conditional<esz == 2, uint16_t, uint8_t>::type;
         if (repack_a) {
-            tn::repack_rows_kernel<T><<<launch_grid(M * ldp, dev->sms * 8), 256, 0, stream>>>(
-                static_cast<const T *>(A), lda, reinterpret_cast<T *>(ws), ldp, M, K);
+            launch_repack<T>(static_cast<const T *>(A), lda, reinterpret_cast<T *>(ws), ldp, M, K, stream);
             a_use = ws;
             lda_use = ka = ldp;
         }
         if (repack_b) {
-            tn::repack_rows_kernel<T><<<launch_grid(N * ldp, dev->sms * 8), 256, 0, stream>>>(
-                static_cast<const T *>(B), ldb, reinterpret_cast<T *>(ws + bytes_a), ldp, N, K);
+            launch_repack<T>(static_cast<const T *>(B), ldb, reinterpret_cast<T *>(ws + bytes_a), ldp, N, K, stream);
             b_use = ws + bytes_a;
             ldb_use = kb = ldp;
         }
@@ -277,7 +318,10 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     const uint32_t rows_a = static_cast<uint32_t>(tn::kTileM / cta_group);
     if ((st = encode_2d(&prm.tmap_a, in_type, a_use, ka, M, lda_use * esz, box_k, rows_a, "A")) != GEMM_OK)
         return st;
-    if ((st = encode_2d(&prm.tmap_b, in_type, b_use, kb, N, ldb_use * esz, box_k, 128, "B")) != GEMM_OK)
+    if ((st = encode_2d(&prm.tmap_a_half, in_type, a_use, ka, M, lda_use * esz, box_k, rows_a / 2, "A half")) !=
+        GEMM_OK)
+        return st;
+    if ((st = encode_2d(&prm.tmap_b, in_type, b_use, kb, N, ldb_use * esz, box_k, 128 / pairs, "B")) != GEMM_OK)
         return st;
     // TMA stores cover rows m < M rounded down to 8 (16 bytes); the kernel
     // writes the ragged rest, or all of C when C's base or stride is unaligned.
@@ -296,12 +340,14 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     prm.tiles_n = static_cast<int32_t>(tiles_n);
     prm.num_tiles = static_cast<int32_t>(tiles_m * tiles_n);
     prm.num_kb = static_cast<int32_t>((K * esz + tn::kBlockKBytes - 1) / tn::kBlockKBytes);
-    prm.group = kGroupM;
+    prm.group = kGroupM / pairs;    // the same m extent per raster group for every cluster shape
     prm.scale = scale;
     prm.flags = (tma_c ? tn::kFlagTmaStore : 0u) | stall_flags(g_inject_stall.load());
     prm.wait_limit_ns = g_wait_limit_ns.load();
 
-    return cta_group == 2 ? launch<Kind, 2>(name, prm, *dev, stream) : launch<Kind, 1>(name, prm, *dev, stream);
+    if (ctas == 4) return launch<Kind, 2, 2>(name, prm, *dev, stream);
+    if (ctas == 2) return launch<Kind, 2, 1>(name, prm, *dev, stream);
+    return launch<Kind, 1, 1>(name, prm, *dev, stream);
 }
 
 }  // namespace
@@ -379,7 +425,7 @@ void gemm_debug_inject_stall(int mode) { g_inject_stall.store(mode >= 0 && mode 
 
 int gemm_debug_force_cta_group(int group)
 {
-    if (group < 0 || group > 2) return -1;
+    if (group != 0 && group != 1 && group != 2 && group != 4) return -1;
     g_force_cta_group.store(group);
     return 0;
 }
@@ -388,10 +434,10 @@ const char *gemm_debug_last_launch(void) { return t_last_launch; }
 
 const char *gemm_build_info(void)
 {
-    static char info[320];
+    static char info[384];
     snprintf(info, sizeof(info),
-             "dense_gemm_tn sm_103a: 2-CTA tile 256x256 (%d stages, %d B smem), 1-CTA tile 128x256 (%d stages, "
-             "%d B smem); K block %d B; TMEM %u cols; raster group %d",
+             "dense_gemm_tn sm_103a: 2x2-CTA cluster 512x256 with B multicast, 2-CTA tile 256x256 (%d stages, "
+             "%d B smem), 1-CTA tile 128x256 (%d stages, %d B smem); K block %d B; TMEM %u cols; raster group %d",
              tn::TileCfg<2>::kStages, tn::TileCfg<2>::kSmemBytes, tn::TileCfg<1>::kStages,
              tn::TileCfg<1>::kSmemBytes, tn::kBlockKBytes, tn::kTmemCols, kGroupM);
     return info;
@@ -475,14 +521,13 @@ extern "C" gemm_status_t gemm_f16_tn_noalloc(int64_t M, int64_t N, int64_t K, co
     const void *a_use = A, *b_use = B;
     int64_t lda_use = lda, ldb_use = ldb;
     if (repack_a) {
-        tn::repack_rows_kernel<uint16_t><<<launch_grid(M * ldp, dev->sms * 8), 256, 0, s>>>(
-            static_cast<const uint16_t *>(A), lda, reinterpret_cast<uint16_t *>(ws), ldp, M, K);
+        launch_repack<uint16_t>(static_cast<const uint16_t *>(A), lda, reinterpret_cast<uint16_t *>(ws), ldp, M, K, s);
         a_use = ws;
         lda_use = ldp;
     }
     if (repack_b) {
-        tn::repack_rows_kernel<uint16_t><<<launch_grid(N * ldp, dev->sms * 8), 256, 0, s>>>(
-            static_cast<const uint16_t *>(B), ldb, reinterpret_cast<uint16_t *>(ws + bytes_a), ldp, N, K);
+        launch_repack<uint16_t>(static_cast<const uint16_t *>(B), ldb, reinterpret_cast<uint16_t *>(ws + bytes_a), ldp,
+                                N, K, s);
         b_use = ws + bytes_a;
         ldb_use = ldp;
     }

@@ -53,13 +53,21 @@ constexpr uint32_t kAccCols = kTileM;
 constexpr uint32_t kTmemCols = 2 * kAccCols;  // double-buffered accumulator = all 512 columns
 
 // kGroup = 1: one CTA computes a 128 (n) x 256 (m) tile with M128 MMAs.
-// kGroup = 2: a 2-CTA cluster computes a 256 (n) x 256 (m) tile with M256
-// MMAs issued by the even CTA; each CTA holds 128 rows of each operand tile
+// kGroup = 2: a CTA pair computes a 256 (n) x 256 (m) tile with M256 MMAs
+// issued by the pair's even CTA; each CTA holds 128 rows of each operand tile
 // per stage and the accumulator rows of its own 128 columns n.
-template <int kGroup>
+// kPairs = 2 (with kGroup = 2): a 4-CTA cluster of two pairs working on
+// neighbouring m tiles of the same n tile.  Both pairs need the same B rows,
+// so each CTA loads half of its 128 B rows and multicasts them to its
+// counterpart in the other pair: 24 instead of 32 KiB leave L2 per CTA and
+// stage.
+template <int kGroup, int kPairs = 1>
 struct TileCfg {
-    static constexpr int kTileN = 128 * kGroup;            // C columns n per tile = MMA M
+    static_assert(kGroup == 1 ? kPairs == 1 : (kPairs == 1 || kPairs == 2), "unsupported cluster shape");
+    static constexpr int kCtas = kGroup * kPairs;           // CTAs per cluster
+    static constexpr int kTileN = 128 * kGroup;            // C columns n per pair tile = MMA M
     static constexpr int kRowsB = 128;                      // B rows (columns n) per CTA and stage
+    static constexpr int kSliceB = kRowsB / kPairs;         // B rows each CTA loads (and multicasts)
     static constexpr int kRowsA = kTileM / kGroup;          // A rows (m) per CTA and stage
     static constexpr int kStages = kGroup == 2 ? 6 : 4;
     static constexpr int kTileBBytes = kRowsB * kBlockKBytes;
@@ -75,9 +83,9 @@ struct TileCfg {
 constexpr uint32_t kFlagTmaStore = 1u;      // C rows m < m_tma are written with TMA stores
 // Test hooks: the named thread first waits on a barrier nobody arrives on, so
 // its bounded wait runs out and the kernel leaves through its abort path.
-constexpr uint32_t kFlagStallMma = 2u;          // the MMA thread
-constexpr uint32_t kFlagStallProducer0 = 4u;    // the producer of the (even) CTA 0 of a pair, or the only CTA
-constexpr uint32_t kFlagStallProducer1 = 8u;    // the producer of the odd CTA of a pair
+constexpr uint32_t kFlagStallMma = 2u;          // the MMA thread(s)
+constexpr uint32_t kFlagStallProducer0 = 4u;    // the producer of cluster CTA 0 (or of the only CTA)
+constexpr uint32_t kFlagStallProducer1 = 8u;    // the producer of cluster CTA 1 (the odd CTA of the first pair)
 
 // Status word of the current device; set (never cleared) by a kernel whose
 // bounded wait ran out: 4 (timeout) | site << 8.
@@ -90,13 +98,20 @@ enum WaitSite : int {
 
 struct KernelParams {
     CUtensorMap tmap_a;      // A: dims {K', M}, box {kBlockKBytes / esz, kRowsA}, 128B swizzle
-    CUtensorMap tmap_b;      // B: dims {K', N}, box {kBlockKBytes / esz, 128}, 128B swizzle
+    CUtensorMap tmap_b;      // B: dims {K', N}, box {kBlockKBytes / esz, kSliceB}, 128B swizzle
     CUtensorMap tmap_c;      // C: dims {m_tma, N}, box {kEpiBoxM, kEpiBoxN}, 128B swizzle
+    CUtensorMap tmap_a_half; // A with box {kBlockKBytes / esz, kRowsA / 2} (half units)
     void *c_ptr;             // C base (direct stores)
     int64_t ldc;
     int32_t M, N, K;
     int32_t m_tma;           // rows m < m_tma are written by TMA stores (a multiple of 8, or 0)
+    // Unit grid: tiles_m rows of kPairs m tiles each, tiles_n columns of one
+    // pair tile; num_tiles = tiles_m * tiles_n.
     int32_t tiles_m, tiles_n, num_tiles, num_kb, group;
+    // Work units: tiles [0, tail_start) are whole units; each later tile is two
+    // units covering one half of its m range (so a last, partly filled wave of
+    // tiles becomes a full wave of half-length units).  num_units counts both.
+    int32_t tail_start, num_units;
     float scale;             // epilogue multiplier (F8: scale_a * scale_b)
     uint32_t flags;
     uint64_t wait_limit_ns;
@@ -120,21 +135,35 @@ __host__ __device__ __forceinline__ void tile_coord(int64_t id, int64_t tiles_m,
     tn = in_group / rows;
 }
 
+// Unit u -> its tile and which half of the tile's m range it covers (-1: all).
+struct Unit {
+    int64_t tile;
+    int32_t half;
+};
+
+__device__ __forceinline__ Unit unit_of(int64_t u, const KernelParams &p)
+{
+    if (u < p.tail_start) return {u, -1};
+    const int64_t v = u - p.tail_start;
+    return {p.tail_start + v / 2, static_cast<int32_t>(v & 1)};
+}
+
 // ------------------------------------------------------------------ waits
 // Every wait is bounded: after `limit` ns the waiting thread raises the abort
-// flag of its CTA (and of the peer CTA of a pair) and the device status word,
-// and returns false; the other roles see the flag and leave their loops.
-// drain() waits for copies already in flight and ignores the flag (those
-// copies always land).
+// flag of every CTA of its cluster and the device status word, and returns
+// false; the other roles see the flag and leave their loops.  drain() waits
+// for copies already in flight and ignores the flag (those copies land).
 struct Waiter {
     volatile uint32_t *abort_flag;
-    uint32_t peer_abort;     // shared::cluster address of the peer CTA's flag, 0 without a peer
+    uint32_t abort_addr;     // shared::cta address of the flag (the same offset in every CTA)
+    uint32_t rank, ctas;     // this CTA's rank in its cluster, CTAs in the cluster
     uint64_t limit;
 
     __device__ __forceinline__ void raise(int site) const
     {
         *abort_flag = 1u;
-        if (peer_abort) ptx::st_shared_cluster_u32(peer_abort, 1u);
+        for (uint32_t q = 0; q < ctas; ++q)
+            if (q != rank) ptx::st_shared_cluster_u32(ptx::mapa_shared(abort_addr, q), 1u);
         atomicCAS(&g_tn_status, 0, 4 | (site << 8));
     }
 
@@ -191,58 +220,79 @@ struct KindE4M3 {
     __device__ static uint32_t pack(float lo, float hi, float s) { return ptx::pack_bf16x2(lo * s, hi * s); }
 };
 
-// ------------------------------------------------------------------ pair drain
-// Run by CTA 0's producer of a pair once it issues no more loads, so that no
-// load of either CTA is still in flight when the pair leaves.  Loads go round
-// the stages in order, and a stage can only be refilled after its previous
-// fill completed (which needs both halves), so per stage the two producers
-// are at most one fill apart.  Where only one of them issued the last fill,
-// CTA 0 settles the other half's account (cancels its bytes, or adds the
-// arrival and bytes it owed) so the phase can complete on the bytes really in
-// flight, then waits for it.  On the normal path both counts are equal and
-// every wait returns at once.
-template <int kStages, int kStageBytes, class LoadedBar>
-__device__ __forceinline__ void drain_pair_loads(const Waiter &w, LoadedBar loaded_bar, uint32_t n_own,
-                                                 uint32_t count_addr, uint32_t done_addr)
+// ------------------------------------------------------------------ cluster drain
+// Run by the even CTA of each pair once its own producer issues no more, so
+// that no load feeding its loaded[] barriers is still in flight when the
+// cluster leaves.  Loads go round the stages in order, and a stage can only
+// be refilled after every pair finished reading its previous fill (which
+// needed all of that fill's bytes), so per stage the producers of the cluster
+// are at most one fill apart.  For the last fill of each stage this CTA adds
+// up the bytes really sent to it by the producers that issued that fill; if
+// it armed the fill itself it cancels the bytes that will not come
+// (mbarrier.complete_tx), otherwise it arms the fill for the bytes that will
+// (arrive.expect_tx).  Then it waits for the phase.  On the normal path every
+// producer issued every fill and each wait returns at once.
+template <int kStages, int kCtas, class LoadedBar, class Contribution>
+__device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar loaded_bar, Contribution contribution,
+                                                    uint32_t n_own, uint32_t count_addr, uint32_t done_addr)
 {
-    const uint32_t peer_done = ptx::mapa_shared(done_addr, 1u);
-    const uint32_t peer_count = ptx::mapa_shared(count_addr, 1u);
+    uint32_t counts[kCtas];
     const uint64_t t0 = ptx::globaltimer();
-    bool peer_stopped = true;
-    while (ptx::ld_acquire_cluster_u32(peer_done) == 0u) {
-        if (ptx::globaltimer() - t0 > w.limit) {
-            atomicCAS(&g_tn_status, 0, 4 | (kSitePeerDone << 8));
-            peer_stopped = false;
-            break;
+    for (uint32_t q = 0; q < kCtas; ++q) {
+        if (q == w.rank) {
+            counts[q] = n_own;
+            continue;
         }
+        bool stopped = true;
+        while (ptx::ld_acquire_cluster_u32(ptx::mapa_shared(done_addr, q)) == 0u) {
+            if (ptx::globaltimer() - t0 > w.limit) {
+                atomicCAS(&g_tn_status, 0, 4 | (kSitePeerDone << 8));
+                stopped = false;
+                break;
+            }
+        }
+        counts[q] = stopped ? ptx::ld_relaxed_cluster_u32(ptx::mapa_shared(count_addr, q)) : n_own;
     }
-    const uint32_t n_peer = peer_stopped ? ptx::ld_relaxed_cluster_u32(peer_count) : n_own;
     for (int s = 0; s < kStages; ++s) {
-        const uint32_t own = n_own / kStages + (static_cast<uint32_t>(s) < n_own % kStages ? 1u : 0u);
-        const uint32_t peer = n_peer / kStages + (static_cast<uint32_t>(s) < n_peer % kStages ? 1u : 0u);
-        const uint32_t last = own > peer ? own : peer;
-        if (last == 0) continue;
-        if (own > peer + 1 || peer > own + 1) {     // cannot happen; never guess
+        uint32_t lo = 0xffffffffu, hi = 0;
+        uint32_t passes[kCtas];
+        for (uint32_t q = 0; q < kCtas; ++q) {
+            passes[q] = counts[q] / kStages + (static_cast<uint32_t>(s) < counts[q] % kStages ? 1u : 0u);
+            lo = passes[q] < lo ? passes[q] : lo;
+            hi = passes[q] > hi ? passes[q] : hi;
+        }
+        if (hi == 0) continue;
+        if (hi > lo + 1) {      // cannot happen; never guess
             atomicCAS(&g_tn_status, 0, 4 | (kSiteReconcile << 8));
             continue;
         }
-        if (own > peer)
-            ptx::mbar_complete_tx(loaded_bar(s), kStageBytes);          // the peer's half will not come
-        else if (peer > own)
-            ptx::mbar_arrive_expect_tx(loaded_bar(s), kStageBytes);     // arm for the peer's half alone
-        w.drain(loaded_bar(s), (last - 1) & 1u);
+        const uint32_t fill = (hi - 1) * kStages + s;   // index of the stage's last fill
+        uint32_t sent = 0, total = 0;
+        for (uint32_t q = 0; q < kCtas; ++q) {
+            const uint32_t c = contribution(q, fill);
+            total += c;
+            if (passes[q] == hi) sent += c;
+        }
+        if (passes[w.rank] == hi) {
+            if (total > sent) ptx::mbar_complete_tx(loaded_bar(s), total - sent);
+        } else {
+            ptx::mbar_arrive_expect_tx(loaded_bar(s), sent);
+        }
+        w.drain(loaded_bar(s), (hi - 1) & 1u);
     }
 }
 
 // ------------------------------------------------------------------ kernel
-template <class Kind, int kGroup>
+template <class Kind, int kGroup, int kPairs>
 __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_constant__ KernelParams p)
 {
-    using Cfg = TileCfg<kGroup>;
+    using Cfg = TileCfg<kGroup, kPairs>;
     constexpr int kStages = Cfg::kStages;
+    constexpr int kCtas = Cfg::kCtas;
     constexpr int kBlockKElems = kBlockKBytes / Kind::kElemBytes;
     constexpr uint32_t kIdesc = ptx::idesc_f32acc(Cfg::kTileN, kTileM, Kind::kFmt, Kind::kFmt);
-    constexpr uint16_t kPairMask = 0x3;
+    constexpr uint32_t kIdescHalf = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 2, Kind::kFmt, Kind::kFmt);
+    constexpr uint16_t kAllMask = static_cast<uint16_t>((1u << kCtas) - 1u);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -253,11 +303,14 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     volatile uint32_t *abort_flag = tmem_holder + 1;
     volatile uint32_t *issued_count = tmem_holder + 2;    // k-block loads this CTA's producer issued
     volatile uint32_t *producer_done = tmem_holder + 3;   // set once this CTA's producer issues no more
+    const uint32_t abort_addr = ptx::smem_addr(const_cast<uint32_t *>(abort_flag));
+    const uint32_t count_addr = ptx::smem_addr(const_cast<uint32_t *>(issued_count));
+    const uint32_t done_addr = ptx::smem_addr(const_cast<uint32_t *>(producer_done));
 
     const uint32_t bar0 = ptx::smem_addr(bars);
-    // loaded[s]: the stage's bytes (of both CTAs of a pair) have landed; used in CTA 0 only
+    // loaded[s]: the stage's bytes (of both CTAs of a pair) have landed; used in even CTAs only
     auto loaded_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };        // MMAs done reading the stage
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };        // every pair done reading
     auto accfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
     auto accempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
@@ -265,14 +318,17 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = kGroup == 2 ? ptx::cluster_ctarank() : 0u;
-    const int64_t cluster_id = blockIdx.x / kGroup;
-    const int64_t num_clusters = gridDim.x / kGroup;
+    const uint32_t rank = kCtas > 1 ? ptx::cluster_ctarank() : 0u;
+    const uint32_t pos = rank % kGroup;            // position within the pair
+    const uint32_t pair = rank / kGroup;           // pair within the cluster
+    const uint32_t lead = pair * kGroup;           // rank of this pair's even CTA
+    const int64_t cluster_id = blockIdx.x / kCtas;
+    const int64_t num_clusters = gridDim.x / kCtas;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(loaded_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), kPairs);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accfull_bar(b), 1);
@@ -296,34 +352,46 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         ptx::tmem_relinquish_alloc_permit<kGroup>();
     }
     ptx::tc_fence_before_sync();
-    if constexpr (kGroup == 2)
-        ptx::cluster_sync();     // peer barriers initialised before any remote arrive
+    if constexpr (kCtas > 1)
+        ptx::cluster_sync();     // every CTA's barriers initialised before any remote arrive
     else
         __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
 
-    const Waiter w{abort_flag,
-                   kGroup == 2 ? ptx::mapa_shared(ptx::smem_addr(const_cast<uint32_t *>(abort_flag)), rank ^ 1u) : 0u,
-                   p.wait_limit_ns};
+    const Waiter w{abort_flag, abort_addr, rank, static_cast<uint32_t>(kCtas), p.wait_limit_ns};
+
+    // Bytes of one CTA's operand A slice in a fill of unit u (B slices are fixed).
+    auto a_bytes = [&](int64_t u) -> uint32_t {
+        return u >= p.tail_start ? Cfg::kTileABytes / 2 : Cfg::kTileABytes;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (every CTA)
-        // 1-CTA: loads complete on the CTA's own loaded[s].  2-CTA: both CTAs'
-        // loads complete on CTA 0's loaded[s], which CTA 0's producer arms with
-        // the bytes of both halves; the MMA thread waits on that one barrier.
+        // 1 CTA: loads complete on the CTA's own loaded[s].  Pairs: every load
+        // meant for a CTA completes on loaded[s] of that CTA's pair leader,
+        // which its own producer arms with the bytes of the whole pair; the MMA
+        // thread waits on that one barrier.
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             uint32_t n_issued = 0;
             bool ok = true;
-            const uint32_t stall = rank == 0 ? kFlagStallProducer0 : kFlagStallProducer1;
+            const uint32_t stall = rank == 0 ? kFlagStallProducer0 : (rank == 1 ? kFlagStallProducer1 : 0u);
             if (p.flags & stall) ok = w.wait(never_bar, 0u, kSiteStall);
-            for (int64_t tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
-                int64_t tm, tn;
-                tile_coord(tile, p.tiles_m, p.tiles_n, p.group, tm, tn);
-                const int32_t m0 = static_cast<int32_t>(tm * kTileM + rank * Cfg::kRowsA);
-                const int32_t n0 = static_cast<int32_t>(tn * Cfg::kTileN + rank * Cfg::kRowsB);
+            for (int64_t u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+                const Unit un = unit_of(u, p);
+                int64_t tmu, tn;
+                tile_coord(un.tile, p.tiles_m, p.tiles_n, p.group, tmu, tn);
+                const int64_t tm = tmu * kPairs + pair;
+                const bool half = un.half >= 0;
+                const int32_t rows_a = half ? Cfg::kRowsA / 2 : Cfg::kRowsA;
+                const uint32_t fill = Cfg::kTileBBytes + a_bytes(u);
+                const CUtensorMap *map_a = half ? &p.tmap_a_half : &p.tmap_a;
+                const int32_t m0 =
+                    static_cast<int32_t>(tm * kTileM + (half ? un.half * (kTileM / 2) : 0) + pos * rows_a);
+                const int32_t n0 =
+                    static_cast<int32_t>(tn * Cfg::kTileN + pos * Cfg::kRowsB + pair * Cfg::kSliceB);
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!w.wait(empty_bar(stage), phase ^ 1u, kSiteEmpty)) {
                         ok = false;
@@ -332,14 +400,22 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     const uint32_t s_b = s_ring + stage * Cfg::kStageBytes;
                     const uint32_t s_a = s_b + Cfg::kTileBBytes;
                     if constexpr (kGroup == 2) {
-                        if (rank == 0) ptx::mbar_arrive_expect_tx(loaded_bar(stage), 2 * Cfg::kStageBytes);
-                        const uint32_t lb = ptx::mapa_shared(loaded_bar(stage), 0u);
-                        ptx::tma_load_2d_pair(s_b, &p.tmap_b, lb, kb * kBlockKElems, n0);
-                        ptx::tma_load_2d_pair(s_a, &p.tmap_a, lb, kb * kBlockKElems, m0);
+                        if (pos == 0) ptx::mbar_arrive_expect_tx(loaded_bar(stage), 2 * fill);
+                        const uint32_t lb = ptx::mapa_shared(loaded_bar(stage), lead);
+                        if constexpr (kPairs == 1) {
+                            ptx::tma_load_2d_pair(s_b, &p.tmap_b, lb, kb * kBlockKElems, n0);
+                        } else {
+                            // this CTA's slice of B rows, into itself and its counterpart(s)
+                            uint16_t mask = 0;
+                            for (int q = 0; q < kPairs; ++q) mask |= static_cast<uint16_t>(1u << (q * kGroup + pos));
+                            ptx::tma_load_2d_pair_multicast(s_b + pair * Cfg::kSliceB * kBlockKBytes, &p.tmap_b, lb,
+                                                            kb * kBlockKElems, n0, mask);
+                        }
+                        ptx::tma_load_2d_pair(s_a, map_a, lb, kb * kBlockKElems, m0);
                     } else {
-                        ptx::mbar_arrive_expect_tx(loaded_bar(stage), Cfg::kStageBytes);
+                        ptx::mbar_arrive_expect_tx(loaded_bar(stage), fill);
                         ptx::tma_load_2d(s_b, &p.tmap_b, loaded_bar(stage), kb * kBlockKElems, n0);
-                        ptx::tma_load_2d(s_a, &p.tmap_a, loaded_bar(stage), kb * kBlockKElems, m0);
+                        ptx::tma_load_2d(s_a, map_a, loaded_bar(stage), kb * kBlockKElems, m0);
                     }
                     *issued_count = ++n_issued;
                     if (++stage == kStages) {
@@ -349,31 +425,39 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 }
             }
             if constexpr (kGroup == 2) {
-                if (rank == 1) {
-                    // publish the final count (release: the count store is ordered before it)
-                    ptx::st_release_cluster_u32(ptx::mapa_shared(ptx::smem_addr(const_cast<uint32_t *>(producer_done)), 1u), 1u);
-                } else {
-                    drain_pair_loads<kStages, Cfg::kStageBytes>(w, loaded_bar, n_issued, ptx::smem_addr(const_cast<uint32_t *>(issued_count)),
-                                     ptx::smem_addr(const_cast<uint32_t *>(producer_done)));
+                // publish the final count (release: the count store is ordered before it)
+                ptx::st_release_cluster_u32(ptx::mapa_shared(done_addr, rank), 1u);
+                if (pos == 0) {
+                    // bytes producer q sent to this leader for fill number i
+                    auto contribution = [&](uint32_t q, uint32_t i) -> uint32_t {
+                        const int64_t u = cluster_id + static_cast<int64_t>(i / p.num_kb) * num_clusters;
+                        const uint32_t b_slice = Cfg::kSliceB * kBlockKBytes;
+                        return q / kGroup == pair ? a_bytes(u) + b_slice : b_slice;
+                    };
+                    drain_cluster_loads<kStages, kCtas>(w, loaded_bar, contribution, n_issued, count_addr,
+                                                        done_addr);
                 }
             } else {
                 // Let every issued load land before the CTA can exit.
                 for (int s = 0; s < kStages; ++s) {
-                    const uint32_t passes = n_issued / kStages + (static_cast<uint32_t>(s) < n_issued % kStages ? 1u : 0u);
+                    const uint32_t passes =
+                        n_issued / kStages + (static_cast<uint32_t>(s) < n_issued % kStages ? 1u : 0u);
                     if (passes) w.drain(loaded_bar(s), (passes - 1) & 1u);
                 }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
-            // ------------------------------------------------ MMA issuer (even CTA)
+        if (lane == 0 && pos == 0) {
+            // ------------------------------------------------ MMA issuer (even CTA of each pair)
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued_any = false;
+            const uint16_t pair_mask = static_cast<uint16_t>(((1u << kGroup) - 1u) << lead);
             if (p.flags & kFlagStallMma) ok = w.wait(never_bar, 0u, kSiteStall);
-            for (int64_t tile = cluster_id; ok && tile < p.num_tiles; tile += num_clusters) {
+            for (int64_t u = cluster_id; ok && u < p.num_units; u += num_clusters) {
+                const uint32_t idesc = u >= p.tail_start ? kIdescHalf : kIdesc;
                 if (!w.wait(accempty_bar(acc), acc_phase ^ 1u, kSiteAccEmpty)) break;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * kAccCols;
@@ -390,18 +474,18 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 #pragma unroll
                     for (int j = 0; j < kBlockKBytes / kMmaKBytes; ++j) {
                         // +32 bytes along K inside the 128-byte swizzle span = +2 in the address field
-                        Kind::template mma<kGroup>(d_tmem, desc_b + 2u * j, desc_a + 2u * j, kIdesc,
+                        Kind::template mma<kGroup>(d_tmem, desc_b + 2u * j, desc_a + 2u * j, idesc,
                                                    (kb | j) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
-                    ptx::mma_commit<kGroup>(empty_bar(stage), kPairMask);   // stage free in both CTAs
+                    ptx::mma_commit<kGroup>(empty_bar(stage), kAllMask);   // stage free for every CTA that writes it
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                ptx::mma_commit<kGroup>(accfull_bar(acc), kPairMask);       // accumulator complete
+                ptx::mma_commit<kGroup>(accfull_bar(acc), pair_mask);      // accumulator complete
                 if (++acc == 2) {
                     acc = 0;
                     acc_phase ^= 1u;
@@ -409,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             }
             // All MMAs this thread issued must finish before TMEM is freed.
             if (issued_any) {
-                ptx::mma_commit<kGroup>(drain_bar, 0x1);
+                ptx::mma_commit<kGroup>(drain_bar, static_cast<uint16_t>(1u << rank));
                 w.drain(drain_bar, 0u);
             }
         }
@@ -421,32 +505,35 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t chunk_ctr = 0;
-        for (int64_t tile = cluster_id; tile < p.num_tiles; tile += num_clusters) {
-            int64_t tm, tn;
-            tile_coord(tile, p.tiles_m, p.tiles_n, p.group, tm, tn);
+        for (int64_t u = cluster_id; u < p.num_units; u += num_clusters) {
+            const Unit un = unit_of(u, p);
+            int64_t tmu, tn;
+            tile_coord(un.tile, p.tiles_m, p.tiles_n, p.group, tmu, tn);
+            const int64_t tm = tmu * kPairs + pair;
+            const int n_chunks = (un.half >= 0 ? kTileM / 2 : kTileM) / kEpiBoxM;
             bool ok = w.wait(accfull_bar(acc), acc_phase, kSiteAccFull);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             __syncwarp();
             ptx::tc_fence_after_sync();
-            const int32_t m0 = static_cast<int32_t>(tm * kTileM);
+            const int32_t m0 = static_cast<int32_t>(tm * kTileM + (un.half >= 0 ? un.half * (kTileM / 2) : 0));
             // this warp's first output column
-            const int32_t nw = static_cast<int32_t>(tn * Cfg::kTileN + rank * Cfg::kRowsB) + 32 * quarter;
+            const int32_t nw = static_cast<int32_t>(tn * Cfg::kTileN + pos * Cfg::kRowsB) + 32 * quarter;
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + acc * kAccCols;
 #pragma unroll 1
-            for (int c = 0; c < kTileM / kEpiBoxM; ++c) {
+            for (int c = 0; c < n_chunks; ++c) {
                 uint32_t r0[32], r1[32];
                 ptx::tmem_ld_32x32b_x32(t_row + c * kEpiBoxM, r0);
                 ptx::tmem_ld_32x32b_x32(t_row + c * kEpiBoxM + 32, r1);
                 ptx::tmem_ld_wait(r0);
                 ptx::reg_dependency(r1);
-                if (c == kTileM / kEpiBoxM - 1) {
+                if (c == n_chunks - 1) {
                     // last read of this accumulator: hand it back to the MMA thread
                     ptx::tc_fence_before_sync();
                     __syncwarp();
                     if (lane == 0) {
                         if constexpr (kGroup == 2)
-                            ptx::mbar_arrive_remote(ptx::mapa_shared(accempty_bar(acc), 0u));
+                            ptx::mbar_arrive_remote(ptx::mapa_shared(accempty_bar(acc), lead));
                         else
                             ptx::mbar_arrive(accempty_bar(acc));
                     }
@@ -506,8 +593,8 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     __syncwarp();                // .aligned barriers below need converged warps
     ptx::tc_fence_before_sync();
-    if constexpr (kGroup == 2)
-        ptx::cluster_sync();     // no CTA leaves while its peer may still touch its shared memory
+    if constexpr (kCtas > 1)
+        ptx::cluster_sync();     // no CTA leaves while another may still touch its shared memory
     else
         __syncthreads();
     if (warp == 1) {
@@ -519,18 +606,28 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
 // ------------------------------------------------------------------ helpers
 // Copies a rows x K operand with row stride ld_src (elements) into a buffer
-// with row stride ld_dst >= K (a multiple of 16 bytes), zero-filling the pad.
+// with row stride ld_dst >= K (a multiple of 16 bytes, 16-byte aligned base),
+// zero-filling columns K .. ld_dst-1.  One thread writes one 16-byte chunk of
+// a destination row; the source row may start at any element boundary, so it
+// is read element by element (consecutive threads read consecutive chunks).
+// Grid: x over the chunks of a row, y (and z for more than 65535 rows) over
+// rows.
 template <typename T>
 __global__ void repack_rows_kernel(const T *__restrict__ src, int64_t ld_src, T *__restrict__ dst, int64_t ld_dst,
                                    int64_t rows, int64_t K)
 {
-    const int64_t total = rows * ld_dst;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / ld_dst;
-        const int64_t k = i - r * ld_dst;
-        dst[i] = k < K ? src[r * ld_src + k] : T(0);
-    }
+    constexpr int kVec = 16 / sizeof(T);
+    const int64_t r = blockIdx.y + static_cast<int64_t>(blockIdx.z) * gridDim.y;
+    const int64_t c = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * kVec;
+    if (r >= rows || c >= ld_dst) return;
+    const T *s = src + r * ld_src;
+    union {
+        T v[kVec];
+        uint4 u;
+    } chunk;
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) chunk.v[i] = c + i < K ? s[c + i] : T(0);
+    *reinterpret_cast<uint4 *>(dst + r * ld_dst + c) = chunk.u;
 }
 
 // C[m + n*ldc] = +0 for m < M, n < N (the K == 0 case).

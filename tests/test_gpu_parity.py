@@ -221,9 +221,9 @@ def force_group():
     g.gemm_debug_force_cta_group(0)
 
 
-@pytest.mark.parametrize("cta_group", [1, 2])
+@pytest.mark.parametrize("cta_group", [1, 2, 4])
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (31, 33, 29), (257, 129, 65), (300, 200, 136), (513, 640, 520),
-                                   (1000, 300, 1000), (64, 600, 64)])
+                                   (1000, 300, 1000), (64, 600, 64), (1100, 700, 300)])
 def test_forced_cta_group_pm1_exact(force_group, cta_group, M, N, K):
     force_group(cta_group)
     A = synth.sign_fp16(M * K, 50 + M)
@@ -231,8 +231,8 @@ def test_forced_cta_group_pm1_exact(force_group, cta_group, M, N, K):
     check_f16_full(M, N, K, A, B, exact=True, what=f"group {cta_group} {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("cta_group", [1, 2])
-@pytest.mark.parametrize("M,N,K", [(300, 200, 136), (513, 640, 520), (200, 1030, 4096)])
+@pytest.mark.parametrize("cta_group", [1, 2, 4])
+@pytest.mark.parametrize("M,N,K", [(300, 200, 136), (513, 640, 520), (200, 1030, 4096), (1300, 900, 700)])
 def test_forced_cta_group_gaussian(force_group, cta_group, M, N, K):
     force_group(cta_group)
     A = synth.gauss_fp16(M * K, 70 + M)
@@ -241,3 +241,41 @@ def test_forced_cta_group_gaussian(force_group, cta_group, M, N, K):
     A8, sa = synth.gauss_e4m3(M * K, 90 + M)
     B8, sb = synth.gauss_e4m3(N * K, 91 + N)
     check_f8_full(M, N, K, A8, B8, sa, sb, what=f"e4m3 group {cta_group} {M}x{N}x{K}")
+
+
+# ---------------------------------------------------------------- split tail wave
+def _launch_record():
+    import re
+    import dense_gemm_tn_gb300 as g
+    rec = g.last_launch()
+    fields = dict(re.findall(r"(\w+)=(\d+)", rec))
+    return {k: int(v) for k, v in fields.items()}
+
+
+@pytest.mark.parametrize("cta_group,M,N,K", [
+    (2, 2000, 3000, 200),      # 8 x 12 = 96 pair tiles: one full wave + a short one
+    (2, 8192, 8192, 192),      # the headline shape's 1024 tiles (13 waves + 36)
+    (1, 2000, 2560, 136),      # 8 x 20 = 160 one-CTA tiles
+    (4, 8192, 8192, 192),      # 512 two-pair units
+    (4, 3000, 12289, 136),     # 6 x 49 = 294 two-pair units, ragged m, n
+])
+def test_tail_wave_split_into_half_units(force_group, cta_group, M, N, K):
+    force_group(cta_group)
+    A = synth.sign_fp16(M * K, 77 + M)
+    B = synth.sign_fp16(N * K, 78 + N)
+    got = run_f16(M, N, K, A, K, B, K)
+    rec = _launch_record()
+    tiles, clusters = rec["tiles"], rec["clusters"]
+    waves, rem = divmod(tiles, clusters)
+    split = waves >= 1 and 0 < rem and 2 * rem <= clusters
+    assert rec["units"] == (tiles + rem if split else tiles)
+    if M * N <= 8_000_000:
+        Cref, _, _ = oracle.gemm_f16_tn(M, N, K, A, K, B, K)
+        assert np.array_equal(got, oracle.c_as_nm(Cref, M, N, M))
+    else:
+        mi, ni = sample_positions(M, N, 20000, seed=M)
+        c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
+        assert np.array_equal(got[ni, mi], c)
+    # with the measured 76 pair / 152 single slots of a GB300 these shapes split
+    if clusters in (76, 152) and cta_group != 4:
+        assert split

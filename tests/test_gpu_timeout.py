@@ -12,7 +12,7 @@ from tests.gpu_helpers import GuardedC, check_f16_full, to_dev_u16
 
 pytestmark = pytest.mark.gpu
 
-CASES = [(1, 1), (1, 2), (2, 1), (2, 2), (2, 3)]     # (cta group, stalled thread)
+CASES = [(1, 1), (1, 2), (2, 1), (2, 2), (2, 3), (4, 1), (4, 2), (4, 3)]   # (CTAs per cluster, stalled thread)
 
 
 @pytest.mark.parametrize("cta_group,mode", CASES)
