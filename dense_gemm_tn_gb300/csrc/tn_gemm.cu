@@ -34,9 +34,9 @@ gemm_status_t fail(gemm_status_t s, const char *fmt, ...)
 struct DeviceState {
     bool ready = false;
     int sms = 0, major = 0, minor = 0;
-    // per kernel, indexed [kind: f16, e4m3][CTAs per cluster: 1, 2 or 4]
-    bool smem_attr[2][5] = {};
-    int max_clusters[2][5] = {};      // co-resident clusters (0 = not queried yet)
+    // per kernel, indexed [kind: f16, e4m3][CTA group: 1 or 2]
+    bool smem_attr[2][3] = {};
+    int max_clusters[2][3] = {};      // co-resident clusters of the kernel's own size (0 = not queried yet)
     void *workspace = nullptr;
     size_t workspace_bytes = 0;
 };
@@ -159,20 +159,21 @@ int launch_grid(int64_t work, int cap)
     return g < 1 ? 1 : static_cast<int>(g);
 }
 
-// Launches the persistent kernel: one CTA (or one 2-CTA cluster) per
-// co-resident slot, each walking the tile raster with a stride of the grid.
-template <class Kind, int G, int P>
-gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, cudaStream_t stream)
+// Launches the persistent kernel: one CTA (or one CTA pair) per co-resident
+// slot, each walking the tile raster with a stride of the grid.  Pairs are
+// launched as 2-CTA clusters with a preferred cluster size of 4 when `quad`:
+// the hardware then joins two pairs into one cluster wherever four CTAs fit
+// together, and the kernel shares B rows between them.
+template <class Kind, int G>
+gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, bool quad, cudaStream_t stream)
 {
-    using Cfg = tn::TileCfg<G, P>;
-    constexpr int kCtas = G * P;
-    static_assert(kCtas == 1 || kCtas == 2 || kCtas == 4, "cluster shape outside the per-device caches");
-    auto kernel = tn::tn_gemm_kernel<Kind, G, P>;
+    using Cfg = tn::TileCfg<G>;
+    auto kernel = tn::tn_gemm_kernel<Kind, G>;
     const int ki = Kind::kF8 ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCtas;
+    attr[0].val.clusterDim.x = G;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(tn::kThreads, 1, 1);
@@ -183,28 +184,40 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     int slots;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
-        if (!dev.smem_attr[ki][kCtas]) {
+        if (!dev.smem_attr[ki][G]) {
             cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
             if (e != cudaSuccess)
                 return fail(GEMM_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", name, cudaGetErrorString(e));
-            dev.smem_attr[ki][kCtas] = true;
+            dev.smem_attr[ki][G] = true;
         }
-        if (dev.max_clusters[ki][kCtas] == 0) {
+        if (dev.max_clusters[ki][G] == 0) {
             int n = 0;
-            cfg.gridDim = dim3(kCtas * (dev.sms / kCtas), 1, 1);
+            cfg.gridDim = dim3(G * (dev.sms / G), 1, 1);
             cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
             if (e != cudaSuccess || n <= 0) {
                 cudaGetLastError();
-                n = dev.sms / kCtas;     // fall back to one slot per group of SMs
+                n = dev.sms / G;     // fall back to one slot per SM (pair)
             }
-            dev.max_clusters[ki][kCtas] = n;
+            dev.max_clusters[ki][G] = n;
         }
-        slots = dev.max_clusters[ki][kCtas];
+        slots = dev.max_clusters[ki][G];
     }
-    const int clusters = prm.num_tiles < slots ? prm.num_tiles : slots;
-    cfg.gridDim = dim3(kCtas * clusters, 1, 1);
-    // A last wave that fills at most half of the clusters is run as twice as
-    // many half-width units, so every cluster finishes at about the same time.
+    int clusters = prm.num_tiles < slots ? prm.num_tiles : slots;
+    if (quad && G == 2) {
+        clusters = (clusters + 1) & ~1;      // whole groups of four CTAs; an odd pair is a phantom
+        if (clusters > slots) clusters = slots & ~1;
+        if (clusters < 2) quad = false;
+    }
+    if (quad && G == 2) {
+        attr[1].id = cudaLaunchAttributePreferredClusterDimension;
+        attr[1].val.preferredClusterDim.x = 2 * G;
+        attr[1].val.preferredClusterDim.y = 1;
+        attr[1].val.preferredClusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
+    cfg.gridDim = dim3(G * clusters, 1, 1);
+    // A last wave that fills at most half of the slots is run as twice as
+    // many half-width units, so every slot finishes at about the same time.
     const int waves = prm.num_tiles / clusters, rem = prm.num_tiles % clusters;
     if (waves >= 1 && rem > 0 && 2 * rem <= clusters) {
         prm.tail_start = waves * clusters;
@@ -214,8 +227,9 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
         prm.num_units = prm.num_tiles;
     }
     snprintf(t_last_launch, sizeof(t_last_launch),
-             "%s: ctas_per_cluster=%d grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d", name, kCtas,
-             kCtas * clusters, clusters, slots, prm.num_tiles, prm.num_units, prm.tail_start);
+             "%s: ctas_per_cluster=%d%s grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d", name, G,
+             quad && G == 2 ? " (preferred 4)" : "", G * clusters, clusters, slots, prm.num_tiles, prm.num_units,
+             prm.tail_start);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));
     return GEMM_OK;
@@ -255,29 +269,27 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         return GEMM_OK;
     }
 
-    // Cluster shape.  One CTA per 128 x 256 tile when N <= 128 (a pair's
-    // second half would idle); else a CTA pair per 256 x 256 tile.  Two pairs
-    // sharing their B rows by multicast (4 CTAs, 512 x 256 units) cut the
-    // operand bytes per SM by a quarter but fit on fewer SMs (144 of a
-    // GB300's 152); measured, they win only when the pair grid's last wave is
-    // a partial wave too full to split into half units, and there are enough
-    // 4-CTA units to fill the GPU.
-    const int64_t m_tiles = (M + tn::kTileM - 1) / tn::kTileM;
+    // Tile shape.  One CTA per 128 x 256 tile when N <= 128 (a pair's second
+    // half would idle); else a CTA pair per 256 x 256 tile.  Pairs can also be
+    // launched so that the hardware joins two of them into a 4-CTA cluster
+    // sharing B rows wherever four CTAs fit together.  Measured on GB300 that
+    // pays only when the pair grid ends in a partial wave too full to split
+    // into half units (3000x12289x4104: +9 %); on the other shapes the
+    // coupling of the two pairs costs more than the saved bytes (4096^3: -12 %,
+    // 8192^3: -0.5 %).
     int ctas = N > 128 ? 2 : 1;
-    if (ctas == 2 && m_tiles >= 2) {
-        const int64_t pair_tiles = m_tiles * ((N + 255) / 256);
+    if (ctas == 2) {
+        const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
         const int64_t pair_slots = dev->sms / 2;
         const int64_t rem = pair_tiles % pair_slots;
-        const int64_t quad_units = ((m_tiles + 1) / 2) * ((N + 255) / 256);
-        if (pair_tiles > pair_slots && 2 * rem > pair_slots && quad_units >= dev->sms / 4) ctas = 4;
+        if (pair_tiles > pair_slots && 2 * rem > pair_slots) ctas = 4;
     }
     if (const int forced = g_force_cta_group.load()) ctas = forced;
     const int cta_group = ctas >= 2 ? 2 : 1;
-    const int pairs = ctas == 4 ? 2 : 1;
-    const int64_t tiles_m = (m_tiles + pairs - 1) / pairs;
+    const bool quad = ctas == 4;
+    const int64_t tiles_m = (M + tn::kTileM - 1) / tn::kTileM;
     const int64_t tiles_n = (N + 128 * cta_group - 1) / (128 * cta_group);
     if (tiles_m * tiles_n > INT32_MAX) return fail(GEMM_ERR_UNSUPPORTED, "%s: too many output tiles", name);
-
 
     // The TMA reads an operand in place only when its base, its row stride and
     // its row length K are all multiples of 16 bytes (a row that ends inside a
@@ -321,7 +333,9 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     if ((st = encode_2d(&prm.tmap_a_half, in_type, a_use, ka, M, lda_use * esz, box_k, rows_a / 2, "A half")) !=
         GEMM_OK)
         return st;
-    if ((st = encode_2d(&prm.tmap_b, in_type, b_use, kb, N, ldb_use * esz, box_k, 128 / pairs, "B")) != GEMM_OK)
+    if ((st = encode_2d(&prm.tmap_b, in_type, b_use, kb, N, ldb_use * esz, box_k, 128, "B")) != GEMM_OK)
+        return st;
+    if ((st = encode_2d(&prm.tmap_b_slice, in_type, b_use, kb, N, ldb_use * esz, box_k, 64, "B slice")) != GEMM_OK)
         return st;
     // TMA stores cover rows m < M rounded down to 8 (16 bytes); the kernel
     // writes the ragged rest, or all of C when C's base or stride is unaligned.
@@ -340,14 +354,13 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     prm.tiles_n = static_cast<int32_t>(tiles_n);
     prm.num_tiles = static_cast<int32_t>(tiles_m * tiles_n);
     prm.num_kb = static_cast<int32_t>((K * esz + tn::kBlockKBytes - 1) / tn::kBlockKBytes);
-    prm.group = kGroupM / pairs;    // the same m extent per raster group for every cluster shape
+    prm.group = kGroupM;            // even, so raster ids 2j, 2j+1 are neighbouring m tiles of one n tile
     prm.scale = scale;
     prm.flags = (tma_c ? tn::kFlagTmaStore : 0u) | stall_flags(g_inject_stall.load());
     prm.wait_limit_ns = g_wait_limit_ns.load();
 
-    if (ctas == 4) return launch<Kind, 2, 2>(name, prm, *dev, stream);
-    if (ctas == 2) return launch<Kind, 2, 1>(name, prm, *dev, stream);
-    return launch<Kind, 1, 1>(name, prm, *dev, stream);
+    if (cta_group == 2) return launch<Kind, 2>(name, prm, *dev, quad, stream);
+    return launch<Kind, 1>(name, prm, *dev, false, stream);
 }
 
 }  // namespace
@@ -436,8 +449,8 @@ const char *gemm_build_info(void)
 {
     static char info[384];
     snprintf(info, sizeof(info),
-             "dense_gemm_tn sm_103a: 2x2-CTA cluster 512x256 with B multicast, 2-CTA tile 256x256 (%d stages, "
-             "%d B smem), 1-CTA tile 128x256 (%d stages, %d B smem); K block %d B; TMEM %u cols; raster group %d",
+             "dense_gemm_tn sm_103a: CTA-pair tile 256x256 in clusters of 2 or 4 (B multicast), %d stages, %d B "
+             "smem; 1-CTA tile 128x256, %d stages, %d B smem; K block %d B; TMEM %u cols; raster group %d",
              tn::TileCfg<2>::kStages, tn::TileCfg<2>::kSmemBytes, tn::TileCfg<1>::kStages,
              tn::TileCfg<1>::kSmemBytes, tn::kBlockKBytes, tn::kTmemCols, kGroupM);
     return info;

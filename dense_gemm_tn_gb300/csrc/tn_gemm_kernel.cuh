@@ -55,22 +55,24 @@ constexpr uint32_t kTmemCols = 2 * kAccCols;  // double-buffered accumulator = a
 // kGroup = 1: one CTA computes a 128 (n) x 256 (m) tile with M128 MMAs.
 // kGroup = 2: a CTA pair computes a 256 (n) x 256 (m) tile with M256 MMAs
 // issued by the pair's even CTA; each CTA holds 128 rows of each operand tile
-// per stage and the accumulator rows of its own 128 columns n.
-// kPairs = 2 (with kGroup = 2): a 4-CTA cluster of two pairs working on
-// neighbouring m tiles of the same n tile.  Both pairs need the same B rows,
-// so each CTA loads half of its 128 B rows and multicasts them to its
-// counterpart in the other pair: 24 instead of 32 KiB leave L2 per CTA and
-// stage.
-template <int kGroup, int kPairs = 1>
+// per stage and the accumulator rows of its own 128 columns n.  Pairs are
+// launched with a cluster size of 2 and a preferred size of 4: where the
+// hardware can place four CTAs together, the cluster's two pairs work on
+// neighbouring m tiles of the same n tile and share their B rows -- each CTA
+// loads half of its 128 B rows and multicasts them to its counterpart in the
+// other pair, so 24 instead of 32 KiB leave L2 per CTA and stage.  Where it
+// cannot (8 of a GB300's 152 SMs), the pair works alone.  The kernel reads its
+// cluster size at run time.
+template <int kGroup>
 struct TileCfg {
-    static_assert(kGroup == 1 ? kPairs == 1 : (kPairs == 1 || kPairs == 2), "unsupported cluster shape");
-    static constexpr int kCtas = kGroup * kPairs;           // CTAs per cluster
+    static constexpr int kMaxCtas = 2 * kGroup;            // CTAs per cluster at most (2 pairs)
     static constexpr int kTileN = 128 * kGroup;            // C columns n per pair tile = MMA M
     static constexpr int kRowsB = 128;                      // B rows (columns n) per CTA and stage
-    static constexpr int kSliceB = kRowsB / kPairs;         // B rows each CTA loads (and multicasts)
+    static constexpr int kSliceB = kRowsB / 2;              // B rows each CTA loads when a cluster shares
     static constexpr int kRowsA = kTileM / kGroup;          // A rows (m) per CTA and stage
     static constexpr int kStages = kGroup == 2 ? 6 : 4;
     static constexpr int kTileBBytes = kRowsB * kBlockKBytes;
+    static constexpr int kSliceBBytes = kSliceB * kBlockKBytes;
     static constexpr int kTileABytes = kRowsA * kBlockKBytes;
     static constexpr int kStageBytes = kTileBBytes + kTileABytes;
     static constexpr int kSmemRing = kStages * kStageBytes;
@@ -98,15 +100,14 @@ enum WaitSite : int {
 
 struct KernelParams {
     CUtensorMap tmap_a;      // A: dims {K', M}, box {kBlockKBytes / esz, kRowsA}, 128B swizzle
-    CUtensorMap tmap_b;      // B: dims {K', N}, box {kBlockKBytes / esz, kSliceB}, 128B swizzle
+    CUtensorMap tmap_b;      // B: dims {K', N}, box {kBlockKBytes / esz, 128}, 128B swizzle
     CUtensorMap tmap_c;      // C: dims {m_tma, N}, box {kEpiBoxM, kEpiBoxN}, 128B swizzle
     CUtensorMap tmap_a_half; // A with box {kBlockKBytes / esz, kRowsA / 2} (half units)
+    CUtensorMap tmap_b_slice; // B with box {kBlockKBytes / esz, 64} (shared B rows of a 4-CTA cluster)
     void *c_ptr;             // C base (direct stores)
     int64_t ldc;
     int32_t M, N, K;
     int32_t m_tma;           // rows m < m_tma are written by TMA stores (a multiple of 8, or 0)
-    // Unit grid: tiles_m rows of kPairs m tiles each, tiles_n columns of one
-    // pair tile; num_tiles = tiles_m * tiles_n.
     int32_t tiles_m, tiles_n, num_tiles, num_kb, group;
     // Work units: tiles [0, tail_start) are whole units; each later tile is two
     // units covering one half of its m range (so a last, partly filled wave of
@@ -122,7 +123,9 @@ struct KernelParams {
 // walk down the region's rows for one tile column (n), then the next column.
 // The last region is short when tiles_m % group != 0.  This is the GROUP_M
 // mapping of hello-gpu ch.11 section 11.3.4 and the grouped block order of
-// the ROCm blog's Step 6.
+// the ROCm blog's Step 6.  With an even group, ids 2j and 2j+1 fall on
+// neighbouring m tiles of one n tile, which is what a 4-CTA cluster's two
+// pairs share.
 __host__ __device__ __forceinline__ void tile_coord(int64_t id, int64_t tiles_m, int64_t tiles_n, int64_t group,
                                                     int64_t &tm, int64_t &tn)
 {
@@ -135,17 +138,25 @@ __host__ __device__ __forceinline__ void tile_coord(int64_t id, int64_t tiles_m,
     tn = in_group / rows;
 }
 
-// Unit u -> its tile and which half of the tile's m range it covers (-1: all).
+// A work unit: a tile, or one m half of a tile of the split last wave.
 struct Unit {
-    int64_t tile;
-    int32_t half;
+    int64_t tm, tn;          // tile coordinates
+    int32_t half;            // -1: the whole tile; 0 / 1: that half of its m range
+    bool phantom;            // no such unit: loads out of bounds, computes zeros, stores nothing
 };
 
 __device__ __forceinline__ Unit unit_of(int64_t u, const KernelParams &p)
 {
-    if (u < p.tail_start) return {u, -1};
-    const int64_t v = u - p.tail_start;
-    return {p.tail_start + v / 2, static_cast<int32_t>(v & 1)};
+    Unit r{0, 0, -1, u >= p.num_units};
+    if (r.phantom) return r;
+    int64_t tile = u;
+    if (u >= p.tail_start) {
+        const int64_t v = u - p.tail_start;
+        tile = p.tail_start + v / 2;
+        r.half = static_cast<int32_t>(v & 1);
+    }
+    tile_coord(tile, p.tiles_m, p.tiles_n, p.group, r.tm, r.tn);
+    return r;
 }
 
 // ------------------------------------------------------------------ waits
@@ -232,13 +243,13 @@ struct KindE4M3 {
 // (mbarrier.complete_tx), otherwise it arms the fill for the bytes that will
 // (arrive.expect_tx).  Then it waits for the phase.  On the normal path every
 // producer issued every fill and each wait returns at once.
-template <int kStages, int kCtas, class LoadedBar, class Contribution>
+template <int kStages, int kMaxCtas, class LoadedBar, class Contribution>
 __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar loaded_bar, Contribution contribution,
                                                     uint32_t n_own, uint32_t count_addr, uint32_t done_addr)
 {
-    uint32_t counts[kCtas];
+    uint32_t counts[kMaxCtas];
     const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t q = 0; q < kCtas; ++q) {
+    for (uint32_t q = 0; q < w.ctas; ++q) {
         if (q == w.rank) {
             counts[q] = n_own;
             continue;
@@ -255,8 +266,8 @@ __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar l
     }
     for (int s = 0; s < kStages; ++s) {
         uint32_t lo = 0xffffffffu, hi = 0;
-        uint32_t passes[kCtas];
-        for (uint32_t q = 0; q < kCtas; ++q) {
+        uint32_t passes[kMaxCtas];
+        for (uint32_t q = 0; q < w.ctas; ++q) {
             passes[q] = counts[q] / kStages + (static_cast<uint32_t>(s) < counts[q] % kStages ? 1u : 0u);
             lo = passes[q] < lo ? passes[q] : lo;
             hi = passes[q] > hi ? passes[q] : hi;
@@ -268,7 +279,7 @@ __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar l
         }
         const uint32_t fill = (hi - 1) * kStages + s;   // index of the stage's last fill
         uint32_t sent = 0, total = 0;
-        for (uint32_t q = 0; q < kCtas; ++q) {
+        for (uint32_t q = 0; q < w.ctas; ++q) {
             const uint32_t c = contribution(q, fill);
             total += c;
             if (passes[q] == hi) sent += c;
@@ -283,16 +294,14 @@ __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar l
 }
 
 // ------------------------------------------------------------------ kernel
-template <class Kind, int kGroup, int kPairs>
+template <class Kind, int kGroup>
 __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_constant__ KernelParams p)
 {
-    using Cfg = TileCfg<kGroup, kPairs>;
+    using Cfg = TileCfg<kGroup>;
     constexpr int kStages = Cfg::kStages;
-    constexpr int kCtas = Cfg::kCtas;
     constexpr int kBlockKElems = kBlockKBytes / Kind::kElemBytes;
     constexpr uint32_t kIdesc = ptx::idesc_f32acc(Cfg::kTileN, kTileM, Kind::kFmt, Kind::kFmt);
     constexpr uint32_t kIdescHalf = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 2, Kind::kFmt, Kind::kFmt);
-    constexpr uint16_t kAllMask = static_cast<uint16_t>((1u << kCtas) - 1u);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -318,17 +327,21 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = kCtas > 1 ? ptx::cluster_ctarank() : 0u;
+    const uint32_t ctas = kGroup == 2 ? ptx::cluster_nctarank() : 1u;   // 2 or 4 for pairs
+    const uint32_t rank = kGroup == 2 ? ptx::cluster_ctarank() : 0u;
     const uint32_t pos = rank % kGroup;            // position within the pair
     const uint32_t pair = rank / kGroup;           // pair within the cluster
+    const uint32_t pairs = ctas / kGroup;          // pairs in this cluster (1 or 2)
     const uint32_t lead = pair * kGroup;           // rank of this pair's even CTA
-    const int64_t cluster_id = blockIdx.x / kCtas;
-    const int64_t num_clusters = gridDim.x / kCtas;
+    // One work slot per pair (per CTA for kGroup = 1); the pairs of a cluster
+    // hold consecutive slots, and each walks units slot, slot + nslots, ...
+    const int64_t nslots = gridDim.x / kGroup;
+    const int64_t slot0 = (blockIdx.x - rank) / kGroup;  // slot of the cluster's first pair
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(loaded_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), kPairs);
+            ptx::mbar_init(empty_bar(s), pairs);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accfull_bar(b), 1);
@@ -352,18 +365,29 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         ptx::tmem_relinquish_alloc_permit<kGroup>();
     }
     ptx::tc_fence_before_sync();
-    if constexpr (kCtas > 1)
+    if constexpr (kGroup == 2)
         ptx::cluster_sync();     // every CTA's barriers initialised before any remote arrive
     else
         __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
 
-    const Waiter w{abort_flag, abort_addr, rank, static_cast<uint32_t>(kCtas), p.wait_limit_ns};
+    const Waiter w{abort_flag, abort_addr, rank, ctas, p.wait_limit_ns};
 
-    // Bytes of one CTA's operand A slice in a fill of unit u (B slices are fixed).
-    auto a_bytes = [&](int64_t u) -> uint32_t {
-        return u >= p.tail_start ? Cfg::kTileABytes / 2 : Cfg::kTileABytes;
+    // Iteration `it` of this cluster: the units of its pairs, and whether the
+    // two pairs share B rows (both units exist and lie on the same n tile).
+    auto cluster_units = [&](int64_t it, Unit &mine, bool &shared) {
+        const int64_t u0 = slot0 + it * nslots;
+        mine = unit_of(u0 + pair, p);
+        shared = false;
+        if (pairs == 2) {
+            const Unit e = pair == 0 ? mine : unit_of(u0, p);
+            const Unit o = pair == 1 ? mine : unit_of(u0 + 1, p);
+            shared = !e.phantom && !o.phantom && e.tn == o.tn;
+        }
+    };
+    auto a_bytes = [&](const Unit &un) -> uint32_t {
+        return un.half >= 0 ? Cfg::kTileABytes / 2 : Cfg::kTileABytes;
     };
 
     if (warp == 0) {
@@ -379,19 +403,21 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             bool ok = true;
             const uint32_t stall = rank == 0 ? kFlagStallProducer0 : (rank == 1 ? kFlagStallProducer1 : 0u);
             if (p.flags & stall) ok = w.wait(never_bar, 0u, kSiteStall);
-            for (int64_t u = cluster_id; ok && u < p.num_units; u += num_clusters) {
-                const Unit un = unit_of(u, p);
-                int64_t tmu, tn;
-                tile_coord(un.tile, p.tiles_m, p.tiles_n, p.group, tmu, tn);
-                const int64_t tm = tmu * kPairs + pair;
+            for (int64_t it = 0; ok && slot0 + it * nslots < p.num_units; ++it) {
+                Unit un;
+                bool shared;
+                cluster_units(it, un, shared);
                 const bool half = un.half >= 0;
                 const int32_t rows_a = half ? Cfg::kRowsA / 2 : Cfg::kRowsA;
-                const uint32_t fill = Cfg::kTileBBytes + a_bytes(u);
+                const uint32_t fill = Cfg::kTileBBytes + a_bytes(un);
                 const CUtensorMap *map_a = half ? &p.tmap_a_half : &p.tmap_a;
-                const int32_t m0 =
-                    static_cast<int32_t>(tm * kTileM + (half ? un.half * (kTileM / 2) : 0) + pos * rows_a);
-                const int32_t n0 =
-                    static_cast<int32_t>(tn * Cfg::kTileN + pos * Cfg::kRowsB + pair * Cfg::kSliceB);
+                // a phantom unit reads past the matrices: zero fill, the box's full byte count
+                const int32_t m0 = un.phantom ? p.M
+                                              : static_cast<int32_t>(un.tm * kTileM + (half ? un.half * (kTileM / 2) : 0) +
+                                                                     pos * rows_a);
+                const int32_t nb = un.phantom ? p.N : static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB);
+                uint16_t mcast = 0;
+                for (uint32_t q = 0; q < pairs; ++q) mcast |= static_cast<uint16_t>(1u << (q * kGroup + pos));
                 for (int kb = 0; kb < p.num_kb; ++kb) {
                     if (!w.wait(empty_bar(stage), phase ^ 1u, kSiteEmpty)) {
                         ok = false;
@@ -402,19 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     if constexpr (kGroup == 2) {
                         if (pos == 0) ptx::mbar_arrive_expect_tx(loaded_bar(stage), 2 * fill);
                         const uint32_t lb = ptx::mapa_shared(loaded_bar(stage), lead);
-                        if constexpr (kPairs == 1) {
-                            ptx::tma_load_2d_pair(s_b, &p.tmap_b, lb, kb * kBlockKElems, n0);
-                        } else {
-                            // this CTA's slice of B rows, into itself and its counterpart(s)
-                            uint16_t mask = 0;
-                            for (int q = 0; q < kPairs; ++q) mask |= static_cast<uint16_t>(1u << (q * kGroup + pos));
-                            ptx::tma_load_2d_pair_multicast(s_b + pair * Cfg::kSliceB * kBlockKBytes, &p.tmap_b, lb,
-                                                            kb * kBlockKElems, n0, mask);
-                        }
+                        if (shared)   // this CTA's half of the B rows, into itself and its counterpart
+                            ptx::tma_load_2d_pair_multicast(s_b + pair * Cfg::kSliceBBytes, &p.tmap_b_slice, lb,
+                                                            kb * kBlockKElems, nb + pair * Cfg::kSliceB, mcast);
+                        else
+                            ptx::tma_load_2d_pair(s_b, &p.tmap_b, lb, kb * kBlockKElems, nb);
                         ptx::tma_load_2d_pair(s_a, map_a, lb, kb * kBlockKElems, m0);
                     } else {
                         ptx::mbar_arrive_expect_tx(loaded_bar(stage), fill);
-                        ptx::tma_load_2d(s_b, &p.tmap_b, loaded_bar(stage), kb * kBlockKElems, n0);
+                        ptx::tma_load_2d(s_b, &p.tmap_b, loaded_bar(stage), kb * kBlockKElems, nb);
                         ptx::tma_load_2d(s_a, map_a, loaded_bar(stage), kb * kBlockKElems, m0);
                     }
                     *issued_count = ++n_issued;
@@ -430,12 +452,18 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 if (pos == 0) {
                     // bytes producer q sent to this leader for fill number i
                     auto contribution = [&](uint32_t q, uint32_t i) -> uint32_t {
-                        const int64_t u = cluster_id + static_cast<int64_t>(i / p.num_kb) * num_clusters;
-                        const uint32_t b_slice = Cfg::kSliceB * kBlockKBytes;
-                        return q / kGroup == pair ? a_bytes(u) + b_slice : b_slice;
+                        Unit un;
+                        bool shared;
+                        const int64_t it = static_cast<int64_t>(i / p.num_kb);
+                        cluster_units(it, un, shared);
+                        // every CTA of the cluster ran iteration it: the units differ by pair only
+                        const Unit uq = (q / kGroup == pair) ? un : unit_of(slot0 + it * nslots + q / kGroup, p);
+                        if (q / kGroup == pair)
+                            return a_bytes(uq) + (shared ? Cfg::kSliceBBytes : Cfg::kTileBBytes);
+                        return shared ? Cfg::kSliceBBytes : 0u;
                     };
-                    drain_cluster_loads<kStages, kCtas>(w, loaded_bar, contribution, n_issued, count_addr,
-                                                        done_addr);
+                    drain_cluster_loads<kStages, Cfg::kMaxCtas>(w, loaded_bar, contribution, n_issued, count_addr,
+                                                                done_addr);
                 }
             } else {
                 // Let every issued load land before the CTA can exit.
@@ -454,10 +482,12 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued_any = false;
+            const uint16_t all_mask = static_cast<uint16_t>((1u << ctas) - 1u);
             const uint16_t pair_mask = static_cast<uint16_t>(((1u << kGroup) - 1u) << lead);
             if (p.flags & kFlagStallMma) ok = w.wait(never_bar, 0u, kSiteStall);
-            for (int64_t u = cluster_id; ok && u < p.num_units; u += num_clusters) {
-                const uint32_t idesc = u >= p.tail_start ? kIdescHalf : kIdesc;
+            for (int64_t it = 0; ok && slot0 + it * nslots < p.num_units; ++it) {
+                const Unit un = unit_of(slot0 + it * nslots + pair, p);
+                const uint32_t idesc = un.half >= 0 ? kIdescHalf : kIdesc;
                 if (!w.wait(accempty_bar(acc), acc_phase ^ 1u, kSiteAccEmpty)) break;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * kAccCols;
@@ -478,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                                                    (kb | j) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
-                    ptx::mma_commit<kGroup>(empty_bar(stage), kAllMask);   // stage free for every CTA that writes it
+                    ptx::mma_commit<kGroup>(empty_bar(stage), all_mask);   // stage free for every CTA that writes it
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -505,79 +535,89 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t chunk_ctr = 0;
-        for (int64_t u = cluster_id; u < p.num_units; u += num_clusters) {
-            const Unit un = unit_of(u, p);
-            int64_t tmu, tn;
-            tile_coord(un.tile, p.tiles_m, p.tiles_n, p.group, tmu, tn);
-            const int64_t tm = tmu * kPairs + pair;
+        for (int64_t it = 0; slot0 + it * nslots < p.num_units; ++it) {
+            const Unit un = unit_of(slot0 + it * nslots + pair, p);
             const int n_chunks = (un.half >= 0 ? kTileM / 2 : kTileM) / kEpiBoxM;
             bool ok = w.wait(accfull_bar(acc), acc_phase, kSiteAccFull);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             __syncwarp();
             ptx::tc_fence_after_sync();
-            const int32_t m0 = static_cast<int32_t>(tm * kTileM + (un.half >= 0 ? un.half * (kTileM / 2) : 0));
-            // this warp's first output column
-            const int32_t nw = static_cast<int32_t>(tn * Cfg::kTileN + pos * Cfg::kRowsB) + 32 * quarter;
-            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + acc * kAccCols;
+            if (un.phantom) {
+                // nothing to store: hand the accumulator straight back
+                if (lane == 0) {
+                    if constexpr (kGroup == 2)
+                        ptx::mbar_arrive_remote(ptx::mapa_shared(accempty_bar(acc), lead));
+                    else
+                        ptx::mbar_arrive(accempty_bar(acc));
+                }
+            } else {
+                const int32_t m0 =
+                    static_cast<int32_t>(un.tm * kTileM + (un.half >= 0 ? un.half * (kTileM / 2) : 0));
+                // this warp's first output column
+                const int32_t nw = static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB) + 32 * quarter;
+                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + acc * kAccCols;
 #pragma unroll 1
-            for (int c = 0; c < n_chunks; ++c) {
-                uint32_t r0[32], r1[32];
-                ptx::tmem_ld_32x32b_x32(t_row + c * kEpiBoxM, r0);
-                ptx::tmem_ld_32x32b_x32(t_row + c * kEpiBoxM + 32, r1);
-                ptx::tmem_ld_wait(r0);
-                ptx::reg_dependency(r1);
-                if (c == n_chunks - 1) {
-                    // last read of this accumulator: hand it back to the MMA thread
-                    ptx::tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (kGroup == 2)
-                            ptx::mbar_arrive_remote(ptx::mapa_shared(accempty_bar(acc), lead));
-                        else
-                            ptx::mbar_arrive(accempty_bar(acc));
+                for (int c = 0; c < n_chunks; ++c) {
+                    uint32_t r0[32], r1[32];
+                    ptx::tmem_ld_32x32b_x32(t_row + c * kEpiBoxM, r0);
+                    ptx::tmem_ld_32x32b_x32(t_row + c * kEpiBoxM + 32, r1);
+                    ptx::tmem_ld_wait(r0);
+                    ptx::reg_dependency(r1);
+                    if (c == n_chunks - 1) {
+                        // last read of this accumulator: hand it back to the MMA thread
+                        ptx::tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if constexpr (kGroup == 2)
+                                ptx::mbar_arrive_remote(ptx::mapa_shared(accempty_bar(acc), lead));
+                            else
+                                ptx::mbar_arrive(accempty_bar(acc));
+                        }
                     }
-                }
-                uint32_t packed[32];
+                    uint32_t packed[32];
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    packed[j] = Kind::pack(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]), p.scale);
+                    for (int j = 0; j < 16; ++j)
+                        packed[j] =
+                            Kind::pack(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]), p.scale);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    packed[16 + j] =
-                        Kind::pack(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]), p.scale);
-                const int32_t mc = m0 + c * kEpiBoxM;
-                if (tma_store && mc < p.m_tma) {
-                    const uint32_t buf = s_epi + (ew * kEpiBufs + (chunk_ctr & 1u)) * kEpiBufBytes;
-                    if (lane == 0) ptx::bulk_wait_group_read<kEpiBufs - 1>();   // buffer's previous store has read it
-                    __syncwarp();
-                    // row = lane (one output column n), 8 chunks of 16 B, 128-byte swizzle
+                    for (int j = 0; j < 16; ++j)
+                        packed[16 + j] =
+                            Kind::pack(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]), p.scale);
+                    const int32_t mc = m0 + c * kEpiBoxM;
+                    if (tma_store && mc < p.m_tma) {
+                        const uint32_t buf = s_epi + (ew * kEpiBufs + (chunk_ctr & 1u)) * kEpiBufBytes;
+                        if (lane == 0) ptx::bulk_wait_group_read<kEpiBufs - 1>();   // buffer's previous store has read it
+                        __syncwarp();
+                        // row = lane (one output column n), 8 chunks of 16 B, 128-byte swizzle
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t addr = buf + lane * 128 + ((j ^ (lane & 7)) << 4);
-                        ptx::st_shared_v4(addr, packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
-                                          packed[4 * j + 3]);
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t addr = buf + lane * 128 + ((j ^ (lane & 7)) << 4);
+                            ptx::st_shared_v4(addr, packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                                              packed[4 * j + 3]);
+                        }
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            ptx::tma_store_2d(&p.tmap_c, buf, mc, nw);   // clipped at m_tma and N
+                            ptx::bulk_commit_group();
+                        }
+                        ++chunk_ctr;
                     }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        ptx::tma_store_2d(&p.tmap_c, buf, mc, nw);   // clipped at m_tma and N
-                        ptx::bulk_commit_group();
-                    }
-                    ++chunk_ctr;
-                }
-                if (mc + kEpiBoxM > p.m_tma) {
-                    // Direct stores with bounds: rows m_tma <= m < M (the ragged tail TMA cannot
-                    // clip at element granularity, or all of C when C is not TMA-addressable).
-                    const int64_t n = nw + lane;
-                    const int32_t lo = mc > p.m_tma ? mc : p.m_tma;
-                    if (n < p.N) {
-                        uint16_t *col = static_cast<uint16_t *>(p.c_ptr) + n * p.ldc;
+                    if (mc + kEpiBoxM > p.m_tma) {
+                        // Direct stores with bounds: rows m_tma <= m < M (the ragged tail TMA cannot
+                        // clip at element granularity, or all of C when C is not TMA-addressable).
+                        const int64_t n = nw + lane;
+                        const int32_t lo = mc > p.m_tma ? mc : p.m_tma;
+                        if (n < p.N) {
+                            uint16_t *col = static_cast<uint16_t *>(p.c_ptr) + n * p.ldc;
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int32_t m = mc + 2 * j;
-                            if (m >= lo && m < p.M) col[m] = static_cast<uint16_t>(packed[j] & 0xFFFFu);
-                            if (m + 1 >= lo && m + 1 < p.M) col[m + 1] = static_cast<uint16_t>(packed[j] >> 16);
+                            for (int j = 0; j < 32; ++j) {
+                                const int32_t m = mc + 2 * j;
+                                if (m >= lo && m < p.M) col[m] = static_cast<uint16_t>(packed[j] & 0xFFFFu);
+                                if (m + 1 >= lo && m + 1 < p.M)
+                                    col[m + 1] = static_cast<uint16_t>(packed[j] >> 16);
+                            }
                         }
                     }
                 }
@@ -593,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     __syncwarp();                // .aligned barriers below need converged warps
     ptx::tc_fence_before_sync();
-    if constexpr (kCtas > 1)
+    if constexpr (kGroup == 2)
         ptx::cluster_sync();     // no CTA leaves while another may still touch its shared memory
     else
         __syncthreads();

@@ -166,10 +166,12 @@ void gemm_set_wait_limit_ns(uint64_t limit_ns);
 void gemm_debug_inject_stall(int mode);
 
 /*
- * Test hook: 0 (default) lets the library choose the cluster shape per call;
- * 1 forces one CTA per 128 x 256 tile, 2 a CTA pair per 256 x 256 tile, 4 two
- * pairs per 512 x 256 unit sharing their B rows through TMA multicast.
- * Returns 0, or -1 for other values.
+ * Test hook: 0 (default) lets the library choose the tile shape per call;
+ * 1 forces one CTA per 128 x 256 tile, 2 a CTA pair per 256 x 256 tile in
+ * 2-CTA clusters, 4 CTA pairs launched with a preferred cluster size of 4
+ * (two pairs sharing B rows through TMA multicast where the hardware places
+ * them together).  Returns 0, or -1 for other
+ * values.
  */
 int gemm_debug_force_cta_group(int group);
 
