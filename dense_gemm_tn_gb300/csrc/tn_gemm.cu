@@ -10,6 +10,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "tn_gemm.h"
 #include "tn_gemm_kernel.cuh"
@@ -39,6 +40,14 @@ struct DeviceState {
     int max_clusters[2][3] = {};      // co-resident clusters of the kernel's own size (0 = not queried yet)
     void *workspace = nullptr;
     size_t workspace_bytes = 0;
+    // Split-K partial sums of the last wave, one buffer per stream (calls on
+    // one stream are ordered, so they may share it): [tickets | partials].
+    struct Split {
+        void *ptr = nullptr;
+        size_t bytes = 0, ticket_bytes = 0;
+    };
+    std::unordered_map<cudaStream_t, Split> split;
+    unsigned long long epoch = 0;
 };
 
 std::mutex g_mutex;
@@ -111,6 +120,36 @@ gemm_status_t ensure_workspace(DeviceState &d, size_t bytes)
     return GEMM_OK;
 }
 
+// The stream's split-K buffer with room for `tickets` ticket words and
+// `partial_bytes` of partial sums; grown (and its tickets zeroed) on demand.
+gemm_status_t split_workspace(DeviceState &d, cudaStream_t stream, size_t tickets, size_t partial_bytes,
+                              unsigned long long **ticket_ptr, float **partial_ptr)
+{
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState::Split &w = d.split[stream];
+    const size_t tb = (tickets * sizeof(unsigned long long) + 255) & ~size_t(255);
+    if (w.ticket_bytes < tb || w.bytes < w.ticket_bytes + partial_bytes) {
+        const size_t new_tb = tb > w.ticket_bytes ? tb : w.ticket_bytes;
+        const size_t need = new_tb + partial_bytes;
+        if (w.ptr) cudaFree(w.ptr);      // synchronises the device: earlier users are done
+        w.ptr = nullptr;
+        w.bytes = w.ticket_bytes = 0;
+        cudaError_t e = cudaMalloc(&w.ptr, need);
+        if (e != cudaSuccess) {
+            w.ptr = nullptr;
+            return fail(GEMM_ERR_CUDA, "cudaMalloc(%zu) for split-K partials: %s", need, cudaGetErrorString(e));
+        }
+        // tickets hold 2*epoch+1 of past launches; zero is older than every epoch
+        e = cudaMemsetAsync(w.ptr, 0, new_tb, stream);
+        if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "clearing split-K tickets: %s", cudaGetErrorString(e));
+        w.bytes = need;
+        w.ticket_bytes = new_tb;
+    }
+    *ticket_ptr = static_cast<unsigned long long *>(w.ptr);
+    *partial_ptr = reinterpret_cast<float *>(static_cast<uint8_t *>(w.ptr) + w.ticket_bytes);
+    return GEMM_OK;
+}
+
 gemm_status_t encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, uint64_t inner,
                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                         const char *what)
@@ -165,7 +204,8 @@ int launch_grid(int64_t work, int cap)
 // the hardware then joins two pairs into one cluster wherever four CTAs fit
 // together, and the kernel shares B rows between them.
 template <class Kind, int G>
-gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, bool quad, cudaStream_t stream)
+gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, bool quad, bool allow_alloc,
+                     cudaStream_t stream)
 {
     using Cfg = tn::TileCfg<G>;
     auto kernel = tn::tn_gemm_kernel<Kind, G>;
@@ -217,19 +257,36 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     }
     cfg.gridDim = dim3(G * clusters, 1, 1);
     // A last wave that fills at most half of the slots is run as twice as
-    // many half-width units, so every slot finishes at about the same time.
+    // many half-length units, so every slot finishes at about the same time:
+    // each of those tiles is split into two halves of its k blocks whose
+    // partial sums meet in a per-stream workspace, or -- without the
+    // workspace, or with few k blocks -- into two halves of its m range.
     const int waves = prm.num_tiles / clusters, rem = prm.num_tiles % clusters;
+    prm.tail_mode = tn::kTailNone;
+    prm.tail_start = prm.num_tiles;
+    prm.num_units = prm.num_tiles;
     if (waves >= 1 && rem > 0 && 2 * rem <= clusters) {
         prm.tail_start = waves * clusters;
         prm.num_units = prm.tail_start + 2 * rem;
-    } else {
-        prm.tail_start = prm.num_tiles;
-        prm.num_units = prm.num_tiles;
+        prm.tail_mode = tn::kTailHalfM;
+        if (allow_alloc && prm.num_kb >= 4) {
+            const size_t partial = size_t(rem) * 2 * G * Cfg::kRowsB * tn::kTileM * sizeof(float);
+            unsigned long long *tickets = nullptr;
+            float *partials = nullptr;
+            gemm_status_t st = split_workspace(dev, stream, size_t(rem) * G, partial, &tickets, &partials);
+            if (st != GEMM_OK) return st;
+            prm.tail_mode = tn::kTailSplitK;
+            prm.kb_half = (prm.num_kb + 1) / 2;
+            prm.split_ws = partials;
+            prm.split_tickets = tickets;
+            std::lock_guard<std::mutex> lock(g_mutex);
+            prm.epoch = ++dev.epoch;
+        }
     }
     snprintf(t_last_launch, sizeof(t_last_launch),
-             "%s: ctas_per_cluster=%d%s grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d", name, G,
-             quad && G == 2 ? " (preferred 4)" : "", G * clusters, clusters, slots, prm.num_tiles, prm.num_units,
-             prm.tail_start);
+             "%s: ctas_per_cluster=%d%s grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d tail_mode=%d",
+             name, G, quad && G == 2 ? " (preferred 4)" : "", G * clusters, clusters, slots, prm.num_tiles,
+             prm.num_units, prm.tail_start, prm.tail_mode);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));
     return GEMM_OK;
@@ -237,7 +294,8 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
 
 template <class Kind>
 gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
-                       const void *B, int64_t ldb, void *C, int64_t ldc, float scale, cudaStream_t stream)
+                       const void *B, int64_t ldb, void *C, int64_t ldc, float scale, cudaStream_t stream,
+                       bool allow_alloc = true)
 {
     constexpr int64_t esz = Kind::kElemBytes;
     const int64_t kmin = K > 1 ? K : 1;
@@ -359,8 +417,8 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     prm.flags = (tma_c ? tn::kFlagTmaStore : 0u) | stall_flags(g_inject_stall.load());
     prm.wait_limit_ns = g_wait_limit_ns.load();
 
-    if (cta_group == 2) return launch<Kind, 2>(name, prm, *dev, quad, stream);
-    return launch<Kind, 1>(name, prm, *dev, false, stream);
+    if (cta_group == 2) return launch<Kind, 2>(name, prm, *dev, quad, allow_alloc, stream);
+    return launch<Kind, 1>(name, prm, *dev, false, allow_alloc, stream);
 }
 
 }  // namespace
@@ -422,6 +480,9 @@ void gemm_release_workspace(void)
     if (d.workspace) cudaFree(d.workspace);
     d.workspace = nullptr;
     d.workspace_bytes = 0;
+    for (auto &kv : d.split)
+        if (kv.second.ptr) cudaFree(kv.second.ptr);
+    d.split.clear();
 }
 
 int gemm_tile_coord(int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t id, int64_t *tile_m, int64_t *tile_n)
@@ -508,12 +569,16 @@ extern "C" gemm_status_t gemm_f16_tn_noalloc(int64_t M, int64_t N, int64_t K, co
                        M > kMaxDim || N > kMaxDim || K > kMaxDim || lda > kMaxDim || ldb > kMaxDim ||
                        ldc > kMaxDim || !A || !B || !C || reinterpret_cast<uintptr_t>(A) % esz ||
                        reinterpret_cast<uintptr_t>(B) % esz;
-    if (plain) return gemm_f16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream);
+    if (plain)
+        return run_gemm<tn::KindF16>(name, M, N, K, A, lda, B, ldb, C, ldc, 1.0f,
+                                     static_cast<cudaStream_t>(stream), false);
 
     const bool k_aligned = (K * esz) % 16 == 0;
     const bool repack_a = !k_aligned || (lda * esz) % 16 != 0 || reinterpret_cast<uintptr_t>(A) % 16 != 0;
     const bool repack_b = !k_aligned || (ldb * esz) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0;
-    if (!repack_a && !repack_b) return gemm_f16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream);
+    if (!repack_a && !repack_b)
+        return run_gemm<tn::KindF16>(name, M, N, K, A, lda, B, ldb, C, ldc, 1.0f,
+                                     static_cast<cudaStream_t>(stream), false);
 
     const int64_t ldp = (K + 7) / 8 * 8;
     const size_t bytes_a = repack_a ? ((size_t(M) * ldp * esz + 255) & ~size_t(255)) : 0;
@@ -549,7 +614,7 @@ extern "C" gemm_status_t gemm_f16_tn_noalloc(int64_t M, int64_t N, int64_t K, co
     // When K is not a multiple of 8 both operands were repacked with zeros in
     // columns K..ldp-1; those extra products are +0 and leave every sum as is.
     const int64_t k_use = k_aligned ? K : ldp;
-    st = gemm_f16_tn(M, N, k_use, a_use, lda_use, b_use, ldb_use, C, ldc, stream);
+    st = run_gemm<tn::KindF16>(name, M, N, k_use, a_use, lda_use, b_use, ldb_use, C, ldc, 1.0f, s, false);
     if (st != GEMM_OK) return st;
     return GEMM_OK;
 }

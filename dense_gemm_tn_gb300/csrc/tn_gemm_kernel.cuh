@@ -78,9 +78,14 @@ struct TileCfg {
     static constexpr int kSmemRing = kStages * kStageBytes;
     // loaded[S], empty[S], accfull[2], accempty[2], drain, never
     static constexpr int kNumBarriers = 2 * kStages + 6;
-    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kSmemRing + kSmemEpi + kNumBarriers * 8 + 16;
+    static constexpr int kSmemBytes = 1024 /* alignment slack */ + kSmemRing + kSmemEpi + kNumBarriers * 8 + 32;
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB shared memory of one CTA");
 };
+
+// How the tiles of a partly filled last wave are cut into two units each.
+constexpr int32_t kTailNone = 0;
+constexpr int32_t kTailHalfM = 1;    // two halves of the tile's m range (MMA N = 128)
+constexpr int32_t kTailSplitK = 2;   // two halves of the k blocks; partial sums meet in a workspace
 
 constexpr uint32_t kFlagTmaStore = 1u;      // C rows m < m_tma are written with TMA stores
 // Test hooks: the named thread first waits on a barrier nobody arrives on, so
@@ -110,9 +115,13 @@ struct KernelParams {
     int32_t m_tma;           // rows m < m_tma are written by TMA stores (a multiple of 8, or 0)
     int32_t tiles_m, tiles_n, num_tiles, num_kb, group;
     // Work units: tiles [0, tail_start) are whole units; each later tile is two
-    // units covering one half of its m range (so a last, partly filled wave of
-    // tiles becomes a full wave of half-length units).  num_units counts both.
-    int32_t tail_start, num_units;
+    // units (so a last, partly filled wave of tiles becomes a full wave of
+    // half-length units), cut as tail_mode says.  num_units counts both kinds.
+    int32_t tail_start, num_units, tail_mode;
+    int32_t kb_half;         // k blocks of each split-K unit: ceil(num_kb / 2), padded with zeros
+    float *split_ws;         // split-K partials: [tail tile][k half][CTA of pair][128 n][256 m] fp32
+    unsigned long long *split_tickets;   // [tail tile][CTA of pair]: 2*epoch+1 once one half arrived
+    unsigned long long epoch;            // distinct per launch that uses split_ws
     float scale;             // epilogue multiplier (F8: scale_a * scale_b)
     uint32_t flags;
     uint64_t wait_limit_ns;
@@ -138,25 +147,59 @@ __host__ __device__ __forceinline__ void tile_coord(int64_t id, int64_t tiles_m,
     tn = in_group / rows;
 }
 
-// A work unit: a tile, or one m half of a tile of the split last wave.
+// A work unit: a tile, or one half of a tile of the split last wave.
 struct Unit {
-    int64_t tm, tn;          // tile coordinates
-    int32_t half;            // -1: the whole tile; 0 / 1: that half of its m range
+    int64_t tile, tm, tn;    // tile id and coordinates
+    int32_t half;            // -1: the whole m range; 0 / 1: that half of it (kTailHalfM)
+    int32_t khalf;           // -1: all k blocks; 0 / 1: that half of them (kTailSplitK)
+    int32_t kb0, nkb;        // the unit's k blocks
     bool phantom;            // no such unit: loads out of bounds, computes zeros, stores nothing
 };
 
 __device__ __forceinline__ Unit unit_of(int64_t u, const KernelParams &p)
 {
-    Unit r{0, 0, -1, u >= p.num_units};
+    Unit r{u, 0, 0, -1, -1, 0, p.num_kb, u >= p.num_units};
     if (r.phantom) return r;
-    int64_t tile = u;
     if (u >= p.tail_start) {
         const int64_t v = u - p.tail_start;
-        tile = p.tail_start + v / 2;
-        r.half = static_cast<int32_t>(v & 1);
+        r.tile = p.tail_start + v / 2;
+        if (p.tail_mode == kTailSplitK) {
+            r.khalf = static_cast<int32_t>(v & 1);
+            r.kb0 = r.khalf * p.kb_half;
+            r.nkb = p.kb_half;
+        } else {
+            r.half = static_cast<int32_t>(v & 1);
+        }
     }
-    tile_coord(tile, p.tiles_m, p.tiles_n, p.group, r.tm, r.tn);
+    tile_coord(r.tile, p.tiles_m, p.tiles_n, p.group, r.tm, r.tn);
     return r;
+}
+
+// The units a work slot walks.  Slot s takes units s, s + nslots, ... of the
+// whole tiles; if the last wave was split, slots s < 2 * (tiles left over)
+// first take split unit tail_start + s, so its combine (split-K) overlaps the
+// slot's later tiles instead of ending the launch.  Slots come in even-aligned
+// pairs that either both have a split unit or both do not.
+__device__ __forceinline__ bool slot_has_tail(int64_t slot, const KernelParams &p)
+{
+    return p.tail_mode != kTailNone && slot < p.num_units - p.tail_start;
+}
+
+__device__ __forceinline__ int64_t slot_iters(int64_t slot, int64_t nslots, const KernelParams &p)
+{
+    const int64_t whole = p.tail_start > slot ? (p.tail_start - slot + nslots - 1) / nslots : 0;
+    return whole + (slot_has_tail(slot, p) ? 1 : 0);
+}
+
+// Unit index of step `it` of slot `slot` (>= num_units: none, a phantom).
+__device__ __forceinline__ int64_t slot_unit(int64_t slot, int64_t it, int64_t nslots, const KernelParams &p)
+{
+    if (slot_has_tail(slot, p)) {
+        if (it == 0) return p.tail_start + slot;
+        --it;
+    }
+    const int64_t u = slot + it * nslots;
+    return u < p.tail_start ? u : p.num_units;   // past the whole tiles: none
 }
 
 // ------------------------------------------------------------------ waits
@@ -376,16 +419,20 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     // Iteration `it` of this cluster: the units of its pairs, and whether the
     // two pairs share B rows (both units exist and lie on the same n tile).
+    // A phantom unit takes its partner's k-block count, so both pairs of a
+    // cluster issue the same number of fills (they share stage barriers).
     auto cluster_units = [&](int64_t it, Unit &mine, bool &shared) {
-        const int64_t u0 = slot0 + it * nslots;
-        mine = unit_of(u0 + pair, p);
+        mine = unit_of(slot_unit(slot0 + pair, it, nslots, p), p);
         shared = false;
         if (pairs == 2) {
-            const Unit e = pair == 0 ? mine : unit_of(u0, p);
-            const Unit o = pair == 1 ? mine : unit_of(u0 + 1, p);
-            shared = !e.phantom && !o.phantom && e.tn == o.tn;
+            const Unit e = pair == 0 ? mine : unit_of(slot_unit(slot0, it, nslots, p), p);
+            const Unit o = pair == 1 ? mine : unit_of(slot_unit(slot0 + 1, it, nslots, p), p);
+            if (mine.phantom) mine.nkb = e.nkb;
+            shared = !e.phantom && !o.phantom && e.tn == o.tn && e.khalf < 0;
         }
     };
+    // Steps of this cluster: those of its first slot (the second never has more).
+    const int64_t iters = slot_iters(slot0, nslots, p);
     auto a_bytes = [&](const Unit &un) -> uint32_t {
         return un.half >= 0 ? Cfg::kTileABytes / 2 : Cfg::kTileABytes;
     };
@@ -403,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             bool ok = true;
             const uint32_t stall = rank == 0 ? kFlagStallProducer0 : (rank == 1 ? kFlagStallProducer1 : 0u);
             if (p.flags & stall) ok = w.wait(never_bar, 0u, kSiteStall);
-            for (int64_t it = 0; ok && slot0 + it * nslots < p.num_units; ++it) {
+            for (int64_t it = 0; ok && it < iters; ++it) {
                 Unit un;
                 bool shared;
                 cluster_units(it, un, shared);
@@ -418,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 const int32_t nb = un.phantom ? p.N : static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB);
                 uint16_t mcast = 0;
                 for (uint32_t q = 0; q < pairs; ++q) mcast |= static_cast<uint16_t>(1u << (q * kGroup + pos));
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kb = un.kb0; kb < un.kb0 + un.nkb; ++kb) {
                     if (!w.wait(empty_bar(stage), phase ^ 1u, kSiteEmpty)) {
                         ok = false;
                         break;
@@ -454,10 +501,15 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     auto contribution = [&](uint32_t q, uint32_t i) -> uint32_t {
                         Unit un;
                         bool shared;
-                        const int64_t it = static_cast<int64_t>(i / p.num_kb);
+                        // a split-K first step issues kb_half fills, every other step num_kb
+                        const uint32_t first = (p.tail_mode == kTailSplitK && slot_has_tail(slot0, p))
+                                                   ? static_cast<uint32_t>(p.kb_half)
+                                                   : static_cast<uint32_t>(p.num_kb);
+                        const int64_t it = i < first ? 0 : 1 + static_cast<int64_t>((i - first) / p.num_kb);
                         cluster_units(it, un, shared);
-                        // every CTA of the cluster ran iteration it: the units differ by pair only
-                        const Unit uq = (q / kGroup == pair) ? un : unit_of(slot0 + it * nslots + q / kGroup, p);
+                        // every CTA of the cluster ran step it: the units differ by pair only
+                        const Unit uq =
+                            q / kGroup == pair ? un : unit_of(slot_unit(slot0 + q / kGroup, it, nslots, p), p);
                         if (q / kGroup == pair)
                             return a_bytes(uq) + (shared ? Cfg::kSliceBBytes : Cfg::kTileBBytes);
                         return shared ? Cfg::kSliceBBytes : 0u;
@@ -485,13 +537,15 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             const uint16_t all_mask = static_cast<uint16_t>((1u << ctas) - 1u);
             const uint16_t pair_mask = static_cast<uint16_t>(((1u << kGroup) - 1u) << lead);
             if (p.flags & kFlagStallMma) ok = w.wait(never_bar, 0u, kSiteStall);
-            for (int64_t it = 0; ok && slot0 + it * nslots < p.num_units; ++it) {
-                const Unit un = unit_of(slot0 + it * nslots + pair, p);
+            for (int64_t it = 0; ok && it < iters; ++it) {
+                Unit un;
+                bool shared;
+                cluster_units(it, un, shared);
                 const uint32_t idesc = un.half >= 0 ? kIdescHalf : kIdesc;
                 if (!w.wait(accempty_bar(acc), acc_phase ^ 1u, kSiteAccEmpty)) break;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * kAccCols;
-                for (int kb = 0; kb < p.num_kb; ++kb) {
+                for (int kk = 0; kk < un.nkb; ++kk) {
                     if (!w.wait(loaded_bar(stage), phase, kSiteLoaded)) {
                         ok = false;
                         break;
@@ -505,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     for (int j = 0; j < kBlockKBytes / kMmaKBytes; ++j) {
                         // +32 bytes along K inside the 128-byte swizzle span = +2 in the address field
                         Kind::template mma<kGroup>(d_tmem, desc_b + 2u * j, desc_a + 2u * j, idesc,
-                                                   (kb | j) != 0 ? 1u : 0u);
+                                                   (kk | j) != 0 ? 1u : 0u);
                     }
                     issued_any = true;
                     ptx::mma_commit<kGroup>(empty_bar(stage), all_mask);   // stage free for every CTA that writes it
@@ -531,95 +585,148 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         // ------------------------------------------------ epilogue (warps 2..5, every CTA)
         const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31 are this warp's
         const int ew = warp - 2;
+        const int row = 32 * quarter + lane;      // this thread's TMEM lane = output column within the CTA
         const bool tma_store = (p.flags & kFlagTmaStore) != 0;
+        volatile uint32_t *second_flag = tmem_holder + 4;   // split-K: this CTA's half came second
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t chunk_ctr = 0;
-        for (int64_t it = 0; slot0 + it * nslots < p.num_units; ++it) {
-            const Unit un = unit_of(slot0 + it * nslots + pair, p);
-            const int n_chunks = (un.half >= 0 ? kTileM / 2 : kTileM) / kEpiBoxM;
+
+        // Hands the accumulator back to the MMA thread (after the last TMEM read).
+        auto release_acc = [&]() {
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (kGroup == 2)
+                    ptx::mbar_arrive_remote(ptx::mapa_shared(accempty_bar(acc), lead));
+                else
+                    ptx::mbar_arrive(accempty_bar(acc));
+            }
+        };
+        // Reads 64 accumulator columns (this thread's lane) starting at column `col`.
+        auto load_chunk = [&](uint32_t t_row, int col, float (&v)[64]) {
+            uint32_t r0[32], r1[32];
+            ptx::tmem_ld_32x32b_x32(t_row + col, r0);
+            ptx::tmem_ld_32x32b_x32(t_row + col + 32, r1);
+            ptx::tmem_ld_wait(r0);
+            ptx::reg_dependency(r1);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                v[j] = __uint_as_float(r0[j]);
+                v[32 + j] = __uint_as_float(r1[j]);
+            }
+        };
+        // Converts 64 values of rows mc .. mc+63 of output column (nw + lane) and
+        // stores them: TMA store for m < m_tma, direct stores for the rest.
+        auto store_chunk = [&](const float (&v)[64], int32_t mc, int32_t nw) {
+            uint32_t packed[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) packed[j] = Kind::pack(v[2 * j], v[2 * j + 1], p.scale);
+            if (tma_store && mc < p.m_tma) {
+                const uint32_t buf = s_epi + (ew * kEpiBufs + (chunk_ctr & 1u)) * kEpiBufBytes;
+                if (lane == 0) ptx::bulk_wait_group_read<kEpiBufs - 1>();   // buffer's previous store has read it
+                __syncwarp();
+                // row = lane (one output column n), 8 chunks of 16 B, 128-byte swizzle
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t addr = buf + lane * 128 + ((j ^ (lane & 7)) << 4);
+                    ptx::st_shared_v4(addr, packed[4 * j], packed[4 * j + 1], packed[4 * j + 2], packed[4 * j + 3]);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    ptx::tma_store_2d(&p.tmap_c, buf, mc, nw);   // clipped at m_tma and N
+                    ptx::bulk_commit_group();
+                }
+                ++chunk_ctr;
+            }
+            if (mc + kEpiBoxM > p.m_tma) {
+                // Direct stores with bounds: rows m_tma <= m < M (the ragged tail TMA cannot
+                // clip at element granularity, or all of C when C is not TMA-addressable).
+                const int64_t n = nw + lane;
+                const int32_t lo = mc > p.m_tma ? mc : p.m_tma;
+                if (n < p.N) {
+                    uint16_t *col = static_cast<uint16_t *>(p.c_ptr) + n * p.ldc;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int32_t m = mc + 2 * j;
+                        if (m >= lo && m < p.M) col[m] = static_cast<uint16_t>(packed[j] & 0xFFFFu);
+                        if (m + 1 >= lo && m + 1 < p.M) col[m + 1] = static_cast<uint16_t>(packed[j] >> 16);
+                    }
+                }
+            }
+        };
+
+        for (int64_t it = 0; it < iters; ++it) {
+            Unit un;
+            bool shared;
+            cluster_units(it, un, shared);
             bool ok = w.wait(accfull_bar(acc), acc_phase, kSiteAccFull);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             __syncwarp();
             ptx::tc_fence_after_sync();
+            const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + acc * kAccCols;
+            const int32_t m0 = static_cast<int32_t>(un.tm * kTileM + (un.half >= 0 ? un.half * (kTileM / 2) : 0));
+            // this warp's first output column
+            const int32_t nw = static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB) + 32 * quarter;
             if (un.phantom) {
-                // nothing to store: hand the accumulator straight back
-                if (lane == 0) {
-                    if constexpr (kGroup == 2)
-                        ptx::mbar_arrive_remote(ptx::mapa_shared(accempty_bar(acc), lead));
-                    else
-                        ptx::mbar_arrive(accempty_bar(acc));
+                release_acc();   // nothing to store
+            } else if (un.khalf >= 0) {
+                // Split-K half: store this half's FP32 partial, then take the tile's
+                // ticket.  The half that comes second adds the other half's partial
+                // (fp32 addition commutes, so either order gives the same C) and
+                // stores C; no CTA ever waits for another.
+                const int64_t t = un.tile - p.tail_start;
+                const int64_t span = static_cast<int64_t>(Cfg::kRowsB) * kTileM;
+                float *mine = p.split_ws + ((t * 2 + un.khalf) * kGroup + pos) * span + row * kTileM;
+                const float *other = p.split_ws + ((t * 2 + (un.khalf ^ 1)) * kGroup + pos) * span + row * kTileM;
+#pragma unroll 1
+                for (int c = 0; c < kTileM / kEpiBoxM; ++c) {
+                    float v[64];
+                    load_chunk(t_row, c * kEpiBoxM, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        reinterpret_cast<float4 *>(mine + c * kEpiBoxM)[j] =
+                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
+                __threadfence();
+                ptx::named_barrier_sync(1, kEpiWarps * 32);
+                if (warp == 2 && lane == 0) {
+                    const unsigned long long mark = 2ull * p.epoch + 1ull;
+                    const unsigned long long old = atomicMax(p.split_tickets + t * kGroup + pos, mark);
+                    *second_flag = old == mark ? 1u : 0u;
+                    __threadfence();
+                }
+                ptx::named_barrier_sync(1, kEpiWarps * 32);
+                if (*second_flag == 0u) {
+                    release_acc();
+                } else {
+                    __threadfence();
+#pragma unroll 1
+                    for (int c = 0; c < kTileM / kEpiBoxM; ++c) {
+                        float v[64];
+                        load_chunk(t_row, c * kEpiBoxM, v);
+                        if (c == kTileM / kEpiBoxM - 1) release_acc();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float4 o = ptx::ld_global_cg_v4(other + c * kEpiBoxM + 4 * j);
+                            v[4 * j] += o.x;
+                            v[4 * j + 1] += o.y;
+                            v[4 * j + 2] += o.z;
+                            v[4 * j + 3] += o.w;
+                        }
+                        store_chunk(v, m0 + c * kEpiBoxM, nw);
+                    }
                 }
             } else {
-                const int32_t m0 =
-                    static_cast<int32_t>(un.tm * kTileM + (un.half >= 0 ? un.half * (kTileM / 2) : 0));
-                // this warp's first output column
-                const int32_t nw = static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB) + 32 * quarter;
-                const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + acc * kAccCols;
+                const int n_chunks = (un.half >= 0 ? kTileM / 2 : kTileM) / kEpiBoxM;
 #pragma unroll 1
                 for (int c = 0; c < n_chunks; ++c) {
-                    uint32_t r0[32], r1[32];
-                    ptx::tmem_ld_32x32b_x32(t_row + c * kEpiBoxM, r0);
-                    ptx::tmem_ld_32x32b_x32(t_row + c * kEpiBoxM + 32, r1);
-                    ptx::tmem_ld_wait(r0);
-                    ptx::reg_dependency(r1);
-                    if (c == n_chunks - 1) {
-                        // last read of this accumulator: hand it back to the MMA thread
-                        ptx::tc_fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) {
-                            if constexpr (kGroup == 2)
-                                ptx::mbar_arrive_remote(ptx::mapa_shared(accempty_bar(acc), lead));
-                            else
-                                ptx::mbar_arrive(accempty_bar(acc));
-                        }
-                    }
-                    uint32_t packed[32];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        packed[j] =
-                            Kind::pack(__uint_as_float(r0[2 * j]), __uint_as_float(r0[2 * j + 1]), p.scale);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        packed[16 + j] =
-                            Kind::pack(__uint_as_float(r1[2 * j]), __uint_as_float(r1[2 * j + 1]), p.scale);
-                    const int32_t mc = m0 + c * kEpiBoxM;
-                    if (tma_store && mc < p.m_tma) {
-                        const uint32_t buf = s_epi + (ew * kEpiBufs + (chunk_ctr & 1u)) * kEpiBufBytes;
-                        if (lane == 0) ptx::bulk_wait_group_read<kEpiBufs - 1>();   // buffer's previous store has read it
-                        __syncwarp();
-                        // row = lane (one output column n), 8 chunks of 16 B, 128-byte swizzle
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const uint32_t addr = buf + lane * 128 + ((j ^ (lane & 7)) << 4);
-                            ptx::st_shared_v4(addr, packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
-                                              packed[4 * j + 3]);
-                        }
-                        ptx::fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            ptx::tma_store_2d(&p.tmap_c, buf, mc, nw);   // clipped at m_tma and N
-                            ptx::bulk_commit_group();
-                        }
-                        ++chunk_ctr;
-                    }
-                    if (mc + kEpiBoxM > p.m_tma) {
-                        // Direct stores with bounds: rows m_tma <= m < M (the ragged tail TMA cannot
-                        // clip at element granularity, or all of C when C is not TMA-addressable).
-                        const int64_t n = nw + lane;
-                        const int32_t lo = mc > p.m_tma ? mc : p.m_tma;
-                        if (n < p.N) {
-                            uint16_t *col = static_cast<uint16_t *>(p.c_ptr) + n * p.ldc;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                const int32_t m = mc + 2 * j;
-                                if (m >= lo && m < p.M) col[m] = static_cast<uint16_t>(packed[j] & 0xFFFFu);
-                                if (m + 1 >= lo && m + 1 < p.M)
-                                    col[m + 1] = static_cast<uint16_t>(packed[j] >> 16);
-                            }
-                        }
-                    }
+                    float v[64];
+                    load_chunk(t_row, c * kEpiBoxM, v);
+                    if (c == n_chunks - 1) release_acc();   // last read of this accumulator
+                    store_chunk(v, m0 + c * kEpiBoxM, nw);
                 }
             }
             if (++acc == 2) {

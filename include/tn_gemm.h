@@ -36,6 +36,11 @@
  *     a multiple of 16 bytes are first copied into a library-owned, lazily
  *     grown device workspace (one per device) with a padded stride.  Calls
  *     that take this path must not run concurrently on different streams.
+ *   - When the tiles of a launch end in a partly filled wave, each leftover
+ *     tile is computed as two halves of its k range whose FP32 partial sums
+ *     meet in a library-owned buffer kept per (device, stream), allocated on
+ *     first need (about 0.5 MiB per leftover tile).  The sum is taken in a
+ *     fixed way, so results do not depend on timing.
  *   - Thread safety: every entry point may be called from several host
  *     threads; the per-device state is guarded internally.
  */
@@ -131,7 +136,8 @@ const char *gemm_last_error(void);
  */
 gemm_status_t gemm_poll_device_status(void *stream);
 
-/* Frees the current device's repack workspace (synchronises the device). */
+/* Frees the current device's workspaces: the repack copy and the per-stream
+ * split-K partial sums (synchronises the device). */
 void gemm_release_workspace(void);
 
 /*

@@ -279,3 +279,35 @@ def test_tail_wave_split_into_half_units(force_group, cta_group, M, N, K):
     # with the measured 76 pair / 152 single slots of a GB300 these shapes split
     if clusters in (76, 152) and cta_group != 4:
         assert split
+
+
+@pytest.mark.parametrize("cta_group,M,N,K", [
+    (2, 8192, 8192, 512),      # 1024 pair tiles: the 36 of the last wave split along K
+    (2, 2000, 3000, 520),      # 96 pair tiles, odd k-block count (zero-padded half)
+    (1, 2000, 2560, 700),      # one-CTA tiles
+    (4, 2000, 3000, 520),      # preferred 4-CTA clusters
+])
+def test_split_k_tail_exact_and_deterministic(force_group, cta_group, M, N, K):
+    force_group(cta_group)
+    A = synth.sign_fp16(M * K, 88 + M)
+    B = synth.sign_fp16(N * K, 89 + N)
+    got = run_f16(M, N, K, A, K, B, K)
+    rec = _launch_record()
+    if rec["clusters"] in (76, 152):
+        assert rec["tail_mode"] == 2, rec
+    if M * N <= 8_000_000:
+        Cref, _, _ = oracle.gemm_f16_tn(M, N, K, A, K, B, K)
+        assert np.array_equal(got, oracle.c_as_nm(Cref, M, N, M))
+    else:
+        mi, ni = sample_positions(M, N, 20000, seed=K)
+        c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
+        assert np.array_equal(got[ni, mi], c)
+    # Gaussian inputs: within tolerance, and the same bits on every run
+    Ag = synth.gauss_fp16(M * K, 90 + M)
+    Bg = synth.gauss_fp16(N * K, 91 + N)
+    g1 = run_f16(M, N, K, Ag, K, Bg, K)
+    g2 = run_f16(M, N, K, Ag, K, Bg, K)
+    assert np.array_equal(g1, g2)
+    mi, ni = sample_positions(M, N, 20000, seed=K + 1)
+    c, s, _ = oracle.gemm_f16_tn_at(M, N, K, Ag, K, Bg, K, mi, ni)
+    assert_tol(f16_values(g1[ni, mi]), f16_values(c), s, F16_TOL, "split-K tail")
