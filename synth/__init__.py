@@ -18,6 +18,8 @@ Workloads (shapes and value distributions of the pages' benchmarks):
   wide_gauss   M=3000, N=12289, K=4097, N(0,1) cast to fp16        (tails)
   e4m3_8192    M=N=K=8192, N(0,1) scaled per tensor to max|x| = 448 and
                cast to E4M3, 4 rotating sets
+  ffn_8192     M=8192, N=28672, K=8192, N(0,1) cast to fp16, 2 rotating
+               sets (the wide feed-forward projection shape)
 """
 from __future__ import annotations
 
@@ -154,6 +156,7 @@ WORKLOADS = {
         Workload("wide_pm1", 3000, 12289, 4097, "pm1", 401, 402),
         Workload("wide_gauss", 3000, 12289, 4097, "gauss", 403, 404),
         Workload("e4m3_8192", 8192, 8192, 8192, "e4m3", 501, 502, rotating=4),
+        Workload("ffn_8192", 8192, 28672, 8192, "gauss", 601, 602, rotating=2),
     ]
 }
 

@@ -203,6 +203,16 @@ def test_workload_sq_8192_sampled():
     assert not np.isnan(f16_values(got)).any()
 
 
+def test_workload_ffn_8192_sampled():
+    """The wide, N-heavy feed-forward shape of the ROCm blog's "Where we are"
+    section (Table 16): M=8192, N=28672, K=8192."""
+    w = synth.WORKLOADS["ffn_8192"]
+    A, B, _, _ = synth.make_inputs(w, 0)
+    got = run_f16(w.M, w.N, w.K, A, w.K, B, w.K)
+    _sampled_f16(w, A, B, got, exact=False, count=8000)
+    assert not np.any((got & 0x7C00) == 0x7C00), "Inf or NaN in C"
+
+
 def test_workload_e4m3_8192_sampled():
     w = synth.WORKLOADS["e4m3_8192"]
     A, B, sa, sb = synth.make_inputs(w, 0)

@@ -64,5 +64,7 @@ def test_workload_table():
     w = synth.WORKLOADS["sq_8192"]
     assert (w.M, w.N, w.K, w.rotating) == (8192, 8192, 8192, 4)
     assert w.seeds(1) == (303, 304)
+    f = synth.WORKLOADS["ffn_8192"]
+    assert (f.M, f.N, f.K, f.dtype) == (8192, 28672, 8192, "f16")
     A, B, sa, sb = synth.make_inputs(synth.WORKLOADS["pm1_512"])
     assert A.size == 512 * 512 and sa == 1.0
