@@ -13,6 +13,9 @@ compute"): A row-major M x K, B column-major K x N, C column-major with
 leading dimension M.  Accumulation is sequential in k in double, rounded once
 to the output type with round-to-nearest-even.
 
+Also: per-tensor E4M3 quantisation (amax, scale to 448, one RNE rounding),
+the step that produces the F8 GEMM's operands.
+
 Pins (tests/test_oracle.py): the worked example and its partial sums, the
 outer-product intermediates, closed forms (all-ones, identity, permutation),
 exact rational brute force on the edge shapes of section 11.4, and exhaustive
@@ -72,6 +75,10 @@ def _load():
     lib.oracle_gemm_f8e4m3_tn_at.argtypes = [i64, i64, i64, p, i64, p, i64,
                                              ctypes.c_float, ctypes.c_float,
                                              i64, p, p, p, p, p]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+    lib.oracle_quantize_e4m3.restype = ctypes.c_int
+    lib.oracle_quantize_e4m3.argtypes = [p, ctypes.c_int, i64, i64, i64, p, i64, p]
     lib.oracle_num_threads.restype = ctypes.c_int
     _lib = lib
     return lib
@@ -104,6 +111,35 @@ def bf16_decode(h: int) -> float:
 
 def e4m3_decode(q: int) -> float:
     return _load().oracle_e4m3_decode(q)
+
+
+def e4m3_encode(x: float) -> int:
+    return _load().oracle_e4m3_encode(x)
+
+
+# --- per-tensor E4M3 quantisation -------------------------------------------
+QUANT_IN = {"f32": (0, np.float32), "f16": (1, np.uint16), "bf16": (2, np.uint16)}
+
+
+def quantize_e4m3(x: np.ndarray, x_type: str, rows: int, cols: int, ldx: int | None = None,
+                  ldq: int | None = None):
+    """amax over the tensor, s_q = 448 / amax (binary32), q = E4M3(x * s_q),
+    scale = amax / 448.  x: float32 values ("f32") or binary16 / bfloat16
+    codes ("f16" / "bf16"), rows x cols with row stride ldx.  Returns
+    (q uint8 flat array with row stride ldq, scale as a Python float that is
+    exactly a binary32 value)."""
+    code, dt = QUANT_IN[x_type]
+    ldx = max(cols, 1) if ldx is None else ldx
+    ldq = max(cols, 1) if ldq is None else ldq
+    x = np.ascontiguousarray(x, dtype=dt).reshape(-1)
+    if rows > 0 and cols > 0 and x.size < (rows - 1) * ldx + cols:
+        raise ValueError("x is smaller than (rows-1)*ldx + cols elements")
+    q = np.zeros(max(rows * ldq, 1), dtype=np.uint8)
+    scale = np.zeros(1, dtype=np.float32)
+    rc = _load().oracle_quantize_e4m3(_ptr(x), code, rows, cols, ldx, _ptr(q), ldq, _ptr(scale))
+    if rc != 0:
+        raise ValueError("oracle_quantize_e4m3 rejected its arguments")
+    return q, float(scale[0])
 
 
 # --- GEMM -------------------------------------------------------------------

@@ -28,6 +28,9 @@
  *     S[m,n] = sum_k |A[m,k] * B[k,n]|  (the magnitude sum used by the
  *              acceptance tolerance), both in double.
  *
+ *   Before the F8 GEMM, an operand may be quantised to E4M3 per tensor
+ *   (oracle_quantize_e4m3 below; amax over the tensor, scale to 448).
+ *
  *   F8 variant: A and B hold E4M3 codes; a = decode(qa), b = decode(qb);
  *   X = sum a*b (double), C = bf16_rne((X * scale_a) * scale_b) and
  *   S = (sum |a*b|) * scale_a * scale_b.  scale_a / scale_b are the
@@ -37,9 +40,11 @@
  * output's k-loop is untouched, so the result does not depend on the thread
  * count.  Build: cc -O2 -fopenmp -shared -fPIC (no -ffast-math).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stddef.h>
+#include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
@@ -153,6 +158,83 @@ double oracle_e4m3_decode(uint8_t q)
     else
         v = ldexp((double)(8 + f), e - 10);
     return sign ? -v : v;
+}
+
+/* double -> E4M3, round to nearest even; magnitudes from 448 (the largest
+ * finite E4M3 value) up -- Inf included -- give +-448 (saturation), NaN gives
+ * the NaN code S.1111.111.  Zero keeps its sign.  Normal values have the
+ * quantum 2^(E-3) for |x| in [2^E, 2^(E+1)), E >= -6; below 2^-6 the quantum
+ * is 2^-9 (subnormals). */
+uint8_t oracle_e4m3_encode(double x)
+{
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    if (isnan(x)) return sign | 0x7f;
+    double ax = fabs(x);
+    if (ax >= 448.0) return sign | 0x7e;
+    if (ax == 0.0) return sign;
+    int e2;
+    frexp(ax, &e2);
+    int E = e2 - 1;                    /* ax in [2^E, 2^(E+1)) */
+    if (E < -6) {
+        double r = round_to_quantum(ax, -9);    /* 0 .. 8; 8 is exactly 2^-6 (0x08) */
+        return sign | (uint8_t)r;
+    }
+    double r = round_to_quantum(ax, E - 3);     /* 8 .. 16 */
+    if (r >= 16.0) { E += 1; r = 8.0; }
+    return sign | (uint8_t)(((E + 7) << 3) | ((int)r - 8));
+}
+
+/* ------------------------------------------------------------------------- */
+/* Per-tensor E4M3 quantisation with the amax over the whole tensor:
+ *   amax = max |x|,  s_q = 448 / amax (binary32),  q = E4M3(binary32(x * s_q)),
+ *   scale = amax / 448 (binary32),
+ * with s_q = 0 for amax = 0 and s_q = FLT_MAX when 448 / amax overflows.  The
+ * pages give no FP8 rule; this is the plain per-tensor scaling to the E4M3
+ * maximum.  The code of each element is an integer decided by floating point,
+ * so the oracle takes that decision in the precision the rule names (binary32
+ * for s_q and for the product), not in double.
+ * x_type: 0 binary32, 1 binary16, 2 bfloat16; x is rows x cols with row
+ * stride ldx elements, q rows x cols with row stride ldq bytes. */
+#if !defined(FLT_EVAL_METHOD) || FLT_EVAL_METHOD != 0
+#error "the quantiser needs binary32 arithmetic evaluated in binary32"
+#endif
+
+static double load_elem(const void *x, int x_type, int64_t i)
+{
+    if (x_type == 0) {
+        float f;
+        memcpy(&f, (const char *)x + 4 * i, 4);
+        return (double)f;
+    }
+    uint16_t h;
+    memcpy(&h, (const char *)x + 2 * i, 2);
+    return x_type == 1 ? oracle_fp16_decode(h) : oracle_bf16_decode(h);
+}
+
+int oracle_quantize_e4m3(const void *x, int x_type, int64_t rows, int64_t cols, int64_t ldx,
+                         uint8_t *q, int64_t ldq, float *scale)
+{
+    if (x_type < 0 || x_type > 2 || rows < 0 || cols < 0) return -1;
+    double amax = 0.0;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            double v = fabs(load_elem(x, x_type, r * ldx + c));
+            if (v > amax) amax = v;
+        }
+    float amax32 = (float)amax;        /* exact: every input is a binary32 value */
+    float s_q = 0.0f;
+    if (amax32 > 0.0f) {
+        s_q = 448.0f / amax32;
+        if (isinf(s_q)) s_q = FLT_MAX;
+    }
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            float xv = (float)load_elem(x, x_type, r * ldx + c);
+            float prod = xv * s_q;
+            q[r * ldq + c] = oracle_e4m3_encode((double)prod);
+        }
+    *scale = amax32 / 448.0f;
+    return 0;
 }
 
 /* ------------------------------------------------------------------------- */

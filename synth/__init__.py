@@ -20,6 +20,9 @@ Workloads (shapes and value distributions of the pages' benchmarks):
                cast to E4M3, 4 rotating sets
   ffn_8192     M=8192, N=28672, K=8192, N(0,1) cast to fp16, 2 rotating
                sets (the wide feed-forward projection shape)
+  fp8_pipeline_8192  M=N=K=8192, N(0,1) cast to bfloat16, 2 rotating sets;
+               each step quantises both operands to E4M3 on the device
+               before the FP8 GEMM
 """
 from __future__ import annotations
 
@@ -54,7 +57,7 @@ def _load():
     build()
     lib = ctypes.CDLL(_LIB)
     p, i64, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64
-    for name in ("synth_sign_fp16", "synth_gauss_f64", "synth_gauss_fp16", "synth_raw"):
+    for name in ("synth_sign_fp16", "synth_gauss_f64", "synth_gauss_fp16", "synth_gauss_bf16", "synth_raw"):
         getattr(lib, name).argtypes = [p, i64, u64]
         getattr(lib, name).restype = None
     lib.synth_gauss_absmax.argtypes = [i64, u64]
@@ -63,6 +66,7 @@ def _load():
     lib.synth_gauss_e4m3.restype = None
     lib.synth_f64_to_fp16.argtypes = [p, p, i64]
     lib.synth_f64_to_e4m3.argtypes = [p, p, i64]
+    lib.synth_f64_to_bf16.argtypes = [p, p, i64]
     _lib = lib
     return lib
 
@@ -97,6 +101,13 @@ def gauss_fp16(n: int, seed: int, out: np.ndarray | None = None) -> np.ndarray:
     return out
 
 
+def gauss_bf16(n: int, seed: int, out: np.ndarray | None = None) -> np.ndarray:
+    """n N(0,1) draws rounded to bfloat16 codes."""
+    out = np.empty(n, np.uint16) if out is None else out
+    _load().synth_gauss_bf16(_p(out), n, seed)
+    return out
+
+
 def gauss_e4m3(n: int, seed: int, out: np.ndarray | None = None):
     """n N(0,1) draws quantised per tensor to E4M3.
 
@@ -121,6 +132,13 @@ def f64_to_fp16(x: np.ndarray) -> np.ndarray:
     return out
 
 
+def f64_to_bf16(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, np.float64)
+    out = np.empty(x.size, np.uint16)
+    _load().synth_f64_to_bf16(_p(out), _p(x), x.size)
+    return out
+
+
 def f64_to_e4m3(x: np.ndarray) -> np.ndarray:
     x = np.ascontiguousarray(x, np.float64)
     out = np.empty(x.size, np.uint8)
@@ -134,14 +152,15 @@ class Workload:
     M: int
     N: int
     K: int
-    values: str          # "pm1", "gauss" or "e4m3"
+    values: str          # "pm1", "gauss", "e4m3", or "bf16" (quantised to E4M3 on the device)
     seed_a: int
     seed_b: int
     rotating: int = 1    # input sets cycled by the benchmark
 
     @property
     def dtype(self) -> str:
-        return "e4m3" if self.values == "e4m3" else "f16"
+        """Element type of the GEMM's operands."""
+        return "e4m3" if self.values in ("e4m3", "bf16") else "f16"
 
     def seeds(self, i: int) -> tuple[int, int]:
         """Seeds of rotating input set i (sets differ by 2 per step)."""
@@ -157,6 +176,7 @@ WORKLOADS = {
         Workload("wide_gauss", 3000, 12289, 4097, "gauss", 403, 404),
         Workload("e4m3_8192", 8192, 8192, 8192, "e4m3", 501, 502, rotating=4),
         Workload("ffn_8192", 8192, 28672, 8192, "gauss", 601, 602, rotating=2),
+        Workload("fp8_pipeline_8192", 8192, 8192, 8192, "bf16", 701, 702, rotating=2),
     ]
 }
 
@@ -172,6 +192,8 @@ def operand(values: str, rows: int, K: int, seed: int):
         return gauss_fp16(n, seed), 1.0
     if values == "e4m3":
         return gauss_e4m3(n, seed)
+    if values == "bf16":
+        return gauss_bf16(n, seed), 1.0
     raise ValueError(values)
 
 

@@ -97,6 +97,22 @@ static inline uint8_t to_e4m3(double x)
     return sign | (uint8_t)q;                   /* q == 8 encodes 2^-6 */
 }
 
+/* finite double -> bfloat16 by its bit fields (inputs here are normal,
+ * |x| < 2^127; smaller than 2^-126 gives signed zero). */
+static inline uint16_t to_bf16(double x)
+{
+    uint64_t u;
+    memcpy(&u, &x, 8);
+    uint16_t sign = (uint16_t)((u >> 48) & 0x8000);
+    int bexp = (int)((u >> 52) & 0x7ff);
+    int e = bexp - 1023;
+    if (bexp == 0 || e < -126) return sign;
+    uint64_t sig = (u & ((1ull << 52) - 1)) | (1ull << 52);
+    uint64_t q = rne_shift(sig, 45);            /* 8-bit significand */
+    if (q == 256) { q = 128; ++e; }
+    return sign | (uint16_t)(((e + 127) << 7) | (int)(q - 128));
+}
+
 void synth_sign_fp16(uint16_t *out, int64_t n, uint64_t seed)
 {
     #pragma omp parallel for schedule(static)
@@ -114,6 +130,12 @@ void synth_gauss_fp16(uint16_t *out, int64_t n, uint64_t seed)
 {
     #pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) out[i] = to_fp16(gauss_at(seed, (uint64_t)i));
+}
+
+void synth_gauss_bf16(uint16_t *out, int64_t n, uint64_t seed)
+{
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) out[i] = to_bf16(gauss_at(seed, (uint64_t)i));
 }
 
 double synth_gauss_absmax(int64_t n, uint64_t seed)
@@ -158,4 +180,9 @@ void synth_f64_to_e4m3(uint8_t *out, const double *in, int64_t n)
         if (v < -448.0) v = -448.0;
         out[i] = to_e4m3(v);
     }
+}
+
+void synth_f64_to_bf16(uint16_t *out, const double *in, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = to_bf16(in[i]);
 }

@@ -42,6 +42,17 @@ def test_e4m3_cast_matches_torch():
     assert synth.f64_to_e4m3(np.array([1e6, -1e6, 460.0])).tolist() == [0x7E, 0xFE, 0x7E]
 
 
+def test_bf16_cast_matches_torch():
+    """On doubles that are binary32 values, torch's binary32 -> bfloat16
+    conversion (one RNE rounding) is the reference."""
+    rng = np.random.default_rng(2)
+    x = (rng.standard_normal(300000) * np.exp2(rng.integers(-60, 60, 300000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(synth.f64_to_bf16(x.astype(np.float64)), ref)
+    h = synth.gauss_bf16(1000, 7)
+    assert np.array_equal(h, synth.f64_to_bf16(synth.gauss_f64(1000, 7)))
+
+
 def test_sign_and_gauss_statistics():
     s = synth.sign_fp16(200000, 101)
     assert set(np.unique(s).tolist()) == {0x3C00, 0xBC00}
