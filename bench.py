@@ -40,6 +40,15 @@ KERNEL_SOURCES = ["dense_gemm_tn_gb300/csrc/tn_gemm_kernel.cuh", "dense_gemm_tn_
 PROFILES_DIR = os.path.join(ROOT, "profiles")
 
 
+def metric_for(w: synth.Workload) -> str:
+    if w.name == "sq_8192":
+        return METRIC
+    what = "FP8 e4m3" if w.dtype == "e4m3" else "FP16"
+    if w.values == "bf16":
+        what = "bf16 -> e4m3 quantise + FP8"
+    return f"TFLOP/s (2MNK/t) {what} TN GEMM {w.M}x{w.N}x{w.K} on 1 GB300; % of dense tensor peak"
+
+
 def kernel_sha() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -193,6 +202,12 @@ def run_reference(args, w: synth.Workload, rank: int) -> None:
         return
     import oracle
     A, B, sa, sb = synth.make_inputs(w, 0)
+    note = ""
+    if w.values == "bf16":
+        # the oracle's quantisation runs once, outside the timed steps
+        A, sa = oracle.quantize_e4m3(A, "bf16", w.M, w.K)
+        B, sb = oracle.quantize_e4m3(B, "bf16", w.N, w.K)
+        note = "; operands quantised by the oracle once, untimed"
     cores = oracle.num_threads()
     # one step = a sample of outputs sized to about 0.5 s of host work
     rng = np.random.default_rng(7)
@@ -219,14 +234,14 @@ def run_reference(args, w: synth.Workload, rank: int) -> None:
     dt = (time.perf_counter() - t0) / max(args.steps, 1)
     value = 2.0 * count * w.K / dt / 1e12
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": metric_for(w), "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": f"{w.name}: M={w.M} N={w.N} K={w.K}, {count} sampled outputs per step",
                    "M": w.M, "N": w.N, "K": w.K},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{count} random outputs per step, full K"},
+                         "sample": f"{count} random outputs per step, full K{note}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -248,10 +263,11 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
     sets = w.rotating if args.sets is None else max(1, args.sets)
     host = host_inputs(w, sets)
     is_f8 = w.dtype == "e4m3"
-    esz = 1 if is_f8 else 2
+    pipeline = w.values == "bf16"          # bf16 operands quantised to E4M3 on the device every step
+    esz = 2 if (pipeline or not is_f8) else 1   # bytes per input element
     dA, dB, scales = [], [], []
     for A, B, sa, sb in host:
-        if is_f8:
+        if esz == 1:
             dA.append(torch.from_numpy(A).to(dev))
             dB.append(torch.from_numpy(B).to(dev))
         else:
@@ -262,17 +278,34 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
     stream = torch.cuda.current_stream(dev)
     sh = int(stream.cuda_stream)
     M, N, K = w.M, w.N, w.K
+    if pipeline:
+        qA = torch.empty((M, K), dtype=torch.uint8, device=dev)
+        qB = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        dscale = torch.empty(2, dtype=torch.float32, device=dev)
+        qa_p, qb_p, sa_p, sb_p = qA.data_ptr(), qB.data_ptr(), dscale.data_ptr(), dscale.data_ptr() + 4
+    launches_per_step = 5 if pipeline else 1
 
-    def step(i):
-        j = i % sets
+    def issue(j, a, b, c, mid=None):
+        """One step's work on the stream: returns the status codes of its calls."""
+        if pipeline:
+            r = [g.lib.gemm_quantize_e4m3(a, g.GEMM_IN_BF16, M, K, K, qa_p, K, sa_p, sh),
+                 g.lib.gemm_quantize_e4m3(b, g.GEMM_IN_BF16, N, K, K, qb_p, K, sb_p, sh)]
+            if mid is not None:
+                mid.record(stream)
+            r.append(g.lib.gemm_f8e4m3_tn_dscale(M, N, K, qa_p, K, qb_p, K, c, M, sa_p, sb_p, sh))
+            return r
         if is_f8:
-            g.lib.gemm_f8e4m3_tn(M, N, K, dA[j].data_ptr(), K, dB[j].data_ptr(), K, C.data_ptr(), M,
-                                 scales[j][0], scales[j][1], sh)
-        else:
-            g.lib.gemm_f16_tn(M, N, K, dA[j].data_ptr(), K, dB[j].data_ptr(), K, C.data_ptr(), M, sh)
+            return [g.lib.gemm_f8e4m3_tn(M, N, K, a, K, b, K, c, M, scales[j][0], scales[j][1], sh)]
+        return [g.lib.gemm_f16_tn(M, N, K, a, K, b, K, c, M, sh)]
+
+    def step(i, mid=None):
+        j = i % sets
+        return issue(j, dA[j].data_ptr(), dB[j].data_ptr(), C.data_ptr(), mid)
 
     # validate once before timing (sampled against the oracle happens in the tests)
-    step(0)
+    rcs = step(0)
+    if any(rc != 0 for rc in rcs):
+        raise RuntimeError(f"GEMM call failed: {rcs}: {g.last_error()}")
     g.gemm_poll_device_status(sh)
 
     clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
@@ -284,9 +317,10 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
         dist.barrier()
     torch.cuda.synchronize(dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    mid = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if pipeline else None
     ev[0].record(stream)
     for i in range(args.steps):
-        step(i)
+        step(i, mid[i] if pipeline else None)
         ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     if dist:
@@ -294,18 +328,22 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     g.gemm_poll_device_status(sh)
-    per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     total_ms = ev[0].elapsed_time(ev[-1])
-    kernel_ms = statistics.mean(per_launch_ms)
+    if pipeline:
+        # the GEMM is the dominant kernel; the two quantisations are timed beside it
+        kernel_ms = statistics.mean(mid[i].elapsed_time(ev[i + 1]) for i in range(args.steps))
+        quant_ms = statistics.mean(ev[i].elapsed_time(mid[i]) for i in range(args.steps))
+    else:
+        kernel_ms = statistics.mean(ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps))
 
     # ---- end to end: pinned host inputs -> device -> GEMM -> pinned host output.
     # Every step copies its own A and B in and its C out; the copies of the
     # neighbouring steps overlap the GEMM (three streams, two buffer slots).
     e2e_steps = max(4, min(args.steps, 50))
     hsets = min(sets, 2)
-    hA = [torch.from_numpy(host[j][0].view(np.int16) if not is_f8 else host[j][0]).pin_memory()
+    hA = [torch.from_numpy(host[j][0].view(np.int16) if esz == 2 else host[j][0]).pin_memory()
           for j in range(hsets)]
-    hB = [torch.from_numpy(host[j][1].view(np.int16) if not is_f8 else host[j][1]).pin_memory()
+    hB = [torch.from_numpy(host[j][1].view(np.int16) if esz == 2 else host[j][1]).pin_memory()
           for j in range(hsets)]
     hC = [torch.empty(C.shape, dtype=C.dtype, pin_memory=True) for _ in range(2)]
     eA = [torch.empty_like(dA[0]) for _ in range(2)]
@@ -327,12 +365,7 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
         in_done[b].record(s_in)
         stream.wait_event(in_done[b])
         stream.wait_event(out_done[b])           # slot b's C was read back by step i-2
-        sa, sb = scales[j]
-        if is_f8:
-            g.lib.gemm_f8e4m3_tn(M, N, K, eA[b].data_ptr(), K, eB[b].data_ptr(), K, eC[b].data_ptr(), M,
-                                 sa, sb, sh)
-        else:
-            g.lib.gemm_f16_tn(M, N, K, eA[b].data_ptr(), K, eB[b].data_ptr(), K, eC[b].data_ptr(), M, sh)
+        issue(j, eA[b].data_ptr(), eB[b].data_ptr(), eC[b].data_ptr())
         gemm_done[b].record(stream)
         s_out.wait_event(gemm_done[b])
         with torch.cuda.stream(s_out):
@@ -372,14 +405,24 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
     achieved = flop / (kernel_ms * 1e-3) / 1e12
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        tf, cores, desc = oracle_sample(w, *host[0], target_s=args.cpu_seconds)
+        if pipeline:
+            import oracle
+            t0 = time.perf_counter()
+            qa_ref, sa_ref = oracle.quantize_e4m3(host[0][0], "bf16", M, K)
+            qb_ref, sb_ref = oracle.quantize_e4m3(host[0][1], "bf16", N, K)
+            t_q = time.perf_counter() - t0
+            tf, cores, desc = oracle_sample(w, qa_ref, qb_ref, sa_ref, sb_ref, target_s=args.cpu_seconds)
+            desc += f"; the oracle's quantisation of both operands took a further {t_q:.1f} s"
+        else:
+            tf, cores, desc = oracle_sample(w, *host[0], target_s=args.cpu_seconds)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": metric_for(w), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": f"{w.name}: {w.dtype} TN GEMM M={M} N={N} K={K}, {w.values} inputs, "
-                               f"{sets} rotating input set(s)",
+                               f"{sets} rotating input set(s)"
+                               + (", both operands quantised to e4m3 on the device each step" if pipeline else ""),
                    "M": M, "N": N, "K": K, "accumulate": "f32",
                    "l2": f"inputs larger than L2: {sets} rotating sets of {(M + N) * K * esz >> 20} MiB"
                          if sets > 1 else "single input set",
@@ -397,8 +440,16 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
                      "traffic": measured_traffic(w.name)},
         "cpu_baseline": cpu,
         "clocks": clk,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
     }
+    if pipeline:
+        # algorithmic bytes: each bf16 input read once, each e4m3 code and scale written once
+        qbytes = 2 * (M * K + N * K) + (M * K + N * K) + 8
+        line["quantize"] = {"bound": "hbm", "achieved": qbytes / (quant_ms * 1e-3) / 1e9,
+                            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": qbytes / (quant_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                            "ms": quant_ms, "algorithmic_bytes": qbytes,
+                            "kernels": "quant_amax_kernel + quant_store_kernel, one pair per operand"}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

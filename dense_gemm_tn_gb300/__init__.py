@@ -8,6 +8,8 @@ The same names as the C ABI:
 
     gemm_f16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream=None)
     gemm_f8e4m3_tn(M, N, K, A, lda, B, ldb, C, ldc, scale_a, scale_b, stream=None)
+    gemm_f8e4m3_tn_dscale(M, N, K, A, lda, B, ldb, C, ldc, scale_a_ptr, scale_b_ptr, stream=None)
+    gemm_quantize_e4m3(x, x_type, rows, cols, ldx, q, ldq, scale_ptr, stream=None)
     gemm_poll_device_status(stream=None)
 
 A, B and C are device pointers given as ints or as CUDA torch tensors (their
@@ -41,7 +43,12 @@ EXPORTS = (
     "gemm_poll_device_status", "gemm_release_workspace", "gemm_tile_coord",
     "gemm_set_wait_limit_ns", "gemm_debug_inject_stall", "gemm_build_info",
     "gemm_f16_tn_noalloc", "gemm_debug_force_cta_group", "gemm_debug_last_launch",
+    "gemm_f8e4m3_tn_dscale", "gemm_quantize_e4m3",
 )
+
+GEMM_IN_F32 = 0
+GEMM_IN_F16 = 1
+GEMM_IN_BF16 = 2
 
 
 class GemmError(RuntimeError):
@@ -62,6 +69,10 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f8e4m3_tn.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64,
                                    ctypes.c_float, ctypes.c_float, vp]
     lib.gemm_f8e4m3_tn.restype = st
+    lib.gemm_f8e4m3_tn_dscale.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp, vp]
+    lib.gemm_f8e4m3_tn_dscale.restype = st
+    lib.gemm_quantize_e4m3.argtypes = [vp, st, i64, i64, i64, vp, i64, vp, vp]
+    lib.gemm_quantize_e4m3.restype = st
     lib.gemm_f16_tn_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp]
     lib.gemm_f16_tn_noalloc.restype = st
     lib.gemm_status_string.argtypes = [st]
@@ -142,6 +153,18 @@ def gemm_f8e4m3_tn(M, N, K, A, lda, B, ldb, C, ldc, scale_a, scale_b, stream=Non
                                       float(scale_a), float(scale_b), _stream(stream)))
 
 
+def gemm_f8e4m3_tn_dscale(M, N, K, A, lda, B, ldb, C, ldc, scale_a, scale_b, stream=None) -> int:
+    """gemm_f8e4m3_tn with scale_a / scale_b as device pointers (one fp32 each)."""
+    return _check(_lib.gemm_f8e4m3_tn_dscale(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
+                                             _ptr(scale_a), _ptr(scale_b), _stream(stream)))
+
+
+def gemm_quantize_e4m3(x, x_type, rows, cols, ldx, q, ldq, scale, stream=None) -> int:
+    """Per-tensor E4M3 quantisation on the device: codes into q, amax / 448 into *scale."""
+    return _check(_lib.gemm_quantize_e4m3(_ptr(x), int(x_type), rows, cols, ldx, _ptr(q), ldq, _ptr(scale),
+                                          _stream(stream)))
+
+
 def gemm_f16_tn_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
     """gemm_f16_tn for callers that cannot let the library allocate device
     memory (their own memory pool or budget, or no implicit synchronisation
@@ -191,6 +214,35 @@ def f16_tn(A, Bt, C=None, stream=None):
         C = torch.empty((N, M), dtype=torch.float16, device=A.device)
     gemm_f16_tn(M, N, K, A, A.stride(0) if M > 0 else max(K, 1), Bt,
                 Bt.stride(0) if N > 0 else max(K, 1), C, C.stride(0) if N > 0 else max(M, 1), stream)
+    return C
+
+
+def quantize_e4m3(x, stream=None):
+    """x: a 2-D float32 / float16 / bfloat16 CUDA tensor with unit column
+    stride.  Returns (codes as a uint8 tensor of x's shape, scale as a
+    1-element float32 tensor), both on x's device."""
+    import torch
+    types = {torch.float32: GEMM_IN_F32, torch.float16: GEMM_IN_F16, torch.bfloat16: GEMM_IN_BF16}
+    if x.dtype not in types or x.dim() != 2 or (x.numel() > 0 and x.stride(1) != 1):
+        raise ValueError("x must be a 2-D float32/float16/bfloat16 tensor with unit column stride")
+    rows, cols = x.shape
+    q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    ld = max(cols, 1)
+    gemm_quantize_e4m3(x, types[x.dtype], rows, cols, x.stride(0) if rows > 1 else ld, q, ld, scale, stream)
+    return q, scale
+
+
+def f8e4m3_tn_dscale(A, Bt, scale_a, scale_b, C=None, stream=None):
+    """f8e4m3_tn with the scales as 1-element float32 CUDA tensors."""
+    import torch
+    M, K = A.shape
+    N = Bt.shape[0]
+    if C is None:
+        C = torch.empty((N, M), dtype=torch.bfloat16, device=A.device)
+    gemm_f8e4m3_tn_dscale(M, N, K, A, A.stride(0) if M > 0 else max(K, 1), Bt,
+                          Bt.stride(0) if N > 0 else max(K, 1), C, C.stride(0) if N > 0 else max(M, 1),
+                          scale_a, scale_b, stream)
     return C
 
 

@@ -14,6 +14,7 @@
 
 #include "tn_gemm.h"
 #include "tn_gemm_kernel.cuh"
+#include "quant_e4m3_kernel.cuh"
 
 namespace {
 
@@ -47,6 +48,9 @@ struct DeviceState {
         size_t bytes = 0, ticket_bytes = 0;
     };
     std::unordered_map<cudaStream_t, Split> split;
+    // Per-CTA maxima of the quantiser, one array per stream.
+    std::unordered_map<cudaStream_t, Split> quant;
+    int quant_blocks[3] = {};         // co-resident quantiser CTAs per SM, by input type (0 = not queried)
     unsigned long long epoch = 0;
 };
 
@@ -120,33 +124,50 @@ gemm_status_t ensure_workspace(DeviceState &d, size_t bytes)
     return GEMM_OK;
 }
 
-// The stream's split-K buffer with room for `tickets` ticket words and
-// `partial_bytes` of partial sums; grown (and its tickets zeroed) on demand.
-gemm_status_t split_workspace(DeviceState &d, cudaStream_t stream, size_t tickets, size_t partial_bytes,
-                              unsigned long long **ticket_ptr, float **partial_ptr)
+// A per-stream buffer of `map` that starts with `zeroed_bytes` of words
+// cleared when it is (re)allocated, followed by `extra_bytes`; grown on demand.
+// Calls on one stream are ordered, so they may share their stream's buffer.
+gemm_status_t stream_buffer(std::unordered_map<cudaStream_t, DeviceState::Split> &map, cudaStream_t stream,
+                            size_t zeroed_bytes, size_t extra_bytes, const char *what, uint8_t **base,
+                            size_t *zeroed_out)
 {
     std::lock_guard<std::mutex> lock(g_mutex);
-    DeviceState::Split &w = d.split[stream];
-    const size_t tb = (tickets * sizeof(unsigned long long) + 255) & ~size_t(255);
-    if (w.ticket_bytes < tb || w.bytes < w.ticket_bytes + partial_bytes) {
+    DeviceState::Split &w = map[stream];
+    const size_t tb = (zeroed_bytes + 255) & ~size_t(255);
+    if (w.ticket_bytes < tb || w.bytes < w.ticket_bytes + extra_bytes) {
         const size_t new_tb = tb > w.ticket_bytes ? tb : w.ticket_bytes;
-        const size_t need = new_tb + partial_bytes;
+        const size_t need = new_tb + extra_bytes;
         if (w.ptr) cudaFree(w.ptr);      // synchronises the device: earlier users are done
         w.ptr = nullptr;
         w.bytes = w.ticket_bytes = 0;
         cudaError_t e = cudaMalloc(&w.ptr, need);
         if (e != cudaSuccess) {
             w.ptr = nullptr;
-            return fail(GEMM_ERR_CUDA, "cudaMalloc(%zu) for split-K partials: %s", need, cudaGetErrorString(e));
+            return fail(GEMM_ERR_CUDA, "cudaMalloc(%zu) for %s: %s", need, what, cudaGetErrorString(e));
         }
-        // tickets hold 2*epoch+1 of past launches; zero is older than every epoch
+        // the words hold tags of past launches' epochs; zero is older than every epoch
         e = cudaMemsetAsync(w.ptr, 0, new_tb, stream);
-        if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "clearing split-K tickets: %s", cudaGetErrorString(e));
+        if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "clearing %s: %s", what, cudaGetErrorString(e));
         w.bytes = need;
         w.ticket_bytes = new_tb;
     }
-    *ticket_ptr = static_cast<unsigned long long *>(w.ptr);
-    *partial_ptr = reinterpret_cast<float *>(static_cast<uint8_t *>(w.ptr) + w.ticket_bytes);
+    *base = static_cast<uint8_t *>(w.ptr);
+    *zeroed_out = w.ticket_bytes;
+    return GEMM_OK;
+}
+
+// The stream's split-K buffer with room for `tickets` ticket words and
+// `partial_bytes` of partial sums.
+gemm_status_t split_workspace(DeviceState &d, cudaStream_t stream, size_t tickets, size_t partial_bytes,
+                              unsigned long long **ticket_ptr, float **partial_ptr)
+{
+    uint8_t *base = nullptr;
+    size_t zeroed = 0;
+    gemm_status_t st = stream_buffer(d.split, stream, tickets * sizeof(unsigned long long), partial_bytes,
+                                     "split-K partials", &base, &zeroed);
+    if (st != GEMM_OK) return st;
+    *ticket_ptr = reinterpret_cast<unsigned long long *>(base);
+    *partial_ptr = reinterpret_cast<float *>(base + zeroed);
     return GEMM_OK;
 }
 
@@ -295,7 +316,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
 template <class Kind>
 gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
                        const void *B, int64_t ldb, void *C, int64_t ldc, float scale, cudaStream_t stream,
-                       bool allow_alloc = true)
+                       bool allow_alloc = true, const float *dscale_a = nullptr, const float *dscale_b = nullptr)
 {
     constexpr int64_t esz = Kind::kElemBytes;
     const int64_t kmin = K > 1 ? K : 1;
@@ -414,11 +435,119 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     prm.num_kb = static_cast<int32_t>((K * esz + tn::kBlockKBytes - 1) / tn::kBlockKBytes);
     prm.group = kGroupM;            // even, so raster ids 2j, 2j+1 are neighbouring m tiles of one n tile
     prm.scale = scale;
+    prm.scale_a_ptr = dscale_a;
+    prm.scale_b_ptr = dscale_b;
     prm.flags = (tma_c ? tn::kFlagTmaStore : 0u) | stall_flags(g_inject_stall.load());
     prm.wait_limit_ns = g_wait_limit_ns.load();
 
     if (cta_group == 2) return launch<Kind, 2>(name, prm, *dev, quad, allow_alloc, stream);
     return launch<Kind, 1>(name, prm, *dev, false, allow_alloc, stream);
+}
+
+// Per-tensor E4M3 quantisation (quant_e4m3_kernel.cuh): the maximum-finding
+// kernel, then the quantising kernel as its programmatic dependent, both with
+// the same grid; the per-CTA maxima go through the stream's slot array.
+template <int kIn>
+gemm_status_t launch_quant(DeviceState &dev, qz::QuantParams &prm, cudaStream_t stream)
+{
+    auto amax_kernel = qz::quant_amax_kernel<kIn>;
+    auto store_kernel = qz::quant_store_kernel<kIn>;
+    int per_sm;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (dev.quant_blocks[kIn] == 0) {
+            int n1 = 0, n2 = 0;
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n1, amax_kernel, qz::kThreads, 0);
+            if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n2, store_kernel, qz::kThreads, 0);
+            if (e != cudaSuccess || n1 <= 0 || n2 <= 0)
+                return fail(GEMM_ERR_CUDA, "gemm_quantize_e4m3: occupancy query: %s", cudaGetErrorString(e));
+            dev.quant_blocks[kIn] = n1 < n2 ? n1 : n2;    // both grids resident in one wave
+        }
+        per_sm = dev.quant_blocks[kIn];
+    }
+    int64_t grid = int64_t(per_sm) * dev.sms;
+    if (grid > prm.num_units) grid = prm.num_units;
+    if (grid < 1) grid = 1;
+    uint8_t *slots = nullptr;
+    size_t zeroed = 0;
+    gemm_status_t st = stream_buffer(dev.quant, stream, 0, size_t(grid) * sizeof(float), "quantiser slots", &slots,
+                                     &zeroed);
+    if (st != GEMM_OK) return st;
+    prm.slots = reinterpret_cast<float *>(slots + zeroed);
+    snprintf(t_last_launch, sizeof(t_last_launch), "gemm_quantize_e4m3: grid=%lld units=%lld vec=%d",
+             (long long)grid, (long long)prm.num_units, prm.vec);
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(qz::kThreads, 1, 1);
+    cfg.stream = stream;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, amax_kernel, prm);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "gemm_quantize_e4m3: launch (amax): %s", cudaGetErrorString(e));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, store_kernel, prm);
+    if (e != cudaSuccess)
+        return fail(GEMM_ERR_CUDA, "gemm_quantize_e4m3: launch (quantise): %s", cudaGetErrorString(e));
+    return GEMM_OK;
+}
+
+gemm_status_t run_quant(const void *x, int x_type, int64_t rows, int64_t cols, int64_t ldx, void *q, int64_t ldq,
+                        float *scale, cudaStream_t stream)
+{
+    const char *name = "gemm_quantize_e4m3";
+    if (x_type < qz::kInF32 || x_type > qz::kInBF16)
+        return fail(GEMM_ERR_INVALID_ARG, "%s: unknown input type %d", name, x_type);
+    const int64_t esz = x_type == qz::kInF32 ? 4 : 2;
+    if (rows < 0 || cols < 0) return fail(GEMM_ERR_INVALID_ARG, "%s: negative size", name);
+    const int64_t cmin = cols > 1 ? cols : 1;
+    if (ldx < cmin || ldq < cmin) return fail(GEMM_ERR_INVALID_ARG, "%s: ldx or ldq < max(1, cols)", name);
+    if (!scale) return fail(GEMM_ERR_INVALID_ARG, "%s: scale is NULL", name);
+    if (reinterpret_cast<uintptr_t>(scale) % 4) return fail(GEMM_ERR_INVALID_ARG, "%s: scale is not 4-byte aligned", name);
+    if (rows > 0 && cols > 0) {
+        if (!x || !q) return fail(GEMM_ERR_INVALID_ARG, "%s: x or q is NULL", name);
+        if (reinterpret_cast<uintptr_t>(x) % esz)
+            return fail(GEMM_ERR_INVALID_ARG, "%s: x is not aligned to its element size", name);
+    }
+    if (rows > (int64_t(1) << 40) / cmin)
+        return fail(GEMM_ERR_UNSUPPORTED, "%s: more than 2^40 elements", name);
+    DeviceState *dev = nullptr;
+    gemm_status_t st = device_state(&dev, nullptr);
+    if (st != GEMM_OK) return st;
+    if (rows == 0 || cols == 0) {
+        // no elements: amax = 0, so the dequantisation scale is 0
+        cudaError_t e = cudaMemsetAsync(scale, 0, sizeof(float), stream);
+        if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: clearing scale: %s", name, cudaGetErrorString(e));
+        return GEMM_OK;
+    }
+    qz::QuantParams prm;
+    memset(&prm, 0, sizeof(prm));
+    prm.x = x;
+    prm.q = static_cast<uint8_t *>(q);
+    prm.scale_out = scale;
+    if (ldx == cols && ldq == cols) {      // contiguous: one long row
+        prm.rows = 1;
+        prm.cols = rows * cols;
+    } else {
+        prm.rows = rows;
+        prm.cols = cols;
+    }
+    prm.ldx = ldx;
+    prm.ldq = ldq;
+    const int64_t unit = qz::unit_elems(x_type);
+    prm.units_per_row = (prm.cols + unit - 1) / unit;
+    prm.num_units = prm.rows * prm.units_per_row;
+    // 16-byte loads of x and 8-byte stores of q need every row start aligned
+    // (a single row starts at the bases).
+    prm.vec = reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(q) % 8 == 0 &&
+              (prm.rows == 1 || ((ldx * esz) % 16 == 0 && ldq % 8 == 0));
+    switch (x_type) {
+    case qz::kInF32: return launch_quant<qz::kInF32>(*dev, prm, stream);
+    case qz::kInF16: return launch_quant<qz::kInF16>(*dev, prm, stream);
+    default: return launch_quant<qz::kInBF16>(*dev, prm, stream);
+    }
 }
 
 }  // namespace
@@ -439,6 +568,25 @@ gemm_status_t gemm_f8e4m3_tn(int64_t M, int64_t N, int64_t K, const void *A, int
     t_last_error[0] = '\0';
     return run_gemm<tn::KindE4M3>("gemm_f8e4m3_tn", M, N, K, A, lda, B, ldb, C, ldc, scale_a * scale_b,
                                   static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_f8e4m3_tn_dscale(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                                    int64_t ldb, void *C, int64_t ldc, const float *scale_a, const float *scale_b,
+                                    void *stream)
+{
+    t_last_error[0] = '\0';
+    if (!scale_a || !scale_b) return fail(GEMM_ERR_INVALID_ARG, "gemm_f8e4m3_tn_dscale: a scale pointer is NULL");
+    if (reinterpret_cast<uintptr_t>(scale_a) % 4 || reinterpret_cast<uintptr_t>(scale_b) % 4)
+        return fail(GEMM_ERR_INVALID_ARG, "gemm_f8e4m3_tn_dscale: a scale pointer is not 4-byte aligned");
+    return run_gemm<tn::KindE4M3>("gemm_f8e4m3_tn_dscale", M, N, K, A, lda, B, ldb, C, ldc, 1.0f,
+                                  static_cast<cudaStream_t>(stream), true, scale_a, scale_b);
+}
+
+gemm_status_t gemm_quantize_e4m3(const void *x, int x_type, int64_t rows, int64_t cols, int64_t ldx, void *q,
+                                 int64_t ldq, float *scale, void *stream)
+{
+    t_last_error[0] = '\0';
+    return run_quant(x, x_type, rows, cols, ldx, q, ldq, scale, static_cast<cudaStream_t>(stream));
 }
 
 const char *gemm_status_string(gemm_status_t s)
@@ -483,6 +631,9 @@ void gemm_release_workspace(void)
     for (auto &kv : d.split)
         if (kv.second.ptr) cudaFree(kv.second.ptr);
     d.split.clear();
+    for (auto &kv : d.quant)
+        if (kv.second.ptr) cudaFree(kv.second.ptr);
+    d.quant.clear();
 }
 
 int gemm_tile_coord(int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t id, int64_t *tile_m, int64_t *tile_n)

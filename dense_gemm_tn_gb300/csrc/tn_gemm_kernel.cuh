@@ -123,6 +123,9 @@ struct KernelParams {
     unsigned long long *split_tickets;   // [tail tile][CTA of pair]: 2*epoch+1 once one half arrived
     unsigned long long epoch;            // distinct per launch that uses split_ws
     float scale;             // epilogue multiplier (F8: scale_a * scale_b)
+    // F8 with device-resident scales: when set, the epilogue multiplies by
+    // (*scale_a_ptr) * (*scale_b_ptr) in FP32 instead of `scale`.
+    const float *scale_a_ptr, *scale_b_ptr;
     uint32_t flags;
     uint64_t wait_limit_ns;
 };
@@ -588,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         const int row = 32 * quarter + lane;      // this thread's TMEM lane = output column within the CTA
         const bool tma_store = (p.flags & kFlagTmaStore) != 0;
         volatile uint32_t *second_flag = tmem_holder + 4;   // split-K: this CTA's half came second
+        const float scale = p.scale_a_ptr ? __fmul_rn(__ldg(p.scale_a_ptr), __ldg(p.scale_b_ptr)) : p.scale;
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t chunk_ctr = 0;
@@ -621,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         auto store_chunk = [&](const float (&v)[64], int32_t mc, int32_t nw) {
             uint32_t packed[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) packed[j] = Kind::pack(v[2 * j], v[2 * j + 1], p.scale);
+            for (int j = 0; j < 32; ++j) packed[j] = Kind::pack(v[2 * j], v[2 * j + 1], scale);
             if (tma_store && mc < p.m_tma) {
                 const uint32_t buf = s_epi + (ew * kEpiBufs + (chunk_ctr & 1u)) * kEpiBufBytes;
                 if (lane == 0) ptx::bulk_wait_group_read<kEpiBufs - 1>();   // buffer's previous store has read it

@@ -90,6 +90,67 @@ gemm_status_t gemm_f8e4m3_tn(int64_t M, int64_t N, int64_t K,
                              void *stream);
 
 /*
+ * FP8 TN GEMM with device-resident per-tensor scales: gemm_f8e4m3_tn with
+ * scale_a and scale_b passed as DEVICE pointers to one fp32 value each.  The
+ * kernel reads them when it runs, so an earlier kernel on the same stream
+ * (gemm_quantize_e4m3) may produce them without a round trip to the host.
+ * C[m,n] = bf16(acc[m,n] * ((*scale_a) * (*scale_b))), the product of the two
+ * scales taken in FP32 -- the same arithmetic as gemm_f8e4m3_tn, so both
+ * entry points give bit-identical C for the same scale values.  The caller
+ * owns the scale buffers.  Errors as for gemm_f8e4m3_tn, plus
+ * GEMM_ERR_INVALID_ARG for a NULL or not 4-byte aligned scale pointer.
+ */
+gemm_status_t gemm_f8e4m3_tn_dscale(int64_t M, int64_t N, int64_t K,
+                                    const void *A, int64_t lda,
+                                    const void *B, int64_t ldb,
+                                    void *C, int64_t ldc,
+                                    const float *scale_a, const float *scale_b,
+                                    void *stream);
+
+/* Element types gemm_quantize_e4m3 reads. */
+typedef enum {
+    GEMM_IN_F32 = 0,    /* IEEE binary32 */
+    GEMM_IN_F16 = 1,    /* IEEE binary16 */
+    GEMM_IN_BF16 = 2    /* bfloat16 */
+} gemm_quant_in_t;
+
+/*
+ * Per-tensor E4M3 quantisation of one operand, the amax taken on the device:
+ *
+ *     amax  = max |x[r,c]|                       over the whole tensor
+ *     s_q   = 448 / amax                         fp32 (0 if amax = 0; FLT_MAX if it overflows)
+ *     q[r,c] = E4M3(fp32(x[r,c] * s_q))          round to nearest even, saturating to +-448
+ *     *scale = amax / 448                        fp32: the dequantisation factor
+ *
+ * so that gemm_f8e4m3_tn_dscale(..., scale_a, scale_b) on two quantised
+ * operands approximates the GEMM of the originals.  (The pages print no FP8
+ * rule; the ROCm blog above only announces an FP8 port.  This is the plain
+ * per-tensor scaling to the E4M3 maximum, 448.)
+ *
+ * x: rows x cols, row-major, element (r,c) at x[r*ldx + c], x_type one of
+ *    gemm_quant_in_t, aligned to its element size; ldx >= max(1, cols).
+ *    For the GEMM's operands: A is M x K with ldx = lda, B (column-major
+ *    K x N) is N x K with ldx = ldb.
+ * q: rows x cols OCP E4M3 ("e4m3fn") codes, q[r*ldq + c], ldq >= max(1, cols).
+ * scale: one fp32 in device memory.
+ * All three are DEVICE pointers owned by the caller; q and scale must not
+ * overlap x.  rows or cols == 0 writes *scale = 0 and nothing else.
+ * Inputs must be finite (an Inf or NaN gives unspecified codes and scale).
+ *
+ * Two kernel launches per call on `stream`: the first finds each CTA's
+ * maximum and leaves it in a small library-owned array kept per (device,
+ * stream) and allocated on first use; the second reads them and quantises.
+ * No CTA waits on another.  Calls on one stream may share the array; calls on
+ * different streams use different arrays.
+ * Errors: GEMM_ERR_INVALID_ARG for an unknown x_type, negative sizes, an ld
+ * below its minimum, NULL pointers with work to do, a misaligned x or scale;
+ * GEMM_ERR_UNSUPPORTED off sm_103 or above 2^40 elements; GEMM_ERR_CUDA on a
+ * failed allocation or launch.
+ */
+gemm_status_t gemm_quantize_e4m3(const void *x, int x_type, int64_t rows, int64_t cols, int64_t ldx,
+                                 void *q, int64_t ldq, float *scale, void *stream);
+
+/*
  * gemm_f16_tn without any device allocation by the library.
  *
  * The paper has no counterpart to this entry point; it exists for callers
@@ -136,8 +197,9 @@ const char *gemm_last_error(void);
  */
 gemm_status_t gemm_poll_device_status(void *stream);
 
-/* Frees the current device's workspaces: the repack copy and the per-stream
- * split-K partial sums (synchronises the device). */
+/* Frees the current device's workspaces: the repack copy, the per-stream
+ * split-K partial sums and the quantiser's per-stream arrays (synchronises
+ * the device). */
 void gemm_release_workspace(void);
 
 /*

@@ -43,3 +43,4 @@ def test_stalled_wait_reports_timeout_and_context_survives(cta_group, mode):
         check_f16_full(M, N, K, A, B, what=f"after timeout, group {cta_group} mode {mode}")
     finally:
         g.gemm_debug_force_cta_group(0)
+
