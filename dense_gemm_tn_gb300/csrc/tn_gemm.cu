@@ -351,18 +351,10 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     // Tile shape.  One CTA per 128 x 256 tile when N <= 128 (a pair's second
     // half would idle); else a CTA pair per 256 x 256 tile.  Pairs can also be
     // launched so that the hardware joins two of them into a 4-CTA cluster
-    // sharing B rows wherever four CTAs fit together.  Measured on GB300 that
-    // pays only when the pair grid ends in a partial wave too full to split
-    // into half units (3000x12289x4104: +9 %); on the other shapes the
-    // coupling of the two pairs costs more than the saved bytes (4096^3: -12 %,
-    // 8192^3: -0.5 %).
+    // sharing B rows (gemm_debug_force_cta_group(4)); with 256-byte K stages
+    // that loses on every shape measured on GB300 (3000x12288x4096: -3.5 %,
+    // the shape where it used to win), so the library does not choose it.
     int ctas = N > 128 ? 2 : 1;
-    if (ctas == 2) {
-        const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-        const int64_t pair_slots = dev->sms / 2;
-        const int64_t rem = pair_tiles % pair_slots;
-        if (pair_tiles > pair_slots && 2 * rem > pair_slots) ctas = 4;
-    }
     if (const int forced = g_force_cta_group.load()) ctas = forced;
     const int cta_group = ctas >= 2 ? 2 : 1;
     const bool quad = ctas == 4;
@@ -374,14 +366,19 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     // its row length K are all multiples of 16 bytes (a row that ends inside a
     // 16-byte unit is not clipped element by element).  Other operands are
     // first copied to a workspace with a padded stride and zero-filled pad,
-    // and the padded length becomes the tensor's inner dimension.
+    // and the padded length becomes the tensor's inner dimension.  The padded
+    // stride is a multiple of 128 bytes, so that every row of every TMA box
+    // (one 128-byte swizzle atom) is one aligned 128-byte line; with a stride
+    // that is only 16-byte aligned each box row straddles two lines, which
+    // measured 13 % slower on 3000 x 12289 x 4097.
     const void *a_use = A, *b_use = B;
     int64_t lda_use = lda, ldb_use = ldb, ka = K, kb = K;
     const bool k_aligned = (K * esz) % 16 == 0;
     const bool repack_a = !k_aligned || (lda * esz) % 16 != 0 || reinterpret_cast<uintptr_t>(A) % 16 != 0;
     const bool repack_b = !k_aligned || (ldb * esz) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0;
     if (repack_a || repack_b) {
-        const int64_t ldp = (K + (16 / esz) - 1) / (16 / esz) * (16 / esz);
+        constexpr int64_t kPad = tn::kBlockKBytes / esz;       // elements per 128 bytes
+        const int64_t ldp = (K + kPad - 1) / kPad * kPad;
         const size_t bytes_a = repack_a ? ((size_t(M) * ldp * esz + 255) & ~size_t(255)) : 0;
         const size_t bytes_b = repack_b ? ((size_t(N) * ldp * esz + 255) & ~size_t(255)) : 0;
         if ((st = ensure_workspace(*dev, bytes_a + bytes_b)) != GEMM_OK) return st;
@@ -432,7 +429,8 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     prm.tiles_m = static_cast<int32_t>(tiles_m);
     prm.tiles_n = static_cast<int32_t>(tiles_n);
     prm.num_tiles = static_cast<int32_t>(tiles_m * tiles_n);
-    prm.num_kb = static_cast<int32_t>((K * esz + tn::kBlockKBytes - 1) / tn::kBlockKBytes);
+    const int64_t stage_k = cta_group == 2 ? tn::TileCfg<2>::kStageKBytes : tn::TileCfg<1>::kStageKBytes;
+    prm.num_kb = static_cast<int32_t>((K * esz + stage_k - 1) / stage_k);   // k blocks = stages per tile
     prm.group = kGroupM;            // even, so raster ids 2j, 2j+1 are neighbouring m tiles of one n tile
     prm.scale = scale;
     prm.scale_a_ptr = dscale_a;
@@ -661,10 +659,11 @@ const char *gemm_build_info(void)
 {
     static char info[384];
     snprintf(info, sizeof(info),
-             "dense_gemm_tn sm_103a: CTA-pair tile 256x256 in clusters of 2 or 4 (B multicast), %d stages, %d B "
-             "smem; 1-CTA tile 128x256, %d stages, %d B smem; K block %d B; TMEM %u cols; raster group %d",
-             tn::TileCfg<2>::kStages, tn::TileCfg<2>::kSmemBytes, tn::TileCfg<1>::kStages,
-             tn::TileCfg<1>::kSmemBytes, tn::kBlockKBytes, tn::kTmemCols, kGroupM);
+             "dense_gemm_tn sm_103a: CTA-pair tile 256x256 in clusters of 2 or 4 (B multicast), %d stages of %d B "
+             "of K, %d B smem; 1-CTA tile 128x256, %d stages of %d B of K, %d B smem; TMEM %u cols; raster group %d",
+             tn::TileCfg<2>::kStages, tn::TileCfg<2>::kStageKBytes, tn::TileCfg<2>::kSmemBytes,
+             tn::TileCfg<1>::kStages, tn::TileCfg<1>::kStageKBytes, tn::TileCfg<1>::kSmemBytes, tn::kTmemCols,
+             kGroupM);
     return info;
 }
 

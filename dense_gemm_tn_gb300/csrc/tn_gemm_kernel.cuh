@@ -40,7 +40,7 @@ namespace tn {
 
 // ------------------------------------------------------------------ config
 constexpr int kThreads = 192;               // warp 0 TMA, warp 1 TMEM + MMA (even CTA), warps 2-5 epilogue
-constexpr int kBlockKBytes = 128;           // bytes of K per stage and row (one swizzle span)
+constexpr int kBlockKBytes = 128;           // bytes of K per row of one swizzle atom (= one TMA box)
 constexpr int kMmaKBytes = 32;              // K bytes per tcgen05.mma (16 fp16 / 32 e4m3)
 constexpr int kEpiWarps = 4;
 constexpr int kEpiBoxM = 64;                // m values per TMA store box (128 B of 16-bit C)
@@ -63,6 +63,12 @@ constexpr uint32_t kTmemCols = 2 * kAccCols;  // double-buffered accumulator = a
 // other pair, so 24 instead of 32 KiB leave L2 per CTA and stage.  Where it
 // cannot (8 of a GB300's 152 SMs), the pair works alone.  The kernel reads its
 // cluster size at run time.
+//
+// A stage holds kAtoms consecutive 128-byte K atoms of each operand (a pair:
+// 256 bytes of K, 8 MMAs per stage), each atom its own 128B-swizzled block:
+//   [B atom 0][B atom 1]...[A atom 0][A atom 1]...
+// Fewer, longer stages halve the barrier waits, commits and TMA issues per
+// MMA; measured on GB300 the MMA pipe then loses less time between stages.
 template <int kGroup>
 struct TileCfg {
     static constexpr int kMaxCtas = 2 * kGroup;            // CTAs per cluster at most (2 pairs)
@@ -70,10 +76,15 @@ struct TileCfg {
     static constexpr int kRowsB = 128;                      // B rows (columns n) per CTA and stage
     static constexpr int kSliceB = kRowsB / 2;              // B rows each CTA loads when a cluster shares
     static constexpr int kRowsA = kTileM / kGroup;          // A rows (m) per CTA and stage
-    static constexpr int kStages = kGroup == 2 ? 6 : 4;
-    static constexpr int kTileBBytes = kRowsB * kBlockKBytes;
-    static constexpr int kSliceBBytes = kSliceB * kBlockKBytes;
-    static constexpr int kTileABytes = kRowsA * kBlockKBytes;
+    static constexpr int kAtoms = kGroup == 2 ? 2 : 1;     // 128-byte K atoms per stage
+    static constexpr int kStageKBytes = kAtoms * kBlockKBytes;
+    static constexpr int kStages = kGroup == 2 ? 3 : 4;
+    static constexpr int kAtomBBytes = kRowsB * kBlockKBytes;
+    static constexpr int kAtomABytes = kRowsA * kBlockKBytes;
+    static constexpr int kSliceAtomBytes = kSliceB * kBlockKBytes;
+    static constexpr int kTileBBytes = kAtoms * kAtomBBytes;
+    static constexpr int kSliceBBytes = kAtoms * kSliceAtomBytes;
+    static constexpr int kTileABytes = kAtoms * kAtomABytes;
     static constexpr int kStageBytes = kTileBBytes + kTileABytes;
     static constexpr int kSmemRing = kStages * kStageBytes;
     // loaded[S], empty[S], accfull[2], accempty[2], drain, never
@@ -345,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 {
     using Cfg = TileCfg<kGroup>;
     constexpr int kStages = Cfg::kStages;
-    constexpr int kBlockKElems = kBlockKBytes / Kind::kElemBytes;
+    constexpr int kBlockKElems = kBlockKBytes / Kind::kElemBytes;   // K elements per atom
     constexpr uint32_t kIdesc = ptx::idesc_f32acc(Cfg::kTileN, kTileM, Kind::kFmt, Kind::kFmt);
     constexpr uint32_t kIdescHalf = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 2, Kind::kFmt, Kind::kFmt);
 
@@ -478,16 +489,25 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     if constexpr (kGroup == 2) {
                         if (pos == 0) ptx::mbar_arrive_expect_tx(loaded_bar(stage), 2 * fill);
                         const uint32_t lb = ptx::mapa_shared(loaded_bar(stage), lead);
-                        if (shared)   // this CTA's half of the B rows, into itself and its counterpart
-                            ptx::tma_load_2d_pair_multicast(s_b + pair * Cfg::kSliceBBytes, &p.tmap_b_slice, lb,
-                                                            kb * kBlockKElems, nb + pair * Cfg::kSliceB, mcast);
-                        else
-                            ptx::tma_load_2d_pair(s_b, &p.tmap_b, lb, kb * kBlockKElems, nb);
-                        ptx::tma_load_2d_pair(s_a, map_a, lb, kb * kBlockKElems, m0);
+#pragma unroll
+                        for (int t = 0; t < Cfg::kAtoms; ++t) {
+                            const int32_t k0 = (kb * Cfg::kAtoms + t) * kBlockKElems;
+                            const uint32_t sb = s_b + t * Cfg::kAtomBBytes;
+                            if (shared)   // this CTA's half of the B rows, into itself and its counterpart
+                                ptx::tma_load_2d_pair_multicast(sb + pair * Cfg::kSliceAtomBytes, &p.tmap_b_slice, lb,
+                                                                k0, nb + pair * Cfg::kSliceB, mcast);
+                            else
+                                ptx::tma_load_2d_pair(sb, &p.tmap_b, lb, k0, nb);
+                            ptx::tma_load_2d_pair(s_a + t * Cfg::kAtomABytes, map_a, lb, k0, m0);
+                        }
                     } else {
                         ptx::mbar_arrive_expect_tx(loaded_bar(stage), fill);
-                        ptx::tma_load_2d(s_b, &p.tmap_b, loaded_bar(stage), kb * kBlockKElems, nb);
-                        ptx::tma_load_2d(s_a, map_a, loaded_bar(stage), kb * kBlockKElems, m0);
+#pragma unroll
+                        for (int t = 0; t < Cfg::kAtoms; ++t) {
+                            const int32_t k0 = (kb * Cfg::kAtoms + t) * kBlockKElems;
+                            ptx::tma_load_2d(s_b + t * Cfg::kAtomBBytes, &p.tmap_b, loaded_bar(stage), k0, nb);
+                            ptx::tma_load_2d(s_a + t * Cfg::kAtomABytes, map_a, loaded_bar(stage), k0, m0);
+                        }
                     }
                     *issued_count = ++n_issued;
                     if (++stage == kStages) {
@@ -556,13 +576,16 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     ptx::tc_fence_after_sync();
                     const uint32_t s_b = s_ring + stage * Cfg::kStageBytes;
                     const uint32_t s_a = s_b + Cfg::kTileBBytes;
-                    const uint64_t desc_b = ptx::desc_kmajor_sw128(s_b);
-                    const uint64_t desc_a = ptx::desc_kmajor_sw128(s_a);
 #pragma unroll
-                    for (int j = 0; j < kBlockKBytes / kMmaKBytes; ++j) {
-                        // +32 bytes along K inside the 128-byte swizzle span = +2 in the address field
-                        Kind::template mma<kGroup>(d_tmem, desc_b + 2u * j, desc_a + 2u * j, idesc,
-                                                   (kk | j) != 0 ? 1u : 0u);
+                    for (int t = 0; t < Cfg::kAtoms; ++t) {
+                        const uint64_t desc_b = ptx::desc_kmajor_sw128(s_b + t * Cfg::kAtomBBytes);
+                        const uint64_t desc_a = ptx::desc_kmajor_sw128(s_a + t * Cfg::kAtomABytes);
+#pragma unroll
+                        for (int j = 0; j < kBlockKBytes / kMmaKBytes; ++j) {
+                            // +32 bytes along K inside the 128-byte swizzle span = +2 in the address field
+                            Kind::template mma<kGroup>(d_tmem, desc_b + 2u * j, desc_a + 2u * j, idesc,
+                                                       (kk | t | j) != 0 ? 1u : 0u);
+                        }
                     }
                     issued_any = true;
                     ptx::mma_commit<kGroup>(empty_bar(stage), all_mask);   // stage free for every CTA that writes it
