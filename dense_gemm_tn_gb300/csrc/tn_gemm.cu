@@ -171,10 +171,47 @@ gemm_status_t split_workspace(DeviceState &d, cudaStream_t stream, size_t ticket
     return GEMM_OK;
 }
 
+// Tensor maps are a pure function of their arguments (address, sizes, stride,
+// box, type), so encoded maps are cached and reused: repeated calls on the
+// same buffers skip cuTensorMapEncodeTiled.  Least recently used entries go.
+struct MapKey {
+    uintptr_t base;
+    uint64_t inner, outer, row_bytes;
+    uint32_t box_inner, box_outer;
+    int type;
+    bool operator==(const MapKey &o) const
+    {
+        return base == o.base && inner == o.inner && outer == o.outer && row_bytes == o.row_bytes &&
+               box_inner == o.box_inner && box_outer == o.box_outer && type == o.type;
+    }
+};
+
+struct MapCache {
+    static constexpr int kEntries = 64;
+    MapKey key[kEntries];
+    CUtensorMap map[kEntries];
+    uint64_t used_at[kEntries] = {};
+    int size = 0;
+    uint64_t clock = 0;
+    std::mutex mutex;
+};
+MapCache g_maps;
+
 gemm_status_t encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *base, uint64_t inner,
                         uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                         const char *what)
 {
+    const MapKey key{reinterpret_cast<uintptr_t>(base), inner, outer, row_bytes, box_inner, box_outer,
+                     static_cast<int>(type)};
+    {
+        std::lock_guard<std::mutex> lock(g_maps.mutex);
+        for (int i = 0; i < g_maps.size; ++i)
+            if (g_maps.key[i] == key) {
+                g_maps.used_at[i] = ++g_maps.clock;
+                *map = g_maps.map[i];
+                return GEMM_OK;
+            }
+    }
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const cuuint64_t dims[2] = {inner, outer};
@@ -185,6 +222,18 @@ gemm_status_t encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
+    std::lock_guard<std::mutex> lock(g_maps.mutex);
+    int slot = g_maps.size;
+    if (slot == MapCache::kEntries) {
+        slot = 0;
+        for (int i = 1; i < MapCache::kEntries; ++i)
+            if (g_maps.used_at[i] < g_maps.used_at[slot]) slot = i;
+    } else {
+        ++g_maps.size;
+    }
+    g_maps.key[slot] = key;
+    g_maps.map[slot] = *map;
+    g_maps.used_at[slot] = ++g_maps.clock;
     return GEMM_OK;
 }
 
@@ -354,7 +403,12 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     // sharing B rows (gemm_debug_force_cta_group(4)); with 256-byte K stages
     // that loses on every shape measured on GB300 (3000x12288x4096: -3.5 %,
     // the shape where it used to win), so the library does not choose it.
+    // A problem of at most half a wave of pair tiles runs on single CTAs: it
+    // is latency-bound, and a CTA without a partner skips the cluster
+    // barriers (measured on GB300: 1024 x 1024 x 128 5.8 -> 4.3 us per
+    // kernel, 512^3 9.1 -> 6.0 us).
     int ctas = N > 128 ? 2 : 1;
+    if (ctas == 2 && 2 * (((M + 255) / 256) * ((N + 255) / 256)) <= dev->sms / 2) ctas = 1;
     if (const int forced = g_force_cta_group.load()) ctas = forced;
     const int cta_group = ctas >= 2 ? 2 : 1;
     const bool quad = ctas == 4;
