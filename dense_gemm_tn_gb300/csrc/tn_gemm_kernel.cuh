@@ -87,8 +87,8 @@ struct TileCfg {
     static constexpr int kTileABytes = kAtoms * kAtomABytes;
     static constexpr int kStageBytes = kTileBBytes + kTileABytes;
     static constexpr int kSmemRing = kStages * kStageBytes;
-    // loaded[S], empty[S], accfull[2], accempty[2], drain, never
-    static constexpr int kNumBarriers = 2 * kStages + 6;
+    // loaded[S][atoms], empty[S], accfull[2], accempty[2], drain, never
+    static constexpr int kNumBarriers = kStages * (kAtoms + 1) + 6;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kSmemRing + kSmemEpi + kNumBarriers * 8 + 32;
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB shared memory of one CTA");
 };
@@ -300,7 +300,7 @@ struct KindE4M3 {
 // (mbarrier.complete_tx), otherwise it arms the fill for the bytes that will
 // (arrive.expect_tx).  Then it waits for the phase.  On the normal path every
 // producer issued every fill and each wait returns at once.
-template <int kStages, int kMaxCtas, class LoadedBar, class Contribution>
+template <int kStages, int kAtoms, int kMaxCtas, class LoadedBar, class Contribution>
 __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar loaded_bar, Contribution contribution,
                                                     uint32_t n_own, uint32_t count_addr, uint32_t done_addr)
 {
@@ -341,12 +341,15 @@ __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar l
             total += c;
             if (passes[q] == hi) sent += c;
         }
-        if (passes[w.rank] == hi) {
-            if (total > sent) ptx::mbar_complete_tx(loaded_bar(s), total - sent);
-        } else {
-            ptx::mbar_arrive_expect_tx(loaded_bar(s), sent);
+        // every atom of a fill carries the same share of its bytes, on its own barrier
+        for (int t = 0; t < kAtoms; ++t) {
+            if (passes[w.rank] == hi) {
+                if (total > sent) ptx::mbar_complete_tx(loaded_bar(s, t), (total - sent) / kAtoms);
+            } else {
+                ptx::mbar_arrive_expect_tx(loaded_bar(s, t), sent / kAtoms);
+            }
+            w.drain(loaded_bar(s, t), (hi - 1) & 1u);
         }
-        w.drain(loaded_bar(s), (hi - 1) & 1u);
     }
 }
 
@@ -375,12 +378,16 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     const uint32_t bar0 = ptx::smem_addr(bars);
     // loaded[s]: the stage's bytes (of both CTAs of a pair) have landed; used in even CTAs only
-    auto loaded_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };        // every pair done reading
-    auto accfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-    auto accempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
-    const uint32_t never_bar = bar0 + 8u * (2 * kStages + 5);                 // nothing ever arrives
+    // One loaded barrier per 128-byte atom of a stage, so the MMAs of an atom
+    // start as soon as its own bytes have landed; one empty barrier per stage.
+    constexpr int kAtoms = Cfg::kAtoms;
+    constexpr int kLoadedBars = kStages * kAtoms;
+    auto loaded_bar = [&](int s, int t) { return bar0 + 8u * (s * kAtoms + t); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kLoadedBars + s); };      // every pair done reading
+    auto accfull_bar = [&](int b) { return bar0 + 8u * (kLoadedBars + kStages + b); };
+    auto accempty_bar = [&](int b) { return bar0 + 8u * (kLoadedBars + kStages + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (kLoadedBars + kStages + 4);
+    const uint32_t never_bar = bar0 + 8u * (kLoadedBars + kStages + 5);        // nothing ever arrives
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -397,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(loaded_bar(s), 1);
+            for (int t = 0; t < kAtoms; ++t) ptx::mbar_init(loaded_bar(s, t), 1);
             ptx::mbar_init(empty_bar(s), pairs);
         }
         for (int b = 0; b < 2; ++b) {
@@ -487,10 +494,10 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     const uint32_t s_b = s_ring + stage * Cfg::kStageBytes;
                     const uint32_t s_a = s_b + Cfg::kTileBBytes;
                     if constexpr (kGroup == 2) {
-                        if (pos == 0) ptx::mbar_arrive_expect_tx(loaded_bar(stage), 2 * fill);
-                        const uint32_t lb = ptx::mapa_shared(loaded_bar(stage), lead);
 #pragma unroll
                         for (int t = 0; t < Cfg::kAtoms; ++t) {
+                            if (pos == 0) ptx::mbar_arrive_expect_tx(loaded_bar(stage, t), 2 * fill / kAtoms);
+                            const uint32_t lb = ptx::mapa_shared(loaded_bar(stage, t), lead);
                             const int32_t k0 = (kb * Cfg::kAtoms + t) * kBlockKElems;
                             const uint32_t sb = s_b + t * Cfg::kAtomBBytes;
                             if (shared)   // this CTA's half of the B rows, into itself and its counterpart
@@ -501,12 +508,12 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                             ptx::tma_load_2d_pair(s_a + t * Cfg::kAtomABytes, map_a, lb, k0, m0);
                         }
                     } else {
-                        ptx::mbar_arrive_expect_tx(loaded_bar(stage), fill);
 #pragma unroll
                         for (int t = 0; t < Cfg::kAtoms; ++t) {
                             const int32_t k0 = (kb * Cfg::kAtoms + t) * kBlockKElems;
-                            ptx::tma_load_2d(s_b + t * Cfg::kAtomBBytes, &p.tmap_b, loaded_bar(stage), k0, nb);
-                            ptx::tma_load_2d(s_a + t * Cfg::kAtomABytes, map_a, loaded_bar(stage), k0, m0);
+                            ptx::mbar_arrive_expect_tx(loaded_bar(stage, t), fill / kAtoms);
+                            ptx::tma_load_2d(s_b + t * Cfg::kAtomBBytes, &p.tmap_b, loaded_bar(stage, t), k0, nb);
+                            ptx::tma_load_2d(s_a + t * Cfg::kAtomABytes, map_a, loaded_bar(stage, t), k0, m0);
                         }
                     }
                     *issued_count = ++n_issued;
@@ -537,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                             return a_bytes(uq) + (shared ? Cfg::kSliceBBytes : Cfg::kTileBBytes);
                         return shared ? Cfg::kSliceBBytes : 0u;
                     };
-                    drain_cluster_loads<kStages, Cfg::kMaxCtas>(w, loaded_bar, contribution, n_issued, count_addr,
+                    drain_cluster_loads<kStages, kAtoms, Cfg::kMaxCtas>(w, loaded_bar, contribution, n_issued, count_addr,
                                                                 done_addr);
                 }
             } else {
@@ -545,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 for (int s = 0; s < kStages; ++s) {
                     const uint32_t passes =
                         n_issued / kStages + (static_cast<uint32_t>(s) < n_issued % kStages ? 1u : 0u);
-                    if (passes) w.drain(loaded_bar(s), (passes - 1) & 1u);
+                    for (int t = 0; t < kAtoms && passes; ++t) w.drain(loaded_bar(s, t), (passes - 1) & 1u);
                 }
             }
         }
@@ -569,15 +576,15 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * kAccCols;
                 for (int kk = 0; kk < un.nkb; ++kk) {
-                    if (!w.wait(loaded_bar(stage), phase, kSiteLoaded)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after_sync();
                     const uint32_t s_b = s_ring + stage * Cfg::kStageBytes;
                     const uint32_t s_a = s_b + Cfg::kTileBBytes;
 #pragma unroll
                     for (int t = 0; t < Cfg::kAtoms; ++t) {
+                        if (!w.wait(loaded_bar(stage, t), phase, kSiteLoaded)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after_sync();
                         const uint64_t desc_b = ptx::desc_kmajor_sw128(s_b + t * Cfg::kAtomBBytes);
                         const uint64_t desc_a = ptx::desc_kmajor_sw128(s_a + t * Cfg::kAtomABytes);
 #pragma unroll
@@ -586,8 +593,9 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                             Kind::template mma<kGroup>(d_tmem, desc_b + 2u * j, desc_a + 2u * j, idesc,
                                                        (kk | t | j) != 0 ? 1u : 0u);
                         }
+                        issued_any = true;
                     }
-                    issued_any = true;
+                    if (!ok) break;
                     ptx::mma_commit<kGroup>(empty_bar(stage), all_mask);   // stage free for every CTA that writes it
                     if (++stage == kStages) {
                         stage = 0;
