@@ -13,7 +13,8 @@ compute"): A row-major M x K, B column-major K x N, C column-major with
 leading dimension M.  Accumulation is sequential in k in double, rounded once
 to the output type with round-to-nearest-even.
 
-Also: per-tensor E4M3 quantisation (amax, scale to 448, one RNE rounding),
+Also: the scaled-score GEMM with the softmax's row statistics (row maximum and
+sum of exponentials), and per-tensor E4M3 quantisation (amax, scale to 448, one RNE rounding),
 the step that produces the F8 GEMM's operands.
 
 Pins (tests/test_oracle.py): the worked example and its partial sums, the
@@ -75,6 +76,9 @@ def _load():
     lib.oracle_gemm_f8e4m3_tn_at.argtypes = [i64, i64, i64, p, i64, p, i64,
                                              ctypes.c_float, ctypes.c_float,
                                              i64, p, p, p, p, p]
+    lib.oracle_gemm_f16_tn_softmax_stats.restype = ctypes.c_int
+    lib.oracle_gemm_f16_tn_softmax_stats.argtypes = [i64, i64, i64, p, i64, p, i64, ctypes.c_double,
+                                                     p, i64, p, p, p]
     lib.oracle_e4m3_encode.restype = ctypes.c_uint8
     lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
     lib.oracle_quantize_e4m3.restype = ctypes.c_int
@@ -185,6 +189,23 @@ def gemm_f16_tn_at(M, N, K, A, lda, B, ldb, m_idx, n_idx):
     if rc != 0:
         raise ValueError("oracle_gemm_f16_tn_at rejected its arguments")
     return c, s, x
+
+
+def gemm_f16_tn_softmax_stats(M, N, K, A, lda, B, ldb, scale, ldc=None):
+    """Scaled scores Y = scale * A B (C = binary16(Y), column-major with ldc)
+    and per row m: row_max = max_n Y[m,n], row_sum = sum_n exp(Y[m,n] - row_max).
+    Returns (C flat codes, row_max (M,), row_sum (M,), S (N, M))."""
+    ldc = M if ldc is None else ldc
+    A, B = _check_operands(A, B, M, N, K, lda, ldb, np.uint16)
+    C = np.zeros(max(ldc * N, 1), dtype=np.uint16)
+    row_max = np.full(M, np.nan)
+    row_sum = np.full(M, np.nan)
+    S = np.zeros((N, M), dtype=np.float64)
+    rc = _load().oracle_gemm_f16_tn_softmax_stats(M, N, K, _ptr(A), lda, _ptr(B), ldb, float(scale),
+                                                  _ptr(C), ldc, _ptr(row_max), _ptr(row_sum), _ptr(S))
+    if rc != 0:
+        raise ValueError("oracle_gemm_f16_tn_softmax_stats rejected its arguments")
+    return C, row_max, row_sum, S
 
 
 def gemm_f8e4m3_tn(M, N, K, A, lda, B, ldb, scale_a, scale_b, ldc=None):

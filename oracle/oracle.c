@@ -28,6 +28,9 @@
  *     S[m,n] = sum_k |A[m,k] * B[k,n]|  (the magnitude sum used by the
  *              acceptance tolerance), both in double.
  *
+ *   Scaled-score variant (QK^T with the softmax's row statistics): see
+ *   oracle_gemm_f16_tn_softmax_stats below.
+ *
  *   Before the F8 GEMM, an operand may be quantised to E4M3 per tensor
  *   (oracle_quantize_e4m3 below; amax over the tensor, scale to 448).
  *
@@ -298,6 +301,47 @@ int oracle_gemm_f16_tn(int64_t M, int64_t N, int64_t K,
             if (S) S[m + n * M] = s;
             if (X) X[m + n * M] = x;
         }
+    }
+    return 0;
+}
+
+/* Scaled scores and the softmax's row statistics (the QK^T step of attention,
+ * followed by the two reductions a softmax over n needs):
+ *   Y[m,n]     = scale * sum_k A[m,k] * B[k,n]          (double)
+ *   C[m,n]     = binary16(Y[m,n])                       (one RNE rounding)
+ *   row_max[m] = max_n Y[m,n]
+ *   row_sum[m] = sum_n exp(Y[m,n] - row_max[m])         (double, n ascending)
+ * S[m,n] (optional) = |scale| * sum_k |A[m,k] * B[k,n]|.  N = 0 leaves the
+ * statistics unwritten. */
+int oracle_gemm_f16_tn_softmax_stats(int64_t M, int64_t N, int64_t K,
+                                     const uint16_t *A, int64_t lda,
+                                     const uint16_t *B, int64_t ldb, double scale,
+                                     uint16_t *C, int64_t ldc,
+                                     double *row_max, double *row_sum, double *S)
+{
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (lda < (K > 1 ? K : 1) || ldb < (K > 1 ? K : 1) || ldc < (M > 1 ? M : 1)) return -1;
+    tables_init();
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t m = 0; m < M; ++m) {
+        double mx = -INFINITY;
+        for (int64_t n = 0; n < N; ++n) {
+            double x, s;
+            dot_f16(K, A + m * lda, B + n * ldb, &x, &s);
+            const double y = scale * x;
+            C[m + n * ldc] = oracle_fp16_encode(y);
+            if (S) S[m + n * M] = fabs(scale) * s;
+            if (y > mx) mx = y;
+        }
+        if (N == 0) continue;
+        double sum = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+            double x, s;
+            dot_f16(K, A + m * lda, B + n * ldb, &x, &s);
+            sum += exp(scale * x - mx);
+        }
+        row_max[m] = mx;
+        row_sum[m] = sum;
     }
     return 0;
 }
