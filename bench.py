@@ -46,6 +46,8 @@ def metric_for(w: synth.Workload) -> str:
     what = "FP8 e4m3" if w.dtype == "e4m3" else "FP16"
     if w.values == "bf16":
         what = "bf16 -> e4m3 quantise + FP8"
+    if w.op == "softmax_stats":
+        what = "FP16 scaled scores + softmax row statistics,"
     return f"TFLOP/s (2MNK/t) {what} TN GEMM {w.M}x{w.N}x{w.K} on 1 GB300; % of dense tensor peak"
 
 
@@ -203,6 +205,27 @@ def run_reference(args, w: synth.Workload, rank: int) -> None:
     import oracle
     A, B, sa, sb = synth.make_inputs(w, 0)
     note = ""
+    if w.op == "softmax_stats":
+        # one step = the whole (small) problem, scores and statistics
+        t_steps = []
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            oracle.gemm_f16_tn_softmax_stats(w.M, w.N, w.K, A, w.K, B, w.K, 1.0 / float(np.sqrt(w.K)))
+            if i >= args.warmup:
+                t_steps.append(time.perf_counter() - t0)
+        dt = sum(t_steps) / len(t_steps)
+        value = 2.0 * w.M * w.N * w.K / dt / 1e12
+        print(json.dumps({
+            "impl": "reference", "metric": metric_for(w), "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name}: M={w.M} N={w.N} K={w.K}, the whole problem per step",
+                       "M": w.M, "N": w.N, "K": w.K},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": "the whole problem per step"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
     if w.values == "bf16":
         # the oracle's quantisation runs once, outside the timed steps
         A, sa = oracle.quantize_e4m3(A, "bf16", w.M, w.K)
@@ -284,6 +307,12 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
         dscale = torch.empty(2, dtype=torch.float32, device=dev)
         qa_p, qb_p, sa_p, sb_p = qA.data_ptr(), qB.data_ptr(), dscale.data_ptr(), dscale.data_ptr() + 4
     launches_per_step = 5 if pipeline else 1
+    stats = w.op == "softmax_stats"
+    if stats:
+        sm_scale = 1.0 / float(np.sqrt(K))
+        row_max = torch.empty(M, dtype=torch.float32, device=dev)
+        row_sum = torch.empty(M, dtype=torch.float32, device=dev)
+        rmax_p, rsum_p = row_max.data_ptr(), row_sum.data_ptr()
 
     def issue(j, a, b, c, mid=None):
         """One step's work on the stream: returns the status codes of its calls."""
@@ -296,6 +325,8 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
             return r
         if is_f8:
             return [g.lib.gemm_f8e4m3_tn(M, N, K, a, K, b, K, c, M, scales[j][0], scales[j][1], sh)]
+        if stats:
+            return [g.lib.gemm_f16_tn_softmax_stats(M, N, K, a, K, b, K, c, M, sm_scale, rmax_p, rsum_p, sh)]
         return [g.lib.gemm_f16_tn(M, N, K, a, K, b, K, c, M, sh)]
 
     def step(i, mid=None):
@@ -388,7 +419,7 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
     g.gemm_poll_device_status(sh)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     h2d = (M * K + N * K) * esz
-    d2h = M * N * 2
+    d2h = M * N * 2 + (8 * M if stats else 0)
     total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, dev)
     ms_per_step = total_ms / args.steps
     flop = 2.0 * M * N * K
@@ -413,6 +444,13 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
             t_q = time.perf_counter() - t0
             tf, cores, desc = oracle_sample(w, qa_ref, qb_ref, sa_ref, sb_ref, target_s=args.cpu_seconds)
             desc += f"; the oracle's quantisation of both operands took a further {t_q:.1f} s"
+        elif stats:
+            import oracle
+            t0 = time.perf_counter()
+            oracle.gemm_f16_tn_softmax_stats(M, N, K, host[0][0], K, host[0][1], K, 1.0 / float(np.sqrt(K)))
+            dt = time.perf_counter() - t0
+            tf, cores = 2.0 * M * N * K / dt / 1e12, oracle.num_threads()
+            desc = f"the whole {w.name} problem (scores and statistics), {dt:.2f} s"
         else:
             tf, cores, desc = oracle_sample(w, *host[0], target_s=args.cpu_seconds)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}

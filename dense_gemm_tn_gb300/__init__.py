@@ -10,6 +10,7 @@ The same names as the C ABI:
     gemm_f8e4m3_tn(M, N, K, A, lda, B, ldb, C, ldc, scale_a, scale_b, stream=None)
     gemm_f8e4m3_tn_dscale(M, N, K, A, lda, B, ldb, C, ldc, scale_a_ptr, scale_b_ptr, stream=None)
     gemm_quantize_e4m3(x, x_type, rows, cols, ldx, q, ldq, scale_ptr, stream=None)
+    gemm_f16_tn_softmax_stats(M, N, K, A, lda, B, ldb, C, ldc, scale, row_max, row_sum, stream=None)
     gemm_poll_device_status(stream=None)
 
 A, B and C are device pointers given as ints or as CUDA torch tensors (their
@@ -43,7 +44,7 @@ EXPORTS = (
     "gemm_poll_device_status", "gemm_release_workspace", "gemm_tile_coord",
     "gemm_set_wait_limit_ns", "gemm_debug_inject_stall", "gemm_build_info",
     "gemm_f16_tn_noalloc", "gemm_debug_force_cta_group", "gemm_debug_last_launch",
-    "gemm_f8e4m3_tn_dscale", "gemm_quantize_e4m3",
+    "gemm_f8e4m3_tn_dscale", "gemm_quantize_e4m3", "gemm_f16_tn_softmax_stats",
 )
 
 GEMM_IN_F32 = 0
@@ -71,6 +72,8 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f8e4m3_tn.restype = st
     lib.gemm_f8e4m3_tn_dscale.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, vp, vp]
     lib.gemm_f8e4m3_tn_dscale.restype = st
+    lib.gemm_f16_tn_softmax_stats.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, ctypes.c_float, vp, vp, vp]
+    lib.gemm_f16_tn_softmax_stats.restype = st
     lib.gemm_quantize_e4m3.argtypes = [vp, st, i64, i64, i64, vp, i64, vp, vp]
     lib.gemm_quantize_e4m3.restype = st
     lib.gemm_f16_tn_noalloc.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, vp]
@@ -159,6 +162,13 @@ def gemm_f8e4m3_tn_dscale(M, N, K, A, lda, B, ldb, C, ldc, scale_a, scale_b, str
                                              _ptr(scale_a), _ptr(scale_b), _stream(stream)))
 
 
+def gemm_f16_tn_softmax_stats(M, N, K, A, lda, B, ldb, C, ldc, scale, row_max, row_sum, stream=None) -> int:
+    """Scaled scores C = fp16(scale * A B) with the softmax row statistics
+    (row_max, row_sum: device float arrays of M)."""
+    return _check(_lib.gemm_f16_tn_softmax_stats(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, float(scale),
+                                                 _ptr(row_max), _ptr(row_sum), _stream(stream)))
+
+
 def gemm_quantize_e4m3(x, x_type, rows, cols, ldx, q, ldq, scale, stream=None) -> int:
     """Per-tensor E4M3 quantisation on the device: codes into q, amax / 448 into *scale."""
     return _check(_lib.gemm_quantize_e4m3(_ptr(x), int(x_type), rows, cols, ldx, _ptr(q), ldq, _ptr(scale),
@@ -215,6 +225,22 @@ def f16_tn(A, Bt, C=None, stream=None):
     gemm_f16_tn(M, N, K, A, A.stride(0) if M > 0 else max(K, 1), Bt,
                 Bt.stride(0) if N > 0 else max(K, 1), C, C.stride(0) if N > 0 else max(M, 1), stream)
     return C
+
+
+def f16_tn_softmax_stats(Q, Kmat, scale, C=None, stream=None):
+    """Q (M, K) and Kmat (N, K) fp16 CUDA tensors -> (S^T as an (N, M) fp16
+    tensor, row_max (M,), row_sum (M,)): S = scale * Q Kmat^T."""
+    import torch
+    M, K = Q.shape
+    N = Kmat.shape[0]
+    if C is None:
+        C = torch.empty((N, M), dtype=torch.float16, device=Q.device)
+    row_max = torch.empty(M, dtype=torch.float32, device=Q.device)
+    row_sum = torch.empty(M, dtype=torch.float32, device=Q.device)
+    gemm_f16_tn_softmax_stats(M, N, K, Q, Q.stride(0) if M > 0 else max(K, 1), Kmat,
+                              Kmat.stride(0) if N > 0 else max(K, 1), C, C.stride(0) if N > 0 else max(M, 1),
+                              scale, row_max, row_sum, stream)
+    return C, row_max, row_sum
 
 
 def quantize_e4m3(x, stream=None):

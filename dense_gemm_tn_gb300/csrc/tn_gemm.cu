@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
@@ -50,6 +51,8 @@ struct DeviceState {
     std::unordered_map<cudaStream_t, Split> split;
     // Per-CTA maxima of the quantiser, one array per stream.
     std::unordered_map<cudaStream_t, Split> quant;
+    // Softmax statistics: [tickets per tile row | parts], one buffer per stream.
+    std::unordered_map<cudaStream_t, Split> stats;
     int quant_blocks[3] = {};         // co-resident quantiser CTAs per SM, by input type (0 = not queried)
     unsigned long long epoch = 0;
 };
@@ -335,7 +338,8 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     prm.tail_mode = tn::kTailNone;
     prm.tail_start = prm.num_tiles;
     prm.num_units = prm.num_tiles;
-    if (waves >= 1 && rem > 0 && 2 * rem <= clusters) {
+    // (The softmax statistics need every tile whole in one CTA pair.)
+    if (waves >= 1 && rem > 0 && 2 * rem <= clusters && !(prm.flags & tn::kFlagStats)) {
         prm.tail_start = waves * clusters;
         prm.num_units = prm.tail_start + 2 * rem;
         prm.tail_mode = tn::kTailHalfM;
@@ -365,8 +369,10 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
 template <class Kind>
 gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda,
                        const void *B, int64_t ldb, void *C, int64_t ldc, float scale, cudaStream_t stream,
-                       bool allow_alloc = true, const float *dscale_a = nullptr, const float *dscale_b = nullptr)
+                       bool allow_alloc = true, const float *dscale_a = nullptr, const float *dscale_b = nullptr,
+                       float *row_max = nullptr, float *row_sum = nullptr)
 {
+    const bool stats = row_max != nullptr;
     constexpr int64_t esz = Kind::kElemBytes;
     const int64_t kmin = K > 1 ? K : 1;
     if (M < 0 || N < 0 || K < 0)
@@ -390,8 +396,13 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     if (st != GEMM_OK) return st;
 
     if (K == 0) {
+        // every sum is +0; scaled scores are scale * +0 (-0 for a negative scale)
+        const uint16_t fill = stats && std::signbit(scale) ? 0x8000u : 0u;
         tn::zero_fill_kernel<<<launch_grid(M * N, dev->sms * 8), 256, 0, stream>>>(static_cast<uint16_t *>(C), ldc,
-                                                                                 M, N);
+                                                                                 M, N, fill);
+        if (stats)
+            tn::fill_stats_kernel<<<launch_grid(M, dev->sms), 256, 0, stream>>>(row_max, row_sum, M,
+                                                                              static_cast<float>(N));
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: zero fill launch: %s", name, cudaGetErrorString(e));
         return GEMM_OK;
@@ -411,7 +422,7 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     if (ctas == 2 && 2 * (((M + 255) / 256) * ((N + 255) / 256)) <= dev->sms / 2) ctas = 1;
     if (const int forced = g_force_cta_group.load()) ctas = forced;
     const int cta_group = ctas >= 2 ? 2 : 1;
-    const bool quad = ctas == 4;
+    const bool quad = ctas == 4 && !stats;
     const int64_t tiles_m = (M + tn::kTileM - 1) / tn::kTileM;
     const int64_t tiles_n = (N + 128 * cta_group - 1) / (128 * cta_group);
     if (tiles_m * tiles_n > INT32_MAX) return fail(GEMM_ERR_UNSUPPORTED, "%s: too many output tiles", name);
@@ -489,7 +500,23 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     prm.scale = scale;
     prm.scale_a_ptr = dscale_a;
     prm.scale_b_ptr = dscale_b;
-    prm.flags = (tma_c ? tn::kFlagTmaStore : 0u) | stall_flags(g_inject_stall.load());
+    if (stats) {
+        prm.flags |= tn::kFlagStats;
+        prm.row_max = row_max;
+        prm.row_sum = row_sum;
+        prm.stat_ctas = static_cast<int32_t>(tiles_n * cta_group);
+        const size_t parts = size_t(tiles_m) * prm.stat_ctas * tn::kEpiWarps * tn::kTileM * sizeof(float2);
+        uint8_t *base = nullptr;
+        size_t zeroed = 0;
+        if ((st = stream_buffer(dev->stats, stream, size_t(tiles_m) * sizeof(unsigned long long), parts,
+                                "softmax statistics", &base, &zeroed)) != GEMM_OK)
+            return st;
+        prm.stat_tickets = reinterpret_cast<unsigned long long *>(base);
+        prm.stat_parts = reinterpret_cast<float2 *>(base + zeroed);
+        std::lock_guard<std::mutex> lock(g_mutex);
+        prm.epoch = ++dev->epoch;
+    }
+    prm.flags |= (tma_c ? tn::kFlagTmaStore : 0u) | stall_flags(g_inject_stall.load());
     prm.wait_limit_ns = g_wait_limit_ns.load();
 
     if (cta_group == 2) return launch<Kind, 2>(name, prm, *dev, quad, allow_alloc, stream);
@@ -634,6 +661,24 @@ gemm_status_t gemm_f8e4m3_tn_dscale(int64_t M, int64_t N, int64_t K, const void 
                                   static_cast<cudaStream_t>(stream), true, scale_a, scale_b);
 }
 
+gemm_status_t gemm_f16_tn_softmax_stats(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                                        int64_t ldb, void *C, int64_t ldc, float scale, float *row_max,
+                                        float *row_sum, void *stream)
+{
+    t_last_error[0] = '\0';
+    if (M > 0 && N > 0) {
+        if (!row_max || !row_sum)
+            return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_tn_softmax_stats: row_max or row_sum is NULL");
+        if (reinterpret_cast<uintptr_t>(row_max) % 4 || reinterpret_cast<uintptr_t>(row_sum) % 4)
+            return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_tn_softmax_stats: row_max or row_sum is not 4-byte aligned");
+        if (!std::isfinite(scale))
+            return fail(GEMM_ERR_INVALID_ARG, "gemm_f16_tn_softmax_stats: scale is not finite");
+    }
+    return run_gemm<tn::KindF16>("gemm_f16_tn_softmax_stats", M, N, K, A, lda, B, ldb, C, ldc, scale,
+                                 static_cast<cudaStream_t>(stream), true, nullptr, nullptr,
+                                 M > 0 && N > 0 ? row_max : nullptr, row_sum);
+}
+
 gemm_status_t gemm_quantize_e4m3(const void *x, int x_type, int64_t rows, int64_t cols, int64_t ldx, void *q,
                                  int64_t ldq, float *scale, void *stream)
 {
@@ -686,6 +731,9 @@ void gemm_release_workspace(void)
     for (auto &kv : d.quant)
         if (kv.second.ptr) cudaFree(kv.second.ptr);
     d.quant.clear();
+    for (auto &kv : d.stats)
+        if (kv.second.ptr) cudaFree(kv.second.ptr);
+    d.stats.clear();
 }
 
 int gemm_tile_coord(int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t id, int64_t *tile_m, int64_t *tile_n)

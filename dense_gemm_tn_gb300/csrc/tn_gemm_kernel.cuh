@@ -31,6 +31,7 @@
 //       the main loop of tile i+1.
 #pragma once
 
+#include <cmath>
 #include <cstdint>
 #include <cuda.h>
 
@@ -104,6 +105,9 @@ constexpr uint32_t kFlagTmaStore = 1u;      // C rows m < m_tma are written with
 constexpr uint32_t kFlagStallMma = 2u;          // the MMA thread(s)
 constexpr uint32_t kFlagStallProducer0 = 4u;    // the producer of cluster CTA 0 (or of the only CTA)
 constexpr uint32_t kFlagStallProducer1 = 8u;    // the producer of cluster CTA 1 (the odd CTA of the first pair)
+// FP16 scaled scores with softmax row statistics: C = fp16(scale * acc), and
+// per row m the maximum and the sum of exp(score - maximum) over all n.
+constexpr uint32_t kFlagStats = 16u;
 
 // Status word of the current device; set (never cleared) by a kernel whose
 // bounded wait ran out: 4 (timeout) | site << 8.
@@ -137,6 +141,15 @@ struct KernelParams {
     // F8 with device-resident scales: when set, the epilogue multiplies by
     // (*scale_a_ptr) * (*scale_b_ptr) in FP32 instead of `scale`.
     const float *scale_a_ptr, *scale_b_ptr;
+    // Softmax statistics (kFlagStats).  Every CTA that computes a tile writes,
+    // per epilogue warp, the (max, sum) of its 32 columns n for each of the
+    // tile's 256 rows m into stat_parts[tile_m][part][256]; the last of the
+    // stat_ctas CTAs of a tile row (ticket in stat_tickets[tile_m], tagged with
+    // the launch's epoch) merges the parts in a fixed order into row_max/row_sum.
+    float *row_max, *row_sum;
+    float2 *stat_parts;
+    unsigned long long *stat_tickets;
+    int32_t stat_ctas;                  // tiles_n * CTAs per tile
     uint32_t flags;
     uint64_t wait_limit_ns;
 };
@@ -351,6 +364,84 @@ __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar l
             w.drain(loaded_bar(s, t), (hi - 1) & 1u);
         }
     }
+}
+
+// ------------------------------------------------------------------ softmax statistics
+// e^x for x <= 0 as 2^(x log2 e), with the ex2 instruction (relative error
+// about 2^-22; results below 2^-126 flush to 0; e^-inf = 0).  Measured on
+// GB300, the ex2 path that keeps subnormals (what expf and __expf compile to
+// without -ftz) made the statistics epilogue 2.6x slower.
+__device__ __forceinline__ float exp_nonpos(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+    return y;
+}
+
+// (max, sum) of two sets of values x, where sum = sum exp(x - max): the merge
+// of the online softmax.  An empty set is (-inf, 0).
+__device__ __forceinline__ void stat_merge(float &m, float &s, float m2, float s2)
+{
+    const float mx = fmaxf(m, m2);
+    if (mx == -INFINITY) {
+        m = mx;
+        s = 0.0f;
+        return;
+    }
+    s = s * exp_nonpos(m - mx) + s2 * exp_nonpos(m2 - mx);
+    m = mx;
+}
+
+// Each lane holds 32 scores x[j] (one per column j; -inf where the lane has
+// no column n).  Afterwards lane l holds, for column l, the maximum over the
+// 32 lanes and the sum of exp(x - maximum).  Two passes: the maximum by five
+// halving exchanges (each lane keeps half of its columns and takes its
+// partner's values for them), a broadcast of the 32 maxima, one exp per
+// score, and the sums by the same five exchanges.
+__device__ __forceinline__ void stat_reduce32_step_max(float (&v)[32], int lane)
+{
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+        const int o = 16 >> step;
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < o; ++j) {
+            const float keep = upper ? v[j + o] : v[j];
+            const float give = upper ? v[j] : v[j + o];
+            v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, o));
+        }
+    }
+}
+
+__device__ __forceinline__ void stat_reduce32_step_sum(float (&v)[32], int lane)
+{
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+        const int o = 16 >> step;
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < o; ++j) {
+            const float keep = upper ? v[j + o] : v[j];
+            const float give = upper ? v[j] : v[j + o];
+            v[j] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+        }
+    }
+}
+
+__device__ __forceinline__ float2 stat_warp_reduce32(const float (&x)[32], int lane)
+{
+    float t[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) t[j] = x[j];
+    stat_reduce32_step_max(t, lane);            // t[0] = maximum of column `lane`
+    const float col_max = t[0];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float mj = __shfl_sync(0xffffffffu, col_max, j);
+        t[j] = mj == -INFINITY ? 0.0f : exp_nonpos(x[j] - mj);
+    }
+    stat_reduce32_step_sum(t, lane);            // t[0] = sum for column `lane`
+    return make_float2(col_max, t[0]);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -756,12 +847,92 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 }
             } else {
                 const int n_chunks = (un.half >= 0 ? kTileM / 2 : kTileM) / kEpiBoxM;
+                const bool stats = !Kind::kF8 && (p.flags & kFlagStats) != 0;
 #pragma unroll 1
                 for (int c = 0; c < n_chunks; ++c) {
                     float v[64];
                     load_chunk(t_row, c * kEpiBoxM, v);
                     if (c == n_chunks - 1) release_acc();   // last read of this accumulator
+                    if constexpr (!Kind::kF8) {
+                        if (stats) {
+#pragma unroll
+                            for (int j = 0; j < 64; ++j) v[j] = __fmul_rn(v[j], p.scale);
+                        }
+                    }
                     store_chunk(v, m0 + c * kEpiBoxM, nw);
+                    if constexpr (!Kind::kF8) {
+                        if (stats) {
+                            // this warp's (max, sum) over its 32 columns n, for the chunk's 64 rows m
+                            const bool valid = nw + lane < p.N;
+                            float2 *part = p.stat_parts +
+                                           (static_cast<int64_t>(un.tm) * p.stat_ctas * kEpiWarps +
+                                            (un.tn * kGroup + pos) * kEpiWarps + quarter) * kTileM;
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                float x[32];
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) x[j] = valid ? v[32 * h + j] : -INFINITY;
+                                part[c * kEpiBoxM + 32 * h + lane] = stat_warp_reduce32(x, lane);
+                            }
+                        }
+                    }
+                }
+                if constexpr (!Kind::kF8) {
+                    if (stats) {
+                        // Take the tile row's ticket; the CTA that comes last merges every
+                        // part of the row in a fixed order, so no CTA waits for another.
+                        __threadfence();
+                        ptx::named_barrier_sync(1, kEpiWarps * 32);
+                        if (warp == 2 && lane == 0) {
+                            unsigned long long *ticket = p.stat_tickets + un.tm;
+                            const unsigned long long base = static_cast<unsigned long long>(p.epoch) << 32;
+                            atomicMax(ticket, base);
+                            const unsigned long long old = atomicAdd(ticket, 1ull);
+                            *second_flag = old - base == static_cast<unsigned long long>(p.stat_ctas - 1) ? 1u : 0u;
+                            __threadfence();
+                        }
+                        ptx::named_barrier_sync(1, kEpiWarps * 32);
+                        if (*second_flag != 0u) {
+                            __threadfence();
+                            const int nparts = p.stat_ctas * kEpiWarps;
+                            const float2 *row_parts =
+                                p.stat_parts + static_cast<int64_t>(un.tm) * nparts * kTileM;
+                            // thread t merges rows 2t and 2t+1, 16 parts of each in flight
+                            constexpr int kRows = kTileM / (kEpiWarps * 32);
+                            constexpr int kBatch = 16;
+                            const int t = ew * 32 + lane;
+                            float mx[kRows], sm[kRows];
+#pragma unroll
+                            for (int r = 0; r < kRows; ++r) {
+                                mx[r] = -INFINITY;
+                                sm[r] = 0.0f;
+                            }
+#pragma unroll 1
+                            for (int q0 = 0; q0 < nparts; q0 += kBatch) {
+                                float2 buf[kRows][kBatch];
+#pragma unroll
+                                for (int i = 0; i < kBatch; ++i)
+#pragma unroll
+                                    for (int r = 0; r < kRows; ++r)
+                                        buf[r][i] = q0 + i < nparts
+                                                        ? __ldcg(row_parts + static_cast<int64_t>(q0 + i) * kTileM +
+                                                                 t * kRows + r)
+                                                        : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+                                for (int i = 0; i < kBatch; ++i)
+#pragma unroll
+                                    for (int r = 0; r < kRows; ++r) stat_merge(mx[r], sm[r], buf[r][i].x, buf[r][i].y);
+                            }
+#pragma unroll
+                            for (int r = 0; r < kRows; ++r) {
+                                const int64_t m = static_cast<int64_t>(un.tm) * kTileM + t * kRows + r;
+                                if (m < p.M) {
+                                    p.row_max[m] = mx[r];
+                                    p.row_sum[m] = sm[r];
+                                }
+                            }
+                        }
+                    }
                 }
             }
             if (++acc == 2) {
@@ -813,13 +984,23 @@ __global__ void repack_rows_kernel(const T *__restrict__ src, int64_t ld_src, T 
 }
 
 // C[m + n*ldc] = +0 for m < M, n < N (the K == 0 case).
-__global__ void zero_fill_kernel(uint16_t *__restrict__ c, int64_t ldc, int64_t M, int64_t N)
+__global__ void zero_fill_kernel(uint16_t *__restrict__ c, int64_t ldc, int64_t M, int64_t N, uint16_t value)
 {
     const int64_t total = M * N;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t n = i / M;
-        c[(i - n * M) + n * ldc] = 0;
+        c[(i - n * M) + n * ldc] = value;
+    }
+}
+
+// Softmax statistics of an all-zero score matrix (K = 0): max 0, sum N.
+__global__ void fill_stats_kernel(float *__restrict__ row_max, float *__restrict__ row_sum, int64_t M, float n)
+{
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < M;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        row_max[i] = 0.0f;
+        row_sum[i] = n;
     }
 }
 

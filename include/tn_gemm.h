@@ -107,6 +107,39 @@ gemm_status_t gemm_f8e4m3_tn_dscale(int64_t M, int64_t N, int64_t K,
                                     const float *scale_a, const float *scale_b,
                                     void *stream);
 
+/*
+ * Attention scores with the softmax's row statistics, fused into the GEMM's
+ * epilogue: the QK^T step of hello-gpu ch.11's closing note (the next chapter
+ * joins the GEMM and the softmax so that less of the intermediate goes back to
+ * memory) and of the TileLang attention article (its QK^T block, M = N = 1024,
+ * K = 128, with the softmax fused into the same kernel).  A holds Q (M x K,
+ * row-major), B holds K (its column n = key n, i.e. an N x K row-major array).
+ * With acc = the FP32 sum over k:
+ *
+ *     C[m,n]     = fp16(fp32(acc[m,n] * scale))           column-major, ldc, as gemm_f16_tn
+ *     row_max[m] = max over n of fp32(acc[m,n] * scale)
+ *     row_sum[m] = sum over n of exp(fp32(acc[m,n] * scale) - row_max[m])
+ *
+ * i.e. the softmax of row m of the scores is exp(s - row_max[m]) / row_sum[m]
+ * (the pages do not fix the statistics; these are the two reductions that
+ * normalise a softmax, from the FP32 scores before their rounding).  The sum
+ * is formed in FP32 (each exp as 2^(x log2 e) with the hardware ex2, relative
+ * error about 2^-22) in a fixed order, so results repeat exactly.
+ * row_max and row_sum: DEVICE arrays of M floats owned by the caller.
+ * scale: any finite float (typically 1/sqrt(K)).  M or N == 0: nothing is
+ * written.  K == 0: C = scale * 0, row_max = 0, row_sum = N.
+ * Uses a library-owned buffer per (device, stream) for the partial
+ * statistics, allocated on first use.  Tiles are never split along K here.
+ * Errors as for gemm_f16_tn, plus GEMM_ERR_INVALID_ARG for NULL or misaligned
+ * row_max / row_sum or a non-finite scale.
+ */
+gemm_status_t gemm_f16_tn_softmax_stats(int64_t M, int64_t N, int64_t K,
+                                        const void *A, int64_t lda,
+                                        const void *B, int64_t ldb,
+                                        void *C, int64_t ldc, float scale,
+                                        float *row_max, float *row_sum,
+                                        void *stream);
+
 /* Element types gemm_quantize_e4m3 reads. */
 typedef enum {
     GEMM_IN_F32 = 0,    /* IEEE binary32 */
@@ -198,8 +231,8 @@ const char *gemm_last_error(void);
 gemm_status_t gemm_poll_device_status(void *stream);
 
 /* Frees the current device's workspaces: the repack copy, the per-stream
- * split-K partial sums and the quantiser's per-stream arrays (synchronises
- * the device). */
+ * split-K partial sums, the quantiser's per-stream arrays and the per-stream
+ * softmax-statistics buffers (synchronises the device). */
 void gemm_release_workspace(void);
 
 /*

@@ -20,6 +20,8 @@ Workloads (shapes and value distributions of the pages' benchmarks):
                cast to E4M3, 4 rotating sets
   ffn_8192     M=8192, N=28672, K=8192, N(0,1) cast to fp16, 2 rotating
                sets (the wide feed-forward projection shape)
+  qk_stats_1024  qk_1024's inputs through the fused attention-score epilogue
+               (scale 1/sqrt(K), softmax row statistics)
   fp8_pipeline_8192  M=N=K=8192, N(0,1) cast to bfloat16, 2 rotating sets;
                each step quantises both operands to E4M3 on the device
                before the FP8 GEMM
@@ -156,6 +158,7 @@ class Workload:
     seed_a: int
     seed_b: int
     rotating: int = 1    # input sets cycled by the benchmark
+    op: str = "gemm"     # "gemm", or "softmax_stats": scaled scores plus softmax row statistics
 
     @property
     def dtype(self) -> str:
@@ -177,6 +180,7 @@ WORKLOADS = {
         Workload("e4m3_8192", 8192, 8192, 8192, "e4m3", 501, 502, rotating=4),
         Workload("ffn_8192", 8192, 28672, 8192, "gauss", 601, 602, rotating=2),
         Workload("fp8_pipeline_8192", 8192, 8192, 8192, "bf16", 701, 702, rotating=2),
+        Workload("qk_stats_1024", 1024, 1024, 128, "gauss", 201, 202, op="softmax_stats"),
     ]
 }
 
