@@ -306,7 +306,9 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
         qB = torch.empty((N, K), dtype=torch.uint8, device=dev)
         dscale = torch.empty(2, dtype=torch.float32, device=dev)
         qa_p, qb_p, sa_p, sb_p = qA.data_ptr(), qB.data_ptr(), dscale.data_ptr(), dscale.data_ptr() + 4
-    launches_per_step = 5 if pipeline else 1
+    # our kernels per step: the GEMM; one repack of the operands when a row of K
+    # elements is not a whole number of 16-byte units; two per quantisation
+    launches_per_step = (5 if pipeline else 1) + (1 if (K * (1 if is_f8 and not pipeline else 2)) % 16 else 0)
     stats = w.op == "softmax_stats"
     if stats:
         sm_scale = 1.0 / float(np.sqrt(K))

@@ -251,17 +251,19 @@ uint32_t stall_flags(int mode)
     }
 }
 
-// Launches repack_rows_kernel: ld_dst is a multiple of 16 bytes.
+// Launches repack_rows_kernel for one or two operands (a job with 0 rows is
+// skipped); ld_dst, common to both, is a multiple of 16 bytes.
 template <typename T>
-void launch_repack(const T *src, int64_t ld_src, T *dst, int64_t ld_dst, int64_t rows, int64_t K,
-                   cudaStream_t stream)
+void launch_repack(const tn::RepackJob<T> &j0, const tn::RepackJob<T> &j1, cudaStream_t stream)
 {
     constexpr int64_t kVec = 16 / sizeof(T);
+    const int64_t ld_dst = j0.rows ? j0.ld_dst : j1.ld_dst;
     const int64_t chunks = ld_dst / kVec;
+    const int64_t rows = j0.rows + j1.rows;
     const int64_t rows_y = rows < 65535 ? rows : 65535;
     const dim3 grid(static_cast<unsigned>((chunks + 127) / 128), static_cast<unsigned>(rows_y),
                     static_cast<unsigned>((rows + rows_y - 1) / rows_y));
-    tn::repack_rows_kernel<T><<<grid, 128, 0, stream>>>(src, ld_src, dst, ld_dst, rows, K);
+    tn::repack_rows_kernel<T><<<grid, 128, 0, stream>>>(j0, j1);
 }
 
 int launch_grid(int64_t work, int cap)
@@ -449,13 +451,15 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         if ((st = ensure_workspace(*dev, bytes_a + bytes_b)) != GEMM_OK) return st;
         uint8_t *ws = static_cast<uint8_t *>(dev->workspace);
         using T = typename std::conditional<esz == 2, uint16_t, uint8_t>::type;
+        tn::RepackJob<T> ja{static_cast<const T *>(A), lda, reinterpret_cast<T *>(ws), ldp, repack_a ? M : 0, K};
+        tn::RepackJob<T> jb{static_cast<const T *>(B), ldb, reinterpret_cast<T *>(ws + bytes_a), ldp,
+                            repack_b ? N : 0, K};
+        launch_repack<T>(ja, jb, stream);       // one launch for both operands
         if (repack_a) {
-            launch_repack<T>(static_cast<const T *>(A), lda, reinterpret_cast<T *>(ws), ldp, M, K, stream);
             a_use = ws;
             lda_use = ka = ldp;
         }
         if (repack_b) {
-            launch_repack<T>(static_cast<const T *>(B), ldb, reinterpret_cast<T *>(ws + bytes_a), ldp, N, K, stream);
             b_use = ws + bytes_a;
             ldb_use = kb = ldp;
         }
@@ -850,14 +854,16 @@ extern "C" gemm_status_t gemm_f16_tn_noalloc(int64_t M, int64_t N, int64_t K, co
     uint8_t *ws = static_cast<uint8_t *>(scratch);
     const void *a_use = A, *b_use = B;
     int64_t lda_use = lda, ldb_use = ldb;
+    tn::RepackJob<uint16_t> ja{static_cast<const uint16_t *>(A), lda, reinterpret_cast<uint16_t *>(ws), ldp,
+                               repack_a ? M : 0, K};
+    tn::RepackJob<uint16_t> jb{static_cast<const uint16_t *>(B), ldb, reinterpret_cast<uint16_t *>(ws + bytes_a), ldp,
+                               repack_b ? N : 0, K};
+    launch_repack<uint16_t>(ja, jb, s);
     if (repack_a) {
-        launch_repack<uint16_t>(static_cast<const uint16_t *>(A), lda, reinterpret_cast<uint16_t *>(ws), ldp, M, K, s);
         a_use = ws;
         lda_use = ldp;
     }
     if (repack_b) {
-        launch_repack<uint16_t>(static_cast<const uint16_t *>(B), ldb, reinterpret_cast<uint16_t *>(ws + bytes_a), ldp,
-                                N, K, s);
         b_use = ws + bytes_a;
         ldb_use = ldp;
     }
