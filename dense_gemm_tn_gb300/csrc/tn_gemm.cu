@@ -47,6 +47,7 @@ struct DeviceState {
     struct Split {
         void *ptr = nullptr;
         size_t bytes = 0, ticket_bytes = 0;
+        bool dirty = false;      // a launch may have stopped part-way (timeout): clear the tickets first
     };
     std::unordered_map<cudaStream_t, Split> split;
     // Per-CTA maxima of the quantiser, one array per stream.
@@ -54,7 +55,6 @@ struct DeviceState {
     // Softmax statistics: [tickets per tile row | parts], one buffer per stream.
     std::unordered_map<cudaStream_t, Split> stats;
     int quant_blocks[3] = {};         // co-resident quantiser CTAs per SM, by input type (0 = not queried)
-    unsigned long long epoch = 0;
 };
 
 std::mutex g_mutex;
@@ -148,11 +148,16 @@ gemm_status_t stream_buffer(std::unordered_map<cudaStream_t, DeviceState::Split>
             w.ptr = nullptr;
             return fail(GEMM_ERR_CUDA, "cudaMalloc(%zu) for %s: %s", need, what, cudaGetErrorString(e));
         }
-        // the words hold tags of past launches' epochs; zero is older than every epoch
+        // the ticket words count arrivals within one launch and start from zero
         e = cudaMemsetAsync(w.ptr, 0, new_tb, stream);
         if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "clearing %s: %s", what, cudaGetErrorString(e));
         w.bytes = need;
         w.ticket_bytes = new_tb;
+        w.dirty = false;
+    } else if (w.dirty) {
+        cudaError_t e = cudaMemsetAsync(w.ptr, 0, w.ticket_bytes, stream);
+        if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "clearing %s: %s", what, cudaGetErrorString(e));
+        w.dirty = false;
     }
     *base = static_cast<uint8_t *>(w.ptr);
     *zeroed_out = w.ticket_bytes;
@@ -355,8 +360,6 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
             prm.kb_half = (prm.num_kb + 1) / 2;
             prm.split_ws = partials;
             prm.split_tickets = tickets;
-            std::lock_guard<std::mutex> lock(g_mutex);
-            prm.epoch = ++dev.epoch;
         }
     }
     snprintf(t_last_launch, sizeof(t_last_launch),
@@ -517,8 +520,6 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
             return st;
         prm.stat_tickets = reinterpret_cast<unsigned long long *>(base);
         prm.stat_parts = reinterpret_cast<float2 *>(base + zeroed);
-        std::lock_guard<std::mutex> lock(g_mutex);
-        prm.epoch = ++dev->epoch;
     }
     prm.flags |= (tma_c ? tn::kFlagTmaStore : 0u) | stall_flags(g_inject_stall.load());
     prm.wait_limit_ns = g_wait_limit_ns.load();
@@ -715,6 +716,14 @@ gemm_status_t gemm_poll_device_status(void *stream)
     if (v != 0) {
         const int zero = 0;
         cudaMemcpyToSymbol(tn::g_tn_status, &zero, sizeof(int));
+        // A kernel that gave up may have left ticket counts part-way: the next
+        // call on each stream clears them before use.
+        int dev = -1;
+        if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices) {
+            std::lock_guard<std::mutex> lock(g_mutex);
+            for (auto &kv : g_devices[dev].split) kv.second.dirty = true;
+            for (auto &kv : g_devices[dev].stats) kv.second.dirty = true;
+        }
         return fail(GEMM_ERR_TIMEOUT, "a kernel's bounded wait ran out (site %d)", v >> 8);
     }
     return GEMM_OK;

@@ -135,8 +135,9 @@ struct KernelParams {
     int32_t tail_start, num_units, tail_mode;
     int32_t kb_half;         // k blocks of each split-K unit: ceil(num_kb / 2), padded with zeros
     float *split_ws;         // split-K partials: [tail tile][k half][CTA of pair][128 n][256 m] fp32
-    unsigned long long *split_tickets;   // [tail tile][CTA of pair]: 2*epoch+1 once one half arrived
-    unsigned long long epoch;            // distinct per launch that uses split_ws
+    // [tail tile][CTA of pair]: halves arrived so far; 0 between launches (the
+    // second half resets it), so a captured graph can replay the launch.
+    unsigned long long *split_tickets;
     float scale;             // epilogue multiplier (F8: scale_a * scale_b)
     // F8 with device-resident scales: when set, the epilogue multiplies by
     // (*scale_a_ptr) * (*scale_b_ptr) in FP32 instead of `scale`.
@@ -144,8 +145,8 @@ struct KernelParams {
     // Softmax statistics (kFlagStats).  Every CTA that computes a tile writes,
     // per epilogue warp, the (max, sum) of its 32 columns n for each of the
     // tile's 256 rows m into stat_parts[tile_m][part][256]; the last of the
-    // stat_ctas CTAs of a tile row (ticket in stat_tickets[tile_m], tagged with
-    // the launch's epoch) merges the parts in a fixed order into row_max/row_sum.
+    // stat_ctas CTAs of a tile row (counted in stat_tickets[tile_m], which the
+    // last resets to 0) merges the parts in a fixed order into row_max/row_sum.
     float *row_max, *row_sum;
     float2 *stat_parts;
     unsigned long long *stat_tickets;
@@ -819,9 +820,10 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 __threadfence();
                 ptx::named_barrier_sync(1, kEpiWarps * 32);
                 if (warp == 2 && lane == 0) {
-                    const unsigned long long mark = 2ull * p.epoch + 1ull;
-                    const unsigned long long old = atomicMax(p.split_tickets + t * kGroup + pos, mark);
-                    *second_flag = old == mark ? 1u : 0u;
+                    unsigned long long *ticket = p.split_tickets + t * kGroup + pos;
+                    const bool second = atomicAdd(ticket, 1ull) == 1ull;
+                    if (second) atomicExch(ticket, 0ull);     // both halves are in: ready for the next launch
+                    *second_flag = second ? 1u : 0u;
                     __threadfence();
                 }
                 ptx::named_barrier_sync(1, kEpiWarps * 32);
@@ -885,10 +887,10 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                         ptx::named_barrier_sync(1, kEpiWarps * 32);
                         if (warp == 2 && lane == 0) {
                             unsigned long long *ticket = p.stat_tickets + un.tm;
-                            const unsigned long long base = static_cast<unsigned long long>(p.epoch) << 32;
-                            atomicMax(ticket, base);
-                            const unsigned long long old = atomicAdd(ticket, 1ull);
-                            *second_flag = old - base == static_cast<unsigned long long>(p.stat_ctas - 1) ? 1u : 0u;
+                            const bool last =
+                                atomicAdd(ticket, 1ull) == static_cast<unsigned long long>(p.stat_ctas - 1);
+                            if (last) atomicExch(ticket, 0ull);   // the row is complete: ready for the next launch
+                            *second_flag = last ? 1u : 0u;
                             __threadfence();
                         }
                         ptx::named_barrier_sync(1, kEpiWarps * 32);

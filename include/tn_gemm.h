@@ -41,6 +41,11 @@
  *     meet in a library-owned buffer kept per (device, stream), allocated on
  *     first need (about 0.5 MiB per leftover tile).  The sum is taken in a
  *     fixed way, so results do not depend on timing.
+ *   - CUDA graphs: once a call has run on a stream (the first call may
+ *     allocate that stream's buffers and set kernel attributes), later calls
+ *     with the same sizes on that stream enqueue kernel launches only and can
+ *     be captured and replayed; the kernels leave their buffers ready for the
+ *     next launch.
  *   - Thread safety: every entry point may be called from several host
  *     threads; the per-device state is guarded internally.
  */

@@ -321,3 +321,28 @@ def test_split_k_tail_exact_and_deterministic(force_group, cta_group, M, N, K):
     mi, ni = sample_positions(M, N, 20000, seed=K + 1)
     c, s, _ = oracle.gemm_f16_tn_at(M, N, K, Ag, K, Bg, K, mi, ni)
     assert_tol(f16_values(g1[ni, mi]), f16_values(c), s, F16_TOL, "split-K tail")
+
+
+def test_cuda_graph_capture_and_replay():
+    """After one warm-up call (which sets the kernel attributes and allocates
+    the split-K buffer of the stream), the calls enqueue only kernel launches,
+    so a stream can be captured into a CUDA graph and replayed; the replays
+    give the same bits as direct calls."""
+    import dense_gemm_tn_gb300 as g
+    M, N, K = 8192, 2304, 1024              # 32 x 9 = 288 pair tiles: a split-K last wave
+    A = synth.gauss_fp16(M * K, 5); B = synth.gauss_fp16(N * K, 6)
+    dA, dB = to_dev_u16(A), to_dev_u16(B)
+    s = torch.cuda.Stream()
+    C_direct = torch.empty((N, M), dtype=torch.float16, device="cuda")
+    C_graph = torch.empty((N, M), dtype=torch.float16, device="cuda")
+    g.gemm_f16_tn(M, N, K, dA, K, dB, K, C_direct, M, s)        # warm-up
+    g.gemm_poll_device_status(s)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        g.gemm_f16_tn(M, N, K, dA, K, dB, K, C_graph, M, s)
+    for _ in range(2):
+        C_graph.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        g.gemm_poll_device_status(s)
+        assert torch.equal(C_graph.view(torch.int16), C_direct.view(torch.int16))

@@ -150,3 +150,31 @@ def test_invalid_arguments():
         g.gemm_f16_tn_softmax_stats(8, 8, 8, x, 8, x, 8, x, 8, 1.0, None, r)
     with pytest.raises(g.GemmError):
         g.gemm_f16_tn_softmax_stats(8, 8, 8, x, 8, x, 8, x, 8, float("inf"), r, r)
+
+
+def test_cuda_graph_replay():
+    """The statistics' tile-row tickets return to zero after each launch, so a
+    captured launch replays correctly (replays give the direct call's bits)."""
+    import dense_gemm_tn_gb300 as g
+    M, N, K = 2048, 2048, 128
+    A = synth.gauss_fp16(M * K, 71); B = synth.gauss_fp16(N * K, 72)
+    dA, dB = to_dev_u16(A), to_dev_u16(B)
+    s = torch.cuda.Stream()
+    out = []
+    for _ in range(2):
+        out.append((torch.empty((N, M), dtype=torch.float16, device="cuda"),
+                    torch.empty(M, device="cuda"), torch.empty(M, device="cuda")))
+    C0, mx0, sm0 = out[0]
+    g.gemm_f16_tn_softmax_stats(M, N, K, dA, K, dB, K, C0, M, 0.1, mx0, sm0, s)     # warm-up
+    g.gemm_poll_device_status(s)
+    C1, mx1, sm1 = out[1]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        g.gemm_f16_tn_softmax_stats(M, N, K, dA, K, dB, K, C1, M, 0.1, mx1, sm1, s)
+    for _ in range(3):
+        mx1.fill_(float("nan")); sm1.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        g.gemm_poll_device_status(s)
+        assert torch.equal(C1.view(torch.int16), C0.view(torch.int16))
+        assert torch.equal(mx1, mx0) and torch.equal(sm1, sm0)
