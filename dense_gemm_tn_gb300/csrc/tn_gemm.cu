@@ -62,7 +62,7 @@ DeviceState g_devices[kMaxDevices];
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_force_cta_group{0};
-thread_local char t_last_launch[160] = "";
+thread_local char t_last_launch[256] = "";
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -322,7 +322,20 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
         }
         slots = dev.max_clusters[ki][G];
     }
-    int clusters = prm.num_tiles < slots ? prm.num_tiles : slots;
+    // A grid of at most half the slots with a long K leaves most SMs idle:
+    // every tile is cut into S ranges of its k blocks (as many as the slots
+    // allow, at most 8, each at least 16 k blocks), the units store FP32
+    // partials, and a reduce kernel sums them in order and stores C.
+    const int cap = quad && G == 2 && slots >= 2 ? (slots & ~1) : slots;
+    int reduce_parts = 1;
+    if (allow_alloc && !(prm.flags & tn::kFlagStats) && 2 * prm.num_tiles <= cap && prm.num_kb >= 32) {
+        int S = cap / prm.num_tiles;
+        if (S > 8) S = 8;
+        if (S > prm.num_kb / 16) S = prm.num_kb / 16;
+        if (S >= 2) reduce_parts = S;
+    }
+    const int units0 = prm.num_tiles * reduce_parts;
+    int clusters = units0 < slots ? units0 : slots;
     if (quad && G == 2) {
         clusters = (clusters + 1) & ~1;      // whole groups of four CTAs; an odd pair is a phantom
         if (clusters > slots) clusters = slots & ~1;
@@ -345,8 +358,21 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     prm.tail_mode = tn::kTailNone;
     prm.tail_start = prm.num_tiles;
     prm.num_units = prm.num_tiles;
-    // (The softmax statistics need every tile whole in one CTA pair.)
-    if (waves >= 1 && rem > 0 && 2 * rem <= clusters && !(prm.flags & tn::kFlagStats)) {
+    prm.split_parts = 1;
+    if (reduce_parts > 1) {
+        const size_t partial = size_t(prm.num_tiles) * reduce_parts * G * Cfg::kRowsB * tn::kTileM * sizeof(float);
+        uint8_t *base = nullptr;
+        size_t zeroed = 0;
+        gemm_status_t st = stream_buffer(dev.split, stream, 0, partial, "split-K partials", &base, &zeroed);
+        if (st != GEMM_OK) return st;
+        prm.tail_mode = tn::kSplitReduce;
+        prm.tail_start = 0;
+        prm.num_units = units0;
+        prm.split_parts = reduce_parts;
+        prm.kb_part = (prm.num_kb + reduce_parts - 1) / reduce_parts;
+        prm.split_ws = reinterpret_cast<float *>(base + zeroed);
+    } else if (waves >= 1 && rem > 0 && 2 * rem <= clusters && !(prm.flags & tn::kFlagStats)) {
+        // (The softmax statistics need every tile whole in one CTA pair.)
         prm.tail_start = waves * clusters;
         prm.num_units = prm.tail_start + 2 * rem;
         prm.tail_mode = tn::kTailHalfM;
@@ -357,17 +383,35 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
             gemm_status_t st = split_workspace(dev, stream, size_t(rem) * G, partial, &tickets, &partials);
             if (st != GEMM_OK) return st;
             prm.tail_mode = tn::kTailSplitK;
-            prm.kb_half = (prm.num_kb + 1) / 2;
+            prm.kb_part = (prm.num_kb + 1) / 2;
             prm.split_ws = partials;
             prm.split_tickets = tickets;
         }
     }
     snprintf(t_last_launch, sizeof(t_last_launch),
-             "%s: ctas_per_cluster=%d%s grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d tail_mode=%d",
+             "%s: ctas_per_cluster=%d%s grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d tail_mode=%d "
+             "split_parts=%d",
              name, G, quad && G == 2 ? " (preferred 4)" : "", G * clusters, clusters, slots, prm.num_tiles,
-             prm.num_units, prm.tail_start, prm.tail_mode);
+             prm.num_units, prm.tail_start, prm.tail_mode, prm.split_parts);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));
+    if (prm.tail_mode == tn::kSplitReduce) {
+        // the reduce kernel, as a programmatic dependent: its launch overlaps the GEMM's end
+        cudaLaunchConfig_t rcfg = {};
+        cudaLaunchAttribute rattr[1];
+        rattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        rattr[0].val.programmaticStreamSerializationAllowed = 1;
+        const int64_t work = (int64_t(prm.M) + 7) / 8 * prm.N;
+        rcfg.gridDim = dim3(static_cast<unsigned>(launch_grid(work, dev.sms * 8)), 1, 1);
+        rcfg.blockDim = dim3(256, 1, 1);
+        rcfg.stream = stream;
+        rcfg.attrs = rattr;
+        rcfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&rcfg, tn::split_reduce_kernel<Kind, G>, static_cast<const float *>(prm.split_ws),
+                               static_cast<int>(prm.split_parts), static_cast<int64_t>(prm.tiles_n), prm.M, prm.N,
+                               prm.c_ptr, prm.ldc, prm.scale, prm.scale_a_ptr, prm.scale_b_ptr);
+        if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: split reduce launch: %s", name, cudaGetErrorString(e));
+    }
     return GEMM_OK;
 }
 

@@ -98,6 +98,10 @@ struct TileCfg {
 constexpr int32_t kTailNone = 0;
 constexpr int32_t kTailHalfM = 1;    // two halves of the tile's m range (MMA N = 128)
 constexpr int32_t kTailSplitK = 2;   // two halves of the k blocks; partial sums meet in a workspace
+// A grid of fewer tiles than half the slots, with a long K: every tile is cut
+// into split_parts ranges of its k blocks; each unit stores its FP32 partial,
+// and split_reduce_kernel (launched next) sums them and stores C.
+constexpr int32_t kSplitReduce = 3;
 
 constexpr uint32_t kFlagTmaStore = 1u;      // C rows m < m_tma are written with TMA stores
 // Test hooks: the named thread first waits on a barrier nobody arrives on, so
@@ -133,7 +137,8 @@ struct KernelParams {
     // units (so a last, partly filled wave of tiles becomes a full wave of
     // half-length units), cut as tail_mode says.  num_units counts both kinds.
     int32_t tail_start, num_units, tail_mode;
-    int32_t kb_half;         // k blocks of each split-K unit: ceil(num_kb / 2), padded with zeros
+    int32_t kb_part;         // k blocks of each split unit: ceil(num_kb / parts), padded with zeros
+    int32_t split_parts;     // kSplitReduce: units per tile
     float *split_ws;         // split-K partials: [tail tile][k half][CTA of pair][128 n][256 m] fp32
     // [tail tile][CTA of pair]: halves arrived so far; 0 between launches (the
     // second half resets it), so a captured graph can replay the launch.
@@ -180,23 +185,31 @@ struct Unit {
     int64_t tile, tm, tn;    // tile id and coordinates
     int32_t half;            // -1: the whole m range; 0 / 1: that half of it (kTailHalfM)
     int32_t khalf;           // -1: all k blocks; 0 / 1: that half of them (kTailSplitK)
+    int32_t kpart;           // -1: all k blocks; else this range of them (kSplitReduce)
     int32_t kb0, nkb;        // the unit's k blocks
     bool phantom;            // no such unit: loads out of bounds, computes zeros, stores nothing
 };
 
 __device__ __forceinline__ Unit unit_of(int64_t u, const KernelParams &p)
 {
-    Unit r{u, 0, 0, -1, -1, 0, p.num_kb, u >= p.num_units};
+    Unit r{u, 0, 0, -1, -1, -1, 0, p.num_kb, u >= p.num_units};
     if (r.phantom) return r;
     if (u >= p.tail_start) {
         const int64_t v = u - p.tail_start;
-        r.tile = p.tail_start + v / 2;
-        if (p.tail_mode == kTailSplitK) {
-            r.khalf = static_cast<int32_t>(v & 1);
-            r.kb0 = r.khalf * p.kb_half;
-            r.nkb = p.kb_half;
+        if (p.tail_mode == kSplitReduce) {
+            r.tile = p.tail_start + v / p.split_parts;
+            r.kpart = static_cast<int32_t>(v % p.split_parts);
+            r.kb0 = r.kpart * p.kb_part;
+            r.nkb = p.kb_part;
         } else {
-            r.half = static_cast<int32_t>(v & 1);
+            r.tile = p.tail_start + v / 2;
+            if (p.tail_mode == kTailSplitK) {
+                r.khalf = static_cast<int32_t>(v & 1);
+                r.kb0 = r.khalf * p.kb_part;
+                r.nkb = p.kb_part;
+            } else {
+                r.half = static_cast<int32_t>(v & 1);
+            }
         }
     }
     tile_coord(r.tile, p.tiles_m, p.tiles_n, p.group, r.tm, r.tn);
@@ -207,7 +220,8 @@ __device__ __forceinline__ Unit unit_of(int64_t u, const KernelParams &p)
 // whole tiles; if the last wave was split, slots s < 2 * (tiles left over)
 // first take split unit tail_start + s, so its combine (split-K) overlaps the
 // slot's later tiles instead of ending the launch.  Slots come in even-aligned
-// pairs that either both have a split unit or both do not.
+// pairs that either both have a split unit or both do not.  (kSplitReduce
+// launches at most one unit per slot: tail_start = 0, num_units <= slots.)
 __device__ __forceinline__ bool slot_has_tail(int64_t slot, const KernelParams &p)
 {
     return p.tail_mode != kTailNone && slot < p.num_units - p.tail_start;
@@ -541,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             const Unit e = pair == 0 ? mine : unit_of(slot_unit(slot0, it, nslots, p), p);
             const Unit o = pair == 1 ? mine : unit_of(slot_unit(slot0 + 1, it, nslots, p), p);
             if (mine.phantom) mine.nkb = e.nkb;
-            shared = !e.phantom && !o.phantom && e.tn == o.tn && e.khalf < 0;
+            shared = !e.phantom && !o.phantom && e.tn == o.tn && e.khalf < 0 && e.kpart < 0;
         }
     };
     // Steps of this cluster: those of its first slot (the second never has more).
@@ -623,10 +637,11 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     auto contribution = [&](uint32_t q, uint32_t i) -> uint32_t {
                         Unit un;
                         bool shared;
-                        // a split-K first step issues kb_half fills, every other step num_kb
-                        const uint32_t first = (p.tail_mode == kTailSplitK && slot_has_tail(slot0, p))
-                                                   ? static_cast<uint32_t>(p.kb_half)
-                                                   : static_cast<uint32_t>(p.num_kb);
+                        // a split first step issues kb_part fills, every other step num_kb
+                        const uint32_t first =
+                            ((p.tail_mode == kTailSplitK || p.tail_mode == kSplitReduce) && slot_has_tail(slot0, p))
+                                ? static_cast<uint32_t>(p.kb_part)
+                                : static_cast<uint32_t>(p.num_kb);
                         const int64_t it = i < first ? 0 : 1 + static_cast<int64_t>((i - first) / p.num_kb);
                         cluster_units(it, un, shared);
                         // every CTA of the cluster ran step it: the units differ by pair only
@@ -799,6 +814,23 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             const int32_t nw = static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB) + 32 * quarter;
             if (un.phantom) {
                 release_acc();   // nothing to store
+            } else if (un.kpart >= 0) {
+                // Split-reduce part: store this part's FP32 partial; the reduce
+                // kernel that follows sums the parts in order and stores C.
+                const int64_t span = static_cast<int64_t>(Cfg::kRowsB) * kTileM;
+                float *mine = p.split_ws +
+                              (((un.tm * p.tiles_n + un.tn) * p.split_parts + un.kpart) * kGroup + pos) * span +
+                              row * kTileM;
+#pragma unroll 1
+                for (int c = 0; c < kTileM / kEpiBoxM; ++c) {
+                    float v[64];
+                    load_chunk(t_row, c * kEpiBoxM, v);
+                    if (c == kTileM / kEpiBoxM - 1) release_acc();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        reinterpret_cast<float4 *>(mine + c * kEpiBoxM)[j] =
+                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                }
             } else if (un.khalf >= 0) {
                 // Split-K half: store this half's FP32 partial, then take the tile's
                 // ticket.  The half that comes second adds the other half's partial
@@ -967,6 +999,55 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 // is read element by element (consecutive threads read consecutive chunks).
 // Grid: x over the chunks of a row, y (and z for more than 65535 rows) over
 // rows.
+// kSplitReduce, second launch: C[m, n] = the sum over parts, in part order,
+// of the FP32 partials of (m, n) -- stored, like the GEMM epilogue, as FP16
+// or as bf16(sum * scale_a * scale_b).  One thread per 8 consecutive m of one
+// column n: 32-byte reads of each partial, a 16-byte store of C.  Launched as
+// a programmatic dependent of the GEMM; waits for it to complete first.
+template <class Kind, int kGroup>
+__global__ void __launch_bounds__(256) split_reduce_kernel(const float *__restrict__ ws, int parts, int64_t tiles_n,
+                                                           int32_t M, int32_t N, void *c_ptr, int64_t ldc,
+                                                           float scale, const float *scale_a, const float *scale_b)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const float s = scale_a ? __fmul_rn(__ldg(scale_a), __ldg(scale_b)) : scale;
+    constexpr int64_t kRows = 128;                       // rows n of one CTA's partial
+    const int64_t part_stride = static_cast<int64_t>(kGroup) * kRows * kTileM;
+    const int64_t groups_m = (M + 7) / 8;
+    const bool vec_c = (ldc * 2) % 16 == 0 && reinterpret_cast<uintptr_t>(c_ptr) % 16 == 0;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < groups_m * N;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t n = i / groups_m;
+        const int64_t m = (i - n * groups_m) * 8;
+        const int64_t tm = m / kTileM, tn = n / (kRows * kGroup);
+        const int64_t pos = (n / kRows) % kGroup, row = n % kRows;
+        const float *src = ws + ((tm * tiles_n + tn) * parts * kGroup + pos) * kRows * kTileM + row * kTileM +
+                           (m % kTileM);
+        float v[8];
+        {
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(src));
+            const float4 b = __ldcg(reinterpret_cast<const float4 *>(src) + 1);
+            v[0] = a.x, v[1] = a.y, v[2] = a.z, v[3] = a.w, v[4] = b.x, v[5] = b.y, v[6] = b.z, v[7] = b.w;
+        }
+        for (int k = 1; k < parts; ++k) {
+            const float4 *q = reinterpret_cast<const float4 *>(src + k * part_stride);
+            const float4 a = __ldcg(q), b = __ldcg(q + 1);
+            v[0] += a.x, v[1] += a.y, v[2] += a.z, v[3] += a.w, v[4] += b.x, v[5] += b.y, v[6] += b.z, v[7] += b.w;
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] = Kind::pack(v[2 * j], v[2 * j + 1], s);
+        uint16_t *col = static_cast<uint16_t *>(c_ptr) + n * ldc;
+        if (vec_c && m + 8 <= M) {
+            *reinterpret_cast<uint4 *>(col + m) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (m + j < M) col[m + j] = static_cast<uint16_t>((w[j / 2] >> (16 * (j & 1))) & 0xFFFFu);
+        }
+    }
+}
+
 template <typename T>
 struct RepackJob {
     const T *src;

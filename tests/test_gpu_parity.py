@@ -346,3 +346,52 @@ def test_cuda_graph_capture_and_replay():
         torch.cuda.synchronize()
         g.gemm_poll_device_status(s)
         assert torch.equal(C_graph.view(torch.int16), C_direct.view(torch.int16))
+
+
+@pytest.mark.parametrize("cta_group,M,N,K,parts", [
+    (0, 1024, 1024, 8192, 4),    # 32 one-CTA tiles on 152 slots: four k ranges each
+    (1, 2000, 700, 4100, 3),     # ragged m, n and k (repacked): 8 x 6 = 48 tiles, three ranges
+    (2, 512, 2048, 16384, 4),    # 16 pair tiles of a long K
+    (4, 512, 2048, 16384, 4),    # the same in preferred 4-CTA clusters
+])
+def test_split_reduce_long_k(force_group, cta_group, M, N, K, parts):
+    """Grids of at most half the slots with a long K: every tile is cut into k
+    ranges whose FP32 partials a second kernel sums in order.  +-1 inputs are
+    bit-exact, Gaussian inputs within tolerance and identical run to run."""
+    force_group(cta_group)
+    A = synth.sign_fp16(M * K, 95 + M)
+    B = synth.sign_fp16(N * K, 96 + N)
+    got = run_f16(M, N, K, A, K, B, K)
+    rec = _launch_record()
+    if rec["slots"] in (76, 152):
+        assert rec["tail_mode"] == 3 and rec["split_parts"] == parts, rec
+    mi, ni = sample_positions(M, N, 20000, seed=K)
+    c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
+    assert np.array_equal(got[ni, mi], c)
+    Ag = synth.gauss_fp16(M * K, 97 + M)
+    Bg = synth.gauss_fp16(N * K, 98 + N)
+    g1 = run_f16(M, N, K, Ag, K, Bg, K)
+    g2 = run_f16(M, N, K, Ag, K, Bg, K)
+    assert np.array_equal(g1, g2)
+    c, s, _ = oracle.gemm_f16_tn_at(M, N, K, Ag, K, Bg, K, mi, ni)
+    assert_tol(f16_values(g1[ni, mi]), f16_values(c), s, F16_TOL, "split-reduce")
+
+
+def test_split_reduce_e4m3_host_and_device_scales():
+    import dense_gemm_tn_gb300 as g
+    M, N, K = 1024, 1024, 8192
+    qa, sa = synth.gauss_e4m3(M * K, 81)
+    qb, sb = synth.gauss_e4m3(N * K, 82)
+    got = run_f8(M, N, K, qa, K, qb, K, sa, sb)
+    rec = _launch_record()
+    if rec["slots"] in (76, 152):
+        assert rec["tail_mode"] == 3, rec
+    mi, ni = sample_positions(M, N, 20000, seed=3)
+    c, s, _ = oracle.gemm_f8e4m3_tn_at(M, N, K, qa, K, qb, K, sa, sb, mi, ni)
+    assert_tol(bf16_values(got[ni, mi]), bf16_values(c), s, F8_TOL, "split-reduce e4m3")
+    dA, dB = to_dev_u8(qa), to_dev_u8(qb)
+    scales = torch.tensor([sa, sb], dtype=torch.float32, device="cuda")
+    C = GuardedC(M, N, M)
+    g.gemm_f8e4m3_tn_dscale(M, N, K, dA, K, dB, K, C.ptr, M, scales.data_ptr(), scales.data_ptr() + 4)
+    g.gemm_poll_device_status()
+    assert np.array_equal(C.nm(), got)
