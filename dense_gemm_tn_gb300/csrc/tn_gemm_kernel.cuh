@@ -974,7 +974,9 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 acc_phase ^= 1u;
             }
         }
-        if (lane == 0) ptx::bulk_wait_group<0>();
+        // Before the CTA leaves, its staging buffers must have been read by the
+        // TMA stores; the stores themselves complete before the grid does.
+        if (lane == 0) ptx::bulk_wait_group_read<0>();
         __syncwarp();
     }
 
