@@ -22,6 +22,21 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// Blocks until every grid this one depends on programmatically has completed
+// and its memory writes are visible; returns at once for an ordinary launch.
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next grid on the stream, if it was launched as a programmatic
+// dependent, start once every CTA of this grid has called this (or exited).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {

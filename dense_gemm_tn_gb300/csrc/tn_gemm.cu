@@ -291,7 +291,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     auto kernel = tn::tn_gemm_kernel<Kind, G>;
     const int ki = Kind::kF8 ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[3];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = G;
     attr[0].val.clusterDim.y = 1;
@@ -341,12 +341,17 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
         if (clusters > slots) clusters = slots & ~1;
         if (clusters < 2) quad = false;
     }
+    // A programmatic dependent of the previous kernel on the stream: the
+    // kernel waits for it (griddepcontrol.wait) before touching memory.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 2;
     if (quad && G == 2) {
-        attr[1].id = cudaLaunchAttributePreferredClusterDimension;
-        attr[1].val.preferredClusterDim.x = 2 * G;
-        attr[1].val.preferredClusterDim.y = 1;
-        attr[1].val.preferredClusterDim.z = 1;
-        cfg.numAttrs = 2;
+        attr[2].id = cudaLaunchAttributePreferredClusterDimension;
+        attr[2].val.preferredClusterDim.x = 2 * G;
+        attr[2].val.preferredClusterDim.y = 1;
+        attr[2].val.preferredClusterDim.z = 1;
+        cfg.numAttrs = 3;
     }
     cfg.gridDim = dim3(G * clusters, 1, 1);
     // A last wave that fills at most half of the slots is run as twice as

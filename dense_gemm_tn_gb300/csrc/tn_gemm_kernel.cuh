@@ -541,6 +541,14 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_holder;
+    // The kernel is launched as a programmatic dependent of whatever precedes
+    // it on the stream, so the setup above (barriers, TMEM, descriptor
+    // prefetch) overlaps the end of that kernel.  Nothing below touches global
+    // memory before that kernel has completed.  The next kernel may then start
+    // its own setup on SMs as this grid's CTAs leave them: it too waits for
+    // this grid to complete before it reads or writes memory.
+    ptx::griddep_wait();
+    ptx::griddep_launch_dependents();
 
     const Waiter w{abort_flag, abort_addr, rank, ctas, p.wait_limit_ns};
 
