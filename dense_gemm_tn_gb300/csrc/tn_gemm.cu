@@ -278,6 +278,15 @@ int launch_grid(int64_t work, int cap)
     return g < 1 ? 1 : static_cast<int>(g);
 }
 
+// What A's tensor maps are made of; the map for units that cover part of a
+// tile's m range is encoded once the number of parts is known.
+struct ASource {
+    CUtensorMapDataType type;
+    const void *base;
+    uint64_t inner, outer, row_bytes;
+    uint32_t box_k, rows;      // rows: A rows per CTA of a whole tile
+};
+
 // Launches the persistent kernel: one CTA (or one CTA pair) per co-resident
 // slot, each walking the tile raster with a stride of the grid.  Pairs are
 // launched as 2-CTA clusters with a preferred cluster size of 4 when `quad`:
@@ -285,7 +294,7 @@ int launch_grid(int64_t work, int cap)
 // together, and the kernel shares B rows between them.
 template <class Kind, int G>
 gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, bool quad, bool allow_alloc,
-                     cudaStream_t stream)
+                     const ASource &asrc, cudaStream_t stream)
 {
     using Cfg = tn::TileCfg<G>;
     auto kernel = tn::tn_gemm_kernel<Kind, G>;
@@ -327,14 +336,21 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     // allow, at most 8, each at least 16 k blocks), the units store FP32
     // partials, and a reduce kernel sums them in order and stores C.
     const int cap = quad && G == 2 && slots >= 2 ? (slots & ~1) : slots;
+    const bool stats = (prm.flags & tn::kFlagStats) != 0;
     int reduce_parts = 1;
-    if (allow_alloc && !(prm.flags & tn::kFlagStats) && 2 * prm.num_tiles <= cap && prm.num_kb >= 32) {
+    if (allow_alloc && !stats && 2 * prm.num_tiles <= cap && prm.num_kb >= 32) {
         int S = cap / prm.num_tiles;
         if (S > 8) S = 8;
         if (S > prm.num_kb / 16) S = prm.num_kb / 16;
         if (S >= 2) reduce_parts = S;
     }
-    const int units0 = prm.num_tiles * reduce_parts;
+    // A grid of at most half the slots with a shorter K: every tile's m range
+    // is cut into 2 or 4 parts (MMA N = 128 or 64).  Such a launch is bound by
+    // latency, mostly the epilogue's TMEM -> shared memory -> TMA store
+    // round trips, and each unit stores a half or a quarter of a tile.
+    int m_parts = 1;
+    if (reduce_parts == 1 && 2 * prm.num_tiles <= cap) m_parts = 4 * prm.num_tiles <= cap ? 4 : 2;
+    const int units0 = prm.num_tiles * reduce_parts * m_parts;
     int clusters = units0 < slots ? units0 : slots;
     if (quad && G == 2) {
         clusters = (clusters + 1) & ~1;      // whole groups of four CTAs; an odd pair is a phantom
@@ -364,6 +380,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     prm.tail_start = prm.num_tiles;
     prm.num_units = prm.num_tiles;
     prm.split_parts = 1;
+    prm.m_part_rows = 0;
     if (reduce_parts > 1) {
         const size_t partial = size_t(prm.num_tiles) * reduce_parts * G * Cfg::kRowsB * tn::kTileM * sizeof(float);
         uint8_t *base = nullptr;
@@ -376,11 +393,17 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
         prm.split_parts = reduce_parts;
         prm.kb_part = (prm.num_kb + reduce_parts - 1) / reduce_parts;
         prm.split_ws = reinterpret_cast<float *>(base + zeroed);
-    } else if (waves >= 1 && rem > 0 && 2 * rem <= clusters && !(prm.flags & tn::kFlagStats)) {
-        // (The softmax statistics need every tile whole in one CTA pair.)
+    } else if (m_parts > 1) {
+        prm.tail_mode = tn::kTailMParts;
+        prm.tail_start = 0;
+        prm.num_units = units0;
+        prm.split_parts = m_parts;
+    } else if (waves >= 1 && rem > 0 && 2 * rem <= clusters && !stats) {
+        // (The softmax statistics count one kind of unit per tile row.)
         prm.tail_start = waves * clusters;
         prm.num_units = prm.tail_start + 2 * rem;
-        prm.tail_mode = tn::kTailHalfM;
+        prm.tail_mode = tn::kTailMParts;
+        prm.split_parts = 2;
         if (allow_alloc && prm.num_kb >= 4) {
             const size_t partial = size_t(rem) * 2 * G * Cfg::kRowsB * tn::kTileM * sizeof(float);
             unsigned long long *tickets = nullptr;
@@ -393,6 +416,13 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
             prm.split_tickets = tickets;
         }
     }
+    if (prm.tail_mode == tn::kTailMParts) {
+        prm.m_part_rows = tn::kTileM / prm.split_parts;
+        gemm_status_t st = encode_2d(&prm.tmap_a_part, asrc.type, asrc.base, asrc.inner, asrc.outer, asrc.row_bytes,
+                                     asrc.box_k, asrc.rows / prm.split_parts, "A part");
+        if (st != GEMM_OK) return st;
+    }
+    if (stats) prm.stat_arrivals = prm.stat_ctas * (prm.tail_mode == tn::kTailMParts ? prm.split_parts : 1);
     snprintf(t_last_launch, sizeof(t_last_launch),
              "%s: ctas_per_cluster=%d%s grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d tail_mode=%d "
              "split_parts=%d",
@@ -527,9 +557,6 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     const uint32_t rows_a = static_cast<uint32_t>(tn::kTileM / cta_group);
     if ((st = encode_2d(&prm.tmap_a, in_type, a_use, ka, M, lda_use * esz, box_k, rows_a, "A")) != GEMM_OK)
         return st;
-    if ((st = encode_2d(&prm.tmap_a_half, in_type, a_use, ka, M, lda_use * esz, box_k, rows_a / 2, "A half")) !=
-        GEMM_OK)
-        return st;
     if ((st = encode_2d(&prm.tmap_b, in_type, b_use, kb, N, ldb_use * esz, box_k, 128, "B")) != GEMM_OK)
         return st;
     if ((st = encode_2d(&prm.tmap_b_slice, in_type, b_use, kb, N, ldb_use * esz, box_k, 64, "B slice")) != GEMM_OK)
@@ -573,8 +600,10 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     prm.flags |= (tma_c ? tn::kFlagTmaStore : 0u) | stall_flags(g_inject_stall.load());
     prm.wait_limit_ns = g_wait_limit_ns.load();
 
-    if (cta_group == 2) return launch<Kind, 2>(name, prm, *dev, quad, allow_alloc, stream);
-    return launch<Kind, 1>(name, prm, *dev, false, allow_alloc, stream);
+    const ASource asrc{in_type, a_use, static_cast<uint64_t>(ka), static_cast<uint64_t>(M),
+                       static_cast<uint64_t>(lda_use * esz), box_k, rows_a};
+    if (cta_group == 2) return launch<Kind, 2>(name, prm, *dev, quad, allow_alloc, asrc, stream);
+    return launch<Kind, 1>(name, prm, *dev, false, allow_alloc, asrc, stream);
 }
 
 // Per-tensor E4M3 quantisation (quant_e4m3_kernel.cuh): the maximum-finding
@@ -800,7 +829,8 @@ void gemm_release_workspace(void)
 
 int gemm_tile_coord(int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t id, int64_t *tile_m, int64_t *tile_n)
 {
-    if (tiles_m <= 0 || tiles_n <= 0 || group <= 0 || id < 0 || id >= tiles_m * tiles_n || !tile_m || !tile_n)
+    if (tiles_m <= 0 || tiles_n <= 0 || group <= 0 || group > INT32_MAX || tiles_m > INT32_MAX / tiles_n || id < 0 ||
+        id >= tiles_m * tiles_n || !tile_m || !tile_n)
         return -1;
     tn::tile_coord(id, tiles_m, tiles_n, group, *tile_m, *tile_n);
     return 0;

@@ -94,9 +94,13 @@ struct TileCfg {
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB shared memory of one CTA");
 };
 
-// How the tiles of a partly filled last wave are cut into two units each.
+// How tiles are cut into several units each (split_parts of them): the tiles
+// of a partly filled last wave, or every tile of a grid that fills at most
+// half of the slots.
 constexpr int32_t kTailNone = 0;
-constexpr int32_t kTailHalfM = 1;    // two halves of the tile's m range (MMA N = 128)
+// split_parts (2 or 4) consecutive ranges of the tile's m rows, m_part_rows
+// each (MMA N = 128 or 64); every unit reads all of the tile's B rows.
+constexpr int32_t kTailMParts = 1;
 constexpr int32_t kTailSplitK = 2;   // two halves of the k blocks; partial sums meet in a workspace
 // A grid of fewer tiles than half the slots, with a long K: every tile is cut
 // into split_parts ranges of its k blocks; each unit stores its FP32 partial,
@@ -126,19 +130,20 @@ struct KernelParams {
     CUtensorMap tmap_a;      // A: dims {K', M}, box {kBlockKBytes / esz, kRowsA}, 128B swizzle
     CUtensorMap tmap_b;      // B: dims {K', N}, box {kBlockKBytes / esz, 128}, 128B swizzle
     CUtensorMap tmap_c;      // C: dims {m_tma, N}, box {kEpiBoxM, kEpiBoxN}, 128B swizzle
-    CUtensorMap tmap_a_half; // A with box {kBlockKBytes / esz, kRowsA / 2} (half units)
+    CUtensorMap tmap_a_part; // kTailMParts: A with box {kBlockKBytes / esz, kRowsA / split_parts}
     CUtensorMap tmap_b_slice; // B with box {kBlockKBytes / esz, 64} (shared B rows of a 4-CTA cluster)
     void *c_ptr;             // C base (direct stores)
     int64_t ldc;
     int32_t M, N, K;
     int32_t m_tma;           // rows m < m_tma are written by TMA stores (a multiple of 8, or 0)
     int32_t tiles_m, tiles_n, num_tiles, num_kb, group;
-    // Work units: tiles [0, tail_start) are whole units; each later tile is two
-    // units (so a last, partly filled wave of tiles becomes a full wave of
-    // half-length units), cut as tail_mode says.  num_units counts both kinds.
+    // Work units: tiles [0, tail_start) are whole units; each later tile is
+    // split_parts units (so a last, partly filled wave of tiles becomes a full
+    // wave of shorter units), cut as tail_mode says.  num_units counts both kinds.
     int32_t tail_start, num_units, tail_mode;
     int32_t kb_part;         // k blocks of each split unit: ceil(num_kb / parts), padded with zeros
-    int32_t split_parts;     // kSplitReduce: units per tile
+    int32_t split_parts;     // units per cut tile: 2 (kTailSplitK), 2 or 4 (kTailMParts), 2..8 (kSplitReduce)
+    int32_t m_part_rows;     // kTailMParts: rows m per unit, kTileM / split_parts
     float *split_ws;         // split-K partials: [tail tile][k half][CTA of pair][128 n][256 m] fp32
     // [tail tile][CTA of pair]: halves arrived so far; 0 between launches (the
     // second half resets it), so a captured graph can replay the launch.
@@ -149,13 +154,15 @@ struct KernelParams {
     const float *scale_a_ptr, *scale_b_ptr;
     // Softmax statistics (kFlagStats).  Every CTA that computes a tile writes,
     // per epilogue warp, the (max, sum) of its 32 columns n for each of the
-    // tile's 256 rows m into stat_parts[tile_m][part][256]; the last of the
-    // stat_ctas CTAs of a tile row (counted in stat_tickets[tile_m], which the
-    // last resets to 0) merges the parts in a fixed order into row_max/row_sum.
+    // tile's 256 rows m into stat_parts[tile_m][part][256] (a unit of a tile
+    // cut along m writes its own rows of them); the last of the stat_arrivals
+    // unit CTAs of a tile row (counted in stat_tickets[tile_m], which the last
+    // resets to 0) merges the parts in a fixed order into row_max/row_sum.
     float *row_max, *row_sum;
     float2 *stat_parts;
     unsigned long long *stat_tickets;
     int32_t stat_ctas;                  // tiles_n * CTAs per tile
+    int32_t stat_arrivals;              // units' CTAs per tile row: stat_ctas, times split_parts if cut
     uint32_t flags;
     uint64_t wait_limit_ns;
 };
@@ -168,22 +175,29 @@ struct KernelParams {
 // the ROCm blog's Step 6.  With an even group, ids 2j and 2j+1 fall on
 // neighbouring m tiles of one n tile, which is what a 4-CTA cluster's two
 // pairs share.
+//
+// The arithmetic is 32-bit (a 64-bit division is a long instruction sequence
+// on the path to every unit's first load): grids have fewer than 2^31 tiles.
+// group * tiles_n then fits too, except when tiles_m < group, where there is
+// one group and every id lies in it.
 __host__ __device__ __forceinline__ void tile_coord(int64_t id, int64_t tiles_m, int64_t tiles_n, int64_t group,
                                                     int64_t &tm, int64_t &tn)
 {
-    const int64_t per_group = group * tiles_n;
-    const int64_t g = id / per_group;
-    const int64_t first_m = g * group;
-    const int64_t rows = (tiles_m - first_m) < group ? (tiles_m - first_m) : group;
-    const int64_t in_group = id - g * per_group;
+    const uint32_t i = static_cast<uint32_t>(id), rows_m = static_cast<uint32_t>(tiles_m);
+    const uint32_t gm = static_cast<uint32_t>(group);
+    const uint32_t per_group = rows_m < gm ? 0xFFFFFFFFu : gm * static_cast<uint32_t>(tiles_n);
+    const uint32_t g = i / per_group;
+    const uint32_t first_m = g * gm;
+    const uint32_t rows = (rows_m - first_m) < gm ? (rows_m - first_m) : gm;
+    const uint32_t in_group = i - g * per_group;
     tm = first_m + in_group % rows;
     tn = in_group / rows;
 }
 
-// A work unit: a tile, or one half of a tile of the split last wave.
+// A work unit: a tile, or one part of a cut tile.
 struct Unit {
     int64_t tile, tm, tn;    // tile id and coordinates
-    int32_t half;            // -1: the whole m range; 0 / 1: that half of it (kTailHalfM)
+    int32_t mpart;           // -1: the whole m range; else that range of m_part_rows rows (kTailMParts)
     int32_t khalf;           // -1: all k blocks; 0 / 1: that half of them (kTailSplitK)
     int32_t kpart;           // -1: all k blocks; else this range of them (kSplitReduce)
     int32_t kb0, nkb;        // the unit's k blocks
@@ -195,21 +209,19 @@ __device__ __forceinline__ Unit unit_of(int64_t u, const KernelParams &p)
     Unit r{u, 0, 0, -1, -1, -1, 0, p.num_kb, u >= p.num_units};
     if (r.phantom) return r;
     if (u >= p.tail_start) {
-        const int64_t v = u - p.tail_start;
+        const uint32_t v = static_cast<uint32_t>(u - p.tail_start), parts = static_cast<uint32_t>(p.split_parts);
+        const int32_t part = static_cast<int32_t>(v % parts);
+        r.tile = p.tail_start + static_cast<int64_t>(v / parts);
         if (p.tail_mode == kSplitReduce) {
-            r.tile = p.tail_start + v / p.split_parts;
-            r.kpart = static_cast<int32_t>(v % p.split_parts);
-            r.kb0 = r.kpart * p.kb_part;
+            r.kpart = part;
+            r.kb0 = part * p.kb_part;
+            r.nkb = p.kb_part;
+        } else if (p.tail_mode == kTailSplitK) {
+            r.khalf = part;
+            r.kb0 = part * p.kb_part;
             r.nkb = p.kb_part;
         } else {
-            r.tile = p.tail_start + v / 2;
-            if (p.tail_mode == kTailSplitK) {
-                r.khalf = static_cast<int32_t>(v & 1);
-                r.kb0 = r.khalf * p.kb_part;
-                r.nkb = p.kb_part;
-            } else {
-                r.half = static_cast<int32_t>(v & 1);
-            }
+            r.mpart = part;
         }
     }
     tile_coord(r.tile, p.tiles_m, p.tiles_n, p.group, r.tm, r.tn);
@@ -217,8 +229,8 @@ __device__ __forceinline__ Unit unit_of(int64_t u, const KernelParams &p)
 }
 
 // The units a work slot walks.  Slot s takes units s, s + nslots, ... of the
-// whole tiles; if the last wave was split, slots s < 2 * (tiles left over)
-// first take split unit tail_start + s, so its combine (split-K) overlaps the
+// whole tiles; if tiles were cut, slots s < split_parts * (tiles cut) first
+// take unit tail_start + s, so its combine (split-K) overlaps the
 // slot's later tiles instead of ending the launch.  Slots come in even-aligned
 // pairs that either both have a split unit or both do not.  (kSplitReduce
 // launches at most one unit per slot: tail_start = 0, num_units <= slots.)
@@ -229,7 +241,9 @@ __device__ __forceinline__ bool slot_has_tail(int64_t slot, const KernelParams &
 
 __device__ __forceinline__ int64_t slot_iters(int64_t slot, int64_t nslots, const KernelParams &p)
 {
-    const int64_t whole = p.tail_start > slot ? (p.tail_start - slot + nslots - 1) / nslots : 0;
+    const int64_t whole = p.tail_start > slot ? static_cast<uint32_t>(p.tail_start - slot + nslots - 1) /
+                                                    static_cast<uint32_t>(nslots)
+                                              : 0;
     return whole + (slot_has_tail(slot, p) ? 1 : 0);
 }
 
@@ -467,7 +481,6 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     constexpr int kStages = Cfg::kStages;
     constexpr int kBlockKElems = kBlockKBytes / Kind::kElemBytes;   // K elements per atom
     constexpr uint32_t kIdesc = ptx::idesc_f32acc(Cfg::kTileN, kTileM, Kind::kFmt, Kind::kFmt);
-    constexpr uint32_t kIdescHalf = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 2, Kind::kFmt, Kind::kFmt);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -568,8 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     };
     // Steps of this cluster: those of its first slot (the second never has more).
     const int64_t iters = slot_iters(slot0, nslots, p);
+    // m-part units cover a half or a quarter of the tile's m range
+    const bool quarter_m = p.m_part_rows == kTileM / 4;
+    // A rows of this CTA per stage, and their bytes
+    const int32_t part_rows_a = quarter_m ? Cfg::kRowsA / 4 : Cfg::kRowsA / 2;
     auto a_bytes = [&](const Unit &un) -> uint32_t {
-        return un.half >= 0 ? Cfg::kTileABytes / 2 : Cfg::kTileABytes;
+        return un.mpart < 0 ? Cfg::kTileABytes : (quarter_m ? Cfg::kTileABytes / 4 : Cfg::kTileABytes / 2);
     };
 
     if (warp == 0) {
@@ -589,13 +606,13 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 Unit un;
                 bool shared;
                 cluster_units(it, un, shared);
-                const bool half = un.half >= 0;
-                const int32_t rows_a = half ? Cfg::kRowsA / 2 : Cfg::kRowsA;
+                const bool cut_m = un.mpart >= 0;
+                const int32_t rows_a = cut_m ? part_rows_a : Cfg::kRowsA;
                 const uint32_t fill = Cfg::kTileBBytes + a_bytes(un);
-                const CUtensorMap *map_a = half ? &p.tmap_a_half : &p.tmap_a;
+                const CUtensorMap *map_a = cut_m ? &p.tmap_a_part : &p.tmap_a;
                 // a phantom unit reads past the matrices: zero fill, the box's full byte count
                 const int32_t m0 = un.phantom ? p.M
-                                              : static_cast<int32_t>(un.tm * kTileM + (half ? un.half * (kTileM / 2) : 0) +
+                                              : static_cast<int32_t>(un.tm * kTileM + (cut_m ? un.mpart * p.m_part_rows : 0) +
                                                                      pos * rows_a);
                 const int32_t nb = un.phantom ? p.N : static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB);
                 uint16_t mcast = 0;
@@ -681,12 +698,16 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             bool ok = true, issued_any = false;
             const uint16_t all_mask = static_cast<uint16_t>((1u << ctas) - 1u);
             const uint16_t pair_mask = static_cast<uint16_t>(((1u << kGroup) - 1u) << lead);
+            // m-part units: MMA N = m_part_rows
+            constexpr uint32_t kIdescHalf = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 2, Kind::kFmt, Kind::kFmt);
+            constexpr uint32_t kIdescQuarter = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 4, Kind::kFmt, Kind::kFmt);
+            const uint32_t idesc_part = quarter_m ? kIdescQuarter : kIdescHalf;
             if (p.flags & kFlagStallMma) ok = w.wait(never_bar, 0u, kSiteStall);
             for (int64_t it = 0; ok && it < iters; ++it) {
                 Unit un;
                 bool shared;
                 cluster_units(it, un, shared);
-                const uint32_t idesc = un.half >= 0 ? kIdescHalf : kIdesc;
+                const uint32_t idesc = un.mpart >= 0 ? idesc_part : kIdesc;
                 if (!w.wait(accempty_bar(acc), acc_phase ^ 1u, kSiteAccEmpty)) break;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * kAccCols;
@@ -817,7 +838,8 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             __syncwarp();
             ptx::tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + acc * kAccCols;
-            const int32_t m0 = static_cast<int32_t>(un.tm * kTileM + (un.half >= 0 ? un.half * (kTileM / 2) : 0));
+            const int32_t m_in_tile = un.mpart >= 0 ? un.mpart * p.m_part_rows : 0;   // the unit's first row m
+            const int32_t m0 = static_cast<int32_t>(un.tm * kTileM) + m_in_tile;
             // this warp's first output column
             const int32_t nw = static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB) + 32 * quarter;
             if (un.phantom) {
@@ -888,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     }
                 }
             } else {
-                const int n_chunks = (un.half >= 0 ? kTileM / 2 : kTileM) / kEpiBoxM;
+                const int n_chunks = un.mpart < 0 ? kTileM / kEpiBoxM : (quarter_m ? kTileM / 4 : kTileM / 2) / kEpiBoxM;
                 const bool stats = !Kind::kF8 && (p.flags & kFlagStats) != 0;
 #pragma unroll 1
                 for (int c = 0; c < n_chunks; ++c) {
@@ -914,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                                 float x[32];
 #pragma unroll
                                 for (int j = 0; j < 32; ++j) x[j] = valid ? v[32 * h + j] : -INFINITY;
-                                part[c * kEpiBoxM + 32 * h + lane] = stat_warp_reduce32(x, lane);
+                                part[m_in_tile + c * kEpiBoxM + 32 * h + lane] = stat_warp_reduce32(x, lane);
                             }
                         }
                     }
@@ -928,7 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                         if (warp == 2 && lane == 0) {
                             unsigned long long *ticket = p.stat_tickets + un.tm;
                             const bool last =
-                                atomicAdd(ticket, 1ull) == static_cast<unsigned long long>(p.stat_ctas - 1);
+                                atomicAdd(ticket, 1ull) == static_cast<unsigned long long>(p.stat_arrivals - 1);
                             if (last) atomicExch(ticket, 0ull);   // the row is complete: ready for the next launch
                             *second_flag = last ? 1u : 0u;
                             __threadfence();

@@ -247,7 +247,7 @@ void gemm_release_workspace(void);
  * ROCm blog's "Step 6" (blocks grouped into tall regions of `group` tile rows,
  * the last group short): consecutive ids walk down `group` rows of one tile
  * column before moving to the next column.  Returns 0, or -1 if an argument
- * is out of range.
+ * is out of range (a grid of more than 2^31 - 1 tiles included).
  */
 int gemm_tile_coord(int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t id,
                     int64_t *tile_m, int64_t *tile_n);

@@ -10,18 +10,21 @@ optimization on AMD RDNA 3 and RDNA 4" (section "What we compute"):
 A row-major M x K (element index m*K + k), B column-major K x N (element index
 k + n*K), i.e. B is handed over as an (N, K) row-major array.
 
-Workloads (shapes and value distributions of the pages' benchmarks):
-  pm1_512      M=N=K=512, entries uniform {-1,+1}                 (exact case)
-  qk_1024      M=N=1024, K=128, N(0,1) cast to fp16 (QK^T-shaped block)
+Workloads (shapes and value distributions of the pages' benchmarks).  The
+benchmark cycles through `rotating` input sets, enough that together they are
+larger than the GPU's L2 (129 MB), so every step reads its operands from HBM:
+  pm1_512      M=N=K=512, entries uniform {-1,+1}, 160 sets of 1 MiB (exact case)
+  qk_1024      M=N=1024, K=128, N(0,1) cast to fp16, 320 sets of 0.5 MiB
+               (QK^T-shaped block)
   sq_8192      M=N=K=8192, N(0,1) cast to fp16, 4 rotating sets (headline)
-  wide_pm1     M=3000, N=12289, K=4097, uniform {-1,+1}            (tails)
-  wide_gauss   M=3000, N=12289, K=4097, N(0,1) cast to fp16        (tails)
+  wide_pm1     M=3000, N=12289, K=4097, uniform {-1,+1}, 2 sets    (tails)
+  wide_gauss   M=3000, N=12289, K=4097, N(0,1) cast to fp16, 2 sets (tails)
   e4m3_8192    M=N=K=8192, N(0,1) scaled per tensor to max|x| = 448 and
                cast to E4M3, 4 rotating sets
   ffn_8192     M=8192, N=28672, K=8192, N(0,1) cast to fp16, 2 rotating
                sets (the wide feed-forward projection shape)
-  qk_stats_1024  qk_1024's inputs through the fused attention-score epilogue
-               (scale 1/sqrt(K), softmax row statistics)
+  qk_stats_1024  qk_1024's inputs (320 sets) through the fused attention-score
+               epilogue (scale 1/sqrt(K), softmax row statistics)
   fp8_pipeline_8192  M=N=K=8192, N(0,1) cast to bfloat16, 2 rotating sets;
                each step quantises both operands to E4M3 on the device
                before the FP8 GEMM
@@ -172,15 +175,15 @@ class Workload:
 
 WORKLOADS = {
     w.name: w for w in [
-        Workload("pm1_512", 512, 512, 512, "pm1", 101, 102),
-        Workload("qk_1024", 1024, 1024, 128, "gauss", 201, 202),
+        Workload("pm1_512", 512, 512, 512, "pm1", 101, 102, rotating=160),
+        Workload("qk_1024", 1024, 1024, 128, "gauss", 201, 202, rotating=320),
         Workload("sq_8192", 8192, 8192, 8192, "gauss", 301, 302, rotating=4),
-        Workload("wide_pm1", 3000, 12289, 4097, "pm1", 401, 402),
-        Workload("wide_gauss", 3000, 12289, 4097, "gauss", 403, 404),
+        Workload("wide_pm1", 3000, 12289, 4097, "pm1", 401, 402, rotating=2),
+        Workload("wide_gauss", 3000, 12289, 4097, "gauss", 403, 404, rotating=2),
         Workload("e4m3_8192", 8192, 8192, 8192, "e4m3", 501, 502, rotating=4),
         Workload("ffn_8192", 8192, 28672, 8192, "gauss", 601, 602, rotating=2),
         Workload("fp8_pipeline_8192", 8192, 8192, 8192, "bf16", 701, 702, rotating=2),
-        Workload("qk_stats_1024", 1024, 1024, 128, "gauss", 201, 202, op="softmax_stats"),
+        Workload("qk_stats_1024", 1024, 1024, 128, "gauss", 201, 202, rotating=320, op="softmax_stats"),
     ]
 }
 

@@ -117,3 +117,5 @@ def test_tile_coord_rejects_out_of_range():
         g.gemm_tile_coord(4, 3, 2, 12)
     with pytest.raises(ValueError):
         g.gemm_tile_coord(0, 3, 2, 0)
+    with pytest.raises(ValueError):             # 2^32 tiles: more than the scheduler's 32-bit ids
+        g.gemm_tile_coord(2 ** 20, 2 ** 12, 8, 0)

@@ -395,3 +395,31 @@ def test_split_reduce_e4m3_host_and_device_scales():
     g.gemm_f8e4m3_tn_dscale(M, N, K, dA, K, dB, K, C.ptr, M, scales.data_ptr(), scales.data_ptr() + 4)
     g.gemm_poll_device_status()
     assert np.array_equal(C.nm(), got)
+
+
+@pytest.mark.parametrize("cta_group,M,N,K,parts", [
+    (0, 1024, 1024, 128, 4),     # 32 one-CTA tiles on 152 slots: each cut into four 64-row m ranges
+    (0, 2048, 1024, 256, 2),     # 64 one-CTA tiles: two 128-row m ranges each
+    (0, 900, 300, 77, 4),        # ragged m (the last range of the last tile row lies past M), repacked K
+    (0, 1, 1000, 40, 4),         # one row m: three of each tile's four ranges are empty
+    (2, 1024, 1024, 128, 4),     # forced CTA pairs: 32 A rows per CTA, MMA N = 64
+    (4, 700, 1000, 136, 4),      # forced 4-CTA clusters (the pairs share B rows)
+])
+def test_small_grid_m_parts(force_group, cta_group, M, N, K, parts):
+    """Grids of at most half the slots with a short K: every tile's m range is
+    cut into 2 or 4 units.  +-1 inputs are bit-exact, Gaussian inputs within
+    tolerance, and E4M3 runs the same cut."""
+    force_group(cta_group)
+    A = synth.sign_fp16(M * K, 60 + M)
+    B = synth.sign_fp16(N * K, 61 + N)
+    check_f16_full(M, N, K, A, B, exact=True, what=f"m parts {M}x{N}x{K}")
+    rec = _launch_record()
+    if rec["slots"] in (76, 152):
+        assert rec["tail_mode"] == 1 and rec["split_parts"] == parts and rec["tail_start"] == 0, rec
+        assert rec["units"] == rec["tiles"] * parts, rec
+    Ag = synth.gauss_fp16(M * K, 62 + M)
+    Bg = synth.gauss_fp16(N * K, 63 + N)
+    check_f16_full(M, N, K, Ag, Bg, what=f"m parts gaussian {M}x{N}x{K}")
+    qa, sa = synth.gauss_e4m3(M * K, 64 + M)
+    qb, sb = synth.gauss_e4m3(N * K, 65 + N)
+    check_f8_full(M, N, K, qa, qb, sa, sb, what=f"m parts e4m3 {M}x{N}x{K}")
