@@ -349,7 +349,8 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     // latency, mostly the epilogue's TMEM -> shared memory -> TMA store
     // round trips, and each unit stores a half or a quarter of a tile.
     int m_parts = 1;
-    if (reduce_parts == 1 && 2 * prm.num_tiles <= cap) m_parts = 4 * prm.num_tiles <= cap ? 4 : 2;
+    if (reduce_parts == 1 && 2 * prm.num_tiles <= cap)
+        m_parts = tn::kMaxMParts * prm.num_tiles <= cap ? tn::kMaxMParts : 2;
     const int units0 = prm.num_tiles * reduce_parts * m_parts;
     int clusters = units0 < slots ? units0 : slots;
     if (quad && G == 2) {
@@ -422,7 +423,6 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
                                      asrc.box_k, asrc.rows / prm.split_parts, "A part");
         if (st != GEMM_OK) return st;
     }
-    if (stats) prm.stat_arrivals = prm.stat_ctas * (prm.tail_mode == tn::kTailMParts ? prm.split_parts : 1);
     snprintf(t_last_launch, sizeof(t_last_launch),
              "%s: ctas_per_cluster=%d%s grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d tail_mode=%d "
              "split_parts=%d",
@@ -591,8 +591,9 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         const size_t parts = size_t(tiles_m) * prm.stat_ctas * tn::kEpiWarps * tn::kTileM * sizeof(float2);
         uint8_t *base = nullptr;
         size_t zeroed = 0;
-        if ((st = stream_buffer(dev->stats, stream, size_t(tiles_m) * sizeof(unsigned long long), parts,
-                                "softmax statistics", &base, &zeroed)) != GEMM_OK)
+        // one ticket per tile row and m part
+        const size_t tickets = size_t(tiles_m) * tn::kMaxMParts * sizeof(unsigned long long);
+        if ((st = stream_buffer(dev->stats, stream, tickets, parts, "softmax statistics", &base, &zeroed)) != GEMM_OK)
             return st;
         prm.stat_tickets = reinterpret_cast<unsigned long long *>(base);
         prm.stat_parts = reinterpret_cast<float2 *>(base + zeroed);

@@ -101,6 +101,7 @@ constexpr int32_t kTailNone = 0;
 // split_parts (2 or 4) consecutive ranges of the tile's m rows, m_part_rows
 // each (MMA N = 128 or 64); every unit reads all of the tile's B rows.
 constexpr int32_t kTailMParts = 1;
+constexpr int kMaxMParts = 4;
 constexpr int32_t kTailSplitK = 2;   // two halves of the k blocks; partial sums meet in a workspace
 // A grid of fewer tiles than half the slots, with a long K: every tile is cut
 // into split_parts ranges of its k blocks; each unit stores its FP32 partial,
@@ -155,14 +156,14 @@ struct KernelParams {
     // Softmax statistics (kFlagStats).  Every CTA that computes a tile writes,
     // per epilogue warp, the (max, sum) of its 32 columns n for each of the
     // tile's 256 rows m into stat_parts[tile_m][part][256] (a unit of a tile
-    // cut along m writes its own rows of them); the last of the stat_arrivals
-    // unit CTAs of a tile row (counted in stat_tickets[tile_m], which the last
-    // resets to 0) merges the parts in a fixed order into row_max/row_sum.
+    // cut along m writes its own rows of them).  The rows of one tile row and
+    // m part are computed by stat_ctas CTAs; the last of them (counted in
+    // stat_tickets[tile_m * kMaxMParts + m part], which the last resets to 0)
+    // merges those rows' parts in a fixed order into row_max/row_sum.
     float *row_max, *row_sum;
     float2 *stat_parts;
     unsigned long long *stat_tickets;
     int32_t stat_ctas;                  // tiles_n * CTAs per tile
-    int32_t stat_arrivals;              // units' CTAs per tile row: stat_ctas, times split_parts if cut
     uint32_t flags;
     uint64_t wait_limit_ns;
 };
@@ -943,56 +944,50 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 }
                 if constexpr (!Kind::kF8) {
                     if (stats) {
-                        // Take the tile row's ticket; the CTA that comes last merges every
-                        // part of the row in a fixed order, so no CTA waits for another.
-                        __threadfence();
+                        // Take the ticket of this unit's rows (its tile row and m part); the CTA
+                        // that comes last merges every part of those rows in a fixed order, so
+                        // no CTA waits for another.  One thread releases the CTA's parts (the
+                        // barrier orders every warp's writes before its fence) and acquires
+                        // the other CTAs' for the merge (the barrier orders the merge after).
                         ptx::named_barrier_sync(1, kEpiWarps * 32);
                         if (warp == 2 && lane == 0) {
-                            unsigned long long *ticket = p.stat_tickets + un.tm;
+                            __threadfence();
+                            unsigned long long *ticket =
+                                p.stat_tickets + un.tm * kMaxMParts + (un.mpart >= 0 ? un.mpart : 0);
                             const bool last =
-                                atomicAdd(ticket, 1ull) == static_cast<unsigned long long>(p.stat_arrivals - 1);
-                            if (last) atomicExch(ticket, 0ull);   // the row is complete: ready for the next launch
+                                atomicAdd(ticket, 1ull) == static_cast<unsigned long long>(p.stat_ctas - 1);
+                            if (last) atomicExch(ticket, 0ull);   // the rows are complete: ready for the next launch
                             *second_flag = last ? 1u : 0u;
                             __threadfence();
                         }
                         ptx::named_barrier_sync(1, kEpiWarps * 32);
                         if (*second_flag != 0u) {
-                            __threadfence();
                             const int nparts = p.stat_ctas * kEpiWarps;
                             const float2 *row_parts =
                                 p.stat_parts + static_cast<int64_t>(un.tm) * nparts * kTileM;
-                            // thread t merges rows 2t and 2t+1, 16 parts of each in flight
-                            constexpr int kRows = kTileM / (kEpiWarps * 32);
-                            constexpr int kBatch = 16;
+                            // thread t merges rows m_in_tile + t (+ 128): 32 parts of a row in flight
+                            const int rows = un.mpart >= 0 ? p.m_part_rows : kTileM;
+                            constexpr int kBatch = 32;
                             const int t = ew * 32 + lane;
-                            float mx[kRows], sm[kRows];
-#pragma unroll
-                            for (int r = 0; r < kRows; ++r) {
-                                mx[r] = -INFINITY;
-                                sm[r] = 0.0f;
-                            }
 #pragma unroll 1
-                            for (int q0 = 0; q0 < nparts; q0 += kBatch) {
-                                float2 buf[kRows][kBatch];
+                            for (int r = t; r < rows; r += kEpiWarps * 32) {
+                                const int row = m_in_tile + r;
+                                float mx = -INFINITY, sm = 0.0f;
+#pragma unroll 1
+                                for (int q0 = 0; q0 < nparts; q0 += kBatch) {
+                                    float2 buf[kBatch];
 #pragma unroll
-                                for (int i = 0; i < kBatch; ++i)
+                                    for (int i = 0; i < kBatch; ++i)
+                                        buf[i] = q0 + i < nparts
+                                                     ? __ldcg(row_parts + static_cast<int64_t>(q0 + i) * kTileM + row)
+                                                     : make_float2(-INFINITY, 0.0f);
 #pragma unroll
-                                    for (int r = 0; r < kRows; ++r)
-                                        buf[r][i] = q0 + i < nparts
-                                                        ? __ldcg(row_parts + static_cast<int64_t>(q0 + i) * kTileM +
-                                                                 t * kRows + r)
-                                                        : make_float2(-INFINITY, 0.0f);
-#pragma unroll
-                                for (int i = 0; i < kBatch; ++i)
-#pragma unroll
-                                    for (int r = 0; r < kRows; ++r) stat_merge(mx[r], sm[r], buf[r][i].x, buf[r][i].y);
-                            }
-#pragma unroll
-                            for (int r = 0; r < kRows; ++r) {
-                                const int64_t m = static_cast<int64_t>(un.tm) * kTileM + t * kRows + r;
+                                    for (int i = 0; i < kBatch; ++i) stat_merge(mx, sm, buf[i].x, buf[i].y);
+                                }
+                                const int64_t m = static_cast<int64_t>(un.tm) * kTileM + row;
                                 if (m < p.M) {
-                                    p.row_max[m] = mx[r];
-                                    p.row_sum[m] = sm[r];
+                                    p.row_max[m] = mx;
+                                    p.row_sum[m] = sm;
                                 }
                             }
                         }
