@@ -43,7 +43,7 @@ EXPORTS = (
     "gemm_f16_tn", "gemm_f8e4m3_tn", "gemm_status_string", "gemm_last_error",
     "gemm_poll_device_status", "gemm_release_workspace", "gemm_tile_coord",
     "gemm_set_wait_limit_ns", "gemm_debug_inject_stall", "gemm_build_info",
-    "gemm_f16_tn_noalloc", "gemm_debug_force_cta_group", "gemm_debug_last_launch",
+    "gemm_f16_tn_noalloc", "gemm_debug_force_cta_group", "gemm_debug_force_wide_tiles", "gemm_debug_last_launch",
     "gemm_f8e4m3_tn_dscale", "gemm_quantize_e4m3", "gemm_f16_tn_softmax_stats",
 )
 
@@ -94,6 +94,8 @@ def _load() -> ctypes.CDLL:
     lib.gemm_debug_inject_stall.restype = None
     lib.gemm_debug_force_cta_group.argtypes = [ctypes.c_int]
     lib.gemm_debug_force_cta_group.restype = ctypes.c_int
+    lib.gemm_debug_force_wide_tiles.argtypes = [ctypes.c_int]
+    lib.gemm_debug_force_wide_tiles.restype = ctypes.c_int
     lib.gemm_debug_last_launch.argtypes = []
     lib.gemm_debug_last_launch.restype = ctypes.c_char_p
     lib.gemm_build_info.argtypes = []
@@ -211,7 +213,13 @@ def gemm_debug_inject_stall(mode) -> None:
 
 def gemm_debug_force_cta_group(group: int) -> None:
     if _lib.gemm_debug_force_cta_group(int(group)) != 0:
-        raise ValueError("cta group must be 0 (automatic), 1 or 2")
+        raise ValueError("cta group must be 0 (automatic), 1, 2 or 4")
+
+
+def gemm_debug_force_wide_tiles(mode: int) -> None:
+    """0 automatic; 1 CTA pairs always compute 256 x 512 tiles; -1 never."""
+    if _lib.gemm_debug_force_wide_tiles(int(mode)) != 0:
+        raise ValueError("mode must be -1, 0 or 1")
 
 
 # ---------------------------------------------------------------- torch helpers

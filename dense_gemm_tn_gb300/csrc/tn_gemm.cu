@@ -37,9 +37,9 @@ gemm_status_t fail(gemm_status_t s, const char *fmt, ...)
 struct DeviceState {
     bool ready = false;
     int sms = 0, major = 0, minor = 0;
-    // per kernel, indexed [kind: f16, e4m3][CTA group: 1 or 2]
-    bool smem_attr[2][3] = {};
-    int max_clusters[2][3] = {};      // co-resident clusters of the kernel's own size (0 = not queried yet)
+    // per kernel, indexed [kind: f16, e4m3][1: one CTA, 2: CTA pairs, 3: CTA pairs with 256 x 512 tiles]
+    bool smem_attr[2][4] = {};
+    int max_clusters[2][4] = {};      // co-resident clusters of the kernel's own size (0 = not queried yet)
     void *workspace = nullptr;
     size_t workspace_bytes = 0;
     // Split-K partial sums of the last wave, one buffer per stream (calls on
@@ -62,6 +62,7 @@ DeviceState g_devices[kMaxDevices];
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_force_cta_group{0};
+std::atomic<int> g_force_wide{0};       // 0: the cost estimate decides; 1: always; -1: never
 thread_local char t_last_launch[256] = "";
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -271,6 +272,21 @@ void launch_repack(const tn::RepackJob<T> &j0, const tn::RepackJob<T> &j1, cudaS
     tn::repack_rows_kernel<T><<<grid, 128, 0, stream>>>(j0, j1);
 }
 
+// Estimated length, in 256 x 256 tile times, of a persistent launch of `tiles`
+// tiles of `tile` times each on `slots` slots.  A last partial wave that fills
+// at most half of the slots is cut in two (`half` each); another one costs a
+// whole tile.
+double launch_estimate(int64_t tiles, int64_t slots, double tile, double half)
+{
+    const int64_t waves = tiles / slots, rem = tiles % slots;
+    if (rem == 0) return waves * tile;
+    return waves * tile + (waves >= 1 && 2 * rem <= slots ? half : tile);
+}
+
+// The time of a 256 x 512 tile in 256 x 256 tile times: measured on GB300,
+// under the power cap, somewhat less than two.
+constexpr double kWideTileCost = 0.95;
+
 int launch_grid(int64_t work, int cap)
 {
     int64_t g = (work + 255) / 256;
@@ -291,14 +307,17 @@ struct ASource {
 // slot, each walking the tile raster with a stride of the grid.  Pairs are
 // launched as 2-CTA clusters with a preferred cluster size of 4 when `quad`:
 // the hardware then joins two pairs into one cluster wherever four CTAs fit
-// together, and the kernel shares B rows between them.
-template <class Kind, int G>
+// together, and the kernel shares B rows between them.  W: CTA pairs with
+// 256 x 512 tiles (never with `quad`, the softmax statistics or a split K).
+template <class Kind, int G, bool W = false>
 gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, bool quad, bool allow_alloc,
                      const ASource &asrc, cudaStream_t stream)
 {
-    using Cfg = tn::TileCfg<G>;
-    auto kernel = tn::tn_gemm_kernel<Kind, G>;
+    static_assert(!W || G == 2, "256 x 512 tiles are CTA-pair tiles");
+    using Cfg = tn::TileCfg<G, W>;
+    auto kernel = tn::tn_gemm_kernel<Kind, G, W>;
     const int ki = Kind::kF8 ? 1 : 0;
+    const int ks = W ? 3 : G;          // kernel index of the per-device caches
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[3];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -313,13 +332,13 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     int slots;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
-        if (!dev.smem_attr[ki][G]) {
+        if (!dev.smem_attr[ki][ks]) {
             cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
             if (e != cudaSuccess)
                 return fail(GEMM_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", name, cudaGetErrorString(e));
-            dev.smem_attr[ki][G] = true;
+            dev.smem_attr[ki][ks] = true;
         }
-        if (dev.max_clusters[ki][G] == 0) {
+        if (dev.max_clusters[ki][ks] == 0) {
             int n = 0;
             cfg.gridDim = dim3(G * (dev.sms / G), 1, 1);
             cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
@@ -327,9 +346,9 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
                 cudaGetLastError();
                 n = dev.sms / G;     // fall back to one slot per SM (pair)
             }
-            dev.max_clusters[ki][G] = n;
+            dev.max_clusters[ki][ks] = n;
         }
-        slots = dev.max_clusters[ki][G];
+        slots = dev.max_clusters[ki][ks];
     }
     // A grid of at most half the slots with a long K leaves most SMs idle:
     // every tile is cut into S ranges of its k blocks (as many as the slots
@@ -338,7 +357,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     const int cap = quad && G == 2 && slots >= 2 ? (slots & ~1) : slots;
     const bool stats = (prm.flags & tn::kFlagStats) != 0;
     int reduce_parts = 1;
-    if (allow_alloc && !stats && 2 * prm.num_tiles <= cap && prm.num_kb >= 32) {
+    if (!W && allow_alloc && !stats && 2 * prm.num_tiles <= cap && prm.num_kb >= 32) {
         int S = cap / prm.num_tiles;
         if (S > 8) S = 8;
         if (S > prm.num_kb / 16) S = prm.num_kb / 16;
@@ -349,7 +368,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     // latency, mostly the epilogue's TMEM -> shared memory -> TMA store
     // round trips, and each unit stores a half or a quarter of a tile.
     int m_parts = 1;
-    if (reduce_parts == 1 && 2 * prm.num_tiles <= cap)
+    if (!W && reduce_parts == 1 && 2 * prm.num_tiles <= cap)
         m_parts = tn::kMaxMParts * prm.num_tiles <= cap ? tn::kMaxMParts : 2;
     const int units0 = prm.num_tiles * reduce_parts * m_parts;
     int clusters = units0 < slots ? units0 : slots;
@@ -405,7 +424,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
         prm.num_units = prm.tail_start + 2 * rem;
         prm.tail_mode = tn::kTailMParts;
         prm.split_parts = 2;
-        if (allow_alloc && prm.num_kb >= 4) {
+        if (!W && allow_alloc && prm.num_kb >= 4) {
             const size_t partial = size_t(rem) * 2 * G * Cfg::kRowsB * tn::kTileM * sizeof(float);
             unsigned long long *tickets = nullptr;
             float *partials = nullptr;
@@ -418,16 +437,18 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
         }
     }
     if (prm.tail_mode == tn::kTailMParts) {
-        prm.m_part_rows = tn::kTileM / prm.split_parts;
-        gemm_status_t st = encode_2d(&prm.tmap_a_part, asrc.type, asrc.base, asrc.inner, asrc.outer, asrc.row_bytes,
-                                     asrc.box_k, asrc.rows / prm.split_parts, "A part");
+        prm.m_part_rows = Cfg::kTileMRows / prm.split_parts;
+        // (a wide tile's parts are its halves, whose rows the A map's boxes already are)
+        gemm_status_t st = W ? GEMM_OK
+                             : encode_2d(&prm.tmap_a_part, asrc.type, asrc.base, asrc.inner, asrc.outer,
+                                         asrc.row_bytes, asrc.box_k, asrc.rows / prm.split_parts, "A part");
         if (st != GEMM_OK) return st;
     }
     snprintf(t_last_launch, sizeof(t_last_launch),
-             "%s: ctas_per_cluster=%d%s grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d tail_mode=%d "
-             "split_parts=%d",
-             name, G, quad && G == 2 ? " (preferred 4)" : "", G * clusters, clusters, slots, prm.num_tiles,
-             prm.num_units, prm.tail_start, prm.tail_mode, prm.split_parts);
+             "%s: ctas_per_cluster=%d%s wide=%d grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d "
+             "tail_mode=%d split_parts=%d",
+             name, G, quad && G == 2 ? " (preferred 4)" : "", W ? 1 : 0, G * clusters, clusters, slots,
+             prm.num_tiles, prm.num_units, prm.tail_start, prm.tail_mode, prm.split_parts);
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));
     if (prm.tail_mode == tn::kSplitReduce) {
@@ -507,8 +528,24 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     if (const int forced = g_force_cta_group.load()) ctas = forced;
     const int cta_group = ctas >= 2 ? 2 : 1;
     const bool quad = ctas == 4 && !stats;
-    const int64_t tiles_m = (M + tn::kTileM - 1) / tn::kTileM;
     const int64_t tiles_n = (N + 128 * cta_group - 1) / (128 * cta_group);
+    // 256 x 512 pair tiles (two N = 256 halves that share the n-side rows) move
+    // a quarter fewer bytes out of L2 per MMA.  Under the power cap that buys a
+    // 7-9 % higher SM clock at about the same work per clock (8192^3 FP16 on
+    // GB300).  But there are half as many of them, a last partial wave can
+    // only be cut into m halves, and their accumulator is not double-buffered.
+    // They are used where an estimate of the launch's length says so.
+    bool wide = false;
+    if (cta_group == 2 && !quad && !stats) {
+        const int force = g_force_wide.load();
+        const int64_t slots = dev->sms / 2;
+        const int64_t tiles256 = (M + tn::kTileM - 1) / tn::kTileM * tiles_n;
+        const int64_t tiles512 = (M + 2 * tn::kTileM - 1) / (2 * tn::kTileM) * tiles_n;
+        wide = force > 0 || (force == 0 && launch_estimate(tiles512, slots, 2.0 * kWideTileCost, 1.0) <
+                                               launch_estimate(tiles256, slots, 1.0, 0.5));
+    }
+    const int64_t tile_m_rows = wide ? 2 * tn::kTileM : tn::kTileM;
+    const int64_t tiles_m = (M + tile_m_rows - 1) / tile_m_rows;
     if (tiles_m * tiles_n > INT32_MAX) return fail(GEMM_ERR_UNSUPPORTED, "%s: too many output tiles", name);
 
     // The TMA reads an operand in place only when its base, its row stride and
@@ -577,7 +614,8 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     prm.tiles_m = static_cast<int32_t>(tiles_m);
     prm.tiles_n = static_cast<int32_t>(tiles_n);
     prm.num_tiles = static_cast<int32_t>(tiles_m * tiles_n);
-    const int64_t stage_k = cta_group == 2 ? tn::TileCfg<2>::kStageKBytes : tn::TileCfg<1>::kStageKBytes;
+    const int64_t stage_k = wide ? tn::TileCfg<2, true>::kStageKBytes
+                                 : cta_group == 2 ? tn::TileCfg<2>::kStageKBytes : tn::TileCfg<1>::kStageKBytes;
     prm.num_kb = static_cast<int32_t>((K * esz + stage_k - 1) / stage_k);   // k blocks = stages per tile
     prm.group = kGroupM;            // even, so raster ids 2j, 2j+1 are neighbouring m tiles of one n tile
     prm.scale = scale;
@@ -603,6 +641,7 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
 
     const ASource asrc{in_type, a_use, static_cast<uint64_t>(ka), static_cast<uint64_t>(M),
                        static_cast<uint64_t>(lda_use * esz), box_k, rows_a};
+    if (wide) return launch<Kind, 2, true>(name, prm, *dev, false, allow_alloc, asrc, stream);
     if (cta_group == 2) return launch<Kind, 2>(name, prm, *dev, quad, allow_alloc, asrc, stream);
     return launch<Kind, 1>(name, prm, *dev, false, allow_alloc, asrc, stream);
 }
@@ -848,15 +887,24 @@ int gemm_debug_force_cta_group(int group)
     return 0;
 }
 
+int gemm_debug_force_wide_tiles(int mode)
+{
+    if (mode < -1 || mode > 1) return -1;
+    g_force_wide.store(mode);
+    return 0;
+}
+
 const char *gemm_debug_last_launch(void) { return t_last_launch; }
 
 const char *gemm_build_info(void)
 {
-    static char info[384];
+    static char info[512];
     snprintf(info, sizeof(info),
              "dense_gemm_tn sm_103a: CTA-pair tile 256x256 in clusters of 2 or 4 (B multicast), %d stages of %d B "
-             "of K, %d B smem; 1-CTA tile 128x256, %d stages of %d B of K, %d B smem; TMEM %u cols; raster group %d",
+             "of K, %d B smem; CTA-pair tile 256x512, %d stages of %d B of K, %d B smem; 1-CTA tile 128x256, "
+             "%d stages of %d B of K, %d B smem; TMEM %u cols; raster group %d",
              tn::TileCfg<2>::kStages, tn::TileCfg<2>::kStageKBytes, tn::TileCfg<2>::kSmemBytes,
+             tn::TileCfg<2, true>::kStages, tn::TileCfg<2, true>::kStageKBytes, tn::TileCfg<2, true>::kSmemBytes,
              tn::TileCfg<1>::kStages, tn::TileCfg<1>::kStageKBytes, tn::TileCfg<1>::kSmemBytes, tn::kTmemCols,
              kGroupM);
     return info;

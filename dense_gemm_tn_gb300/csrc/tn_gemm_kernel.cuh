@@ -70,16 +70,31 @@ constexpr uint32_t kTmemCols = 2 * kAccCols;  // double-buffered accumulator = a
 //   [B atom 0][B atom 1]...[A atom 0][A atom 1]...
 // Fewer, longer stages halve the barrier waits, commits and TMA issues per
 // MMA; measured on GB300 the MMA pipe then loses less time between stages.
-template <int kGroup>
+//
+// kWide (pairs only): a CTA pair computes a 256 (n) x 512 (m) tile as two M256
+// N256 halves that share the n-side operand.  Each CTA holds, per stage, one
+// 128-byte atom of its 128 B rows and of its 2 x 128 A rows (one block per
+// half, the second at +kHalfABytes): 48 KiB, so four stages fit.  A quarter
+// fewer bytes leave L2 per MMA, and four stages of 1024 MMA cycles hide more
+// load latency than three of 2048 bytes per CTA and 1024 cycles.  The
+// accumulator takes all 512 TMEM columns (half h at column 256 h), so it is
+// not double-buffered: the next tile's MMAs wait for the epilogue to read it.
+// Measured on GB300 under the power cap (8192^3 FP16), the lower L2 traffic
+// lets the SMs run at a 7-9 % higher clock for the same work per clock.
+template <int kGroup, bool kWide = false>
 struct TileCfg {
+    static_assert(!kWide || kGroup == 2, "256 x 512 tiles are CTA-pair tiles");
     static constexpr int kMaxCtas = 2 * kGroup;            // CTAs per cluster at most (2 pairs)
     static constexpr int kTileN = 128 * kGroup;            // C columns n per pair tile = MMA M
+    static constexpr int kTileMRows = kWide ? 2 * kTileM : kTileM;   // C rows m per tile
+    static constexpr int kHalves = kWide ? 2 : 1;           // MMA N = 256 halves per tile
     static constexpr int kRowsB = 128;                      // B rows (columns n) per CTA and stage
     static constexpr int kSliceB = kRowsB / 2;              // B rows each CTA loads when a cluster shares
-    static constexpr int kRowsA = kTileM / kGroup;          // A rows (m) per CTA and stage
-    static constexpr int kAtoms = kGroup == 2 ? 2 : 1;     // 128-byte K atoms per stage
+    static constexpr int kRowsA = kTileMRows / kGroup;      // A rows (m) per CTA and stage
+    static constexpr int kAtoms = kGroup == 2 && !kWide ? 2 : 1;   // 128-byte K atoms per stage
     static constexpr int kStageKBytes = kAtoms * kBlockKBytes;
-    static constexpr int kStages = kGroup == 2 ? 3 : 4;
+    static constexpr int kStages = kGroup == 2 && !kWide ? 3 : 4;
+    static constexpr int kHalfABytes = kTileM / kGroup * kBlockKBytes;   // one half's A rows of one atom
     static constexpr int kAtomBBytes = kRowsB * kBlockKBytes;
     static constexpr int kAtomABytes = kRowsA * kBlockKBytes;
     static constexpr int kSliceAtomBytes = kSliceB * kBlockKBytes;
@@ -475,10 +490,10 @@ __device__ __forceinline__ float2 stat_warp_reduce32(const float (&x)[32], int l
 }
 
 // ------------------------------------------------------------------ kernel
-template <class Kind, int kGroup>
+template <class Kind, int kGroup, bool kWide = false>
 __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_constant__ KernelParams p)
 {
-    using Cfg = TileCfg<kGroup>;
+    using Cfg = TileCfg<kGroup, kWide>;
     constexpr int kStages = Cfg::kStages;
     constexpr int kBlockKElems = kBlockKBytes / Kind::kElemBytes;   // K elements per atom
     constexpr uint32_t kIdesc = ptx::idesc_f32acc(Cfg::kTileN, kTileM, Kind::kFmt, Kind::kFmt);
@@ -608,13 +623,17 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 bool shared;
                 cluster_units(it, un, shared);
                 const bool cut_m = un.mpart >= 0;
-                const int32_t rows_a = cut_m ? part_rows_a : Cfg::kRowsA;
+                // A rows of this CTA: one box per stage, or (a whole wide tile) one per half,
+                // the second kTileM rows further on.  A wide tile's A map has boxes of one
+                // half's rows, which are also an m part's.
+                const int32_t rows_a = kWide ? kTileM / kGroup : (cut_m ? part_rows_a : Cfg::kRowsA);
+                const bool two_halves = kWide && !cut_m;
                 const uint32_t fill = Cfg::kTileBBytes + a_bytes(un);
-                const CUtensorMap *map_a = cut_m ? &p.tmap_a_part : &p.tmap_a;
+                const CUtensorMap *map_a = cut_m && !kWide ? &p.tmap_a_part : &p.tmap_a;
                 // a phantom unit reads past the matrices: zero fill, the box's full byte count
                 const int32_t m0 = un.phantom ? p.M
-                                              : static_cast<int32_t>(un.tm * kTileM + (cut_m ? un.mpart * p.m_part_rows : 0) +
-                                                                     pos * rows_a);
+                                              : static_cast<int32_t>(un.tm * Cfg::kTileMRows +
+                                                                     (cut_m ? un.mpart * p.m_part_rows : 0) + pos * rows_a);
                 const int32_t nb = un.phantom ? p.N : static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB);
                 uint16_t mcast = 0;
                 for (uint32_t q = 0; q < pairs; ++q) mcast |= static_cast<uint16_t>(1u << (q * kGroup + pos));
@@ -638,6 +657,9 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                             else
                                 ptx::tma_load_2d_pair(sb, &p.tmap_b, lb, k0, nb);
                             ptx::tma_load_2d_pair(s_a + t * Cfg::kAtomABytes, map_a, lb, k0, m0);
+                            if (two_halves)
+                                ptx::tma_load_2d_pair(s_a + t * Cfg::kAtomABytes + Cfg::kHalfABytes, map_a, lb, k0,
+                                                      m0 + kTileM);
                         }
                     } else {
 #pragma unroll
@@ -702,7 +724,8 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             // m-part units: MMA N = m_part_rows
             constexpr uint32_t kIdescHalf = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 2, Kind::kFmt, Kind::kFmt);
             constexpr uint32_t kIdescQuarter = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 4, Kind::kFmt, Kind::kFmt);
-            const uint32_t idesc_part = quarter_m ? kIdescQuarter : kIdescHalf;
+            // (a wide tile's m parts are its halves: MMA N = 256)
+            const uint32_t idesc_part = kWide ? kIdesc : (quarter_m ? kIdescQuarter : kIdescHalf);
             if (p.flags & kFlagStallMma) ok = w.wait(never_bar, 0u, kSiteStall);
             for (int64_t it = 0; ok && it < iters; ++it) {
                 Unit un;
@@ -723,12 +746,20 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                         }
                         ptx::tc_fence_after_sync();
                         const uint64_t desc_b = ptx::desc_kmajor_sw128(s_b + t * Cfg::kAtomBBytes);
-                        const uint64_t desc_a = ptx::desc_kmajor_sw128(s_a + t * Cfg::kAtomABytes);
+                        // a whole wide tile: both halves (the second half's A rows and
+                        // accumulator columns follow the first's); otherwise one
+                        const int halves = kWide && un.mpart < 0 ? 2 : 1;
 #pragma unroll
-                        for (int j = 0; j < kBlockKBytes / kMmaKBytes; ++j) {
-                            // +32 bytes along K inside the 128-byte swizzle span = +2 in the address field
-                            Kind::template mma<kGroup>(d_tmem, desc_b + 2u * j, desc_a + 2u * j, idesc,
-                                                       (kk | t | j) != 0 ? 1u : 0u);
+                        for (int h = 0; h < Cfg::kHalves; ++h) {
+                            if (h >= halves) break;
+                            const uint64_t desc_a =
+                                ptx::desc_kmajor_sw128(s_a + t * Cfg::kAtomABytes + h * Cfg::kHalfABytes);
+#pragma unroll
+                            for (int j = 0; j < kBlockKBytes / kMmaKBytes; ++j) {
+                                // +32 bytes along K inside the 128-byte swizzle span = +2 in the address field
+                                Kind::template mma<kGroup>(d_tmem + h * kTileM, desc_b + 2u * j, desc_a + 2u * j, idesc,
+                                                           (kk | t | j) != 0 ? 1u : 0u);
+                            }
                         }
                         issued_any = true;
                     }
@@ -741,7 +772,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 }
                 if (!ok) break;
                 ptx::mma_commit<kGroup>(accfull_bar(acc), pair_mask);      // accumulator complete
-                if (++acc == 2) {
+                if (kWide || ++acc == 2) {          // a wide tile's accumulator is not double-buffered
                     acc = 0;
                     acc_phase ^= 1u;
                 }
@@ -840,12 +871,12 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             ptx::tc_fence_after_sync();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * quarter) << 16) + acc * kAccCols;
             const int32_t m_in_tile = un.mpart >= 0 ? un.mpart * p.m_part_rows : 0;   // the unit's first row m
-            const int32_t m0 = static_cast<int32_t>(un.tm * kTileM) + m_in_tile;
+            const int32_t m0 = static_cast<int32_t>(un.tm * Cfg::kTileMRows) + m_in_tile;
             // this warp's first output column
             const int32_t nw = static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB) + 32 * quarter;
             if (un.phantom) {
                 release_acc();   // nothing to store
-            } else if (un.kpart >= 0) {
+            } else if (!kWide && un.kpart >= 0) {
                 // Split-reduce part: store this part's FP32 partial; the reduce
                 // kernel that follows sums the parts in order and stores C.
                 const int64_t span = static_cast<int64_t>(Cfg::kRowsB) * kTileM;
@@ -862,7 +893,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                         reinterpret_cast<float4 *>(mine + c * kEpiBoxM)[j] =
                             make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                 }
-            } else if (un.khalf >= 0) {
+            } else if (!kWide && un.khalf >= 0) {
                 // Split-K half: store this half's FP32 partial, then take the tile's
                 // ticket.  The half that comes second adds the other half's partial
                 // (fp32 addition commutes, so either order gives the same C) and
@@ -911,8 +942,10 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     }
                 }
             } else {
-                const int n_chunks = un.mpart < 0 ? kTileM / kEpiBoxM : (quarter_m ? kTileM / 4 : kTileM / 2) / kEpiBoxM;
-                const bool stats = !Kind::kF8 && (p.flags & kFlagStats) != 0;
+                // (a wide tile's m parts are its 256-row halves)
+                const int n_chunks = un.mpart < 0 ? Cfg::kTileMRows / kEpiBoxM
+                                                  : (kWide ? kTileM : (quarter_m ? kTileM / 4 : kTileM / 2)) / kEpiBoxM;
+                const bool stats = !Kind::kF8 && !kWide && (p.flags & kFlagStats) != 0;
 #pragma unroll 1
                 for (int c = 0; c < n_chunks; ++c) {
                     float v[64];
@@ -994,7 +1027,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     }
                 }
             }
-            if (++acc == 2) {
+            if (kWide || ++acc == 2) {          // a wide tile's accumulator is not double-buffered
                 acc = 0;
                 acc_phase ^= 1u;
             }

@@ -281,6 +281,16 @@ void gemm_debug_inject_stall(int mode);
  */
 int gemm_debug_force_cta_group(int group);
 
+/*
+ * Test hook: whether CTA pairs compute 256 x 512 tiles (two N = 256 halves
+ * sharing the n-side rows, a 512-column accumulator) instead of 256 x 256.
+ * 0 (default): an estimate of the launch's length in tile times decides;
+ * 1: always, wherever CTA pairs run without the softmax statistics and
+ * without a preferred cluster size of 4; -1: never.  Returns 0, or -1 for
+ * other values.
+ */
+int gemm_debug_force_wide_tiles(int mode);
+
 /* Description of the last GEMM kernel launch on the calling host thread
  * (tile shape, grid, co-resident cluster slots), for logs and tests
  * (thread-local storage; "" before the first launch). */

@@ -269,8 +269,9 @@ def _launch_record():
     (4, 8192, 8192, 192),      # 512 two-pair units
     (4, 3000, 12289, 136),     # 6 x 49 = 294 two-pair units, ragged m, n
 ])
-def test_tail_wave_split_into_half_units(force_group, cta_group, M, N, K):
+def test_tail_wave_split_into_half_units(force_group, force_wide, cta_group, M, N, K):
     force_group(cta_group)
+    force_wide(-1)                # the split tail of 256 x 256 tiles
     A = synth.sign_fp16(M * K, 77 + M)
     B = synth.sign_fp16(N * K, 78 + N)
     got = run_f16(M, N, K, A, K, B, K)
@@ -297,8 +298,9 @@ def test_tail_wave_split_into_half_units(force_group, cta_group, M, N, K):
     (1, 2000, 2560, 700),      # one-CTA tiles
     (4, 2000, 3000, 520),      # preferred 4-CTA clusters
 ])
-def test_split_k_tail_exact_and_deterministic(force_group, cta_group, M, N, K):
+def test_split_k_tail_exact_and_deterministic(force_group, force_wide, cta_group, M, N, K):
     force_group(cta_group)
+    force_wide(-1)                # the split tail of 256 x 256 tiles
     A = synth.sign_fp16(M * K, 88 + M)
     B = synth.sign_fp16(N * K, 89 + N)
     got = run_f16(M, N, K, A, K, B, K)
@@ -323,13 +325,17 @@ def test_split_k_tail_exact_and_deterministic(force_group, cta_group, M, N, K):
     assert_tol(f16_values(g1[ni, mi]), f16_values(c), s, F16_TOL, "split-K tail")
 
 
-def test_cuda_graph_capture_and_replay():
+@pytest.mark.parametrize("wide", [-1, 1])
+def test_cuda_graph_capture_and_replay(force_wide, wide):
     """After one warm-up call (which sets the kernel attributes and allocates
     the split-K buffer of the stream), the calls enqueue only kernel launches,
     so a stream can be captured into a CUDA graph and replayed; the replays
-    give the same bits as direct calls."""
+    give the same bits as direct calls.  256 x 256 tiles: 32 x 9 = 288 pair
+    tiles with a split-K last wave (its tickets reset within each launch);
+    256 x 512 tiles: 16 x 9 = 144."""
     import dense_gemm_tn_gb300 as g
-    M, N, K = 8192, 2304, 1024              # 32 x 9 = 288 pair tiles: a split-K last wave
+    force_wide(wide)
+    M, N, K = 8192, 2304, 1024
     A = synth.gauss_fp16(M * K, 5); B = synth.gauss_fp16(N * K, 6)
     dA, dB = to_dev_u16(A), to_dev_u16(B)
     s = torch.cuda.Stream()
@@ -423,3 +429,70 @@ def test_small_grid_m_parts(force_group, cta_group, M, N, K, parts):
     qa, sa = synth.gauss_e4m3(M * K, 64 + M)
     qb, sb = synth.gauss_e4m3(N * K, 65 + N)
     check_f8_full(M, N, K, qa, qb, sa, sb, what=f"m parts e4m3 {M}x{N}x{K}")
+
+
+# ---------------------------------------------------------------- 256 x 512 pair tiles
+@pytest.fixture
+def force_wide():
+    import dense_gemm_tn_gb300 as g
+    yield g.gemm_debug_force_wide_tiles
+    g.gemm_debug_force_wide_tiles(0)
+    g.gemm_debug_force_cta_group(0)
+
+
+@pytest.mark.parametrize("M,N,K,cut", [
+    (1, 1, 1, False),
+    (257, 129, 65, False),       # one ragged tile
+    (513, 640, 520, False),      # ragged m across the two halves, ragged k
+    (300, 1000, 4097, False),    # K not a 16-byte multiple: repacked operands
+    (4096, 2560, 136, True),     # 8 x 10 = 80 tiles: the last 4 cut into m halves
+    (3000, 12289, 136, False),   # 6 x 49 = 294 tiles: a last wave too full to cut
+])
+def test_wide_tiles_pm1_exact(force_group, force_wide, M, N, K, cut):
+    """CTA pairs computing 256 x 512 tiles (two N = 256 halves), forced on shapes
+    the library would give other tiles: +-1 inputs bit-exact, Gaussian inputs
+    within tolerance, E4M3 too."""
+    import dense_gemm_tn_gb300 as g
+    force_group(2)
+    force_wide(1)
+    A = synth.sign_fp16(M * K, 66 + M)
+    B = synth.sign_fp16(N * K, 67 + N)
+    if M * N <= 4_000_000:
+        check_f16_full(M, N, K, A, B, exact=True, what=f"wide {M}x{N}x{K}")
+    else:
+        got = run_f16(M, N, K, A, K, B, K)
+        mi, ni = sample_positions(M, N, 20000, seed=M + K)
+        c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
+        assert np.array_equal(got[ni, mi], c)
+    rec = _launch_record()
+    assert rec["wide"] == 1 and rec["ctas_per_cluster"] == 2, rec
+    if rec["slots"] == 76:
+        assert (rec["tail_mode"] == 1) == cut, rec
+        if cut:
+            assert rec["units"] == rec["tiles"] + rec["tiles"] % 76, rec
+    if M * N <= 4_000_000:
+        Ag = synth.gauss_fp16(M * K, 68 + M)
+        Bg = synth.gauss_fp16(N * K, 69 + N)
+        check_f16_full(M, N, K, Ag, Bg, what=f"wide gaussian {M}x{N}x{K}")
+        qa, sa = synth.gauss_e4m3(M * K, 70 + M)
+        qb, sb = synth.gauss_e4m3(N * K, 71 + N)
+        check_f8_full(M, N, K, qa, qb, sa, sb, what=f"wide e4m3 {M}x{N}x{K}")
+        assert _launch_record()["wide"] == 1
+
+
+def test_wide_tiles_chosen_by_estimate():
+    """The library picks 256 x 512 tiles where they shorten the launch (8192^3,
+    the feed-forward shape) and 256 x 256 tiles where the last wave would waste
+    them (4096^3), on a GB300's 76 pair slots."""
+    import dense_gemm_tn_gb300 as g
+    cases = [((8192, 8192, 64), 1), ((8192, 28672, 64), 1), ((4096, 4096, 64), 0), ((2048, 3072, 64), 0)]
+    for (M, N, K), want in cases:
+        A = synth.sign_fp16(M * K, 5)
+        B = synth.sign_fp16(N * K, 6)
+        got = run_f16(M, N, K, A, K, B, K)
+        rec = _launch_record()
+        if rec["slots"] == 76 and rec["ctas_per_cluster"] == 2:
+            assert rec["wide"] == want, (M, N, K, rec)
+        mi, ni = sample_positions(M, N, 5000, seed=K)
+        c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
+        assert np.array_equal(got[ni, mi], c)

@@ -12,11 +12,13 @@ from tests.gpu_helpers import GuardedC, check_f16_full, to_dev_u16
 
 pytestmark = pytest.mark.gpu
 
-CASES = [(1, 1), (1, 2), (2, 1), (2, 2), (2, 3), (4, 1), (4, 2), (4, 3)]   # (CTAs per cluster, stalled thread)
+# (CTAs per cluster, 256 x 512 pair tiles, stalled thread)
+CASES = [(1, 0, 1), (1, 0, 2), (2, 0, 1), (2, 0, 2), (2, 0, 3), (4, 0, 1), (4, 0, 2), (4, 0, 3),
+         (2, 1, 1), (2, 1, 2), (2, 1, 3)]
 
 
-@pytest.mark.parametrize("cta_group,mode", CASES)
-def test_stalled_wait_reports_timeout_and_context_survives(cta_group, mode):
+@pytest.mark.parametrize("cta_group,wide,mode", CASES)
+def test_stalled_wait_reports_timeout_and_context_survives(cta_group, wide, mode):
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     import dense_gemm_tn_gb300 as g
@@ -26,6 +28,7 @@ def test_stalled_wait_reports_timeout_and_context_survives(cta_group, mode):
     dA, dB = to_dev_u16(A), to_dev_u16(B)
     C = GuardedC(M, N, M)
     g.gemm_debug_force_cta_group(cta_group)
+    g.gemm_debug_force_wide_tiles(wide if wide else -1)
     g.gemm_set_wait_limit_ns(50_000_000)      # 50 ms
     g.gemm_debug_inject_stall(mode)
     try:
@@ -40,7 +43,8 @@ def test_stalled_wait_reports_timeout_and_context_survives(cta_group, mode):
     # the status word was cleared and the next call (same tile shape) is right
     g.gemm_poll_device_status()
     try:
-        check_f16_full(M, N, K, A, B, what=f"after timeout, group {cta_group} mode {mode}")
+        check_f16_full(M, N, K, A, B, what=f"after timeout, group {cta_group} wide {wide} mode {mode}")
     finally:
         g.gemm_debug_force_cta_group(0)
+        g.gemm_debug_force_wide_tiles(0)
 
