@@ -286,6 +286,12 @@ double launch_estimate(int64_t tiles, int64_t slots, double tile, double half)
 // The time of a 256 x 512 tile in 256 x 256 tile times: measured on GB300,
 // under the power cap, somewhat less than two.
 constexpr double kWideTileCost = 0.95;
+// The time of one m half of a 256 x 512 tile, run in the wide tiles' stages
+// (half the MMAs per stage), in 256 x 256 tile times.  Not measured alone:
+// cutting 8192^3's last 56 wide tiles into 76 such halves and 72 k-half
+// quarters made the launch 4 % slower than leaving them whole, which puts a
+// half plus a quarter above one wide tile.
+constexpr double kWideHalfCost = 1.3;
 
 int launch_grid(int64_t work, int cap)
 {
@@ -541,7 +547,7 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         const int64_t slots = dev->sms / 2;
         const int64_t tiles256 = (M + tn::kTileM - 1) / tn::kTileM * tiles_n;
         const int64_t tiles512 = (M + 2 * tn::kTileM - 1) / (2 * tn::kTileM) * tiles_n;
-        wide = force > 0 || (force == 0 && launch_estimate(tiles512, slots, 2.0 * kWideTileCost, 1.0) <
+        wide = force > 0 || (force == 0 && launch_estimate(tiles512, slots, 2.0 * kWideTileCost, kWideHalfCost) <
                                                launch_estimate(tiles256, slots, 1.0, 0.5));
     }
     const int64_t tile_m_rows = wide ? 2 * tn::kTileM : tn::kTileM;
