@@ -496,3 +496,28 @@ def test_wide_tiles_chosen_by_estimate():
         mi, ni = sample_positions(M, N, 5000, seed=K)
         c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
         assert np.array_equal(got[ni, mi], c)
+
+
+LAYOUTS = [(136, 136, 304, 0, 0, 0), (141, 137, 303, 0, 0, 0), (136, 136, 300, 1, 0, 0), (144, 144, 312, 0, 0, 0),
+           (130, 130, 300, 0, 3, 5)]      # lda, ldb, ldc, C offset, A offset, B offset (elements)
+
+
+@pytest.mark.parametrize("cta_group,wide", [(1, -1), (2, -1), (2, 1), (4, -1)])
+def test_layouts_on_every_tile_shape(force_group, force_wide, cta_group, wide):
+    """Padded, odd and unaligned leading dimensions and bases (TMA in place,
+    repacked operands, direct C stores) on each tile shape, FP16 and E4M3."""
+    force_group(cta_group)
+    force_wide(wide)
+    M, N, K = 300, 700, 130
+    A = synth.gauss_fp16(M * K, 31)
+    B = synth.gauss_fp16(N * K, 32)
+    A8, sa = synth.gauss_e4m3(M * K, 33)
+    B8, sb = synth.gauss_e4m3(N * K, 34)
+    for lda, ldb, ldc, c_off, a_off, b_off in LAYOUTS:
+        what = f"group {cta_group} wide {wide} ld {lda},{ldb},{ldc} offsets {c_off},{a_off},{b_off}"
+        check_f16_full(M, N, K, A, B, lda=lda, ldb=ldb, ldc=ldc, c_offset=c_off, a_offset=a_off, b_offset=b_off,
+                       what=what)
+        if cta_group == 2:
+            assert _launch_record()["wide"] == (1 if wide == 1 else 0)
+        check_f8_full(M, N, K, A8, B8, sa, sb, lda=lda, ldb=ldb, ldc=ldc, c_offset=c_off, a_offset=a_off,
+                      b_offset=b_off, what="e4m3 " + what)

@@ -24,10 +24,22 @@ def _run(entry, M, N, K, dA, a_off, lda, dB, b_off, ldb):
     return C
 
 
-def test_noalloc_matches_gemm_f16_tn_on_two_calls():
+@pytest.mark.parametrize("tiles", ["auto", "256x512 pairs"])
+def test_noalloc_matches_gemm_f16_tn_on_two_calls(tiles):
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     import dense_gemm_tn_gb300 as g
+    if tiles != "auto":
+        g.gemm_debug_force_cta_group(2)
+        g.gemm_debug_force_wide_tiles(1)
+    try:
+        _compare_two_calls(g)
+    finally:
+        g.gemm_debug_force_cta_group(0)
+        g.gemm_debug_force_wide_tiles(0)
+
+
+def _compare_two_calls(g):
     cases = [
         # M, N, K, lda, ldb, a_off, b_off: every case needs an operand copy
         (300, 200, 130, 141, 137, 0, 0),     # K and strides not 16-byte multiples
