@@ -51,11 +51,37 @@ def metric_for(w: synth.Workload) -> str:
     return f"TFLOP/s (2MNK/t) {what} TN GEMM {w.M}x{w.N}x{w.K} on 1 GB300; % of dense tensor peak"
 
 
+def code_of(src: str) -> str:
+    """C++ source without its comments and with whitespace runs collapsed, so
+    that editing a comment does not count as changing the kernel."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":                       # string or character literal
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_sha() -> str:
+    """Hash of the kernel sources' code: a traffic record taken on other code is stale."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            h.update(code_of(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -8,10 +8,14 @@
 //
 // Orientation.  C column-major is C^T row-major: row n of C^T (= column n of
 // C) is contiguous in m.  The kernel therefore computes C^T = B^T A^T: the
-// tensor core's first operand ("lanes") is a 128-row tile of B's columns, its
-// second operand ("columns") a 256-row tile of A's rows.  TMEM lane i then
-// holds one output column n and 256 consecutive m values, so every epilogue
+// tensor core's first operand ("lanes") is a tile of B's columns, its second
+// operand ("columns") a tile of A's rows.  TMEM lane i then holds one output
+// column n and up to 256 consecutive m values per MMA, so every epilogue
 // thread owns a contiguous run of C.
+//
+// Tiles (n x m): one CTA per 128 x 256 (MMA M128 N256); a CTA pair per
+// 256 x 256 (cta_group::2, M256 N256); or a CTA pair per 256 x 512, two M256
+// N256 halves that share the n-side rows (TileCfg below).
 //
 // The blog's RDNA design problems and their Blackwell re-solutions:
 //   LDS padding / XOR permutation (its Step 3)   -> TMA 128-byte swizzle that
@@ -21,14 +25,18 @@
 //       the tile (hello-gpu ch.11, section 11.4);
 //   double buffer + staged commit (Steps 2, 8)   -> a kStages-deep shared
 //       memory ring with full/empty mbarriers;
-//   deeper K slices (Step 5)                     -> 128-byte K blocks (64 fp16
-//       or 128 e4m3 values) per stage, 4 MMAs per stage;
+//   deeper K slices (Step 5)                     -> 128- or 256-byte K stages
+//       (64 / 128 fp16 or 128 / 256 e4m3 values), 4 or 8 MMAs per stage;
 //   block reordering for cache reuse (Step 6)    -> persistent CTAs walking a
 //       grouped raster (tile_coord below);
 //   prefetch / WMMA interleave (Step 7)          -> warp specialisation: a TMA
-//       producer warp, a single-thread MMA issuer, 4 epilogue warps, and a
-//       double-buffered TMEM accumulator so the epilogue of tile i overlaps
-//       the main loop of tile i+1.
+//       producer warp, a single-thread MMA issuer, 4 epilogue warps; for tiles
+//       up to 256 wide in m a double-buffered TMEM accumulator, so the
+//       epilogue of tile i overlaps the main loop of tile i+1.
+//
+// Each launch is a programmatic dependent of the previous kernel on its
+// stream: setup overlaps that kernel's end, and griddepcontrol.wait orders
+// every global access after it.
 #pragma once
 
 #include <cmath>

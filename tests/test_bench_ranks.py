@@ -89,3 +89,13 @@ def test_reference_arm_rank0_json_line():
     assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_kernel_hash_ignores_comments_only():
+    """A traffic record stays valid across comment edits, not across code edits."""
+    import bench
+    src = 'int a = 1; // one\n/* block\n comment */ const char *s = "x // not a comment";\n'
+    assert bench.code_of(src) == 'int a = 1; const char *s = "x // not a comment";'
+    assert bench.code_of(src.replace("// one", "// uno")) == bench.code_of(src)
+    assert bench.code_of(src.replace("a = 1", "a = 2")) != bench.code_of(src)
+    assert bench.code_of("char c = '\\\\'; // x") == "char c = '\\\\';"
