@@ -195,6 +195,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) quant_amax_kernel(const 
     using T = In<kIn>;
     constexpr int kB = elem_bytes(kIn);
     __shared__ float red[kThreads / 32];
+    // Launched as a programmatic dependent of the previous kernel on the
+    // stream (which may still read the slot array, or write x): nothing below
+    // touches global memory before that kernel has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     int64_t ub, ue;
     unit_range(p, ub, ue);
     const int64_t unit = unit_elems(kIn);

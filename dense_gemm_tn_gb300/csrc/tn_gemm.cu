@@ -685,17 +685,19 @@ gemm_status_t launch_quant(DeviceState &dev, qz::QuantParams &prm, cudaStream_t 
     snprintf(t_last_launch, sizeof(t_last_launch), "gemm_quantize_e4m3: grid=%lld units=%lld vec=%d",
              (long long)grid, (long long)prm.num_units, prm.vec);
 
+    // Both kernels are programmatic dependents of the kernel before them on
+    // the stream, and wait for it (griddepcontrol.wait) before any access.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(qz::kThreads, 1, 1);
     cfg.stream = stream;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, amax_kernel, prm);
-    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "gemm_quantize_e4m3: launch (amax): %s", cudaGetErrorString(e));
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, amax_kernel, prm);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "gemm_quantize_e4m3: launch (amax): %s", cudaGetErrorString(e));
     e = cudaLaunchKernelEx(&cfg, store_kernel, prm);
     if (e != cudaSuccess)
         return fail(GEMM_ERR_CUDA, "gemm_quantize_e4m3: launch (quantise): %s", cudaGetErrorString(e));

@@ -581,11 +581,9 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     // The kernel is launched as a programmatic dependent of whatever precedes
     // it on the stream, so the setup above (barriers, TMEM, descriptor
     // prefetch) overlaps the end of that kernel.  Nothing below touches global
-    // memory before that kernel has completed.  The next kernel may then start
-    // its own setup on SMs as this grid's CTAs leave them: it too waits for
-    // this grid to complete before it reads or writes memory.
+    // memory before that kernel has completed.  (The next kernel is let in by
+    // the producer once it has issued its last load, below.)
     ptx::griddep_wait();
-    ptx::griddep_launch_dependents();
 
     const Waiter w{abort_flag, abort_addr, rank, ctas, p.wait_limit_ns};
 
@@ -685,6 +683,13 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     }
                 }
             }
+            // This CTA issues no more loads: the next kernel on the stream may
+            // start its setup (it too waits for this grid to complete before it
+            // touches memory).  Not earlier: a dependent's CTAs that wait on SMs
+            // beside this grid's for a whole launch slowed it (by 2 % for a
+            // 305 us FP8 GEMM followed by the quantiser).  A single thread's
+            // signal counts for its CTA, else the CTA's exit does.
+            ptx::griddep_launch_dependents();
             if constexpr (kGroup == 2) {
                 // publish the final count (release: the count store is ordered before it)
                 ptx::st_release_cluster_u32(ptx::mapa_shared(done_addr, rank), 1u);

@@ -148,3 +148,41 @@ def test_softmax_stats_then_gemm_on_its_scores():
         assert np.array_equal(C.cpu().numpy().view(np.uint16), scores)
         assert np.array_equal(row_max.cpu().numpy().astype(np.float64), mx_ref)     # integer scores x 0.5: exact
         assert np.array_equal(C2.cpu().numpy().view(np.uint16), ref2), f"rep {rep}"
+
+
+def test_gemm_then_quantise_then_fp8_gemm():
+    """An FP16 GEMM's C is quantised to E4M3 on the device and fed, with its
+    device-resident scale, to an FP8 GEMM: three programmatic dependents back
+    to back.  C and the codes are bit-exact (integer sums, the same binary32
+    quantisation arithmetic), the FP8 result within the FP8 tolerance."""
+    import dense_gemm_tn_gb300 as g
+    from tests.gpu_helpers import F8_TOL, assert_tol, bf16_values
+    M, N, K = 1024, 768, 64
+    A = synth.sign_fp16(M * K, 7401)
+    B = synth.sign_fp16(N * K, 7402)
+    C1 = ref_nm(M, N, K, A, B)                                # (N, M) fp16 codes
+    q_ref, s_ref = oracle.quantize_e4m3(C1.reshape(-1), "f16", N, M)
+    N2 = 512
+    qb, sb = synth.gauss_e4m3(N2 * M, 7403)                   # the second GEMM: M' = N, K' = M
+    C2_ref, S2, _ = oracle.gemm_f8e4m3_tn(N, N2, M, q_ref, M, qb, M, s_ref, sb)
+    s = torch.cuda.Stream()
+    dA, dB = to_dev_u16(A), to_dev_u16(B)
+    dqb = torch.from_numpy(qb).cuda()
+    scales = torch.tensor([0.0, sb], dtype=torch.float32, device="cuda")
+    for rep in range(3):
+        C = torch.full((N, M), 0x7E00, dtype=torch.int16, device="cuda")
+        q = torch.zeros((N, M), dtype=torch.uint8, device="cuda")
+        C2 = torch.full((N2, N), 0x7FC0, dtype=torch.int16, device="cuda")
+        scales[0] = float("nan")
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            g.gemm_f16_tn(M, N, K, dA, K, dB, K, C, M, s)
+            g.gemm_quantize_e4m3(C, g.GEMM_IN_F16, N, M, M, q, M, scales.data_ptr(), s)
+            g.gemm_f8e4m3_tn_dscale(N, N2, M, q, M, dqb, M, C2, N, scales.data_ptr(), scales.data_ptr() + 4, s)
+        g.gemm_poll_device_status(s)
+        assert np.array_equal(C.cpu().numpy().view(np.uint16), C1), f"rep {rep}: C"
+        assert np.array_equal(q.cpu().numpy().reshape(-1), q_ref[: N * M]), f"rep {rep}: codes"
+        assert scales[0].item() == s_ref, f"rep {rep}: scale"
+        got2 = C2.cpu().numpy().view(np.uint16)
+        ref2 = oracle.c_as_nm(C2_ref, N, N2, N)
+        assert_tol(bf16_values(got2), bf16_values(ref2), S2, F8_TOL, f"rep {rep}: FP8 GEMM")
