@@ -283,15 +283,23 @@ double launch_estimate(int64_t tiles, int64_t slots, double tile, double half)
     return waves * tile + (waves >= 1 && 2 * rem <= slots ? half : tile);
 }
 
-// The time of a 256 x 512 tile in 256 x 256 tile times: measured on GB300,
-// under the power cap, somewhat less than two.
-constexpr double kWideTileCost = 0.95;
-// The time of one m half of a 256 x 512 tile, run in the wide tiles' stages
-// (half the MMAs per stage), in 256 x 256 tile times.  Not measured alone:
-// cutting 8192^3's last 56 wide tiles into 76 such halves and 72 k-half
-// quarters made the launch 4 % slower than leaving them whole, which puts a
-// half plus a quarter above one wide tile.
-constexpr double kWideHalfCost = 1.3;
+// Tile times for the choice between 256 x 256 and 256 x 512 pair tiles, in
+// units of a 256 x 256 tile's time; kb is the tile's number of 256-byte k
+// stages.  Fitted to A/B timings on GB300 under the power cap (sustained FP16
+// runs of 14 shapes from 3072^2 x 8192 to 16384^2 x 1024; on each the
+// estimate picks the faster tile):
+//  - a 256 x 512 tile: two 256 x 256 tiles' work at 0.913 each (a quarter
+//    fewer bytes out of L2 buys a higher clock), plus its epilogue, which the
+//    next tile's MMAs wait for: a fixed time, 1.76 tile times at kb = 1;
+//  - one m half of one, run in the wide stages: 1.36 (see below);
+//  - a cut half of a 256 x 256 tile in a last partial wave: 0.9, not 0.5;
+//    the partial sums cost more than a launch with few waves can hide.
+// Cutting 8192^3's last 56 wide tiles into 76 m halves and 72 k-half quarters
+// made the launch 4 % slower than leaving them whole, which puts a half plus
+// a quarter above one wide tile; so only m halves are used, at 1.36.
+double wide_tile_cost(double kb) { return 2.0 * 0.913 + 1.76 / kb; }
+constexpr double kWideHalfCost = 1.36;
+constexpr double kNarrowHalfCost = 0.9;
 
 int launch_grid(int64_t work, int cap)
 {
@@ -547,8 +555,10 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         const int64_t slots = dev->sms / 2;
         const int64_t tiles256 = (M + tn::kTileM - 1) / tn::kTileM * tiles_n;
         const int64_t tiles512 = (M + 2 * tn::kTileM - 1) / (2 * tn::kTileM) * tiles_n;
-        wide = force > 0 || (force == 0 && launch_estimate(tiles512, slots, 2.0 * kWideTileCost, kWideHalfCost) <
-                                               launch_estimate(tiles256, slots, 1.0, 0.5));
+        const int64_t kb = (K * esz + 255) / 256;                       // 256-byte k stages
+        const double t_wide = launch_estimate(tiles512, slots, wide_tile_cost(double(kb)), kWideHalfCost);
+        const double t_narrow = launch_estimate(tiles256, slots, 1.0, kNarrowHalfCost);
+        wide = force > 0 || (force == 0 && t_wide < t_narrow);
     }
     const int64_t tile_m_rows = wide ? 2 * tn::kTileM : tn::kTileM;
     const int64_t tiles_m = (M + tile_m_rows - 1) / tile_m_rows;

@@ -481,11 +481,12 @@ def test_wide_tiles_pm1_exact(force_group, force_wide, M, N, K, cut):
 
 
 def test_wide_tiles_chosen_by_estimate():
-    """The library picks 256 x 512 tiles where they shorten the launch (8192^3,
-    the feed-forward shape) and 256 x 256 tiles where the last wave would waste
-    them (4096^3), on a GB300's 76 pair slots."""
+    """The library picks 256 x 512 tiles where its estimate of the launch's
+    length says they are faster (a long K: the wide tile's exposed epilogue is
+    a small part of it) and 256 x 256 tiles elsewhere (a short K, or a grid
+    whose wide tiles would leave most of a wave idle), on 76 pair slots."""
     import dense_gemm_tn_gb300 as g
-    cases = [((8192, 8192, 64), 1), ((8192, 28672, 64), 1), ((4096, 4096, 64), 0), ((2048, 3072, 64), 0)]
+    cases = [((8192, 8192, 2048), 1), ((3072, 3072, 8192), 1), ((8192, 8192, 256), 0), ((2048, 3072, 64), 0)]
     for (M, N, K), want in cases:
         A = synth.sign_fp16(M * K, 5)
         B = synth.sign_fp16(N * K, 6)
