@@ -286,7 +286,7 @@ double launch_estimate(int64_t tiles, int64_t slots, double tile, double half)
 // Tile times for the choice between 256 x 256 and 256 x 512 pair tiles, in
 // units of a 256 x 256 tile's time; kb is the tile's number of 256-byte k
 // stages.  Fitted to A/B timings on GB300 under the power cap (sustained FP16
-// runs of 14 shapes from 3072^2 x 8192 to 16384^2 x 1024; on each the
+// runs of 12 shapes from 3072^2 x 8192 to 16384^2 x 1024; on each the
 // estimate picks the faster tile):
 //  - a 256 x 512 tile: two 256 x 256 tiles' work at 0.913 each (a quarter
 //    fewer bytes out of L2 buys a higher clock), plus its epilogue, which the
