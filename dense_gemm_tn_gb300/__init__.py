@@ -223,15 +223,53 @@ def gemm_debug_force_wide_tiles(mode: int) -> None:
 
 
 # ---------------------------------------------------------------- torch helpers
-def f16_tn(A, Bt, C=None, stream=None):
-    """C^T (N, M) = Bt (N, K) @ A (M, K)^T, i.e. column-major C = A x B."""
+def _rows(t, dtype, name, shape=None, cuda=True):
+    """Checks a 2-D CUDA tensor of `dtype` whose rows are contiguous (the layout
+    the C ABI reads with a leading dimension) and returns its row stride."""
     import torch
-    M, K = A.shape
-    N = Bt.shape[0]
+    if not isinstance(t, torch.Tensor) or t.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D torch tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, not {t.dtype}")
+    if t.numel() > 0 and t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} must have unit stride along its second dimension")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, not {tuple(t.shape)}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+
+def _operands(A, Bt, dtype):
+    """(M, N, K, lda, ldb) of A (M, K) and Bt (N, K), both checked by _rows."""
+    lda = _rows(A, dtype, "A", cuda=False)
+    ldb = _rows(Bt, dtype, "Bt", cuda=False)
+    (M, K), N = A.shape, Bt.shape[0]
+    if Bt.shape[1] != K:
+        raise ValueError(f"A is {tuple(A.shape)} and Bt {tuple(Bt.shape)}: their second dimensions (K) differ")
+    for t, name in ((A, "A"), (Bt, "Bt")):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    if A.device != Bt.device:
+        raise ValueError("A and Bt must be on the same device")
+    return M, N, K, lda, ldb
+
+
+def _output(C, M, N, dtype, device):
+    import torch
     if C is None:
-        C = torch.empty((N, M), dtype=torch.float16, device=A.device)
-    gemm_f16_tn(M, N, K, A, A.stride(0) if M > 0 else max(K, 1), Bt,
-                Bt.stride(0) if N > 0 else max(K, 1), C, C.stride(0) if N > 0 else max(M, 1), stream)
+        C = torch.empty((N, M), dtype=dtype, device=device)
+    ldc = _rows(C, dtype, "C", (N, M))
+    return C, ldc
+
+
+def f16_tn(A, Bt, C=None, stream=None):
+    """C^T (N, M) = Bt (N, K) @ A (M, K)^T, i.e. column-major C = A x B.
+    A, Bt (and C) are fp16 CUDA tensors whose rows are contiguous."""
+    import torch
+    M, N, K, lda, ldb = _operands(A, Bt, torch.float16)
+    C, ldc = _output(C, M, N, torch.float16, A.device)
+    gemm_f16_tn(M, N, K, A, lda, Bt, ldb, C, ldc, stream)
     return C
 
 
@@ -239,15 +277,11 @@ def f16_tn_softmax_stats(Q, Kmat, scale, C=None, stream=None):
     """Q (M, K) and Kmat (N, K) fp16 CUDA tensors -> (S^T as an (N, M) fp16
     tensor, row_max (M,), row_sum (M,)): S = scale * Q Kmat^T."""
     import torch
-    M, K = Q.shape
-    N = Kmat.shape[0]
-    if C is None:
-        C = torch.empty((N, M), dtype=torch.float16, device=Q.device)
+    M, N, K, lda, ldb = _operands(Q, Kmat, torch.float16)
+    C, ldc = _output(C, M, N, torch.float16, Q.device)
     row_max = torch.empty(M, dtype=torch.float32, device=Q.device)
     row_sum = torch.empty(M, dtype=torch.float32, device=Q.device)
-    gemm_f16_tn_softmax_stats(M, N, K, Q, Q.stride(0) if M > 0 else max(K, 1), Kmat,
-                              Kmat.stride(0) if N > 0 else max(K, 1), C, C.stride(0) if N > 0 else max(M, 1),
-                              scale, row_max, row_sum, stream)
+    gemm_f16_tn_softmax_stats(M, N, K, Q, lda, Kmat, ldb, C, ldc, scale, row_max, row_sum, stream)
     return C, row_max, row_sum
 
 
@@ -267,26 +301,29 @@ def quantize_e4m3(x, stream=None):
     return q, scale
 
 
-def f8e4m3_tn_dscale(A, Bt, scale_a, scale_b, C=None, stream=None):
-    """f8e4m3_tn with the scales as 1-element float32 CUDA tensors."""
+def _scale_tensor(t, name):
     import torch
-    M, K = A.shape
-    N = Bt.shape[0]
-    if C is None:
-        C = torch.empty((N, M), dtype=torch.bfloat16, device=A.device)
-    gemm_f8e4m3_tn_dscale(M, N, K, A, A.stride(0) if M > 0 else max(K, 1), Bt,
-                          Bt.stride(0) if N > 0 else max(K, 1), C, C.stride(0) if N > 0 else max(M, 1),
-                          scale_a, scale_b, stream)
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda or t.numel() < 1:
+        raise ValueError(f"{name} must be a float32 CUDA tensor with at least one element")
+
+
+def f8e4m3_tn_dscale(A, Bt, scale_a, scale_b, C=None, stream=None):
+    """f8e4m3_tn with the scales as 1-element float32 CUDA tensors.  A, Bt:
+    uint8 E4M3 codes (CUDA, rows contiguous); C: bf16 (N, M)."""
+    import torch
+    M, N, K, lda, ldb = _operands(A, Bt, torch.uint8)
+    _scale_tensor(scale_a, "scale_a")
+    _scale_tensor(scale_b, "scale_b")
+    C, ldc = _output(C, M, N, torch.bfloat16, A.device)
+    gemm_f8e4m3_tn_dscale(M, N, K, A, lda, Bt, ldb, C, ldc, scale_a, scale_b, stream)
     return C
 
 
 def f8e4m3_tn(A, Bt, scale_a, scale_b, C=None, stream=None):
+    """C^T (N, M) = bf16(scale_a * scale_b * Bt A^T) for uint8 E4M3 codes A
+    (M, K) and Bt (N, K); the scales are Python floats."""
     import torch
-    M, K = A.shape
-    N = Bt.shape[0]
-    if C is None:
-        C = torch.empty((N, M), dtype=torch.bfloat16, device=A.device)
-    gemm_f8e4m3_tn(M, N, K, A, A.stride(0) if M > 0 else max(K, 1), Bt,
-                   Bt.stride(0) if N > 0 else max(K, 1), C, C.stride(0) if N > 0 else max(M, 1),
-                   scale_a, scale_b, stream)
+    M, N, K, lda, ldb = _operands(A, Bt, torch.uint8)
+    C, ldc = _output(C, M, N, torch.bfloat16, A.device)
+    gemm_f8e4m3_tn(M, N, K, A, lda, Bt, ldb, C, ldc, float(scale_a), float(scale_b), stream)
     return C
