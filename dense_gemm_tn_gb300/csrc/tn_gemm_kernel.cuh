@@ -740,6 +740,95 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             // (a wide tile's m parts are its halves: MMA N = 256)
             const uint32_t idesc_part = kWide ? kIdesc : (quarter_m ? kIdescQuarter : kIdescHalf);
             if (p.flags & kFlagStallMma) ok = w.wait(never_bar, 0u, kSiteStall);
+            if constexpr (kWide) {
+                // 256 x 512 tiles.  The epilogue hands the accumulator back one half at a
+                // time (accempty[0], then accempty[1]), each as soon as it has read that
+                // half into registers.  A whole tile's first MMAs need only half 0:
+                // while half 1 is still being read, stages are held with only their
+                // half-0 MMAs issued (at most kStages - 1, so the producer can always
+                // fill the next one); once half 1 is back, the held stages' half-1 MMAs
+                // are issued in order and each stage is freed after its own.  An m-part
+                // unit uses half 0 only and waits for both halves.
+                auto advance = [&](int &s, uint32_t &ph) {
+                    if (++s == kStages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                };
+                auto issue_half = [&](int s, int kk, int h) {
+                    const uint32_t s_b = s_ring + s * Cfg::kStageBytes;
+                    const uint64_t desc_b = ptx::desc_kmajor_sw128(s_b);
+                    const uint64_t desc_a = ptx::desc_kmajor_sw128(s_b + Cfg::kTileBBytes + h * Cfg::kHalfABytes);
+#pragma unroll
+                    for (int j = 0; j < kBlockKBytes / kMmaKBytes; ++j)
+                        Kind::template mma<kGroup>(tmem_base + h * kTileM, desc_b + 2u * j, desc_a + 2u * j, kIdesc,
+                                                   (kk | j) != 0 ? 1u : 0u);
+                };
+                for (int64_t it = 0; ok && it < iters; ++it) {
+                    Unit un;
+                    bool shared;
+                    cluster_units(it, un, shared);
+                    const bool two = un.mpart < 0;
+                    if (!w.wait(accempty_bar(0), acc_phase ^ 1u, kSiteAccEmpty)) break;
+                    bool h1 = false;
+                    if (!two) {
+                        if (!w.wait(accempty_bar(1), acc_phase ^ 1u, kSiteAccEmpty)) break;
+                        h1 = true;
+                    }
+                    ptx::tc_fence_after_sync();
+                    int held = 0, h_stage = 0, h_kk = 0;
+                    uint32_t h_phase = 0;
+                    auto flush = [&]() {
+                        ptx::tc_fence_after_sync();      // after the wait that returned half 1
+                        for (int q = 0; q < held; ++q) {
+                            issue_half(h_stage, h_kk + q, 1);
+                            ptx::mma_commit<kGroup>(empty_bar(h_stage), all_mask);
+                            advance(h_stage, h_phase);
+                        }
+                        held = 0;
+                    };
+                    for (int kk = 0; kk < un.nkb; ++kk) {
+                        if (!w.wait(loaded_bar(stage, 0), phase, kSiteLoaded)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after_sync();
+                        issue_half(stage, kk, 0);
+                        issued_any = true;
+                        if (two && !h1) h1 = ptx::mbar_try_wait(accempty_bar(1), acc_phase ^ 1u);
+                        if (two && !h1 && held + 1 < kStages) {
+                            if (held == 0) {
+                                h_stage = stage;
+                                h_phase = phase;
+                                h_kk = kk;
+                            }
+                            ++held;
+                            advance(stage, phase);
+                            continue;
+                        }
+                        if (two && !h1) {
+                            if (!w.wait(accempty_bar(1), acc_phase ^ 1u, kSiteAccEmpty)) {
+                                ok = false;
+                                break;
+                            }
+                            h1 = true;
+                        }
+                        if (two) {
+                            flush();
+                            issue_half(stage, kk, 1);
+                        }
+                        ptx::mma_commit<kGroup>(empty_bar(stage), all_mask);   // stage free for every CTA that writes it
+                        advance(stage, phase);
+                    }
+                    if (!ok) break;
+                    if (held > 0) {                      // fewer k blocks than held stages: half 1 last
+                        if (!h1 && !w.wait(accempty_bar(1), acc_phase ^ 1u, kSiteAccEmpty)) break;
+                        flush();
+                    }
+                    ptx::mma_commit<kGroup>(accfull_bar(0), pair_mask);      // accumulator complete
+                    acc_phase ^= 1u;
+                }
+            } else
             for (int64_t it = 0; ok && it < iters; ++it) {
                 Unit un;
                 bool shared;
@@ -808,15 +897,25 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         uint32_t acc_phase = 0;
         uint32_t chunk_ctr = 0;
 
-        // Hands the accumulator back to the MMA thread (after the last TMEM read).
-        auto release_acc = [&]() {
+        // Hands accumulator barrier b's TMEM columns back to the MMA thread (after
+        // their last TMEM read).
+        auto release_bar = [&](int b) {
             ptx::tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) {
                 if constexpr (kGroup == 2)
-                    ptx::mbar_arrive_remote(ptx::mapa_shared(accempty_bar(acc), lead));
+                    ptx::mbar_arrive_remote(ptx::mapa_shared(accempty_bar(b), lead));
                 else
-                    ptx::mbar_arrive(accempty_bar(acc));
+                    ptx::mbar_arrive(accempty_bar(b));
+            }
+        };
+        // The whole accumulator: a wide tile's is two halves with a barrier each.
+        auto release_acc = [&]() {
+            if constexpr (kWide) {
+                release_bar(0);
+                release_bar(1);
+            } else {
+                release_bar(acc);
             }
         };
         // Reads 64 accumulator columns (this thread's lane) starting at column `col`.
@@ -832,12 +931,14 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 v[32 + j] = __uint_as_float(r1[j]);
             }
         };
-        // Converts 64 values of rows mc .. mc+63 of output column (nw + lane) and
-        // stores them: TMA store for m < m_tma, direct stores for the rest.
-        auto store_chunk = [&](const float (&v)[64], int32_t mc, int32_t nw) {
-            uint32_t packed[32];
+        // Converts 64 values of rows mc .. mc+63 of output column (nw + lane) to
+        // 16-bit pairs, and stores them: TMA store for m < m_tma, direct stores
+        // for the rest.
+        auto pack_chunk = [&](const float (&v)[64], uint32_t (&packed)[32]) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) packed[j] = Kind::pack(v[2 * j], v[2 * j + 1], scale);
+        };
+        auto store_packed = [&](const uint32_t (&packed)[32], int32_t mc, int32_t nw) {
             if (tma_store && mc < p.m_tma) {
                 const uint32_t buf = s_epi + (ew * kEpiBufs + (chunk_ctr & 1u)) * kEpiBufBytes;
                 if (lane == 0) ptx::bulk_wait_group_read<kEpiBufs - 1>();   // buffer's previous store has read it
@@ -871,6 +972,11 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     }
                 }
             }
+        };
+        auto store_chunk = [&](const float (&v)[64], int32_t mc, int32_t nw) {
+            uint32_t packed[32];
+            pack_chunk(v, packed);
+            store_packed(packed, mc, nw);
         };
 
         for (int64_t it = 0; it < iters; ++it) {
@@ -959,6 +1065,36 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 const int n_chunks = un.mpart < 0 ? Cfg::kTileMRows / kEpiBoxM
                                                   : (kWide ? kTileM : (quarter_m ? kTileM / 4 : kTileM / 2)) / kEpiBoxM;
                 const bool stats = !Kind::kF8 && !kWide && (p.flags & kFlagStats) != 0;
+                if (kWide && un.mpart < 0) {
+                    // A whole wide tile, half by half: the first two chunks of the half go
+                    // through the staging buffers, the last two are read into registers
+                    // (16-bit pairs); then the half is handed back, so the next tile's MMAs
+                    // on it can start while this warp stores those two.
+#pragma unroll 1
+                    for (int h = 0; h < 2; ++h) {
+                        const int c0 = 4 * h;
+#pragma unroll 1
+                        for (int c = c0; c < c0 + 2; ++c) {
+                            float v[64];
+                            load_chunk(t_row, c * kEpiBoxM, v);
+                            store_chunk(v, m0 + c * kEpiBoxM, nw);
+                        }
+                        uint32_t pk0[32], pk1[32];
+                        {
+                            float v[64];
+                            load_chunk(t_row, (c0 + 2) * kEpiBoxM, v);
+                            pack_chunk(v, pk0);
+                        }
+                        {
+                            float v[64];
+                            load_chunk(t_row, (c0 + 3) * kEpiBoxM, v);
+                            pack_chunk(v, pk1);
+                        }
+                        release_bar(h);
+                        store_packed(pk0, m0 + (c0 + 2) * kEpiBoxM, nw);
+                        store_packed(pk1, m0 + (c0 + 3) * kEpiBoxM, nw);
+                    }
+                } else
 #pragma unroll 1
                 for (int c = 0; c < n_chunks; ++c) {
                     float v[64];
