@@ -285,19 +285,22 @@ double launch_estimate(int64_t tiles, int64_t slots, double tile, double half)
 
 // Tile times for the choice between 256 x 256 and 256 x 512 pair tiles, in
 // units of a 256 x 256 tile's time; kb is the tile's number of 256-byte k
-// stages.  Fitted to A/B timings on GB300 under the power cap (sustained FP16
-// runs of 12 shapes from 3072^2 x 8192 to 16384^2 x 1024; on each the
-// estimate picks the faster tile):
+// stages.  Fitted to sustained A/B timings on GB300 under the power cap (FP16
+// shapes from 3072^2 x 8192 to 16384^2 x 1024, and E4M3 ones):
 //  - a 256 x 512 tile: two 256 x 256 tiles' work at 0.913 each (a quarter
-//    fewer bytes out of L2 buys a higher clock), plus its epilogue, which the
-//    next tile's MMAs wait for: a fixed time, 1.76 tile times at kb = 1;
+//    fewer bytes out of L2 buys a higher clock), plus the part of its
+//    epilogue that the next tile's MMAs wait for (a half of the accumulator
+//    is handed back once read): a fixed time, 0.6 tile times at kb = 1;
 //  - one m half of one, run in the wide stages: 1.36 (see below);
 //  - a cut half of a 256 x 256 tile in a last partial wave: 0.9, not 0.5;
 //    the partial sums cost more than a launch with few waves can hide.
+// One family of shapes is still missed: 16384 x 8192 with 8 k stages, where
+// 256 x 256 tiles are 4-5 % faster (FP16 and E4M3); 8192^2 with 8 stages,
+// 7 % faster on wide tiles, rules out a larger epilogue term.
 // Cutting 8192^3's last 56 wide tiles into 76 m halves and 72 k-half quarters
 // made the launch 4 % slower than leaving them whole, which puts a half plus
 // a quarter above one wide tile; so only m halves are used, at 1.36.
-double wide_tile_cost(double kb) { return 2.0 * 0.913 + 1.76 / kb; }
+double wide_tile_cost(double kb) { return 2.0 * 0.913 + 0.6 / kb; }
 constexpr double kWideHalfCost = 1.36;
 constexpr double kNarrowHalfCost = 0.9;
 
