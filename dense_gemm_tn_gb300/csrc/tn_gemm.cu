@@ -15,6 +15,7 @@
 
 #include "tn_gemm.h"
 #include "tn_gemm_kernel.cuh"
+#include "repack_kernel.cuh"
 #include "quant_e4m3_kernel.cuh"
 
 namespace {
@@ -264,12 +265,10 @@ void launch_repack(const tn::RepackJob<T> &j0, const tn::RepackJob<T> &j1, cudaS
 {
     constexpr int64_t kVec = 16 / sizeof(T);
     const int64_t ld_dst = j0.rows ? j0.ld_dst : j1.ld_dst;
-    const int64_t chunks = ld_dst / kVec;
-    const int64_t rows = j0.rows + j1.rows;
-    const int64_t rows_y = rows < 65535 ? rows : 65535;
-    const dim3 grid(static_cast<unsigned>((chunks + 127) / 128), static_cast<unsigned>(rows_y),
-                    static_cast<unsigned>((rows + rows_y - 1) / rows_y));
-    tn::repack_rows_kernel<T><<<grid, 128, 0, stream>>>(j0, j1);
+    const int64_t segs = (ld_dst / kVec + tn::kRepackSeg - 1) / tn::kRepackSeg;
+    const int64_t units = (j0.rows + j1.rows) * segs;
+    const unsigned blocks = static_cast<unsigned>((units + tn::kRepackWarps - 1) / tn::kRepackWarps);
+    tn::repack_rows_kernel<T><<<blocks, tn::kRepackWarps * 32, 0, stream>>>(j0, j1, segs);
 }
 
 // Estimated length, in 256 x 256 tile times, of a persistent launch of `tiles`

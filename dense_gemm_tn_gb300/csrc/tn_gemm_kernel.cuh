@@ -1258,37 +1258,6 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const float *__restri
     }
 }
 
-template <typename T>
-struct RepackJob {
-    const T *src;
-    int64_t ld_src;
-    T *dst;
-    int64_t ld_dst;
-    int64_t rows, K;
-};
-
-// Both operands in one launch: rows 0 .. j0.rows-1 come from job 0, the rest
-// from job 1 (which may have no rows); the two share ld_dst.
-template <typename T>
-__global__ void repack_rows_kernel(const RepackJob<T> j0, const RepackJob<T> j1)
-{
-    constexpr int kVec = 16 / sizeof(T);
-    int64_t r = blockIdx.y + static_cast<int64_t>(blockIdx.z) * gridDim.y;
-    const bool second = r >= j0.rows;
-    const RepackJob<T> &j = second ? j1 : j0;
-    if (second) r -= j0.rows;
-    const int64_t c = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * kVec;
-    if (r >= j.rows || c >= j.ld_dst) return;
-    const T *s = j.src + r * j.ld_src;
-    union {
-        T v[kVec];
-        uint4 u;
-    } chunk;
-#pragma unroll
-    for (int i = 0; i < kVec; ++i) chunk.v[i] = c + i < j.K ? s[c + i] : T(0);
-    *reinterpret_cast<uint4 *>(j.dst + r * j.ld_dst + c) = chunk.u;
-}
-
 // C[m + n*ldc] = +0 for m < M, n < N (the K == 0 case).
 __global__ void zero_fill_kernel(uint16_t *__restrict__ c, int64_t ldc, int64_t M, int64_t N, uint16_t value)
 {

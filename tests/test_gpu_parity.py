@@ -121,6 +121,32 @@ def test_unaligned_operand_bases():
     check_f8_full(M, N, K, A8, B8, sa, sb, a_offset=7, b_offset=1, what="e4m3 offset bases")
 
 
+@pytest.mark.parametrize("pad", [1, 3, 8])
+@pytest.mark.parametrize("off", [0, 1, 3, 7])
+def test_repack_every_row_offset_f16(pad, off):
+    """Operands the TMA cannot address (K = 2100 is not a 16-byte multiple),
+    with strides and bases that start rows at every 2-byte offset from 16-byte
+    alignment; rows of 263 chunks span three copy segments.  The padding
+    holds +-Inf, which must never reach a product."""
+    M, N, K = 40, 36, 2100
+    A = synth.sign_fp16(M * K, 31 + pad)
+    B = synth.sign_fp16(N * K, 32 + off)
+    check_f16_full(M, N, K, A, B, exact=True, lda=K + pad, ldb=K + pad + 2, a_offset=off, b_offset=(off + 5) % 8,
+                   what=f"repack f16 pad {pad} off {off}")
+
+
+@pytest.mark.parametrize("pad", [1, 5, 16])
+@pytest.mark.parametrize("off", [0, 1, 5, 15])
+def test_repack_every_row_offset_e4m3(pad, off):
+    """As above for E4M3 rows (K = 2100 bytes): every byte offset occurs.
+    The padding holds NaN codes."""
+    M, N, K = 40, 36, 2100
+    A, sa = synth.gauss_e4m3(M * K, 41 + pad)
+    B, sb = synth.gauss_e4m3(N * K, 42 + off)
+    check_f8_full(M, N, K, A, B, sa, sb, lda=K + pad, ldb=K + pad + 3, a_offset=off, b_offset=(off + 9) % 16,
+                  what=f"repack e4m3 pad {pad} off {off}")
+
+
 def test_k_zero_writes_zeros_and_empty_is_noop():
     import dense_gemm_tn_gb300 as g
     got = run_f16(5, 3, 0, np.zeros(1, np.uint16), 1, np.zeros(1, np.uint16), 1)
