@@ -1202,13 +1202,6 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 }
 
 // ------------------------------------------------------------------ helpers
-// Copies a rows x K operand with row stride ld_src (elements) into a buffer
-// with row stride ld_dst >= K (a multiple of 16 bytes, 16-byte aligned base),
-// zero-filling columns K .. ld_dst-1.  One thread writes one 16-byte chunk of
-// a destination row; the source row may start at any element boundary, so it
-// is read element by element (consecutive threads read consecutive chunks).
-// Grid: x over the chunks of a row, y (and z for more than 65535 rows) over
-// rows.
 // kSplitReduce, second launch: C[m, n] = the sum over parts, in part order,
 // of the FP32 partials of (m, n) -- stored, like the GEMM epilogue, as FP16
 // or as bf16(sum * scale_a * scale_b).  One thread per 8 consecutive m of one
