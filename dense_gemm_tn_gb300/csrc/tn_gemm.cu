@@ -4,14 +4,17 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
+#include <iterator>
 #include <mutex>
 #include <unordered_map>
+#include <vector>
 
 #include "tn_gemm.h"
 #include "tn_gemm_kernel.cuh"
@@ -64,6 +67,17 @@ std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_force_cta_group{0};
 std::atomic<int> g_force_wide{0};       // 0: the cost estimate decides; 1: always; -1: never
+// The last launch on this host thread, for gemm_debug_last_launch: the
+// numbers are kept and formatted only when asked for (formatting every call
+// cost host time on the path of back-to-back small GEMMs).
+struct LaunchRecord {
+    const char *name = nullptr;     // nullptr: nothing launched yet
+    bool quant = false;
+    int G = 0, quad = 0, wide = 0, grid = 0, clusters = 0, slots = 0;
+    int tiles = 0, units = 0, tail_start = 0, tail_mode = 0, split_parts = 0, vec = 0;
+    long long qgrid = 0, qunits = 0;
+};
+thread_local LaunchRecord t_rec;
 thread_local char t_last_launch[256] = "";
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -183,7 +197,11 @@ gemm_status_t split_workspace(DeviceState &d, cudaStream_t stream, size_t ticket
 
 // Tensor maps are a pure function of their arguments (address, sizes, stride,
 // box, type), so encoded maps are cached and reused: repeated calls on the
-// same buffers skip cuTensorMapEncodeTiled.  Least recently used entries go.
+// same buffers skip cuTensorMapEncodeTiled (about a microsecond of host time
+// each, three per call).  A hash map holds up to kMaxEntries of them, enough
+// for callers that cycle through many buffers (a serving loop over many
+// weights, or a benchmark's rotating inputs); when it is full, the older half
+// (by last use) goes at once, so eviction costs O(1) per insertion on average.
 struct MapKey {
     uintptr_t base;
     uint64_t inner, outer, row_bytes;
@@ -196,12 +214,29 @@ struct MapKey {
     }
 };
 
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const
+    {
+        // 64-bit multiplicative mixing of the fields
+        uint64_t h = 0x9E3779B97F4A7C15ull;
+        const uint64_t f[6] = {static_cast<uint64_t>(k.base), k.inner, k.outer, k.row_bytes,
+                               (static_cast<uint64_t>(k.box_inner) << 32) | k.box_outer,
+                               static_cast<uint64_t>(static_cast<uint32_t>(k.type))};
+        for (uint64_t x : f) {
+            h ^= x + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+            h *= 0xBF58476D1CE4E5B9ull;
+        }
+        return static_cast<size_t>(h ^ (h >> 31));
+    }
+};
+
 struct MapCache {
-    static constexpr int kEntries = 64;
-    MapKey key[kEntries];
-    CUtensorMap map[kEntries];
-    uint64_t used_at[kEntries] = {};
-    int size = 0;
+    static constexpr size_t kMaxEntries = 8192;
+    struct Entry {
+        CUtensorMap map;
+        uint64_t used_at;
+    };
+    std::unordered_map<MapKey, Entry, MapKeyHash> entries;
     uint64_t clock = 0;
     std::mutex mutex;
 };
@@ -215,12 +250,12 @@ gemm_status_t encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *
                      static_cast<int>(type)};
     {
         std::lock_guard<std::mutex> lock(g_maps.mutex);
-        for (int i = 0; i < g_maps.size; ++i)
-            if (g_maps.key[i] == key) {
-                g_maps.used_at[i] = ++g_maps.clock;
-                *map = g_maps.map[i];
-                return GEMM_OK;
-            }
+        auto it = g_maps.entries.find(key);
+        if (it != g_maps.entries.end()) {
+            it->second.used_at = ++g_maps.clock;
+            *map = it->second.map;
+            return GEMM_OK;
+        }
     }
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -233,17 +268,16 @@ gemm_status_t encode_2d(CUtensorMap *map, CUtensorMapDataType type, const void *
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(GEMM_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
     std::lock_guard<std::mutex> lock(g_maps.mutex);
-    int slot = g_maps.size;
-    if (slot == MapCache::kEntries) {
-        slot = 0;
-        for (int i = 1; i < MapCache::kEntries; ++i)
-            if (g_maps.used_at[i] < g_maps.used_at[slot]) slot = i;
-    } else {
-        ++g_maps.size;
+    if (g_maps.entries.size() >= MapCache::kMaxEntries) {
+        std::vector<uint64_t> ages;
+        ages.reserve(g_maps.entries.size());
+        for (const auto &kv : g_maps.entries) ages.push_back(kv.second.used_at);
+        std::nth_element(ages.begin(), ages.begin() + ages.size() / 2, ages.end());
+        const uint64_t cut = ages[ages.size() / 2];
+        for (auto it = g_maps.entries.begin(); it != g_maps.entries.end();)
+            it = it->second.used_at < cut ? g_maps.entries.erase(it) : std::next(it);
     }
-    g_maps.key[slot] = key;
-    g_maps.map[slot] = *map;
-    g_maps.used_at[slot] = ++g_maps.clock;
+    g_maps.entries[key] = MapCache::Entry{*map, ++g_maps.clock};
     return GEMM_OK;
 }
 
@@ -460,11 +494,19 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
                                          asrc.row_bytes, asrc.box_k, asrc.rows / prm.split_parts, "A part");
         if (st != GEMM_OK) return st;
     }
-    snprintf(t_last_launch, sizeof(t_last_launch),
-             "%s: ctas_per_cluster=%d%s wide=%d grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d "
-             "tail_mode=%d split_parts=%d",
-             name, G, quad && G == 2 ? " (preferred 4)" : "", W ? 1 : 0, G * clusters, clusters, slots,
-             prm.num_tiles, prm.num_units, prm.tail_start, prm.tail_mode, prm.split_parts);
+    t_rec.name = name;
+    t_rec.quant = false;
+    t_rec.G = G;
+    t_rec.quad = quad && G == 2;
+    t_rec.wide = W ? 1 : 0;
+    t_rec.grid = G * clusters;
+    t_rec.clusters = clusters;
+    t_rec.slots = slots;
+    t_rec.tiles = prm.num_tiles;
+    t_rec.units = prm.num_units;
+    t_rec.tail_start = prm.tail_start;
+    t_rec.tail_mode = prm.tail_mode;
+    t_rec.split_parts = prm.split_parts;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));
     if (prm.tail_mode == tn::kSplitReduce) {
@@ -614,7 +656,8 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         return st;
     if ((st = encode_2d(&prm.tmap_b, in_type, b_use, kb, N, ldb_use * esz, box_k, 128, "B")) != GEMM_OK)
         return st;
-    if ((st = encode_2d(&prm.tmap_b_slice, in_type, b_use, kb, N, ldb_use * esz, box_k, 64, "B slice")) != GEMM_OK)
+    if (quad &&    // the B rows each CTA of a 4-CTA cluster loads and shares
+        (st = encode_2d(&prm.tmap_b_slice, in_type, b_use, kb, N, ldb_use * esz, box_k, 64, "B slice")) != GEMM_OK)
         return st;
     // TMA stores cover rows m < M rounded down to 8 (16 bytes); the kernel
     // writes the ragged rest, or all of C when C's base or stride is unaligned.
@@ -694,8 +737,11 @@ gemm_status_t launch_quant(DeviceState &dev, qz::QuantParams &prm, cudaStream_t 
                                      &zeroed);
     if (st != GEMM_OK) return st;
     prm.slots = reinterpret_cast<float *>(slots + zeroed);
-    snprintf(t_last_launch, sizeof(t_last_launch), "gemm_quantize_e4m3: grid=%lld units=%lld vec=%d",
-             (long long)grid, (long long)prm.num_units, prm.vec);
+    t_rec.name = "gemm_quantize_e4m3";
+    t_rec.quant = true;
+    t_rec.qgrid = grid;
+    t_rec.qunits = prm.num_units;
+    t_rec.vec = prm.vec;
 
     // Both kernels are programmatic dependents of the kernel before them on
     // the stream, and wait for it (griddepcontrol.wait) before any access.
@@ -914,7 +960,22 @@ int gemm_debug_force_wide_tiles(int mode)
     return 0;
 }
 
-const char *gemm_debug_last_launch(void) { return t_last_launch; }
+const char *gemm_debug_last_launch(void)
+{
+    const LaunchRecord &r = t_rec;
+    if (!r.name)
+        t_last_launch[0] = '\0';
+    else if (r.quant)
+        snprintf(t_last_launch, sizeof(t_last_launch), "%s: grid=%lld units=%lld vec=%d", r.name, r.qgrid, r.qunits,
+                 r.vec);
+    else
+        snprintf(t_last_launch, sizeof(t_last_launch),
+                 "%s: ctas_per_cluster=%d%s wide=%d grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d "
+                 "tail_mode=%d split_parts=%d",
+                 r.name, r.G, r.quad ? " (preferred 4)" : "", r.wide, r.grid, r.clusters, r.slots, r.tiles, r.units,
+                 r.tail_start, r.tail_mode, r.split_parts);
+    return t_last_launch;
+}
 
 const char *gemm_build_info(void)
 {
