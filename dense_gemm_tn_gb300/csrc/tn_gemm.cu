@@ -407,7 +407,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     const int cap = quad && G == 2 && slots >= 2 ? (slots & ~1) : slots;
     const bool stats = (prm.flags & tn::kFlagStats) != 0;
     int reduce_parts = 1;
-    if (!W && allow_alloc && !stats && 2 * prm.num_tiles <= cap && prm.num_kb >= 32) {
+    if (allow_alloc && !stats && 2 * prm.num_tiles <= cap && prm.num_kb >= 32) {
         int S = cap / prm.num_tiles;
         if (S > 8) S = 8;
         if (S > prm.num_kb / 16) S = prm.num_kb / 16;
@@ -452,7 +452,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     prm.split_parts = 1;
     prm.m_part_rows = 0;
     if (reduce_parts > 1) {
-        const size_t partial = size_t(prm.num_tiles) * reduce_parts * G * Cfg::kRowsB * tn::kTileM * sizeof(float);
+        const size_t partial = size_t(prm.num_tiles) * reduce_parts * G * Cfg::kRowsB * Cfg::kTileMRows * sizeof(float);
         uint8_t *base = nullptr;
         size_t zeroed = 0;
         gemm_status_t st = stream_buffer(dev.split, stream, 0, partial, "split-K partials", &base, &zeroed);
@@ -521,7 +521,8 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
         rcfg.stream = stream;
         rcfg.attrs = rattr;
         rcfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&rcfg, tn::split_reduce_kernel<Kind, G>, static_cast<const float *>(prm.split_ws),
+        e = cudaLaunchKernelEx(&rcfg, tn::split_reduce_kernel<Kind, G, Cfg::kTileMRows>,
+                               static_cast<const float *>(prm.split_ws),
                                static_cast<int>(prm.split_parts), static_cast<int64_t>(prm.tiles_n), prm.M, prm.N,
                                prm.c_ptr, prm.ldc, prm.scale, prm.scale_a_ptr, prm.scale_b_ptr);
         if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: split reduce launch: %s", name, cudaGetErrorString(e));

@@ -996,22 +996,36 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             const int32_t nw = static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB) + 32 * quarter;
             if (un.phantom) {
                 release_acc();   // nothing to store
-            } else if (!kWide && un.kpart >= 0) {
+            } else if (un.kpart >= 0) {
                 // Split-reduce part: store this part's FP32 partial; the reduce
-                // kernel that follows sums the parts in order and stores C.
-                const int64_t span = static_cast<int64_t>(Cfg::kRowsB) * kTileM;
+                // kernel that follows sums the parts in order and stores C.  Only
+                // the columns n < N (a few rows of a skinny problem's partial): the
+                // reduce kernel reads no others.  A wide tile hands each half of
+                // its accumulator back once read.
+                constexpr int kRowM = Cfg::kTileMRows;          // floats of one column n's partial
+                constexpr int kChunks = kRowM / kEpiBoxM;
+                const int64_t span = static_cast<int64_t>(Cfg::kRowsB) * kRowM;
                 float *mine = p.split_ws +
                               (((un.tm * p.tiles_n + un.tn) * p.split_parts + un.kpart) * kGroup + pos) * span +
-                              row * kTileM;
+                              row * kRowM;
+                const bool valid_n = nw + lane < p.N;
 #pragma unroll 1
-                for (int c = 0; c < kTileM / kEpiBoxM; ++c) {
+                for (int c = 0; c < kChunks; ++c) {
                     float v[64];
                     load_chunk(t_row, c * kEpiBoxM, v);
-                    if (c == kTileM / kEpiBoxM - 1) release_acc();
+                    if (kWide && c == kChunks / 2 - 1) release_bar(0);
+                    if (c == kChunks - 1) {
+                        if constexpr (kWide)
+                            release_bar(1);
+                        else
+                            release_acc();
+                    }
+                    if (valid_n) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        reinterpret_cast<float4 *>(mine + c * kEpiBoxM)[j] =
-                            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        for (int j = 0; j < 16; ++j)
+                            reinterpret_cast<float4 *>(mine + c * kEpiBoxM)[j] =
+                                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    }
                 }
             } else if (!kWide && un.khalf >= 0) {
                 // Split-K half: store this half's FP32 partial, then take the tile's
@@ -1207,7 +1221,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 // or as bf16(sum * scale_a * scale_b).  One thread per 8 consecutive m of one
 // column n: 32-byte reads of each partial, a 16-byte store of C.  Launched as
 // a programmatic dependent of the GEMM; waits for it to complete first.
-template <class Kind, int kGroup>
+template <class Kind, int kGroup, int kTileRows = kTileM>
 __global__ void __launch_bounds__(256) split_reduce_kernel(const float *__restrict__ ws, int parts, int64_t tiles_n,
                                                            int32_t M, int32_t N, void *c_ptr, int64_t ldc,
                                                            float scale, const float *scale_a, const float *scale_b)
@@ -1215,17 +1229,17 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const float *__restri
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const float s = scale_a ? __fmul_rn(__ldg(scale_a), __ldg(scale_b)) : scale;
     constexpr int64_t kRows = 128;                       // rows n of one CTA's partial
-    const int64_t part_stride = static_cast<int64_t>(kGroup) * kRows * kTileM;
+    const int64_t part_stride = static_cast<int64_t>(kGroup) * kRows * kTileRows;
     const int64_t groups_m = (M + 7) / 8;
     const bool vec_c = (ldc * 2) % 16 == 0 && reinterpret_cast<uintptr_t>(c_ptr) % 16 == 0;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < groups_m * N;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t n = i / groups_m;
         const int64_t m = (i - n * groups_m) * 8;
-        const int64_t tm = m / kTileM, tn = n / (kRows * kGroup);
+        const int64_t tm = m / kTileRows, tn = n / (kRows * kGroup);
         const int64_t pos = (n / kRows) % kGroup, row = n % kRows;
-        const float *src = ws + ((tm * tiles_n + tn) * parts * kGroup + pos) * kRows * kTileM + row * kTileM +
-                           (m % kTileM);
+        const float *src = ws + ((tm * tiles_n + tn) * parts * kGroup + pos) * kRows * kTileRows + row * kTileRows +
+                           (m % kTileRows);
         float v[8];
         {
             const float4 a = __ldcg(reinterpret_cast<const float4 *>(src));

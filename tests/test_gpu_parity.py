@@ -409,6 +409,41 @@ def test_split_reduce_long_k(force_group, cta_group, M, N, K, parts):
     assert_tol(f16_values(g1[ni, mi]), f16_values(c), s, F16_TOL, "split-reduce")
 
 
+@pytest.mark.parametrize("M,N,K,parts", [
+    (512, 2048, 16384, 8),      # 8 wide tiles: eight k ranges each
+    (1000, 300, 8199, 8),       # ragged m, n, k (repacked to 129 stages): 2 x 2 = 4 tiles
+    (4096, 16, 8192, 8),        # a skinny problem: 8 tiles, 16 valid columns of 256
+])
+def test_split_reduce_on_wide_tiles(force_group, force_wide, M, N, K, parts):
+    """The split-reduce of a small grid with a long K, run on 256 x 512 pair
+    tiles (each part stores both halves of its partial).  +-1 inputs
+    bit-exact; Gaussian inputs within tolerance and identical run to run;
+    E4M3 within its tolerance."""
+    force_group(2)
+    force_wide(1)
+    A = synth.sign_fp16(M * K, 97 + M)
+    B = synth.sign_fp16(N * K, 98 + N)
+    got = run_f16(M, N, K, A, K, B, K)
+    rec = _launch_record()
+    assert rec["wide"] == 1, rec
+    if rec["slots"] == 76:
+        assert rec["tail_mode"] == 3 and rec["split_parts"] == parts, rec
+    mi, ni = sample_positions(M, N, 20000, seed=K + 1)
+    c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
+    assert np.array_equal(got[ni, mi], c)
+    Ag = synth.gauss_fp16(M * K, 99 + M)
+    Bg = synth.gauss_fp16(N * K, 100 + N)
+    g1 = run_f16(M, N, K, Ag, K, Bg, K)
+    assert np.array_equal(g1, run_f16(M, N, K, Ag, K, Bg, K))
+    c, s, _ = oracle.gemm_f16_tn_at(M, N, K, Ag, K, Bg, K, mi, ni)
+    assert_tol(f16_values(g1[ni, mi]), f16_values(c), s, F16_TOL, "wide split-reduce")
+    qa, sa = synth.gauss_e4m3(M * K, 101 + M)
+    qb, sb = synth.gauss_e4m3(N * K, 102 + N)
+    got8 = run_f8(M, N, K, qa, K, qb, K, sa, sb)
+    c, s, _ = oracle.gemm_f8e4m3_tn_at(M, N, K, qa, K, qb, K, sa, sb, mi, ni)
+    assert_tol(bf16_values(got8[ni, mi]), bf16_values(c), s, F8_TOL, "wide split-reduce e4m3")
+
+
 def test_split_reduce_e4m3_host_and_device_scales():
     import dense_gemm_tn_gb300 as g
     M, N, K = 1024, 1024, 8192
