@@ -18,6 +18,7 @@
 
 #include "tn_gemm.h"
 #include "tn_gemm_kernel.cuh"
+#include "aux_kernels.cuh"
 #include "repack_kernel.cuh"
 #include "quant_e4m3_kernel.cuh"
 
