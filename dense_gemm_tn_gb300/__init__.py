@@ -260,7 +260,16 @@ def _output(C, M, N, dtype, device):
     if C is None:
         C = torch.empty((N, M), dtype=dtype, device=device)
     ldc = _rows(C, dtype, "C", (N, M))
+    if C.device != device:
+        raise ValueError(f"C is on {C.device}, the operands on {device}")
     return C, ldc
+
+
+def _on(device):
+    """The C ABI works on the calling thread's current device: make it the
+    operands' device for the call."""
+    import torch
+    return torch.cuda.device(device)
 
 
 def f16_tn(A, Bt, C=None, stream=None):
@@ -269,7 +278,8 @@ def f16_tn(A, Bt, C=None, stream=None):
     import torch
     M, N, K, lda, ldb = _operands(A, Bt, torch.float16)
     C, ldc = _output(C, M, N, torch.float16, A.device)
-    gemm_f16_tn(M, N, K, A, lda, Bt, ldb, C, ldc, stream)
+    with _on(A.device):
+        gemm_f16_tn(M, N, K, A, lda, Bt, ldb, C, ldc, stream)
     return C
 
 
@@ -281,7 +291,8 @@ def f16_tn_softmax_stats(Q, Kmat, scale, C=None, stream=None):
     C, ldc = _output(C, M, N, torch.float16, Q.device)
     row_max = torch.empty(M, dtype=torch.float32, device=Q.device)
     row_sum = torch.empty(M, dtype=torch.float32, device=Q.device)
-    gemm_f16_tn_softmax_stats(M, N, K, Q, lda, Kmat, ldb, C, ldc, scale, row_max, row_sum, stream)
+    with _on(Q.device):
+        gemm_f16_tn_softmax_stats(M, N, K, Q, lda, Kmat, ldb, C, ldc, scale, row_max, row_sum, stream)
     return C, row_max, row_sum
 
 
@@ -293,11 +304,14 @@ def quantize_e4m3(x, stream=None):
     types = {torch.float32: GEMM_IN_F32, torch.float16: GEMM_IN_F16, torch.bfloat16: GEMM_IN_BF16}
     if x.dtype not in types or x.dim() != 2 or (x.numel() > 0 and x.stride(1) != 1):
         raise ValueError("x must be a 2-D float32/float16/bfloat16 tensor with unit column stride")
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
     rows, cols = x.shape
     q = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
     scale = torch.empty(1, dtype=torch.float32, device=x.device)
     ld = max(cols, 1)
-    gemm_quantize_e4m3(x, types[x.dtype], rows, cols, x.stride(0) if rows > 1 else ld, q, ld, scale, stream)
+    with _on(x.device):
+        gemm_quantize_e4m3(x, types[x.dtype], rows, cols, x.stride(0) if rows > 1 else ld, q, ld, scale, stream)
     return q, scale
 
 
@@ -314,8 +328,11 @@ def f8e4m3_tn_dscale(A, Bt, scale_a, scale_b, C=None, stream=None):
     M, N, K, lda, ldb = _operands(A, Bt, torch.uint8)
     _scale_tensor(scale_a, "scale_a")
     _scale_tensor(scale_b, "scale_b")
+    if scale_a.device != A.device or scale_b.device != A.device:
+        raise ValueError("scale_a and scale_b must be on the operands' device")
     C, ldc = _output(C, M, N, torch.bfloat16, A.device)
-    gemm_f8e4m3_tn_dscale(M, N, K, A, lda, Bt, ldb, C, ldc, scale_a, scale_b, stream)
+    with _on(A.device):
+        gemm_f8e4m3_tn_dscale(M, N, K, A, lda, Bt, ldb, C, ldc, scale_a, scale_b, stream)
     return C
 
 
@@ -325,5 +342,6 @@ def f8e4m3_tn(A, Bt, scale_a, scale_b, C=None, stream=None):
     import torch
     M, N, K, lda, ldb = _operands(A, Bt, torch.uint8)
     C, ldc = _output(C, M, N, torch.bfloat16, A.device)
-    gemm_f8e4m3_tn(M, N, K, A, lda, Bt, ldb, C, ldc, float(scale_a), float(scale_b), stream)
+    with _on(A.device):
+        gemm_f8e4m3_tn(M, N, K, A, lda, Bt, ldb, C, ldc, float(scale_a), float(scale_b), stream)
     return C

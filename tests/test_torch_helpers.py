@@ -23,6 +23,8 @@ def test_helpers_reject_wrong_tensors_before_any_call():
         g.f16_tn(a, torch.zeros((4, 9), dtype=torch.float16))
     with pytest.raises(ValueError, match="shape"):
         g._output(torch.zeros((5, 4), dtype=torch.float16), 4, 4, torch.float16, None)
+    with pytest.raises(ValueError, match="CUDA"):
+        g.quantize_e4m3(torch.zeros((4, 8), dtype=torch.bfloat16))
 
 
 @pytest.mark.gpu
