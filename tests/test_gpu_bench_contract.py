@@ -35,8 +35,11 @@ def test_json_line(workload):
     assert d["gpu_launches"] == 20
     assert "workload" in d["config"]
     rf = d["roofline"]
-    assert rf["bound"] == "tensor" and rf["unit"] == "TFLOP/s" and rf["peak"] > 0
+    # these small shapes lie below the ridge point: HBM-bound by the roofline
+    assert rf["intensity_flop_per_byte"] < rf["ridge_flop_per_byte"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["peak"] > 0
     assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"])
+    assert rf["achieved"] == pytest.approx(rf["algorithmic_bytes"] / (rf["kernel_ms"] * 1e-3) / 1e9)
     e2e = d["e2e"]
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     cpu = d["cpu_baseline"]
