@@ -44,6 +44,7 @@ EXPORTS = (
     "gemm_poll_device_status", "gemm_release_workspace", "gemm_tile_coord",
     "gemm_set_wait_limit_ns", "gemm_debug_inject_stall", "gemm_build_info",
     "gemm_f16_tn_noalloc", "gemm_debug_force_cta_group", "gemm_debug_force_wide_tiles", "gemm_debug_last_launch",
+    "gemm_debug_set_raster_group",
     "gemm_f8e4m3_tn_dscale", "gemm_quantize_e4m3", "gemm_f16_tn_softmax_stats",
 )
 
@@ -96,6 +97,8 @@ def _load() -> ctypes.CDLL:
     lib.gemm_debug_force_cta_group.restype = ctypes.c_int
     lib.gemm_debug_force_wide_tiles.argtypes = [ctypes.c_int]
     lib.gemm_debug_force_wide_tiles.restype = ctypes.c_int
+    lib.gemm_debug_set_raster_group.argtypes = [ctypes.c_int]
+    lib.gemm_debug_set_raster_group.restype = ctypes.c_int
     lib.gemm_debug_last_launch.argtypes = []
     lib.gemm_debug_last_launch.restype = ctypes.c_char_p
     lib.gemm_build_info.argtypes = []
@@ -220,6 +223,12 @@ def gemm_debug_force_wide_tiles(mode: int) -> None:
     """0 automatic; 1 CTA pairs always compute 256 x 512 tiles; -1 never."""
     if _lib.gemm_debug_force_wide_tiles(int(mode)) != 0:
         raise ValueError("mode must be -1, 0 or 1")
+
+
+def gemm_debug_set_raster_group(rows: int) -> None:
+    """Tile rows per raster group of the scheduler (even, 2 .. 64); 0 the default."""
+    if _lib.gemm_debug_set_raster_group(int(rows)) != 0:
+        raise ValueError("rows must be 0 or an even number up to 64")
 
 
 # ---------------------------------------------------------------- torch helpers

@@ -68,6 +68,7 @@ std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_force_cta_group{0};
 std::atomic<int> g_force_wide{0};       // 0: the cost estimate decides; 1: always; -1: never
+std::atomic<int> g_raster_group{0};     // tile rows per raster group; 0: kGroupM
 // The last launch on this host thread, for gemm_debug_last_launch: the
 // numbers are kept and formatted only when asked for (formatting every call
 // cost host time on the path of back-to-back small GEMMs).
@@ -680,7 +681,10 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     const int64_t stage_k = wide ? tn::TileCfg<2, true>::kStageKBytes
                                  : cta_group == 2 ? tn::TileCfg<2>::kStageKBytes : tn::TileCfg<1>::kStageKBytes;
     prm.num_kb = static_cast<int32_t>((K * esz + stage_k - 1) / stage_k);   // k blocks = stages per tile
-    prm.group = kGroupM;            // even, so raster ids 2j, 2j+1 are neighbouring m tiles of one n tile
+    {
+        const int rg = g_raster_group.load();
+        prm.group = rg > 0 ? rg : kGroupM;   // even, so raster ids 2j, 2j+1 are neighbouring m tiles of one n tile
+    }
     prm.scale = scale;
     prm.scale_a_ptr = dscale_a;
     prm.scale_b_ptr = dscale_b;
@@ -959,6 +963,13 @@ int gemm_debug_force_wide_tiles(int mode)
 {
     if (mode < -1 || mode > 1) return -1;
     g_force_wide.store(mode);
+    return 0;
+}
+
+int gemm_debug_set_raster_group(int rows)
+{
+    if (rows < 0 || rows > 64 || rows % 2) return -1;
+    g_raster_group.store(rows);
     return 0;
 }
 

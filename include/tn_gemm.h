@@ -291,6 +291,14 @@ int gemm_debug_force_cta_group(int group);
  */
 int gemm_debug_force_wide_tiles(int mode);
 
+/*
+ * Test hook: the height, in tile rows, of the scheduler's raster groups
+ * (see gemm_tile_coord); 0 restores the default (8).  Even values only, so
+ * that raster ids 2j and 2j + 1 stay neighbouring m tiles of one n tile.
+ * Returns 0, or -1 for odd values or values outside 0 .. 64.
+ */
+int gemm_debug_set_raster_group(int rows);
+
 /* Description of the last GEMM kernel launch on the calling host thread
  * (tile shape, grid, co-resident cluster slots), for logs and tests
  * (thread-local storage; "" before the first launch). */

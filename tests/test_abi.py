@@ -119,3 +119,10 @@ def test_tile_coord_rejects_out_of_range():
         g.gemm_tile_coord(0, 3, 2, 0)
     with pytest.raises(ValueError):             # 2^32 tiles: more than the scheduler's 32-bit ids
         g.gemm_tile_coord(2 ** 20, 2 ** 12, 8, 0)
+
+
+def test_raster_group_hook_rejects_odd_and_large():
+    for bad in (-2, 3, 66):
+        with pytest.raises(ValueError):
+            g.gemm_debug_set_raster_group(bad)
+    g.gemm_debug_set_raster_group(0)

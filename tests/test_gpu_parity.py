@@ -541,6 +541,21 @@ def test_wide_tiles_pm1_exact(force_group, force_wide, M, N, K, cut):
         assert _launch_record()["wide"] == 1
 
 
+@pytest.mark.parametrize("rows", [2, 6, 16])
+def test_raster_group_heights_exact(rows):
+    """Other raster group heights reorder the tiles only: +-1 inputs give the
+    same bits (a short last group included: 11 tile rows)."""
+    import dense_gemm_tn_gb300 as g
+    M, N, K = 2816, 1536, 192
+    A = synth.sign_fp16(M * K, 111)
+    B = synth.sign_fp16(N * K, 112)
+    g.gemm_debug_set_raster_group(rows)
+    try:
+        check_f16_full(M, N, K, A, B, exact=True, what=f"raster group {rows}")
+    finally:
+        g.gemm_debug_set_raster_group(0)
+
+
 def test_wide_tiles_chosen_by_estimate():
     """The library picks 256 x 512 tiles where its estimate of the launch's
     length says they are faster (a long K: the wide tile's exposed epilogue is
