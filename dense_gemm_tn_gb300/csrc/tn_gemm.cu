@@ -103,12 +103,23 @@ EncodeTiledFn encode_fn()
 }
 
 // Current device's state, initialised on first use (caller holds no lock).
+// The device whose primary context this host thread has made current.
+thread_local int t_context_dev = -1;
+
 gemm_status_t device_state(DeviceState **out, int *dev_out)
 {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return fail(GEMM_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    if (t_context_dev != dev) {
+        // A host thread that has made no runtime call yet has no current
+        // context, and the driver calls made here (tensor-map encoding) need
+        // one: make the device's primary context current, once per thread.
+        if ((e = cudaSetDevice(dev)) != cudaSuccess)
+            return fail(GEMM_ERR_CUDA, "cudaSetDevice(%d): %s", dev, cudaGetErrorString(e));
+        t_context_dev = dev;
+    }
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState &d = g_devices[dev];
     if (!d.ready) {

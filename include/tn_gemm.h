@@ -47,7 +47,10 @@
  *     be captured and replayed; the kernels leave their buffers ready for the
  *     next launch.
  *   - Thread safety: every entry point may be called from several host
- *     threads; the per-device state is guarded internally.
+ *     threads; the per-device state is guarded internally.  On a thread's
+ *     first call for a device, the library makes that device's primary
+ *     context current on the thread (cudaSetDevice), so a thread that has
+ *     made no CUDA call of its own can call it.
  */
 #ifndef DENSE_GEMM_TN_H
 #define DENSE_GEMM_TN_H

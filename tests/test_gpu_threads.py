@@ -1,0 +1,92 @@
+"""Calls from several host threads at once, each on its own stream.
+
+The library keeps per-device state (tile-shape caches, the tensor-map cache)
+and per-(device, stream) buffers (split-K and split-reduce partials), guarded
+internally.  Four threads drive every launch mode concurrently -- split
+reduce, split-K tail, m-part units, 256 x 512 tiles, plain tiles -- each on
+its own stream and buffers (ctypes releases the GIL during each call).  +-1
+inputs: every sampled output is the oracle's bits.  A thread that has made
+no CUDA call before its first GEMM gets the device's context from the
+library.  Operands the TMA cannot address in place
+are left out: their row copy shares one workspace per device, which the
+header says concurrent streams must not use at once.
+"""
+import threading
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.gpu_helpers import sample_positions, to_dev_u16
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    (1024, 1024, 8192),     # split-reduce: 32 one-CTA tiles, four k ranges each
+    (2000, 3000, 520),      # 96 pair tiles: a split-K last wave
+    (1024, 1024, 128),      # m-part units
+    (4096, 4096, 1024),     # 256 x 512 pair tiles
+    (3000, 2000, 136),      # plain pair tiles
+]
+THREADS = 4
+ROUNDS = 6
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import dense_gemm_tn_gb300 as g
+    return g
+
+
+def test_concurrent_threads_each_on_its_own_stream():
+    import dense_gemm_tn_gb300 as g
+    host = {}
+    dev = {}
+    for t in range(THREADS):
+        for i, (M, N, K) in enumerate(SHAPES):
+            A = synth.sign_fp16(M * K, 1000 * t + 2 * i + 1)
+            B = synth.sign_fp16(N * K, 1000 * t + 2 * i + 2)
+            host[t, i] = (A, B)
+            dev[t, i] = (to_dev_u16(A), to_dev_u16(B),
+                         torch.full((N, M), 0x7E00, dtype=torch.int16, device="cuda"))
+    torch.cuda.synchronize()
+    errors, records = [], {}
+    streams = [torch.cuda.Stream() for _ in range(THREADS)]   # made here: the workers make no torch call
+
+    def worker(t):
+        try:
+            s = streams[t]
+            for r in range(ROUNDS):
+                for i, (M, N, K) in enumerate(SHAPES):
+                    dA, dB, C = dev[t, i]
+                    rc = g.lib.gemm_f16_tn(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, C.data_ptr(), M,
+                                           s.cuda_stream)
+                    if rc != 0:
+                        errors.append(f"thread {t} shape {i}: status {rc}: {g.last_error()}")
+                        return
+                    records[t, i] = g.last_launch()
+        except Exception as e:          # reported below, on the main thread
+            errors.append(f"thread {t}: {e!r}")
+
+    workers = [threading.Thread(target=worker, args=(t,)) for t in range(THREADS)]
+    for w in workers:
+        w.start()
+    for w in workers:
+        w.join()
+    torch.cuda.synchronize()
+    g.gemm_poll_device_status()
+    assert not errors, errors
+    for t in range(THREADS):
+        for i, (M, N, K) in enumerate(SHAPES):
+            # the launch record is per host thread: set by this thread's own call of this shape
+            assert records[t, i].startswith("gemm_f16_tn:"), (t, i, records[t, i])
+            A, B = host[t, i]
+            got = dev[t, i][2].cpu().numpy().view(np.uint16)
+            mi, ni = sample_positions(M, N, 4000, seed=7 * t + i)
+            c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
+            bad = np.flatnonzero(got[ni, mi] != c)
+            assert bad.size == 0, f"thread {t} shape {(M, N, K)}: {bad.size} sampled outputs differ"
