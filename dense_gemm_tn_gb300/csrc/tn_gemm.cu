@@ -156,6 +156,17 @@ gemm_status_t ensure_workspace(DeviceState &d, size_t bytes)
     return GEMM_OK;
 }
 
+// The key of a stream's buffers.  cudaStreamPerThread is one handle value
+// that names a different stream on every host thread, so it is keyed per
+// thread: small odd-shifted values no stream object has as its address.
+cudaStream_t stream_key(cudaStream_t stream)
+{
+    if (stream != cudaStreamPerThread) return stream;
+    static std::atomic<uint64_t> next_thread{1};
+    thread_local const uint64_t thread_index = next_thread.fetch_add(1);
+    return reinterpret_cast<cudaStream_t>(static_cast<uintptr_t>((thread_index << 8) | 0x2u));
+}
+
 // A per-stream buffer of `map` that starts with `zeroed_bytes` of words
 // cleared when it is (re)allocated, followed by `extra_bytes`; grown on demand.
 // Calls on one stream are ordered, so they may share their stream's buffer.
@@ -164,7 +175,7 @@ gemm_status_t stream_buffer(std::unordered_map<cudaStream_t, DeviceState::Split>
                             size_t *zeroed_out)
 {
     std::lock_guard<std::mutex> lock(g_mutex);
-    DeviceState::Split &w = map[stream];
+    DeviceState::Split &w = map[stream_key(stream)];
     const size_t tb = (zeroed_bytes + 255) & ~size_t(255);
     if (w.ticket_bytes < tb || w.bytes < w.ticket_bytes + extra_bytes) {
         const size_t new_tb = tb > w.ticket_bytes ? tb : w.ticket_bytes;

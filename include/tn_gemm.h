@@ -40,7 +40,8 @@
  *     tile is computed as two halves of its k range whose FP32 partial sums
  *     meet in a library-owned buffer kept per (device, stream), allocated on
  *     first need (about 0.5 MiB per leftover tile).  The sum is taken in a
- *     fixed way, so results do not depend on timing.
+ *     fixed way, so results do not depend on timing.  cudaStreamPerThread
+ *     counts as one stream per host thread.
  *   - CUDA graphs: once a call has run on a stream (the first call may
  *     allocate that stream's buffers and set kernel attributes), later calls
  *     with the same sizes on that stream enqueue kernel launches only and can

@@ -42,7 +42,10 @@ def _lib():
     return g
 
 
-def test_concurrent_threads_each_on_its_own_stream():
+@pytest.mark.parametrize("per_thread_default", [False, True])
+def test_concurrent_threads_each_on_its_own_stream(per_thread_default):
+    """per_thread_default: every thread passes cudaStreamPerThread (one handle
+    value, a different stream on each thread) instead of a stream of its own."""
     import dense_gemm_tn_gb300 as g
     host = {}
     dev = {}
@@ -59,12 +62,11 @@ def test_concurrent_threads_each_on_its_own_stream():
 
     def worker(t):
         try:
-            s = streams[t]
+            handle = 0x2 if per_thread_default else streams[t].cuda_stream
             for r in range(ROUNDS):
                 for i, (M, N, K) in enumerate(SHAPES):
                     dA, dB, C = dev[t, i]
-                    rc = g.lib.gemm_f16_tn(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, C.data_ptr(), M,
-                                           s.cuda_stream)
+                    rc = g.lib.gemm_f16_tn(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, C.data_ptr(), M, handle)
                     if rc != 0:
                         errors.append(f"thread {t} shape {i}: status {rc}: {g.last_error()}")
                         return
@@ -77,7 +79,7 @@ def test_concurrent_threads_each_on_its_own_stream():
         w.start()
     for w in workers:
         w.join()
-    torch.cuda.synchronize()
+    torch.cuda.synchronize()          # (the per-thread default streams synchronise with the device too)
     g.gemm_poll_device_status()
     assert not errors, errors
     for t in range(THREADS):
