@@ -45,8 +45,6 @@ struct DeviceState {
     // per kernel, indexed [kind: f16, e4m3][1: one CTA, 2: CTA pairs, 3: CTA pairs with 256 x 512 tiles]
     bool smem_attr[2][4] = {};
     int max_clusters[2][4] = {};      // co-resident clusters of the kernel's own size (0 = not queried yet)
-    void *workspace = nullptr;
-    size_t workspace_bytes = 0;
     // Split-K partial sums of the last wave, one buffer per stream (calls on
     // one stream are ordered, so they may share it): [tickets | partials].
     struct Split {
@@ -57,6 +55,9 @@ struct DeviceState {
     std::unordered_map<cudaStream_t, Split> split;
     // Per-CTA maxima of the quantiser, one array per stream.
     std::unordered_map<cudaStream_t, Split> quant;
+    // Row copies of operands the TMA cannot address in place, one workspace
+    // per stream, so calls on different streams may copy at the same time.
+    std::unordered_map<cudaStream_t, Split> repack;
     // Softmax statistics: [tickets per tile row | parts], one buffer per stream.
     std::unordered_map<cudaStream_t, Split> stats;
     int quant_blocks[3] = {};         // co-resident quantiser CTAs per SM, by input type (0 = not queried)
@@ -137,24 +138,6 @@ gemm_status_t device_state(DeviceState **out, int *dev_out)
     return GEMM_OK;
 }
 
-gemm_status_t ensure_workspace(DeviceState &d, size_t bytes)
-{
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (d.workspace_bytes >= bytes) return GEMM_OK;
-    if (d.workspace) {
-        cudaFree(d.workspace);   // synchronises the device: earlier users are done
-        d.workspace = nullptr;
-        d.workspace_bytes = 0;
-    }
-    const size_t rounded = (bytes + (size_t(2) << 20) - 1) & ~((size_t(2) << 20) - 1);
-    cudaError_t e = cudaMalloc(&d.workspace, rounded);
-    if (e != cudaSuccess) {
-        d.workspace = nullptr;
-        return fail(GEMM_ERR_CUDA, "cudaMalloc(%zu) for the repack workspace: %s", rounded, cudaGetErrorString(e));
-    }
-    d.workspace_bytes = rounded;
-    return GEMM_OK;
-}
 
 // The key of a stream's buffers.  cudaStreamPerThread is one handle value
 // that names a different stream on every host thread, so it is keyed per
@@ -652,8 +635,11 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         const int64_t ldp = (K + kPad - 1) / kPad * kPad;
         const size_t bytes_a = repack_a ? ((size_t(M) * ldp * esz + 255) & ~size_t(255)) : 0;
         const size_t bytes_b = repack_b ? ((size_t(N) * ldp * esz + 255) & ~size_t(255)) : 0;
-        if ((st = ensure_workspace(*dev, bytes_a + bytes_b)) != GEMM_OK) return st;
-        uint8_t *ws = static_cast<uint8_t *>(dev->workspace);
+        uint8_t *ws = nullptr;
+        size_t zeroed = 0;
+        if ((st = stream_buffer(dev->repack, stream, 0, bytes_a + bytes_b, "the row-copy workspace", &ws, &zeroed)) !=
+            GEMM_OK)
+            return st;
         using T = typename std::conditional<esz == 2, uint16_t, uint8_t>::type;
         tn::RepackJob<T> ja{static_cast<const T *>(A), lda, reinterpret_cast<T *>(ws), ldp, repack_a ? M : 0, K};
         tn::RepackJob<T> jb{static_cast<const T *>(B), ldb, reinterpret_cast<T *>(ws + bytes_a), ldp,
@@ -947,9 +933,9 @@ void gemm_release_workspace(void)
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState &d = g_devices[dev];
-    if (d.workspace) cudaFree(d.workspace);
-    d.workspace = nullptr;
-    d.workspace_bytes = 0;
+    for (auto &kv : d.repack)
+        if (kv.second.ptr) cudaFree(kv.second.ptr);
+    d.repack.clear();
     for (auto &kv : d.split)
         if (kv.second.ptr) cudaFree(kv.second.ptr);
     d.split.clear();

@@ -34,8 +34,8 @@
  *   - C must not overlap A or B (undefined result).
  *   - Operands whose row stride (ld * element size) or base address is not
  *     a multiple of 16 bytes are first copied into a library-owned, lazily
- *     grown device workspace (one per device) with a padded stride.  Calls
- *     that take this path must not run concurrently on different streams.
+ *     grown device workspace with a padded stride, one per (device,
+ *     stream), so calls on different streams may take this path at once.
  *   - When the tiles of a launch end in a partly filled wave, each leftover
  *     tile is computed as two halves of its k range whose FP32 partial sums
  *     meet in a library-owned buffer kept per (device, stream), allocated on

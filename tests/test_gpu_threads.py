@@ -7,9 +7,8 @@ reduce, split-K tail, m-part units, 256 x 512 tiles, plain tiles -- each on
 its own stream and buffers (ctypes releases the GIL during each call).  +-1
 inputs: every sampled output is the oracle's bits.  A thread that has made
 no CUDA call before its first GEMM gets the device's context from the
-library.  Operands the TMA cannot address in place
-are left out: their row copy shares one workspace per device, which the
-header says concurrent streams must not use at once.
+library.  Operands the TMA cannot address in place are copied into each
+stream's own workspace, so those calls run at once too.
 """
 import threading
 
@@ -29,6 +28,7 @@ SHAPES = [
     (1024, 1024, 128),      # m-part units
     (4096, 4096, 1024),     # 256 x 512 pair tiles
     (3000, 2000, 136),      # plain pair tiles
+    (1000, 700, 1001),      # K * 2 bytes not a 16-byte multiple: operands copied into the stream's workspace
 ]
 THREADS = 4
 ROUNDS = 6
