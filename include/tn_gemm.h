@@ -239,9 +239,9 @@ const char *gemm_last_error(void);
  */
 gemm_status_t gemm_poll_device_status(void *stream);
 
-/* Frees the current device's workspaces: the repack copy, the per-stream
- * split-K partial sums, the quantiser's per-stream arrays and the per-stream
- * softmax-statistics buffers (synchronises the device). */
+/* Frees the current device's workspaces, all kept per stream: the row
+ * copies of unaligned operands, the split-K partial sums, the quantiser's
+ * arrays and the softmax-statistics buffers (synchronises the device). */
 void gemm_release_workspace(void);
 
 /*
