@@ -180,19 +180,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
-// The pair load with cluster multicast: the box is written at offset `dst`
-// of every CTA in `cta_mask`, and each destination's bytes are signalled on
-// the barrier at `bar`'s offset in the even CTA of that destination's pair.
-__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                                           int32_t x, int32_t y, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%4, %5}], [%2], %3;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "h"(cta_mask), "r"(x), "r"(y)
-        : "memory");
-}
-
 // 2-D tiled store shared -> global (elements outside the tensor are skipped).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int32_t x, int32_t y)
 {

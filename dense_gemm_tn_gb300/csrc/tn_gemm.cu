@@ -76,7 +76,7 @@ std::atomic<int> g_raster_group{0};     // tile rows per raster group; 0: kGroup
 struct LaunchRecord {
     const char *name = nullptr;     // nullptr: nothing launched yet
     bool quant = false;
-    int G = 0, quad = 0, wide = 0, grid = 0, clusters = 0, slots = 0;
+    int G = 0, wide = 0, grid = 0, clusters = 0, slots = 0;
     int tiles = 0, units = 0, tail_start = 0, tail_mode = 0, split_parts = 0, vec = 0;
     long long qgrid = 0, qunits = 0;
 };
@@ -360,14 +360,12 @@ struct ASource {
     uint32_t box_k, rows;      // rows: A rows per CTA of a whole tile
 };
 
-// Launches the persistent kernel: one CTA (or one CTA pair) per co-resident
-// slot, each walking the tile raster with a stride of the grid.  Pairs are
-// launched as 2-CTA clusters with a preferred cluster size of 4 when `quad`:
-// the hardware then joins two pairs into one cluster wherever four CTAs fit
-// together, and the kernel shares B rows between them.  W: CTA pairs with
-// 256 x 512 tiles (never with `quad`, the softmax statistics or a split K).
+// Launches the persistent kernel: one CTA (or one CTA pair, a 2-CTA cluster)
+// per co-resident slot, each walking the tile raster with a stride of the
+// grid.  W: CTA pairs with 256 x 512 tiles (never with the softmax statistics
+// or a split K).
 template <class Kind, int G, bool W = false>
-gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, bool quad, bool allow_alloc,
+gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, bool allow_alloc,
                      const ASource &asrc, cudaStream_t stream)
 {
     static_assert(!W || G == 2, "256 x 512 tiles are CTA-pair tiles");
@@ -376,7 +374,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     const int ki = Kind::kF8 ? 1 : 0;
     const int ks = W ? 3 : G;          // kernel index of the per-device caches
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[3];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = G;
     attr[0].val.clusterDim.y = 1;
@@ -411,7 +409,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     // every tile is cut into S ranges of its k blocks (as many as the slots
     // allow, at most 8, each at least 16 k blocks), the units store FP32
     // partials, and a reduce kernel sums them in order and stores C.
-    const int cap = quad && G == 2 && slots >= 2 ? (slots & ~1) : slots;
+    const int cap = slots;
     const bool stats = (prm.flags & tn::kFlagStats) != 0;
     int reduce_parts = 1;
     if (allow_alloc && !stats && 2 * prm.num_tiles <= cap && prm.num_kb >= 32) {
@@ -428,24 +426,12 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     if (!W && reduce_parts == 1 && 2 * prm.num_tiles <= cap)
         m_parts = tn::kMaxMParts * prm.num_tiles <= cap ? tn::kMaxMParts : 2;
     const int units0 = prm.num_tiles * reduce_parts * m_parts;
-    int clusters = units0 < slots ? units0 : slots;
-    if (quad && G == 2) {
-        clusters = (clusters + 1) & ~1;      // whole groups of four CTAs; an odd pair is a phantom
-        if (clusters > slots) clusters = slots & ~1;
-        if (clusters < 2) quad = false;
-    }
+    const int clusters = units0 < slots ? units0 : slots;
     // A programmatic dependent of the previous kernel on the stream: the
     // kernel waits for it (griddepcontrol.wait) before touching memory.
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.numAttrs = 2;
-    if (quad && G == 2) {
-        attr[2].id = cudaLaunchAttributePreferredClusterDimension;
-        attr[2].val.preferredClusterDim.x = 2 * G;
-        attr[2].val.preferredClusterDim.y = 1;
-        attr[2].val.preferredClusterDim.z = 1;
-        cfg.numAttrs = 3;
-    }
     cfg.gridDim = dim3(G * clusters, 1, 1);
     // A last wave that fills at most half of the slots is run as twice as
     // many half-length units, so every slot finishes at about the same time:
@@ -504,7 +490,6 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     t_rec.name = name;
     t_rec.quant = false;
     t_rec.G = G;
-    t_rec.quad = quad && G == 2;
     t_rec.wide = W ? 1 : 0;
     t_rec.grid = G * clusters;
     t_rec.clusters = clusters;
@@ -580,12 +565,7 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     }
 
     // Tile shape.  One CTA per 128 x 256 tile when N <= 128 (a pair's second
-    // half would idle); else a CTA pair per 256 x 256 tile.  Pairs can also be
-    // launched so that the hardware joins two of them into a 4-CTA cluster
-    // sharing B rows (gemm_debug_force_cta_group(4)); with 256-byte K stages
-    // that loses on every shape measured on GB300 (3000x12288x4096: -3.5 %,
-    // the shape where it used to win), so the library does not choose it.
-    // A problem of at most half a wave of pair tiles runs on single CTAs: it
+    // half would idle); else a CTA pair per 256 x 256 tile.  A problem of at most half a wave of pair tiles runs on single CTAs: it
     // is latency-bound, and a CTA without a partner skips the cluster
     // barriers (measured on GB300: 1024 x 1024 x 128 5.8 -> 4.3 us per
     // kernel, 512^3 9.1 -> 6.0 us).
@@ -593,7 +573,6 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     if (ctas == 2 && 2 * (((M + 255) / 256) * ((N + 255) / 256)) <= dev->sms / 2) ctas = 1;
     if (const int forced = g_force_cta_group.load()) ctas = forced;
     const int cta_group = ctas >= 2 ? 2 : 1;
-    const bool quad = ctas == 4 && !stats;
     const int64_t tiles_n = (N + 128 * cta_group - 1) / (128 * cta_group);
     // 256 x 512 pair tiles (two N = 256 halves that share the n-side rows) move
     // a quarter fewer bytes out of L2 per MMA.  Under the power cap that buys a
@@ -602,7 +581,7 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     // only be cut into m halves, and their accumulator is not double-buffered.
     // They are used where an estimate of the launch's length says so.
     bool wide = false;
-    if (cta_group == 2 && !quad && !stats) {
+    if (cta_group == 2 && !stats) {
         const int force = g_force_wide.load();
         const int64_t slots = dev->sms / 2;
         const int64_t tiles256 = (M + tn::kTileM - 1) / tn::kTileM * tiles_n;
@@ -667,9 +646,6 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         return st;
     if ((st = encode_2d(&prm.tmap_b, in_type, b_use, kb, N, ldb_use * esz, box_k, 128, "B")) != GEMM_OK)
         return st;
-    if (quad &&    // the B rows each CTA of a 4-CTA cluster loads and shares
-        (st = encode_2d(&prm.tmap_b_slice, in_type, b_use, kb, N, ldb_use * esz, box_k, 64, "B slice")) != GEMM_OK)
-        return st;
     // TMA stores cover rows m < M rounded down to 8 (16 bytes); the kernel
     // writes the ragged rest, or all of C when C's base or stride is unaligned.
     const int64_t m_tma = M & ~int64_t(7);
@@ -691,7 +667,7 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     prm.num_kb = static_cast<int32_t>((K * esz + stage_k - 1) / stage_k);   // k blocks = stages per tile
     {
         const int rg = g_raster_group.load();
-        prm.group = rg > 0 ? rg : kGroupM;   // even, so raster ids 2j, 2j+1 are neighbouring m tiles of one n tile
+        prm.group = rg > 0 ? rg : kGroupM;
     }
     prm.scale = scale;
     prm.scale_a_ptr = dscale_a;
@@ -716,9 +692,9 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
 
     const ASource asrc{in_type, a_use, static_cast<uint64_t>(ka), static_cast<uint64_t>(M),
                        static_cast<uint64_t>(lda_use * esz), box_k, rows_a};
-    if (wide) return launch<Kind, 2, true>(name, prm, *dev, false, allow_alloc, asrc, stream);
-    if (cta_group == 2) return launch<Kind, 2>(name, prm, *dev, quad, allow_alloc, asrc, stream);
-    return launch<Kind, 1>(name, prm, *dev, false, allow_alloc, asrc, stream);
+    if (wide) return launch<Kind, 2, true>(name, prm, *dev, allow_alloc, asrc, stream);
+    if (cta_group == 2) return launch<Kind, 2>(name, prm, *dev, allow_alloc, asrc, stream);
+    return launch<Kind, 1>(name, prm, *dev, allow_alloc, asrc, stream);
 }
 
 // Per-tensor E4M3 quantisation (quant_e4m3_kernel.cuh): the maximum-finding
@@ -962,7 +938,7 @@ void gemm_debug_inject_stall(int mode) { g_inject_stall.store(mode >= 0 && mode 
 
 int gemm_debug_force_cta_group(int group)
 {
-    if (group != 0 && group != 1 && group != 2 && group != 4) return -1;
+    if (group != 0 && group != 1 && group != 2) return -1;
     g_force_cta_group.store(group);
     return 0;
 }
@@ -991,9 +967,9 @@ const char *gemm_debug_last_launch(void)
                  r.vec);
     else
         snprintf(t_last_launch, sizeof(t_last_launch),
-                 "%s: ctas_per_cluster=%d%s wide=%d grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d "
+                 "%s: ctas_per_cluster=%d wide=%d grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d "
                  "tail_mode=%d split_parts=%d",
-                 r.name, r.G, r.quad ? " (preferred 4)" : "", r.wide, r.grid, r.clusters, r.slots, r.tiles, r.units,
+                 r.name, r.G, r.wide, r.grid, r.clusters, r.slots, r.tiles, r.units,
                  r.tail_start, r.tail_mode, r.split_parts);
     return t_last_launch;
 }
@@ -1002,7 +978,7 @@ const char *gemm_build_info(void)
 {
     static char info[512];
     snprintf(info, sizeof(info),
-             "dense_gemm_tn sm_103a: CTA-pair tile 256x256 in clusters of 2 or 4 (B multicast), %d stages of %d B "
+             "dense_gemm_tn sm_103a: CTA-pair tile 256x256 in 2-CTA clusters, %d stages of %d B "
              "of K, %d B smem; CTA-pair tile 256x512, %d stages of %d B of K, %d B smem; 1-CTA tile 128x256, "
              "%d stages of %d B of K, %d B smem; TMEM %u cols; raster group %d",
              tn::TileCfg<2>::kStages, tn::TileCfg<2>::kStageKBytes, tn::TileCfg<2>::kSmemBytes,

@@ -62,16 +62,11 @@ constexpr uint32_t kAccCols = kTileM;
 constexpr uint32_t kTmemCols = 2 * kAccCols;  // double-buffered accumulator = all 512 columns
 
 // kGroup = 1: one CTA computes a 128 (n) x 256 (m) tile with M128 MMAs.
-// kGroup = 2: a CTA pair computes a 256 (n) x 256 (m) tile with M256 MMAs
-// issued by the pair's even CTA; each CTA holds 128 rows of each operand tile
-// per stage and the accumulator rows of its own 128 columns n.  Pairs are
-// launched with a cluster size of 2 and a preferred size of 4: where the
-// hardware can place four CTAs together, the cluster's two pairs work on
-// neighbouring m tiles of the same n tile and share their B rows -- each CTA
-// loads half of its 128 B rows and multicasts them to its counterpart in the
-// other pair, so 24 instead of 32 KiB leave L2 per CTA and stage.  Where it
-// cannot (8 of a GB300's 152 SMs), the pair works alone.  The kernel reads its
-// cluster size at run time.
+// kGroup = 2: a CTA pair (a cluster of two CTAs) computes a 256 (n) x 256 (m)
+// tile with M256 MMAs issued by the pair's even CTA; each CTA holds 128 rows
+// of each operand tile per stage and the accumulator rows of its own 128
+// columns n.  Every CTA loads its own operand rows from global memory; no
+// load is shared between CTAs.
 //
 // A stage holds kAtoms consecutive 128-byte K atoms of each operand (a pair:
 // 256 bytes of K, 8 MMAs per stage), each atom its own 128B-swizzled block:
@@ -93,12 +88,11 @@ constexpr uint32_t kTmemCols = 2 * kAccCols;  // double-buffered accumulator = a
 template <int kGroup, bool kWide = false>
 struct TileCfg {
     static_assert(!kWide || kGroup == 2, "256 x 512 tiles are CTA-pair tiles");
-    static constexpr int kMaxCtas = 2 * kGroup;            // CTAs per cluster at most (2 pairs)
+    static constexpr int kCtas = kGroup;                   // CTAs per cluster
     static constexpr int kTileN = 128 * kGroup;            // C columns n per pair tile = MMA M
     static constexpr int kTileMRows = kWide ? 2 * kTileM : kTileM;   // C rows m per tile
     static constexpr int kHalves = kWide ? 2 : 1;           // MMA N = 256 halves per tile
     static constexpr int kRowsB = 128;                      // B rows (columns n) per CTA and stage
-    static constexpr int kSliceB = kRowsB / 2;              // B rows each CTA loads when a cluster shares
     static constexpr int kRowsA = kTileMRows / kGroup;      // A rows (m) per CTA and stage
     static constexpr int kAtoms = kGroup == 2 && !kWide ? 2 : 1;   // 128-byte K atoms per stage
     static constexpr int kStageKBytes = kAtoms * kBlockKBytes;
@@ -106,9 +100,7 @@ struct TileCfg {
     static constexpr int kHalfABytes = kTileM / kGroup * kBlockKBytes;   // one half's A rows of one atom
     static constexpr int kAtomBBytes = kRowsB * kBlockKBytes;
     static constexpr int kAtomABytes = kRowsA * kBlockKBytes;
-    static constexpr int kSliceAtomBytes = kSliceB * kBlockKBytes;
     static constexpr int kTileBBytes = kAtoms * kAtomBBytes;
-    static constexpr int kSliceBBytes = kAtoms * kSliceAtomBytes;
     static constexpr int kTileABytes = kAtoms * kAtomABytes;
     static constexpr int kStageBytes = kTileBBytes + kTileABytes;
     static constexpr int kSmemRing = kStages * kStageBytes;
@@ -156,7 +148,6 @@ struct KernelParams {
     CUtensorMap tmap_b;      // B: dims {K', N}, box {kBlockKBytes / esz, 128}, 128B swizzle
     CUtensorMap tmap_c;      // C: dims {m_tma, N}, box {kEpiBoxM, kEpiBoxN}, 128B swizzle
     CUtensorMap tmap_a_part; // kTailMParts: A with box {kBlockKBytes / esz, kRowsA / split_parts}
-    CUtensorMap tmap_b_slice; // B with box {kBlockKBytes / esz, 64} (shared B rows of a 4-CTA cluster)
     void *c_ptr;             // C base (direct stores)
     int64_t ldc;
     int32_t M, N, K;
@@ -197,9 +188,7 @@ struct KernelParams {
 // walk down the region's rows for one tile column (n), then the next column.
 // The last region is short when tiles_m % group != 0.  This is the GROUP_M
 // mapping of hello-gpu ch.11 section 11.3.4 and the grouped block order of
-// the ROCm blog's Step 6.  With an even group, ids 2j and 2j+1 fall on
-// neighbouring m tiles of one n tile, which is what a 4-CTA cluster's two
-// pairs share.
+// the ROCm blog's Step 6.
 //
 // The arithmetic is 32-bit (a 64-bit division is a long instruction sequence
 // on the path to every unit's first load): grids have fewer than 2^31 tiles.
@@ -256,9 +245,8 @@ __device__ __forceinline__ Unit unit_of(int64_t u, const KernelParams &p)
 // The units a work slot walks.  Slot s takes units s, s + nslots, ... of the
 // whole tiles; if tiles were cut, slots s < split_parts * (tiles cut) first
 // take unit tail_start + s, so its combine (split-K) overlaps the
-// slot's later tiles instead of ending the launch.  Slots come in even-aligned
-// pairs that either both have a split unit or both do not.  (kSplitReduce
-// launches at most one unit per slot: tail_start = 0, num_units <= slots.)
+// slot's later tiles instead of ending the launch.  (kSplitReduce launches at
+// most one unit per slot: tail_start = 0, num_units <= slots.)
 __device__ __forceinline__ bool slot_has_tail(int64_t slot, const KernelParams &p)
 {
     return p.tail_mode != kTailNone && slot < p.num_units - p.tail_start;
@@ -359,19 +347,19 @@ struct KindE4M3 {
 // Run by the even CTA of each pair once its own producer issues no more, so
 // that no load feeding its loaded[] barriers is still in flight when the
 // cluster leaves.  Loads go round the stages in order, and a stage can only
-// be refilled after every pair finished reading its previous fill (which
-// needed all of that fill's bytes), so per stage the producers of the cluster
-// are at most one fill apart.  For the last fill of each stage this CTA adds
+// be refilled after the pair's MMAs finished reading its previous fill (which
+// needed all of that fill's bytes), so per stage the producers of the two
+// CTAs are at most one fill apart.  For the last fill of each stage this CTA adds
 // up the bytes really sent to it by the producers that issued that fill; if
 // it armed the fill itself it cancels the bytes that will not come
 // (mbarrier.complete_tx), otherwise it arms the fill for the bytes that will
 // (arrive.expect_tx).  Then it waits for the phase.  On the normal path every
 // producer issued every fill and each wait returns at once.
-template <int kStages, int kAtoms, int kMaxCtas, class LoadedBar, class Contribution>
+template <int kStages, int kAtoms, int kCtas, class LoadedBar, class Contribution>
 __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar loaded_bar, Contribution contribution,
                                                     uint32_t n_own, uint32_t count_addr, uint32_t done_addr)
 {
-    uint32_t counts[kMaxCtas];
+    uint32_t counts[kCtas];
     const uint64_t t0 = ptx::globaltimer();
     for (uint32_t q = 0; q < w.ctas; ++q) {
         if (q == w.rank) {
@@ -390,7 +378,7 @@ __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar l
     }
     for (int s = 0; s < kStages; ++s) {
         uint32_t lo = 0xffffffffu, hi = 0;
-        uint32_t passes[kMaxCtas];
+        uint32_t passes[kCtas];
         for (uint32_t q = 0; q < w.ctas; ++q) {
             passes[q] = counts[q] / kStages + (static_cast<uint32_t>(s) < counts[q] % kStages ? 1u : 0u);
             lo = passes[q] < lo ? passes[q] : lo;
@@ -527,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     constexpr int kAtoms = Cfg::kAtoms;
     constexpr int kLoadedBars = kStages * kAtoms;
     auto loaded_bar = [&](int s, int t) { return bar0 + 8u * (s * kAtoms + t); };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (kLoadedBars + s); };      // every pair done reading
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kLoadedBars + s); };      // the MMAs have read the stage
     auto accfull_bar = [&](int b) { return bar0 + 8u * (kLoadedBars + kStages + b); };
     auto accempty_bar = [&](int b) { return bar0 + 8u * (kLoadedBars + kStages + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (kLoadedBars + kStages + 4);
@@ -535,21 +523,19 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t ctas = kGroup == 2 ? ptx::cluster_nctarank() : 1u;   // 2 or 4 for pairs
+    constexpr uint32_t ctas = Cfg::kCtas;
     const uint32_t rank = kGroup == 2 ? ptx::cluster_ctarank() : 0u;
-    const uint32_t pos = rank % kGroup;            // position within the pair
-    const uint32_t pair = rank / kGroup;           // pair within the cluster
-    const uint32_t pairs = ctas / kGroup;          // pairs in this cluster (1 or 2)
-    const uint32_t lead = pair * kGroup;           // rank of this pair's even CTA
-    // One work slot per pair (per CTA for kGroup = 1); the pairs of a cluster
-    // hold consecutive slots, and each walks units slot, slot + nslots, ...
+    const uint32_t pos = rank;                     // position within the pair
+    constexpr uint32_t lead = 0;                   // rank of the pair's even CTA
+    // One work slot per pair (per CTA for kGroup = 1), walking units slot,
+    // slot + nslots, ...
     const int64_t nslots = gridDim.x / kGroup;
-    const int64_t slot0 = (blockIdx.x - rank) / kGroup;  // slot of the cluster's first pair
+    const int64_t slot0 = blockIdx.x / kGroup;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             for (int t = 0; t < kAtoms; ++t) ptx::mbar_init(loaded_bar(s, t), 1);
-            ptx::mbar_init(empty_bar(s), pairs);
+            ptx::mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accfull_bar(b), 1);
@@ -588,21 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     const Waiter w{abort_flag, abort_addr, rank, ctas, p.wait_limit_ns};
 
-    // Iteration `it` of this cluster: the units of its pairs, and whether the
-    // two pairs share B rows (both units exist and lie on the same n tile).
-    // A phantom unit takes its partner's k-block count, so both pairs of a
-    // cluster issue the same number of fills (they share stage barriers).
-    auto cluster_units = [&](int64_t it, Unit &mine, bool &shared) {
-        mine = unit_of(slot_unit(slot0 + pair, it, nslots, p), p);
-        shared = false;
-        if (pairs == 2) {
-            const Unit e = pair == 0 ? mine : unit_of(slot_unit(slot0, it, nslots, p), p);
-            const Unit o = pair == 1 ? mine : unit_of(slot_unit(slot0 + 1, it, nslots, p), p);
-            if (mine.phantom) mine.nkb = e.nkb;
-            shared = !e.phantom && !o.phantom && e.tn == o.tn && e.khalf < 0 && e.kpart < 0;
-        }
-    };
-    // Steps of this cluster: those of its first slot (the second never has more).
+    // The unit of step `it` of this CTA's slot (both CTAs of a pair run the same one).
+    auto slot_unit_at = [&](int64_t it) { return unit_of(slot_unit(slot0, it, nslots, p), p); };
     const int64_t iters = slot_iters(slot0, nslots, p);
     // m-part units cover a half or a quarter of the tile's m range
     const bool quarter_m = p.m_part_rows == kTileM / 4;
@@ -626,9 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             const uint32_t stall = rank == 0 ? kFlagStallProducer0 : (rank == 1 ? kFlagStallProducer1 : 0u);
             if (p.flags & stall) ok = w.wait(never_bar, 0u, kSiteStall);
             for (int64_t it = 0; ok && it < iters; ++it) {
-                Unit un;
-                bool shared;
-                cluster_units(it, un, shared);
+                const Unit un = slot_unit_at(it);
                 const bool cut_m = un.mpart >= 0;
                 // A rows of this CTA: one box per stage, or (a whole wide tile) one per half,
                 // the second kTileM rows further on.  A wide tile's A map has boxes of one
@@ -642,8 +613,6 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                                               : static_cast<int32_t>(un.tm * Cfg::kTileMRows +
                                                                      (cut_m ? un.mpart * p.m_part_rows : 0) + pos * rows_a);
                 const int32_t nb = un.phantom ? p.N : static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB);
-                uint16_t mcast = 0;
-                for (uint32_t q = 0; q < pairs; ++q) mcast |= static_cast<uint16_t>(1u << (q * kGroup + pos));
                 for (int kb = un.kb0; kb < un.kb0 + un.nkb; ++kb) {
                     if (!w.wait(empty_bar(stage), phase ^ 1u, kSiteEmpty)) {
                         ok = false;
@@ -657,12 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                             if (pos == 0) ptx::mbar_arrive_expect_tx(loaded_bar(stage, t), 2 * fill / kAtoms);
                             const uint32_t lb = ptx::mapa_shared(loaded_bar(stage, t), lead);
                             const int32_t k0 = (kb * Cfg::kAtoms + t) * kBlockKElems;
-                            const uint32_t sb = s_b + t * Cfg::kAtomBBytes;
-                            if (shared)   // this CTA's half of the B rows, into itself and its counterpart
-                                ptx::tma_load_2d_pair_multicast(sb + pair * Cfg::kSliceAtomBytes, &p.tmap_b_slice, lb,
-                                                                k0, nb + pair * Cfg::kSliceB, mcast);
-                            else
-                                ptx::tma_load_2d_pair(sb, &p.tmap_b, lb, k0, nb);
+                            ptx::tma_load_2d_pair(s_b + t * Cfg::kAtomBBytes, &p.tmap_b, lb, k0, nb);
                             ptx::tma_load_2d_pair(s_a + t * Cfg::kAtomABytes, map_a, lb, k0, m0);
                             if (two_halves)
                                 ptx::tma_load_2d_pair(s_a + t * Cfg::kAtomABytes + Cfg::kHalfABytes, map_a, lb, k0,
@@ -695,26 +659,19 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 // publish the final count (release: the count store is ordered before it)
                 ptx::st_release_cluster_u32(ptx::mapa_shared(done_addr, rank), 1u);
                 if (pos == 0) {
-                    // bytes producer q sent to this leader for fill number i
-                    auto contribution = [&](uint32_t q, uint32_t i) -> uint32_t {
-                        Unit un;
-                        bool shared;
+                    // bytes producer q sent to this leader for fill number i (both
+                    // CTAs of the pair run the same unit, so the same bytes)
+                    auto contribution = [&](uint32_t, uint32_t i) -> uint32_t {
                         // a split first step issues kb_part fills, every other step num_kb
                         const uint32_t first =
                             ((p.tail_mode == kTailSplitK || p.tail_mode == kSplitReduce) && slot_has_tail(slot0, p))
                                 ? static_cast<uint32_t>(p.kb_part)
                                 : static_cast<uint32_t>(p.num_kb);
                         const int64_t it = i < first ? 0 : 1 + static_cast<int64_t>((i - first) / p.num_kb);
-                        cluster_units(it, un, shared);
-                        // every CTA of the cluster ran step it: the units differ by pair only
-                        const Unit uq =
-                            q / kGroup == pair ? un : unit_of(slot_unit(slot0 + q / kGroup, it, nslots, p), p);
-                        if (q / kGroup == pair)
-                            return a_bytes(uq) + (shared ? Cfg::kSliceBBytes : Cfg::kTileBBytes);
-                        return shared ? Cfg::kSliceBBytes : 0u;
+                        return a_bytes(slot_unit_at(it)) + Cfg::kTileBBytes;
                     };
-                    drain_cluster_loads<kStages, kAtoms, Cfg::kMaxCtas>(w, loaded_bar, contribution, n_issued, count_addr,
-                                                                done_addr);
+                    drain_cluster_loads<kStages, kAtoms, Cfg::kCtas>(w, loaded_bar, contribution, n_issued, count_addr,
+                                                                     done_addr);
                 }
             } else {
                 // Let every issued load land before the CTA can exit.
@@ -733,8 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued_any = false;
-            const uint16_t all_mask = static_cast<uint16_t>((1u << ctas) - 1u);
-            const uint16_t pair_mask = static_cast<uint16_t>(((1u << kGroup) - 1u) << lead);
+            constexpr uint16_t all_mask = static_cast<uint16_t>((1u << ctas) - 1u);   // both CTAs of a pair
+            constexpr uint16_t pair_mask = all_mask;
             // m-part units: MMA N = m_part_rows
             constexpr uint32_t kIdescHalf = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 2, Kind::kFmt, Kind::kFmt);
             constexpr uint32_t kIdescQuarter = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 4, Kind::kFmt, Kind::kFmt);
@@ -766,9 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                                                    (kk | j) != 0 ? 1u : 0u);
                 };
                 for (int64_t it = 0; ok && it < iters; ++it) {
-                    Unit un;
-                    bool shared;
-                    cluster_units(it, un, shared);
+                    const Unit un = slot_unit_at(it);
                     const bool two = un.mpart < 0;
                     if (!w.wait(accempty_bar(0), acc_phase ^ 1u, kSiteAccEmpty)) break;
                     bool h1 = false;
@@ -831,9 +786,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 }
             } else
             for (int64_t it = 0; ok && it < iters; ++it) {
-                Unit un;
-                bool shared;
-                cluster_units(it, un, shared);
+                const Unit un = slot_unit_at(it);
                 const uint32_t idesc = un.mpart >= 0 ? idesc_part : kIdesc;
                 if (!w.wait(accempty_bar(acc), acc_phase ^ 1u, kSiteAccEmpty)) break;
                 ptx::tc_fence_after_sync();
@@ -981,9 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         };
 
         for (int64_t it = 0; it < iters; ++it) {
-            Unit un;
-            bool shared;
-            cluster_units(it, un, shared);
+            const Unit un = slot_unit_at(it);
             bool ok = w.wait(accfull_bar(acc), acc_phase, kSiteAccFull);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;

@@ -278,10 +278,7 @@ void gemm_debug_inject_stall(int mode);
 /*
  * Test hook: 0 (default) lets the library choose the tile shape per call;
  * 1 forces one CTA per 128 x 256 tile, 2 a CTA pair per 256 x 256 tile in
- * 2-CTA clusters, 4 CTA pairs launched with a preferred cluster size of 4
- * (two pairs sharing B rows through TMA multicast where the hardware places
- * them together).  Returns 0, or -1 for other
- * values.
+ * 2-CTA clusters.  Returns 0, or -1 for other values.
  */
 int gemm_debug_force_cta_group(int group);
 
@@ -289,8 +286,8 @@ int gemm_debug_force_cta_group(int group);
  * Test hook: whether CTA pairs compute 256 x 512 tiles (two N = 256 halves
  * sharing the n-side rows, a 512-column accumulator) instead of 256 x 256.
  * 0 (default): an estimate of the launch's length in tile times decides;
- * 1: always, wherever CTA pairs run without the softmax statistics and
- * without a preferred cluster size of 4; -1: never.  Returns 0, or -1 for
+ * 1: always, wherever CTA pairs run without the softmax statistics; -1:
+ * never.  Returns 0, or -1 for
  * other values.
  */
 int gemm_debug_force_wide_tiles(int mode);

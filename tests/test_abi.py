@@ -126,3 +126,23 @@ def test_raster_group_hook_rejects_odd_and_large():
         with pytest.raises(ValueError):
             g.gemm_debug_set_raster_group(bad)
     g.gemm_debug_set_raster_group(0)
+
+
+def test_cta_group_hook_accepts_one_and_two_only():
+    assert g.lib.gemm_debug_force_cta_group(4) == -1
+    assert g.lib.gemm_debug_force_cta_group(3) == -1
+    for v in (1, 2, 0):
+        assert g.lib.gemm_debug_force_cta_group(v) == 0
+
+
+def test_no_multicast_bulk_loads_in_library_sources():
+    """No TMA copy in the library writes to several CTAs (cluster multicast):
+    every CTA loads its own operand rows.  The one multicast form left is the
+    tcgen05.commit that signals both CTAs of a pair that a stage was read."""
+    csrc = os.path.join(ROOT, "dense_gemm_tn_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        text = open(os.path.join(csrc, name)).read()
+        for line in text.splitlines():
+            if "multicast::cluster" in line:
+                assert "tcgen05.commit" in line, (name, line)
+            assert not re.search(r"cp\.async\.bulk.*multicast", line), (name, line)

@@ -257,7 +257,7 @@ def force_group():
     g.gemm_debug_force_cta_group(0)
 
 
-@pytest.mark.parametrize("cta_group", [1, 2, 4])
+@pytest.mark.parametrize("cta_group", [1, 2])
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (31, 33, 29), (257, 129, 65), (300, 200, 136), (513, 640, 520),
                                    (1000, 300, 1000), (64, 600, 64), (1100, 700, 300)])
 def test_forced_cta_group_pm1_exact(force_group, cta_group, M, N, K):
@@ -267,7 +267,7 @@ def test_forced_cta_group_pm1_exact(force_group, cta_group, M, N, K):
     check_f16_full(M, N, K, A, B, exact=True, what=f"group {cta_group} {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("cta_group", [1, 2, 4])
+@pytest.mark.parametrize("cta_group", [1, 2])
 @pytest.mark.parametrize("M,N,K", [(300, 200, 136), (513, 640, 520), (200, 1030, 4096), (1300, 900, 700)])
 def test_forced_cta_group_gaussian(force_group, cta_group, M, N, K):
     force_group(cta_group)
@@ -292,8 +292,7 @@ def _launch_record():
     (2, 2000, 3000, 200),      # 8 x 12 = 96 pair tiles: one full wave + a short one
     (2, 8192, 8192, 192),      # the headline shape's 1024 tiles (13 waves + 36)
     (1, 2000, 2560, 136),      # 8 x 20 = 160 one-CTA tiles
-    (4, 8192, 8192, 192),      # 512 two-pair units
-    (4, 3000, 12289, 136),     # 6 x 49 = 294 two-pair units, ragged m, n
+    (2, 3000, 12289, 136),     # 12 x 49 = 588 pair tiles, ragged m, n
 ])
 def test_tail_wave_split_into_half_units(force_group, force_wide, cta_group, M, N, K):
     force_group(cta_group)
@@ -314,7 +313,7 @@ def test_tail_wave_split_into_half_units(force_group, force_wide, cta_group, M, 
         c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
         assert np.array_equal(got[ni, mi], c)
     # with the measured 76 pair / 152 single slots of a GB300 these shapes split
-    if clusters in (76, 152) and cta_group != 4:
+    if clusters in (76, 152):
         assert split
 
 
@@ -322,7 +321,6 @@ def test_tail_wave_split_into_half_units(force_group, force_wide, cta_group, M, 
     (2, 8192, 8192, 512),      # 1024 pair tiles: the 36 of the last wave split along K
     (2, 2000, 3000, 520),      # 96 pair tiles, odd k-block count (zero-padded half)
     (1, 2000, 2560, 700),      # one-CTA tiles
-    (4, 2000, 3000, 520),      # preferred 4-CTA clusters
 ])
 def test_split_k_tail_exact_and_deterministic(force_group, force_wide, cta_group, M, N, K):
     force_group(cta_group)
@@ -384,7 +382,6 @@ def test_cuda_graph_capture_and_replay(force_wide, wide):
     (0, 1024, 1024, 8192, 4),    # 32 one-CTA tiles on 152 slots: four k ranges each
     (1, 2000, 700, 4100, 3),     # ragged m, n and k (repacked): 8 x 6 = 48 tiles, three ranges
     (2, 512, 2048, 16384, 4),    # 16 pair tiles of a long K
-    (4, 512, 2048, 16384, 4),    # the same in preferred 4-CTA clusters
 ])
 def test_split_reduce_long_k(force_group, cta_group, M, N, K, parts):
     """Grids of at most half the slots with a long K: every tile is cut into k
@@ -470,7 +467,7 @@ def test_split_reduce_e4m3_host_and_device_scales():
     (0, 900, 300, 77, 4),        # ragged m (the last range of the last tile row lies past M), repacked K
     (0, 1, 1000, 40, 4),         # one row m: three of each tile's four ranges are empty
     (2, 1024, 1024, 128, 4),     # forced CTA pairs: 32 A rows per CTA, MMA N = 64
-    (4, 700, 1000, 136, 4),      # forced 4-CTA clusters (the pairs share B rows)
+    (2, 700, 1000, 136, 4),      # forced CTA pairs, ragged m and n
 ])
 def test_small_grid_m_parts(force_group, cta_group, M, N, K, parts):
     """Grids of at most half the slots with a short K: every tile's m range is
@@ -579,7 +576,7 @@ LAYOUTS = [(136, 136, 304, 0, 0, 0), (141, 137, 303, 0, 0, 0), (136, 136, 300, 1
            (130, 130, 300, 0, 3, 5)]      # lda, ldb, ldc, C offset, A offset, B offset (elements)
 
 
-@pytest.mark.parametrize("cta_group,wide", [(1, -1), (2, -1), (2, 1), (4, -1)])
+@pytest.mark.parametrize("cta_group,wide", [(1, -1), (2, -1), (2, 1)])
 def test_layouts_on_every_tile_shape(force_group, force_wide, cta_group, wide):
     """Padded, odd and unaligned leading dimensions and bases (TMA in place,
     repacked operands, direct C stores) on each tile shape, FP16 and E4M3."""

@@ -13,8 +13,7 @@ from tests.gpu_helpers import GuardedC, check_f16_full, to_dev_u16
 pytestmark = pytest.mark.gpu
 
 # (CTAs per cluster, 256 x 512 pair tiles, stalled thread)
-CASES = [(1, 0, 1), (1, 0, 2), (2, 0, 1), (2, 0, 2), (2, 0, 3), (4, 0, 1), (4, 0, 2), (4, 0, 3),
-         (2, 1, 1), (2, 1, 2), (2, 1, 3)]
+CASES = [(1, 0, 1), (1, 0, 2), (2, 0, 1), (2, 0, 2), (2, 0, 3), (2, 1, 1), (2, 1, 2), (2, 1, 3)]
 
 
 @pytest.mark.parametrize("cta_group,wide,mode", CASES)
