@@ -19,6 +19,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -191,6 +192,101 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(pw)}
 
 
+class NvmlSampler:
+    """SM clock, board power and clock-event reasons of one GPU, read with
+    NVML's read-only queries from a thread about once a millisecond and
+    stamped with the host clock, so that the samples taken inside a timed
+    region can be picked out (the 200 ms nvidia-smi loop misses a region of a
+    few milliseconds).  NVML is the driver's library (libnvidia-ml.so.1),
+    loaded with ctypes; nothing is set."""
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, torch_device, period_s: float = 0.001):
+        import ctypes
+        self.ct = ctypes
+        self.period = period_s
+        self.samples: list[tuple[float, float, float, int]] = []   # (host time, SM MHz, W, reason bits)
+        self.max_mhz = None
+        self.handle = None
+        self._stop = threading.Event()
+        self.thread = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+        except OSError:
+            return
+        self.lib = lib
+        h = ctypes.c_void_p()
+        found = False
+        try:
+            import torch
+            props = torch.cuda.get_device_properties(torch_device)
+            uuid = str(getattr(props, "uuid", "") or "")
+            if uuid:
+                key = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+                found = lib.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(h)) == 0
+            if not found and hasattr(props, "pci_bus_id"):
+                bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+                found = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+        except Exception:
+            found = False
+        if not found:
+            return
+        self.handle = h
+        v = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(v)) == 0:
+            self.max_mhz = float(v.value)
+        self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+
+    @property
+    def ok(self) -> bool:
+        return self.handle is not None
+
+    def _query(self):
+        ct, lib, h = self.ct, self.lib, self.handle
+        clk, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if lib.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ct.byref(clk)) != 0:
+            return None
+        power = float(pw.value) / 1000.0 if lib.nvmlDeviceGetPowerUsage(h, ct.byref(pw)) == 0 else float("nan")
+        bits = int(rs.value) if self._reasons_fn and self._reasons_fn(h, ct.byref(rs)) == 0 else 0
+        return float(clk.value), power, bits
+
+    def _run(self):
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            q = self._query()
+            if q is not None:
+                self.samples.append((t, *q))
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok and self.thread is None:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+
+    def stop(self):
+        if self.thread is not None:
+            self._stop.set()
+            self.thread.join(timeout=2)
+            self.thread = None
+
+    def window(self, t0: float, t1: float) -> dict | None:
+        """Clock record of the samples taken between host times t0 and t1."""
+        inside = [s for s in list(self.samples) if t0 <= s[0] <= t1]
+        if not inside:
+            return None
+        sm = [s[1] for s in inside]
+        pw = [s[2] for s in inside if s[2] == s[2]]
+        reasons = sorted({name for s in inside for bit, name in self.REASON_BITS.items() if s[3] & bit})
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": self.max_mhz or max(sm),
+                "reasons": reasons, "samples": len(inside), "power_w_max": max(pw) if pw else None,
+                "source": "NVML read-only queries every ~1 ms inside the timed region"}
+
+
 # ---------------------------------------------------------------- CPU oracle timing
 def oracle_sample(w: synth.Workload, A, B, sa, sb, target_s: float):
     """Times the oracle on a random sample of the workload's outputs (full K
@@ -306,6 +402,174 @@ def run_reference(args, w: synth.Workload, rank: int) -> None:
 
 
 # ---------------------------------------------------------------- our arm
+BURST_REGION_MS = 1000.0     # a timed region shorter than this runs before the power cap settles
+
+
+def timed_loop(torch, dev, stream, call, sets: int, steps: int, warmup: int, sampler, dist=None):
+    """W untimed calls, then exactly `steps` calls bracketed by a barrier and a
+    device synchronisation on both sides, timed with CUDA events on the
+    launching stream.  Events are recorded only before and after the loop: an
+    event between two launches would end the overlap of a kernel's setup
+    with the previous kernel's tail, which back-to-back calls otherwise get.
+    Returns (device ms, clock record of the timed region, any call failed)."""
+    for i in range(warmup):
+        call(i % sets)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    failed = 0
+    for i in range(steps):
+        failed |= call(i % sets)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.perf_counter()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1), sampler.window(t0, t1), failed
+
+
+def roofline_of(w: synth.Workload, kernel_ms: float, region_ms: float, peaks: dict, clk: dict | None,
+                sms: int, stats: bool) -> dict:
+    """The dominant kernel's roofline.  Below the ridge point (tensor peak over
+    HBM bytes/s) the bound is HBM and `achieved` is the algorithmic bytes per
+    launch (operands read once, C and any row statistics written once) over
+    the launch's time; above it, 2MNK per launch over that time against the
+    tensor peak.  The tensor peak is the measured cuBLAS bf16 rate (x2 for
+    E4M3, the nominal fp8 / bf16 ratio): its burst figure for a timed region
+    under a second (the GPU has not reached its power cap yet), its sustained
+    figure for a longer one; both fractions are given."""
+    M, N, K = w.M, w.N, w.K
+    is_f8 = w.dtype == "e4m3" or w.values == "bf16"
+    flop = 2.0 * M * N * K
+    ratio = 2.0 if is_f8 else 1.0
+    burst, sustained = peaks["bf16_burst"] * ratio, peaks["bf16_sustained"] * ratio
+    kind = "burst" if region_ms < BURST_REGION_MS else "sustained"
+    peak = burst if kind == "burst" else sustained
+    achieved = flop / (kernel_ms * 1e-3) / 1e12
+    alg_bytes = (M * K + N * K) * (1 if is_f8 else 2) + 2 * M * N + (8 * M if stats else 0)
+    ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    intensity = flop / alg_bytes
+    rf = {"intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
+          "kernel": KERNEL_NAME["e4m3" if is_f8 else "f16"], "kernel_ms": kernel_ms,
+          "traffic": measured_traffic(w.name), "algorithmic_bytes": alg_bytes}
+    dtype_note = " x2 (nominal fp8/bf16)" if is_f8 else " (fp16 = bf16 rate)"
+    if intensity < ridge:
+        gbs = alg_bytes / (kernel_ms * 1e-3) / 1e9
+        rf.update({"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                   "frac": gbs / peaks["hbm_gbs"], "peak_src": f"{peaks['src']} copy bandwidth",
+                   "tensor_frac": achieved / peak})
+    else:
+        rf.update({"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                   "frac": achieved / peak, "peak_kind": kind,
+                   "peak_src": f"{peaks['src']} bf16 {kind}{dtype_note}; {kind} because the timed region "
+                               f"lasted {region_ms:.0f} ms ({'<' if kind == 'burst' else '>='} "
+                               f"{BURST_REGION_MS:.0f} ms)",
+                   "frac_burst": achieved / burst, "frac_sustained": achieved / sustained,
+                   "peak_burst": burst, "peak_sustained": sustained})
+    # per-clock view: cycles of the launch at the sampled SM clock against the
+    # cycles its MMAs take at the tensor peak (8192 dense FP16 FLOP per clock
+    # per SM, twice that for E4M3)
+    mma_cycles = flop / ((16384.0 if is_f8 else 8192.0) * sms)
+    rf["tensor_cycles_per_launch"] = mma_cycles
+    if clk and clk.get("sm_mhz"):
+        cyc = kernel_ms * 1e-3 * clk["sm_mhz"] * 1e6
+        rf["cycles_per_launch"] = cyc
+        rf["tensor_frac_per_clock"] = mma_cycles / cyc
+        rf["sm_mhz_in_region"] = clk["sm_mhz"]
+    return rf
+
+
+def clocks_record(nvml_clk: dict | None, smi: dict | None) -> dict | None:
+    """The timed region's clocks: the NVML samples taken inside it; without
+    NVML, the nvidia-smi loop (which may have no sample inside a short region)."""
+    if nvml_clk:
+        out = dict(nvml_clk)
+        if smi:
+            out["nvidia_smi"] = smi
+        return out
+    return smi
+
+
+def cpu_line(w: synth.Workload, host0, seconds: float, stats: bool) -> dict:
+    if w.values == "bf16":
+        import oracle
+        t0 = time.perf_counter()
+        qa_ref, sa_ref = oracle.quantize_e4m3(host0[0], "bf16", w.M, w.K)
+        qb_ref, sb_ref = oracle.quantize_e4m3(host0[1], "bf16", w.N, w.K)
+        t_q = time.perf_counter() - t0
+        tf, cores, desc = oracle_sample(w, qa_ref, qb_ref, sa_ref, sb_ref, target_s=seconds)
+        desc += f"; the oracle's quantisation of both operands took a further {t_q:.1f} s"
+    elif stats:
+        import oracle
+        t0 = time.perf_counter()
+        oracle.gemm_f16_tn_softmax_stats(w.M, w.N, w.K, host0[0], w.K, host0[1], w.K, 1.0 / float(np.sqrt(w.K)))
+        dt = time.perf_counter() - t0
+        tf, cores = 2.0 * w.M * w.N * w.K / dt / 1e12, oracle.num_threads()
+        desc = f"the whole {w.name} problem (scores and statistics), {dt:.2f} s"
+    else:
+        tf, cores, desc = oracle_sample(w, *host0, target_s=seconds)
+    return {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+
+
+def device_operands(torch, dev, host, esz: int):
+    dA, dB = [], []
+    for A, B, _, _ in host:
+        if esz == 1:
+            dA.append(torch.from_numpy(A).to(dev))
+            dB.append(torch.from_numpy(B).to(dev))
+        else:
+            dA.append(torch.from_numpy(A.view(np.int16)).to(dev))
+            dB.append(torch.from_numpy(B.view(np.int16)).to(dev))
+    return dA, dB
+
+
+def run_secondary(args, torch, g, dev, stream, sampler, peaks, sms) -> dict:
+    """The FP8 headline shape (e4m3_8192: E4M3 operands with per-tensor
+    scales, bf16 C, 4 rotating sets) with the same steps and warm-up as the
+    main line, and its own clocks, roofline and CPU baseline."""
+    w = synth.WORKLOADS["e4m3_8192"]
+    sets = w.rotating
+    host = host_inputs(w, sets)
+    dA, dB = device_operands(torch, dev, host, 1)
+    C = torch.empty((w.N, w.M), dtype=torch.bfloat16, device=dev)
+    sh = int(stream.cuda_stream)
+    M, N, K = w.M, w.N, w.K
+    pa, pb, pc = [t.data_ptr() for t in dA], [t.data_ptr() for t in dB], C.data_ptr()
+    sa, sb = [h[2] for h in host], [h[3] for h in host]
+    f_f8 = g.lib.gemm_f8e4m3_tn
+
+    def call(j):
+        return f_f8(M, N, K, pa[j], K, pb[j], K, pc, M, sa[j], sb[j], sh)
+
+    if call(0) != 0:
+        raise RuntimeError(f"FP8 GEMM call failed: {g.last_error()}")
+    g.gemm_poll_device_status(sh)
+    total_ms, clk, failed = timed_loop(torch, dev, stream, call, sets, args.steps, args.warmup, sampler)
+    if failed:
+        raise RuntimeError(f"an FP8 GEMM call in the timed loop failed: {g.last_error()}")
+    g.gemm_poll_device_status(sh)
+    kernel_ms = total_ms / args.steps
+    value = 2.0 * M * N * K / (kernel_ms * 1e-3) / 1e12
+    out = {"metric": metric_for(w), "value": value, "unit": "TFLOP/s", "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": kernel_ms, "dtype": "e4m3",
+           "config": {"workload": f"{w.name}: e4m3 TN GEMM M={M} N={N} K={K}, per-tensor scales, bf16 C, "
+                                  f"{sets} rotating input sets",
+                      "l2": l2_note(sets, (M + N) * K)},
+           "pct_of_dense_peak": 100.0 * value / NOMINAL_PEAK["e4m3"],
+           "roofline": roofline_of(w, kernel_ms, total_ms, peaks, clk, sms, False),
+           "clocks": clk, "gpu_launches": args.steps}
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_line(w, host[0], args.cpu_seconds / 2, False)
+    del dA, dB, C
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) -> None:
     import torch
 
@@ -317,21 +581,15 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
     sets = w.rotating if args.sets is None else max(1, args.sets)
     host = host_inputs(w, sets)
     is_f8 = w.dtype == "e4m3"
     pipeline = w.values == "bf16"          # bf16 operands quantised to E4M3 on the device every step
     esz = 2 if (pipeline or not is_f8) else 1   # bytes per input element
-    dA, dB, scales = [], [], []
-    for A, B, sa, sb in host:
-        if esz == 1:
-            dA.append(torch.from_numpy(A).to(dev))
-            dB.append(torch.from_numpy(B).to(dev))
-        else:
-            dA.append(torch.from_numpy(A.view(np.int16)).to(dev))
-            dB.append(torch.from_numpy(B.view(np.int16)).to(dev))
-        scales.append((sa, sb))
+    dA, dB = device_operands(torch, dev, host, esz)
+    scales = [(h[2], h[3]) for h in host]
     C = torch.empty((w.N, w.M), dtype=torch.bfloat16 if is_f8 else torch.float16, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = int(stream.cuda_stream)
@@ -396,48 +654,69 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
         raise RuntimeError(f"GEMM call failed: {rcs}: {g.last_error()}")
     g.gemm_poll_device_status(sh)
 
-    clocks = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
-    clocks.start()
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize(dev)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    # Only the pipeline records events inside the timed region (to time its
-    # quantisations apart from its GEMMs): an event between two launches ends
-    # the overlap of a kernel's setup with the previous kernel's tail, which
-    # back-to-back calls of a small problem otherwise get.
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1 if pipeline else 2)]
-    mid = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if pipeline else None
-    ev[0].record(stream)
+    smi = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    smi.start()
+    sampler = NvmlSampler(dev)
+    sampler.start()
     if pipeline:
+        # The pipeline also records one event between its quantisations and its
+        # GEMM per step, to time them apart.
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        mid = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        t0 = time.perf_counter()
+        ev[0].record(stream)
         for i in range(args.steps):
             step(i, mid[i])
             ev[i + 1].record(stream)
-    else:
-        # one C ABI call per step, its arguments bound beforehand: the loop's own
-        # Python work per step stays well under a microsecond-scale GEMM's time
-        call = one_call()
-        failed = 0
-        for i in range(args.steps):
-            failed |= call(i % sets)
-        ev[-1].record(stream)
-        if failed:
-            raise RuntimeError(f"a GEMM call in the timed loop failed: {g.last_error()}")
-    torch.cuda.synchronize(dev)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize(dev)
-    clk = clocks.stop()
-    g.gemm_poll_device_status(sh)
-    total_ms = ev[0].elapsed_time(ev[-1])
-    if pipeline:
+        torch.cuda.synchronize(dev)
+        t1 = time.perf_counter()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        nvml_clk = sampler.window(t0, t1)
+        total_ms = ev[0].elapsed_time(ev[-1])
         # the GEMM is the dominant kernel; the two quantisations are timed beside it
         kernel_ms = statistics.mean(mid[i].elapsed_time(ev[i + 1]) for i in range(args.steps))
         quant_ms = statistics.mean(ev[i].elapsed_time(mid[i]) for i in range(args.steps))
     else:
+        # one C ABI call per step, its arguments bound beforehand: the loop's own
+        # Python work per step stays well under a microsecond-scale GEMM's time
+        total_ms, nvml_clk, failed = timed_loop(torch, dev, stream, one_call(), sets, args.steps, args.warmup,
+                                                sampler, dist)
+        if failed:
+            raise RuntimeError(f"a GEMM call in the timed loop failed: {g.last_error()}")
         kernel_ms = total_ms / args.steps      # one GEMM per step (after a repack where one is needed)
+    smi_clk = smi.stop()
+    clk = clocks_record(nvml_clk, smi_clk)
+    g.gemm_poll_device_status(sh)
+
+    peaks = load_peaks()
+    flop = 2.0 * M * N * K
+    roofline = roofline_of(w, kernel_ms, total_ms, peaks, clk, sms, stats)
+
+    # ---- sustained: the same calls back to back for about `sustained_s`
+    # seconds, long enough for the GPU to settle at its power cap
+    sustained = None
+    if args.sustained_s > 0 and roofline["bound"] == "tensor" and not pipeline:
+        s_steps = max(args.steps, int(math.ceil(args.sustained_s * 1e3 / max(kernel_ms, 1e-3))))
+        s_ms, s_clk, failed = timed_loop(torch, dev, stream, one_call(), sets, s_steps, 0, sampler, dist)
+        if failed:
+            raise RuntimeError(f"a GEMM call in the sustained loop failed: {g.last_error()}")
+        g.gemm_poll_device_status(sh)
+        s_ms = max_over_ranks([s_ms], dist, dev)[0]
+        s_kernel = s_ms / s_steps
+        s_rf = roofline_of(w, s_kernel, s_ms, peaks, s_clk, sms, stats)
+        sustained = {"steps": s_steps, "seconds": s_ms * 1e-3, "ms_per_step": s_kernel,
+                     "value": replica_tflops(world, flop, s_steps, s_ms), "unit": "TFLOP/s",
+                     "frac": s_rf["frac"], "peak": s_rf["peak"], "peak_kind": s_rf["peak_kind"],
+                     "cycles_per_launch": s_rf.get("cycles_per_launch"),
+                     "tensor_frac_per_clock": s_rf.get("tensor_frac_per_clock"), "clocks": s_clk}
 
     # ---- end to end: pinned host inputs -> device -> GEMM -> pinned host output.
     # Every step copies its own A and B in and its C out; the copies of the
@@ -492,60 +771,25 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     h2d = (M * K + N * K) * esz
     d2h = M * N * 2 + (8 * M if stats else 0)
+    del hA, hB, hC, eA, eB, eC
     total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, dev)
     ms_per_step = total_ms / args.steps
-    flop = 2.0 * M * N * K
     value = replica_tflops(world, flop, args.steps, total_ms)
+
+    # ---- the FP8 headline shape beside the FP16 one (one GPU only)
+    secondary = None
+    if world == 1 and w.name == "sq_8192" and not args.no_secondary:
+        secondary = run_secondary(args, torch, g, dev, stream, sampler, peaks, sms)
+    sampler.stop()
 
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
 
-    peaks = load_peaks()
-    ratio = 2.0 if is_f8 else 1.0      # nominal fp8 / bf16 dense ratio (4.5 / 2.25 PF)
-    peak = peaks["bf16_sustained"] * ratio
-    achieved = flop / (kernel_ms * 1e-3) / 1e12
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        if pipeline:
-            import oracle
-            t0 = time.perf_counter()
-            qa_ref, sa_ref = oracle.quantize_e4m3(host[0][0], "bf16", M, K)
-            qb_ref, sb_ref = oracle.quantize_e4m3(host[0][1], "bf16", N, K)
-            t_q = time.perf_counter() - t0
-            tf, cores, desc = oracle_sample(w, qa_ref, qb_ref, sa_ref, sb_ref, target_s=args.cpu_seconds)
-            desc += f"; the oracle's quantisation of both operands took a further {t_q:.1f} s"
-        elif stats:
-            import oracle
-            t0 = time.perf_counter()
-            oracle.gemm_f16_tn_softmax_stats(M, N, K, host[0][0], K, host[0][1], K, 1.0 / float(np.sqrt(K)))
-            dt = time.perf_counter() - t0
-            tf, cores = 2.0 * M * N * K / dt / 1e12, oracle.num_threads()
-            desc = f"the whole {w.name} problem (scores and statistics), {dt:.2f} s"
-        else:
-            tf, cores, desc = oracle_sample(w, *host[0], target_s=args.cpu_seconds)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
-    # The dominant kernel's roofline: below the ridge point (peak FLOP/s over HBM
-    # bytes/s) the bound is HBM, and the achieved figure is the algorithmic bytes
-    # (operands read once, C and the row statistics written once) per launch
-    # over the launch's time; above it, FLOP/s against the tensor peak.
-    alg_bytes = (M * K + N * K) * (1 if is_f8 or pipeline else 2) + 2 * M * N + (8 * M if stats else 0)
-    ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    intensity = flop / alg_bytes
-    roofline = {"intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
-                "kernel": KERNEL_NAME[w.dtype], "kernel_ms": kernel_ms, "traffic": measured_traffic(w.name),
-                "algorithmic_bytes": alg_bytes}
-    if intensity < ridge:
-        gbs = alg_bytes / (kernel_ms * 1e-3) / 1e9
-        roofline.update({"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm_gbs"], "peak_src": f"{peaks['src']} copy bandwidth",
-                         "tensor_frac": achieved / peak})
-    else:
-        roofline.update({"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak,
-                         "peak_src": f"{peaks['src']} bf16 sustained" + (" x2 (nominal fp8/bf16)" if is_f8 else
-                                                                          " (fp16 = bf16 rate)")})
+        cpu = cpu_line(w, host[0], args.cpu_seconds, stats)
     line = {
         "metric": metric_for(w), "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -566,6 +810,10 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
         "clocks": clk,
         "gpu_launches": args.steps * launches_per_step,
     }
+    if sustained is not None:
+        line["sustained"] = sustained
+    if secondary is not None:
+        line["secondary"] = secondary
     if pipeline:
         # algorithmic bytes: each bf16 input read once, each e4m3 code and scale written once
         qbytes = 2 * (M * K + N * K) + (M * K + N * K) + 8
@@ -588,6 +836,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the FP8 8192^3 measurement that follows the default FP16 one")
+    ap.add_argument("--sustained-s", type=float, default=2.0,
+                    help="seconds of back-to-back calls for the sustained figure (0: skip)")
     ap.add_argument("--sets", type=int, default=None,
                     help="input sets to rotate (default: the workload's; 1 for small profiling runs)")
     args = ap.parse_args()

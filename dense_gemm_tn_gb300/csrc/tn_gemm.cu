@@ -13,6 +13,7 @@
 #include <cstring>
 #include <iterator>
 #include <mutex>
+#include <shared_mutex>
 #include <unordered_map>
 #include <vector>
 
@@ -61,9 +62,17 @@ struct DeviceState {
     // Softmax statistics: [tickets per tile row | parts], one buffer per stream.
     std::unordered_map<cudaStream_t, Split> stats;
     int quant_blocks[3] = {};         // co-resident quantiser CTAs per SM, by input type (0 = not queried)
+    // Buffers replaced by larger ones.  Another host thread may have looked one
+    // up and not yet enqueued the kernel that uses it, so they are freed only
+    // by gemm_release_workspace.
+    std::vector<void *> retired;
 };
 
 std::mutex g_mutex;
+// Held shared by every call from its first workspace lookup through its last
+// launch, and exclusively by gemm_release_workspace: the buffers a call looked
+// up stay allocated until its kernels are enqueued.
+std::shared_mutex g_workspace_lock;
 DeviceState g_devices[kMaxDevices];
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
@@ -151,19 +160,27 @@ cudaStream_t stream_key(cudaStream_t stream)
 }
 
 // A per-stream buffer of `map` that starts with `zeroed_bytes` of words
-// cleared when it is (re)allocated, followed by `extra_bytes`; grown on demand.
-// Calls on one stream are ordered, so they may share their stream's buffer.
-gemm_status_t stream_buffer(std::unordered_map<cudaStream_t, DeviceState::Split> &map, cudaStream_t stream,
-                            size_t zeroed_bytes, size_t extra_bytes, const char *what, uint8_t **base,
-                            size_t *zeroed_out)
+// cleared when it is (re)allocated, followed by `extra_bytes`; grown on demand
+// (to at least twice its size, so that few buffers are ever retired).  Calls
+// on one stream are ordered, so they may share their stream's buffer, also
+// when different host threads issue them.  The caller holds
+// g_workspace_lock (shared).
+gemm_status_t stream_buffer(DeviceState &d, std::unordered_map<cudaStream_t, DeviceState::Split> &map,
+                            cudaStream_t stream, size_t zeroed_bytes, size_t extra_bytes, const char *what,
+                            uint8_t **base, size_t *zeroed_out)
 {
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState::Split &w = map[stream_key(stream)];
     const size_t tb = (zeroed_bytes + 255) & ~size_t(255);
     if (w.ticket_bytes < tb || w.bytes < w.ticket_bytes + extra_bytes) {
         const size_t new_tb = tb > w.ticket_bytes ? tb : w.ticket_bytes;
-        const size_t need = new_tb + extra_bytes;
-        if (w.ptr) cudaFree(w.ptr);      // synchronises the device: earlier users are done
+        size_t need = new_tb + extra_bytes;
+        if (w.ptr) {
+            // Not freed here: a call on another host thread may hold its address
+            // and not have enqueued its kernels yet.
+            d.retired.push_back(w.ptr);
+            if (need < 2 * w.bytes) need = 2 * w.bytes;
+        }
         w.ptr = nullptr;
         w.bytes = w.ticket_bytes = 0;
         cudaError_t e = cudaMalloc(&w.ptr, need);
@@ -194,7 +211,7 @@ gemm_status_t split_workspace(DeviceState &d, cudaStream_t stream, size_t ticket
 {
     uint8_t *base = nullptr;
     size_t zeroed = 0;
-    gemm_status_t st = stream_buffer(d.split, stream, tickets * sizeof(unsigned long long), partial_bytes,
+    gemm_status_t st = stream_buffer(d, d.split, stream, tickets * sizeof(unsigned long long), partial_bytes,
                                      "split-K partials", &base, &zeroed);
     if (st != GEMM_OK) return st;
     *ticket_ptr = reinterpret_cast<unsigned long long *>(base);
@@ -448,7 +465,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
         const size_t partial = size_t(prm.num_tiles) * reduce_parts * G * Cfg::kRowsB * Cfg::kTileMRows * sizeof(float);
         uint8_t *base = nullptr;
         size_t zeroed = 0;
-        gemm_status_t st = stream_buffer(dev.split, stream, 0, partial, "split-K partials", &base, &zeroed);
+        gemm_status_t st = stream_buffer(dev, dev.split, stream, 0, partial, "split-K partials", &base, &zeroed);
         if (st != GEMM_OK) return st;
         prm.tail_mode = tn::kSplitReduce;
         prm.tail_start = 0;
@@ -547,6 +564,8 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         if (reinterpret_cast<uintptr_t>(A) % esz || reinterpret_cast<uintptr_t>(B) % esz)
             return fail(GEMM_ERR_INVALID_ARG, "%s: A or B is not aligned to its element size", name);
     }
+    // buffers looked up below stay allocated until this call's launches are enqueued
+    std::shared_lock<std::shared_mutex> workspace_guard(g_workspace_lock);
     DeviceState *dev = nullptr;
     gemm_status_t st = device_state(&dev, nullptr);
     if (st != GEMM_OK) return st;
@@ -616,8 +635,8 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         const size_t bytes_b = repack_b ? ((size_t(N) * ldp * esz + 255) & ~size_t(255)) : 0;
         uint8_t *ws = nullptr;
         size_t zeroed = 0;
-        if ((st = stream_buffer(dev->repack, stream, 0, bytes_a + bytes_b, "the row-copy workspace", &ws, &zeroed)) !=
-            GEMM_OK)
+        if ((st = stream_buffer(*dev, dev->repack, stream, 0, bytes_a + bytes_b, "the row-copy workspace", &ws,
+                                &zeroed)) != GEMM_OK)
             return st;
         using T = typename std::conditional<esz == 2, uint16_t, uint8_t>::type;
         tn::RepackJob<T> ja{static_cast<const T *>(A), lda, reinterpret_cast<T *>(ws), ldp, repack_a ? M : 0, K};
@@ -682,7 +701,8 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         size_t zeroed = 0;
         // one ticket per tile row and m part
         const size_t tickets = size_t(tiles_m) * tn::kMaxMParts * sizeof(unsigned long long);
-        if ((st = stream_buffer(dev->stats, stream, tickets, parts, "softmax statistics", &base, &zeroed)) != GEMM_OK)
+        if ((st = stream_buffer(*dev, dev->stats, stream, tickets, parts, "softmax statistics", &base, &zeroed)) !=
+            GEMM_OK)
             return st;
         prm.stat_tickets = reinterpret_cast<unsigned long long *>(base);
         prm.stat_parts = reinterpret_cast<float2 *>(base + zeroed);
@@ -723,8 +743,8 @@ gemm_status_t launch_quant(DeviceState &dev, qz::QuantParams &prm, cudaStream_t 
     if (grid < 1) grid = 1;
     uint8_t *slots = nullptr;
     size_t zeroed = 0;
-    gemm_status_t st = stream_buffer(dev.quant, stream, 0, size_t(grid) * sizeof(float), "quantiser slots", &slots,
-                                     &zeroed);
+    gemm_status_t st = stream_buffer(dev, dev.quant, stream, 0, size_t(grid) * sizeof(float), "quantiser slots",
+                                     &slots, &zeroed);
     if (st != GEMM_OK) return st;
     prm.slots = reinterpret_cast<float *>(slots + zeroed);
     t_rec.name = "gemm_quantize_e4m3";
@@ -771,6 +791,7 @@ gemm_status_t run_quant(const void *x, int x_type, int64_t rows, int64_t cols, i
     }
     if (rows > (int64_t(1) << 40) / cmin)
         return fail(GEMM_ERR_UNSUPPORTED, "%s: more than 2^40 elements", name);
+    std::shared_lock<std::shared_mutex> workspace_guard(g_workspace_lock);
     DeviceState *dev = nullptr;
     gemm_status_t st = device_state(&dev, nullptr);
     if (st != GEMM_OK) return st;
@@ -907,8 +928,12 @@ void gemm_release_workspace(void)
 {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return;
+    // waits for calls on other threads to have enqueued their launches
+    std::unique_lock<std::shared_mutex> workspace_guard(g_workspace_lock);
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState &d = g_devices[dev];
+    for (void *p : d.retired) cudaFree(p);
+    d.retired.clear();
     for (auto &kv : d.repack)
         if (kv.second.ptr) cudaFree(kv.second.ptr);
     d.repack.clear();

@@ -409,10 +409,10 @@ __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar l
 }
 
 // ------------------------------------------------------------------ softmax statistics
-// e^x for x <= 0 as 2^(x log2 e), with the ex2 instruction (relative error
-// about 2^-22; results below 2^-126 flush to 0; e^-inf = 0).  Measured on
-// GB300, the ex2 path that keeps subnormals (what expf and __expf compile to
-// without -ftz) made the statistics epilogue 2.6x slower.
+// e^x for x <= 0 as 2^(x log2 e), with the PTX ex2.approx.ftz.f32
+// instruction (the PTX ISA gives its maximum relative error as about 2^-22;
+// results below 2^-126 flush to 0; e^-inf = 0).  Measured on GB300, the
+// statistics epilogue ran 2.6x slower with CUDA's expf / __expf instead.
 __device__ __forceinline__ float exp_nonpos(float x)
 {
     float y;

@@ -48,10 +48,14 @@
  *     be captured and replayed; the kernels leave their buffers ready for the
  *     next launch.
  *   - Thread safety: every entry point may be called from several host
- *     threads; the per-device state is guarded internally.  On a thread's
- *     first call for a device, the library makes that device's primary
- *     context current on the thread (cudaSetDevice), so a thread that has
- *     made no CUDA call of its own can call it.
+ *     threads, also on one stream (the legacy default stream included); the
+ *     per-device state is guarded internally.  A buffer that a call has
+ *     looked up stays allocated until that call's kernels are enqueued: a
+ *     buffer replaced by a larger one is kept until
+ *     gemm_release_workspace(), which waits for calls in progress on other
+ *     threads.  On a thread's first call for a device, the library makes
+ *     that device's primary context current on the thread (cudaSetDevice),
+ *     so a thread that has made no CUDA call of its own can call it.
  */
 #ifndef DENSE_GEMM_TN_H
 #define DENSE_GEMM_TN_H
@@ -241,7 +245,10 @@ gemm_status_t gemm_poll_device_status(void *stream);
 
 /* Frees the current device's workspaces, all kept per stream: the row
  * copies of unaligned operands, the split-K partial sums, the quantiser's
- * arrays and the softmax-statistics buffers (synchronises the device). */
+ * arrays and the softmax-statistics buffers, and the smaller buffers that
+ * growth replaced.  It first waits for calls in progress on other host
+ * threads to have enqueued their kernels, then synchronises the device
+ * (cudaFree).  The next call that needs a buffer allocates it again. */
 void gemm_release_workspace(void);
 
 /*

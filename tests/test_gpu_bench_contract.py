@@ -46,6 +46,32 @@ def test_json_line(workload):
     assert cpu["kind"] == "oracle" and cpu["value"] > 0 and cpu["cores"] >= 1 and cpu["sample"]
 
 
+def test_headline_line_carries_fp8_sustained_and_clocks():
+    """The default workload's line: a burst peak for a timed region of a few
+    milliseconds, clocks sampled inside it, the FP8 8192^3 secondary with its
+    own roofline, clocks and CPU baseline, and a sustained sub-measurement
+    against the sustained peak."""
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    d = run_bench("--steps", "20", "--warmup", "3", "--cpu-seconds", "1", "--sustained-s", "1.5")
+    assert d["config"]["workload"].startswith("sq_8192") and d["gpu_launches"] == 20
+    rf = d["roofline"]
+    assert rf["bound"] == "tensor" and rf["peak_kind"] == "burst"
+    assert rf["frac"] == pytest.approx(rf["achieved"] / rf["peak"])
+    assert rf["frac_burst"] == pytest.approx(rf["frac"]) and rf["frac_sustained"] > rf["frac_burst"]
+    clk = d["clocks"]
+    assert clk["samples"] >= 1 and clk["sm_mhz"] > 0
+    assert rf["cycles_per_launch"] > rf["tensor_cycles_per_launch"] * 0.9
+    sec = d["secondary"]
+    assert sec["config"]["workload"].startswith("e4m3_8192") and sec["dtype"] == "e4m3"
+    assert sec["value"] > 0 and sec["roofline"]["bound"] == "tensor"
+    assert sec["roofline"]["peak"] == pytest.approx(2 * rf["peak"])
+    assert sec["cpu_baseline"]["kind"] == "oracle" and sec["clocks"]["samples"] >= 1
+    sus = d["sustained"]
+    assert sus["seconds"] >= 1.4 and sus["peak_kind"] == "sustained"
+    assert sus["clocks"]["samples"] >= 100
+
+
 def test_reference_arm_line():
     d = run_bench("--impl", "reference", "--workload", "qk_1024", "--steps", "1", "--warmup", "3")
     assert d["impl"] == "reference" and d["value"] > 0

@@ -92,3 +92,68 @@ def test_concurrent_threads_each_on_its_own_stream(per_thread_default):
             c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
             bad = np.flatnonzero(got[ni, mi] != c)
             assert bad.size == 0, f"thread {t} shape {(M, N, K)}: {bad.size} sampled outputs differ"
+
+
+GROWING = [(500, 300, 1001), (1000, 700, 1001), (1024, 1024, 8192), (2000, 1500, 2049), (2048, 1024, 8192),
+           (3000, 2000, 4097)]
+
+
+def test_threads_share_the_default_stream_while_buffers_grow():
+    """Every thread issues its calls on the legacy default stream, so all of
+    them share that stream's buffers.  The shapes grow the row-copy workspace
+    (K * 2 bytes not a 16-byte multiple) and the split-reduce partials (a long
+    K on a small grid) while other threads may be between looking a buffer up
+    and launching into it; one more thread releases the workspaces now and
+    then.  +-1 inputs: every sampled output is the oracle's bits."""
+    import dense_gemm_tn_gb300 as g
+    host, dev = {}, {}
+    for t in range(THREADS):
+        for i, (M, N, K) in enumerate(GROWING):
+            A = synth.sign_fp16(M * K, 5000 + 100 * t + 2 * i)
+            B = synth.sign_fp16(N * K, 5001 + 100 * t + 2 * i)
+            host[t, i] = (A, B)
+            dev[t, i] = (to_dev_u16(A), to_dev_u16(B),
+                         torch.full((N, M), 0x7E00, dtype=torch.int16, device="cuda"))
+    torch.cuda.synchronize()
+    g.gemm_release_workspace()
+    errors = []
+    stop = threading.Event()
+
+    def worker(t):
+        try:
+            for r in range(3):
+                order = GROWING if (t + r) % 2 == 0 else GROWING[::-1]
+                for (M, N, K) in order:
+                    i = GROWING.index((M, N, K))
+                    dA, dB, C = dev[t, i]
+                    rc = g.lib.gemm_f16_tn(M, N, K, dA.data_ptr(), K, dB.data_ptr(), K, C.data_ptr(), M, None)
+                    if rc != 0:
+                        errors.append(f"thread {t} shape {i}: status {rc}: {g.last_error()}")
+                        return
+        except Exception as e:          # reported below, on the main thread
+            errors.append(f"thread {t}: {e!r}")
+
+    def releaser():
+        while not stop.wait(0.02):
+            g.gemm_release_workspace()
+
+    workers = [threading.Thread(target=worker, args=(t,)) for t in range(THREADS)]
+    rel = threading.Thread(target=releaser)
+    rel.start()
+    for w in workers:
+        w.start()
+    for w in workers:
+        w.join()
+    stop.set()
+    rel.join()
+    torch.cuda.synchronize()
+    g.gemm_poll_device_status()
+    assert not errors, errors
+    for t in range(THREADS):
+        for i, (M, N, K) in enumerate(GROWING):
+            A, B = host[t, i]
+            got = dev[t, i][2].cpu().numpy().view(np.uint16)
+            mi, ni = sample_positions(M, N, 3000, seed=11 * t + i)
+            c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
+            bad = np.flatnonzero(got[ni, mi] != c)
+            assert bad.size == 0, f"thread {t} shape {(M, N, K)}: {bad.size} sampled outputs differ"

@@ -3,63 +3,86 @@ library allocate device memory -- programs that hand out all device memory
 from their own pool or fixed budget, or hot paths where the implicit device
 synchronisation of cudaMalloc / cudaFree is not acceptable.  Instead of a
 cudaMalloc'd workspace it copies unaligned operands into a fixed array in
-the library's device image.
+the library's device image, and it never takes the paths that need the
+library's per-stream buffers (split-K partial sums).
 
-Its results must match gemm_f16_tn's within the FP16 tolerance of the other
-tests, on two calls in a row (the second reuses the array the first wrote).
-This file is named so pytest collects it last."""
+Every call is checked against the CPU oracle: bit-exact on +-1 inputs, within
+the FP16 tolerance of the other tests on Gaussian inputs, on two calls in a
+row (the second reuses the array the first wrote).  The workspaces of the
+ordinary entry points are released first, and the device's free memory must
+not change across the second call.  This file is named so pytest collects it
+last."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
-from tests.gpu_helpers import F16_TOL, assert_tol, f16_values, pad_rows, to_dev_u16
+from tests.gpu_helpers import F16_TOL, GuardedC, assert_tol, f16_values, pad_rows, to_dev_u16
 
 pytestmark = pytest.mark.gpu
 
+CASES = [
+    # M, N, K, lda, ldb, a_off, b_off (elements)
+    (300, 200, 130, 141, 137, 0, 0),       # K % 8 != 0: both operands copied, zero-padded to K = 136
+    (257, 129, 72, 72, 72, 3, 5),          # aligned K and strides, unaligned bases: copied
+    (700, 1000, 4097, 4097, 4097, 1, 0),   # K % 8 != 0, ragged m and n, several tiles
+    (256, 256, 8192, 8192, 8192, 0, 0),    # aligned long K on a small grid: no copy, no split-K buffer
+]
 
-def _run(entry, M, N, K, dA, a_off, lda, dB, b_off, ldb):
-    C = torch.full((N, M), float("nan"), dtype=torch.float16, device="cuda")
-    entry(M, N, K, dA.data_ptr() + 2 * a_off, lda, dB.data_ptr() + 2 * b_off, ldb, C.data_ptr(), M)
-    return C
+
+def _call(g, M, N, K, dA, a_off, lda, dB, b_off, ldb):
+    C = GuardedC(M, N, M)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    st = g.lib.gemm_f16_tn_noalloc(M, N, K, dA.data_ptr() + 2 * a_off, lda, dB.data_ptr() + 2 * b_off, ldb,
+                                   C.ptr, M, None)
+    assert st == g.GEMM_OK, g.last_error()
+    g.gemm_poll_device_status()
+    free1 = torch.cuda.mem_get_info()[0]
+    return C.nm(), free0 - free1
+
+
+def _check_case(g, M, N, K, lda, ldb, a_off, b_off, values, seed):
+    make = synth.sign_fp16 if values == "pm1" else synth.gauss_fp16
+    A = make(M * K, seed)
+    B = make(N * K, seed + 1)
+    # the padding of each row holds +-Inf, which must never reach a product
+    Ap = np.concatenate([np.zeros(a_off, np.uint16), pad_rows(A, M, K, lda, 0x7C00)])
+    Bp = np.concatenate([np.zeros(b_off, np.uint16), pad_rows(B, N, K, ldb, 0xFC00)])
+    dA, dB = to_dev_u16(Ap), to_dev_u16(Bp)
+    Cref, S, _ = oracle.gemm_f16_tn(M, N, K, A, K, B, K)
+    ref = oracle.c_as_nm(Cref, M, N, M)
+    for call in (1, 2):
+        got, grown = _call(g, M, N, K, dA, a_off, lda, dB, b_off, ldb)
+        what = f"noalloc {values} {M}x{N}x{K} call {call}"
+        if values == "pm1":
+            assert np.array_equal(got, ref), f"{what}: {np.sum(got != ref)} outputs differ from the oracle"
+        else:
+            assert_tol(f16_values(got), f16_values(ref), S, F16_TOL, what)
+        if call == 2:      # the first call may still load kernels lazily
+            assert grown == 0, f"{what}: device free memory fell by {grown} bytes"
 
 
 @pytest.mark.parametrize("tiles", ["auto", "256x512 pairs"])
-def test_noalloc_matches_gemm_f16_tn_on_two_calls(tiles):
+@pytest.mark.parametrize("values", ["pm1", "gauss"])
+def test_noalloc_matches_the_oracle_on_two_calls(tiles, values):
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     import dense_gemm_tn_gb300 as g
+    g.gemm_release_workspace()
     if tiles != "auto":
         g.gemm_debug_force_cta_group(2)
         g.gemm_debug_force_wide_tiles(1)
     try:
-        _compare_two_calls(g)
+        for i, (M, N, K, lda, ldb, a_off, b_off) in enumerate(CASES):
+            _check_case(g, M, N, K, lda, ldb, a_off, b_off, values, 900 + 10 * i)
+            if tiles != "auto":
+                assert "wide=1" in g.last_launch(), g.last_launch()
+            assert "tail_mode=2" not in g.last_launch() and "tail_mode=3" not in g.last_launch(), g.last_launch()
     finally:
         g.gemm_debug_force_cta_group(0)
         g.gemm_debug_force_wide_tiles(0)
-
-
-def _compare_two_calls(g):
-    cases = [
-        # M, N, K, lda, ldb, a_off, b_off: every case needs an operand copy
-        (300, 200, 130, 141, 137, 0, 0),     # K and strides not 16-byte multiples
-        (257, 129, 72, 72, 72, 3, 5),        # aligned K and strides, unaligned bases
-    ]
-    for i, (M, N, K, lda, ldb, a_off, b_off) in enumerate(cases):
-        A = synth.gauss_fp16(M * K, 900 + i)
-        B = synth.gauss_fp16(N * K, 950 + i)
-        Ap = np.concatenate([np.zeros(a_off, np.uint16), pad_rows(A, M, K, lda, 0x7C00)])
-        Bp = np.concatenate([np.zeros(b_off, np.uint16), pad_rows(B, N, K, ldb, 0xFC00)])
-        dA, dB = to_dev_u16(Ap), to_dev_u16(Bp)
-        ref = _run(g.gemm_f16_tn, M, N, K, dA, a_off, lda, dB, b_off, ldb)
-        got = _run(g.gemm_f16_tn_noalloc, M, N, K, dA, a_off, lda, dB, b_off, ldb)
-        g.gemm_poll_device_status()
-        r = ref.float().cpu().numpy().astype(np.float64)
-        o = got.float().cpu().numpy().astype(np.float64)
-        Am = f16_values(A).reshape(M, K)
-        Bn = f16_values(B).reshape(N, K)
-        S = np.abs(Bn) @ np.abs(Am).T                      # (N, M): sum_k |a b|
-        assert_tol(o, r, S, F16_TOL, f"noalloc call {i + 1}")
 
 
 def test_noalloc_rejects_copies_beyond_its_array():
