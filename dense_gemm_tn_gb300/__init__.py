@@ -44,7 +44,7 @@ EXPORTS = (
     "gemm_poll_device_status", "gemm_release_workspace", "gemm_tile_coord",
     "gemm_set_wait_limit_ns", "gemm_debug_inject_stall", "gemm_build_info",
     "gemm_f16_tn_noalloc", "gemm_debug_force_cta_group", "gemm_debug_force_wide_tiles", "gemm_debug_last_launch",
-    "gemm_debug_set_raster_group",
+    "gemm_debug_set_raster_group", "gemm_debug_set_k_order", "gemm_debug_set_l2_hints",
     "gemm_f8e4m3_tn_dscale", "gemm_quantize_e4m3", "gemm_f16_tn_softmax_stats",
 )
 
@@ -99,6 +99,10 @@ def _load() -> ctypes.CDLL:
     lib.gemm_debug_force_wide_tiles.restype = ctypes.c_int
     lib.gemm_debug_set_raster_group.argtypes = [ctypes.c_int]
     lib.gemm_debug_set_raster_group.restype = ctypes.c_int
+    lib.gemm_debug_set_l2_hints.argtypes = [ctypes.c_int]
+    lib.gemm_debug_set_l2_hints.restype = ctypes.c_int
+    lib.gemm_debug_set_k_order.argtypes = [ctypes.c_int]
+    lib.gemm_debug_set_k_order.restype = ctypes.c_int
     lib.gemm_debug_last_launch.argtypes = []
     lib.gemm_debug_last_launch.restype = ctypes.c_char_p
     lib.gemm_build_info.argtypes = []
@@ -216,7 +220,7 @@ def gemm_debug_inject_stall(mode) -> None:
 
 def gemm_debug_force_cta_group(group: int) -> None:
     if _lib.gemm_debug_force_cta_group(int(group)) != 0:
-        raise ValueError("cta group must be 0 (automatic), 1, 2 or 4")
+        raise ValueError("cta group must be 0 (automatic), 1 or 2")
 
 
 def gemm_debug_force_wide_tiles(mode: int) -> None:
@@ -229,6 +233,18 @@ def gemm_debug_set_raster_group(rows: int) -> None:
     """Tile rows per raster group of the scheduler (even, 2 .. 64); 0 the default."""
     if _lib.gemm_debug_set_raster_group(int(rows)) != 0:
         raise ValueError("rows must be 0 or an even number up to 64")
+
+
+def gemm_debug_set_k_order(mode: int) -> None:
+    """0 the library's choice; 1 every tile walks K forward; 2 odd waves walk it backwards."""
+    if _lib.gemm_debug_set_k_order(int(mode)) != 0:
+        raise ValueError("mode must be 0, 1 or 2")
+
+
+def gemm_debug_set_l2_hints(mask: int) -> None:
+    """-1 the library's choice; else bits 1 A evict_last, 2 B evict_first, 4 C evict_first."""
+    if _lib.gemm_debug_set_l2_hints(int(mask)) != 0:
+        raise ValueError("mask must be -1 .. 7")
 
 
 # ---------------------------------------------------------------- torch helpers

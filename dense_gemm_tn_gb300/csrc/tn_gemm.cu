@@ -28,6 +28,8 @@ namespace {
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 256;   // TMA coordinates are signed 32-bit
 constexpr int kMaxDevices = 64;
 constexpr int kGroupM = 8;                               // tile rows per raster group
+constexpr bool kAltKDefault = false;                     // odd waves walk K backwards (kFlagAltK)
+constexpr int kL2HintsDefault = 0;                       // L2 eviction hints: bits 1 A, 2 B, 4 C
 
 thread_local char t_last_error[512] = "";
 
@@ -79,6 +81,8 @@ std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_force_cta_group{0};
 std::atomic<int> g_force_wide{0};       // 0: the cost estimate decides; 1: always; -1: never
 std::atomic<int> g_raster_group{0};     // tile rows per raster group; 0: kGroupM
+std::atomic<int> g_k_order{0};          // 0: the library's choice; 1: every tile forward; 2: odd waves reversed
+std::atomic<int> g_l2_hints{-1};        // -1: the library's choice; else bits 1 A, 2 B, 4 C (gemm_debug_set_l2_hints)
 // The last launch on this host thread, for gemm_debug_last_launch: the
 // numbers are kept and formatted only when asked for (formatting every call
 // cost host time on the path of back-to-back small GEMMs).
@@ -708,6 +712,13 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         prm.stat_parts = reinterpret_cast<float2 *>(base + zeroed);
     }
     prm.flags |= (tma_c ? tn::kFlagTmaStore : 0u) | stall_flags(g_inject_stall.load());
+    {
+        const int ko = g_k_order.load();
+        if (ko == 2 || (ko == 0 && kAltKDefault)) prm.flags |= tn::kFlagAltK;
+        int h = g_l2_hints.load();
+        if (h < 0) h = kL2HintsDefault;
+        prm.flags |= (h & 1 ? tn::kFlagHintA : 0u) | (h & 2 ? tn::kFlagHintB : 0u) | (h & 4 ? tn::kFlagHintC : 0u);
+    }
     prm.wait_limit_ns = g_wait_limit_ns.load();
 
     const ASource asrc{in_type, a_use, static_cast<uint64_t>(ka), static_cast<uint64_t>(M),
@@ -979,6 +990,20 @@ int gemm_debug_set_raster_group(int rows)
 {
     if (rows < 0 || rows > 64 || rows % 2) return -1;
     g_raster_group.store(rows);
+    return 0;
+}
+
+int gemm_debug_set_k_order(int mode)
+{
+    if (mode < 0 || mode > 2) return -1;
+    g_k_order.store(mode);
+    return 0;
+}
+
+int gemm_debug_set_l2_hints(int mask)
+{
+    if (mask < -1 || mask > 7) return -1;
+    g_l2_hints.store(mask);
     return 0;
 }
 

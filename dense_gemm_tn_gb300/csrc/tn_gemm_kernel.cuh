@@ -133,6 +133,19 @@ constexpr uint32_t kFlagStallProducer1 = 8u;    // the producer of cluster CTA 1
 // FP16 scaled scores with softmax row statistics: C = fp16(scale * acc), and
 // per row m the maximum and the sum of exp(score - maximum) over all n.
 constexpr uint32_t kFlagStats = 16u;
+// Whole tiles of odd waves (tile id / slots odd) walk their k blocks from the
+// last to the first.  The tiles of one wave read their shared A and B panels
+// in lockstep; the next wave shares panels with it (the grouped raster keeps
+// its tile rows), and walking K the other way it starts on the k slices the
+// previous wave read last, which are the likeliest to be still in L2.  The
+// order of the FP32 sums changes, not their terms.
+constexpr uint32_t kFlagAltK = 32u;
+// L2 eviction priorities: A loads evict_last (the A panels of a raster group
+// are read again by the group's later waves), B loads evict_first (a wave's
+// B panels are not), C stores evict_first (C is not read back).
+constexpr uint32_t kFlagHintA = 64u;
+constexpr uint32_t kFlagHintB = 128u;
+constexpr uint32_t kFlagHintC = 256u;
 
 // Status word of the current device; set (never cleared) by a kernel whose
 // bounded wait ran out: 4 (timeout) | site << 8.
@@ -597,10 +610,28 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             uint32_t n_issued = 0;
             bool ok = true;
             const uint32_t stall = rank == 0 ? kFlagStallProducer0 : (rank == 1 ? kFlagStallProducer1 : 0u);
+            const bool hint_a = (p.flags & kFlagHintA) != 0, hint_b = (p.flags & kFlagHintB) != 0;
+            const uint64_t pol_a = ptx::policy_evict_last(), pol_b = ptx::policy_evict_first();
+            auto load = [&](uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x, int32_t y, bool hint,
+                            uint64_t pol) {
+                if constexpr (kGroup == 2) {
+                    if (hint)
+                        ptx::tma_load_2d_pair_hint(dst, map, bar, x, y, pol);
+                    else
+                        ptx::tma_load_2d_pair(dst, map, bar, x, y);
+                } else {
+                    if (hint)
+                        ptx::tma_load_2d_hint(dst, map, bar, x, y, pol);
+                    else
+                        ptx::tma_load_2d(dst, map, bar, x, y);
+                }
+            };
             if (p.flags & stall) ok = w.wait(never_bar, 0u, kSiteStall);
             for (int64_t it = 0; ok && it < iters; ++it) {
                 const Unit un = slot_unit_at(it);
                 const bool cut_m = un.mpart >= 0;
+                const bool rev = (p.flags & kFlagAltK) && !un.phantom && un.tile < p.tail_start &&
+                                 ((static_cast<uint32_t>(un.tile) / static_cast<uint32_t>(nslots)) & 1u);
                 // A rows of this CTA: one box per stage, or (a whole wide tile) one per half,
                 // the second kTileM rows further on.  A wide tile's A map has boxes of one
                 // half's rows, which are also an m part's.
@@ -613,7 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                                               : static_cast<int32_t>(un.tm * Cfg::kTileMRows +
                                                                      (cut_m ? un.mpart * p.m_part_rows : 0) + pos * rows_a);
                 const int32_t nb = un.phantom ? p.N : static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB);
-                for (int kb = un.kb0; kb < un.kb0 + un.nkb; ++kb) {
+                for (int i = 0; i < un.nkb; ++i) {
+                    const int kb = rev ? un.kb0 + un.nkb - 1 - i : un.kb0 + i;
                     if (!w.wait(empty_bar(stage), phase ^ 1u, kSiteEmpty)) {
                         ok = false;
                         break;
@@ -626,19 +658,19 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                             if (pos == 0) ptx::mbar_arrive_expect_tx(loaded_bar(stage, t), 2 * fill / kAtoms);
                             const uint32_t lb = ptx::mapa_shared(loaded_bar(stage, t), lead);
                             const int32_t k0 = (kb * Cfg::kAtoms + t) * kBlockKElems;
-                            ptx::tma_load_2d_pair(s_b + t * Cfg::kAtomBBytes, &p.tmap_b, lb, k0, nb);
-                            ptx::tma_load_2d_pair(s_a + t * Cfg::kAtomABytes, map_a, lb, k0, m0);
+                            load(s_b + t * Cfg::kAtomBBytes, &p.tmap_b, lb, k0, nb, hint_b, pol_b);
+                            load(s_a + t * Cfg::kAtomABytes, map_a, lb, k0, m0, hint_a, pol_a);
                             if (two_halves)
-                                ptx::tma_load_2d_pair(s_a + t * Cfg::kAtomABytes + Cfg::kHalfABytes, map_a, lb, k0,
-                                                      m0 + kTileM);
+                                load(s_a + t * Cfg::kAtomABytes + Cfg::kHalfABytes, map_a, lb, k0, m0 + kTileM,
+                                     hint_a, pol_a);
                         }
                     } else {
 #pragma unroll
                         for (int t = 0; t < Cfg::kAtoms; ++t) {
                             const int32_t k0 = (kb * Cfg::kAtoms + t) * kBlockKElems;
                             ptx::mbar_arrive_expect_tx(loaded_bar(stage, t), fill / kAtoms);
-                            ptx::tma_load_2d(s_b + t * Cfg::kAtomBBytes, &p.tmap_b, loaded_bar(stage, t), k0, nb);
-                            ptx::tma_load_2d(s_a + t * Cfg::kAtomABytes, map_a, loaded_bar(stage, t), k0, m0);
+                            load(s_b + t * Cfg::kAtomBBytes, &p.tmap_b, loaded_bar(stage, t), k0, nb, hint_b, pol_b);
+                            load(s_a + t * Cfg::kAtomABytes, map_a, loaded_bar(stage, t), k0, m0, hint_a, pol_a);
                         }
                     }
                     *issued_count = ++n_issued;
@@ -845,6 +877,8 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         const int ew = warp - 2;
         const int row = 32 * quarter + lane;      // this thread's TMEM lane = output column within the CTA
         const bool tma_store = (p.flags & kFlagTmaStore) != 0;
+        const bool hint_c = (p.flags & kFlagHintC) != 0;
+        const uint64_t pol_c = ptx::policy_evict_first();
         volatile uint32_t *second_flag = tmem_holder + 4;   // split-K: this CTA's half came second
         const float scale = p.scale_a_ptr ? __fmul_rn(__ldg(p.scale_a_ptr), __ldg(p.scale_b_ptr)) : p.scale;
         int acc = 0;
@@ -906,7 +940,10 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    ptx::tma_store_2d(&p.tmap_c, buf, mc, nw);   // clipped at m_tma and N
+                    if (hint_c)                                   // clipped at m_tma and N
+                        ptx::tma_store_2d_hint(&p.tmap_c, buf, mc, nw, pol_c);
+                    else
+                        ptx::tma_store_2d(&p.tmap_c, buf, mc, nw);
                     ptx::bulk_commit_group();
                 }
                 ++chunk_ctr;

@@ -307,6 +307,26 @@ int gemm_debug_force_wide_tiles(int mode);
  */
 int gemm_debug_set_raster_group(int rows);
 
+/*
+ * Test hook: the order in which whole tiles walk their k blocks.  0
+ * (default): the library's choice; 1: every tile from the first k block to
+ * the last; 2: tiles of odd waves (tile id / co-resident slots odd) from the
+ * last to the first, so that a wave starts on the k slices that the wave
+ * before it, which shares its A panels, read last.  Only the order of the
+ * FP32 partial sums changes (results on integer inputs are identical).
+ * Returns 0, or -1 for other values.
+ */
+int gemm_debug_set_k_order(int mode);
+
+/*
+ * Test hook: L2 eviction priorities of the kernel's bulk copies.  -1
+ * (default): the library's choice; otherwise a mask: 1 A loads evict_last
+ * (later waves of a raster group read the same A panels), 2 B loads
+ * evict_first, 4 C stores evict_first.  Results do not change.  Returns 0,
+ * or -1 for values outside -1 .. 7.
+ */
+int gemm_debug_set_l2_hints(int mask);
+
 /* Description of the last GEMM kernel launch on the calling host thread
  * (tile shape, grid, co-resident cluster slots), for logs and tests
  * (thread-local storage; "" before the first launch). */

@@ -146,3 +146,10 @@ def test_no_multicast_bulk_loads_in_library_sources():
             if "multicast::cluster" in line:
                 assert "tcgen05.commit" in line, (name, line)
             assert not re.search(r"cp\.async\.bulk.*multicast", line), (name, line)
+
+
+def test_k_order_hook_values():
+    assert g.lib.gemm_debug_set_k_order(3) == -1
+    assert g.lib.gemm_debug_set_k_order(-1) == -1
+    for v in (1, 2, 0):
+        assert g.lib.gemm_debug_set_k_order(v) == 0
