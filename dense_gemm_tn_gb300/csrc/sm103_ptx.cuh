@@ -86,6 +86,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// The same wait with acquire semantics at cluster scope: writes that other
+// CTAs of the cluster published with a cluster-scope release before their
+// arrive are visible once it returns true.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -123,6 +137,32 @@ __device__ __forceinline__ void cluster_sync()
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar)
 {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// Arrive with release semantics at cluster scope: the calling thread's
+// earlier writes, and those ordered before them (by a CTA barrier), are
+// visible to a thread of the barrier's CTA that observes the phase with a
+// cluster-scope acquire.
+__device__ __forceinline__ void mbar_arrive_remote_release_cluster(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// 16-byte store into another CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ void st_shared_cluster_v4(uint32_t cluster_addr, float a, float b, float c, float d)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+// 16-byte load from this CTA's shared memory.
+__device__ __forceinline__ float4 ld_shared_v4_f32(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
 }
 
 // Word accesses to another CTA's shared memory (shared::cluster address).

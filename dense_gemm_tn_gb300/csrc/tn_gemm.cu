@@ -12,6 +12,7 @@
 #include <cstdio>
 #include <cstring>
 #include <iterator>
+#include <memory>
 #include <mutex>
 #include <shared_mutex>
 #include <unordered_map>
@@ -28,7 +29,10 @@ namespace {
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 256;   // TMA coordinates are signed 32-bit
 constexpr int kMaxDevices = 64;
 constexpr int kGroupM = 8;                               // tile rows per raster group
-constexpr bool kAltKDefault = false;                     // odd waves walk K backwards (kFlagAltK)
+// Odd waves walk K backwards (kFlagAltK).  Measured on GB300 at 8192^3 (256 x
+// 512 tiles, FP16, under the power cap): DRAM reads 815 -> 684 MB per launch,
+// 1612 -> 1626 TFLOP/s; E4M3 3212 -> 3225.
+constexpr bool kAltKDefault = true;
 constexpr int kL2HintsDefault = 0;                       // L2 eviction hints: bits 1 A, 2 B, 4 C
 
 thread_local char t_last_error[512] = "";
@@ -48,6 +52,8 @@ struct DeviceState {
     // per kernel, indexed [kind: f16, e4m3][1: one CTA, 2: CTA pairs, 3: CTA pairs with 256 x 512 tiles]
     bool smem_attr[2][4] = {};
     int max_clusters[2][4] = {};      // co-resident clusters of the kernel's own size (0 = not queried yet)
+    // co-resident clusters of S single CTAs (kClusterReduce), by kind and S (0 = not queried, -1 = none)
+    int cluster_slots[2][5] = {};
     // Split-K partial sums of the last wave, one buffer per stream (calls on
     // one stream are ordered, so they may share it): [tickets | partials].
     struct Split {
@@ -64,10 +70,10 @@ struct DeviceState {
     // Softmax statistics: [tickets per tile row | parts], one buffer per stream.
     std::unordered_map<cudaStream_t, Split> stats;
     int quant_blocks[3] = {};         // co-resident quantiser CTAs per SM, by input type (0 = not queried)
-    // Buffers replaced by larger ones.  Another host thread may have looked one
-    // up and not yet enqueued the kernel that uses it, so they are freed only
-    // by gemm_release_workspace.
-    std::vector<void *> retired;
+    // One lock per stream, held by a call from its first buffer lookup through
+    // its last launch: a call is several launches (row copy, GEMM, reduce),
+    // and two host threads' calls on one stream must not interleave them.
+    std::unordered_map<cudaStream_t, std::unique_ptr<std::mutex>> stream_locks;
 };
 
 std::mutex g_mutex;
@@ -75,6 +81,9 @@ std::mutex g_mutex;
 // launch, and exclusively by gemm_release_workspace: the buffers a call looked
 // up stay allocated until its kernels are enqueued.
 std::shared_mutex g_workspace_lock;
+
+// The calling call's lock of `stream` on device state d (see stream_locks).
+std::unique_lock<std::mutex> lock_stream(DeviceState &d, cudaStream_t stream);
 DeviceState g_devices[kMaxDevices];
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
@@ -82,6 +91,7 @@ std::atomic<int> g_force_cta_group{0};
 std::atomic<int> g_force_wide{0};       // 0: the cost estimate decides; 1: always; -1: never
 std::atomic<int> g_raster_group{0};     // tile rows per raster group; 0: kGroupM
 std::atomic<int> g_k_order{0};          // 0: the library's choice; 1: every tile forward; 2: odd waves reversed
+std::atomic<int> g_long_k{0};           // small grids with a long K: 0 the library's choice; 1 split-reduce; 2 cluster
 std::atomic<int> g_l2_hints{-1};        // -1: the library's choice; else bits 1 A, 2 B, 4 C (gemm_debug_set_l2_hints)
 // The last launch on this host thread, for gemm_debug_last_launch: the
 // numbers are kept and formatted only when asked for (formatting every call
@@ -90,7 +100,7 @@ struct LaunchRecord {
     const char *name = nullptr;     // nullptr: nothing launched yet
     bool quant = false;
     int G = 0, wide = 0, grid = 0, clusters = 0, slots = 0;
-    int tiles = 0, units = 0, tail_start = 0, tail_mode = 0, split_parts = 0, vec = 0;
+    int tiles = 0, units = 0, tail_start = 0, tail_mode = 0, split_parts = 0, vec = 0, cluster = 0;
     long long qgrid = 0, qunits = 0;
 };
 thread_local LaunchRecord t_rec;
@@ -164,12 +174,12 @@ cudaStream_t stream_key(cudaStream_t stream)
 }
 
 // A per-stream buffer of `map` that starts with `zeroed_bytes` of words
-// cleared when it is (re)allocated, followed by `extra_bytes`; grown on demand
-// (to at least twice its size, so that few buffers are ever retired).  Calls
-// on one stream are ordered, so they may share their stream's buffer, also
-// when different host threads issue them.  The caller holds
+// cleared when it is (re)allocated, followed by `extra_bytes`; grown on demand.
+// The calls on one stream are ordered, and the caller holds the stream's lock
+// (lock_stream) from here through its last launch, so calls on one stream
+// share its buffers whatever host thread issues them; it also holds
 // g_workspace_lock (shared).
-gemm_status_t stream_buffer(DeviceState &d, std::unordered_map<cudaStream_t, DeviceState::Split> &map,
+gemm_status_t stream_buffer(DeviceState &, std::unordered_map<cudaStream_t, DeviceState::Split> &map,
                             cudaStream_t stream, size_t zeroed_bytes, size_t extra_bytes, const char *what,
                             uint8_t **base, size_t *zeroed_out)
 {
@@ -178,13 +188,8 @@ gemm_status_t stream_buffer(DeviceState &d, std::unordered_map<cudaStream_t, Dev
     const size_t tb = (zeroed_bytes + 255) & ~size_t(255);
     if (w.ticket_bytes < tb || w.bytes < w.ticket_bytes + extra_bytes) {
         const size_t new_tb = tb > w.ticket_bytes ? tb : w.ticket_bytes;
-        size_t need = new_tb + extra_bytes;
-        if (w.ptr) {
-            // Not freed here: a call on another host thread may hold its address
-            // and not have enqueued its kernels yet.
-            d.retired.push_back(w.ptr);
-            if (need < 2 * w.bytes) need = 2 * w.bytes;
-        }
+        const size_t need = new_tb + extra_bytes;
+        if (w.ptr) cudaFree(w.ptr);      // synchronises the device: earlier users are done
         w.ptr = nullptr;
         w.bytes = w.ticket_bytes = 0;
         cudaError_t e = cudaMalloc(&w.ptr, need);
@@ -206,6 +211,18 @@ gemm_status_t stream_buffer(DeviceState &d, std::unordered_map<cudaStream_t, Dev
     *base = static_cast<uint8_t *>(w.ptr);
     *zeroed_out = w.ticket_bytes;
     return GEMM_OK;
+}
+
+std::unique_lock<std::mutex> lock_stream(DeviceState &d, cudaStream_t stream)
+{
+    std::mutex *m;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        std::unique_ptr<std::mutex> &slot = d.stream_locks[stream_key(stream)];
+        if (!slot) slot.reset(new std::mutex);
+        m = slot.get();
+    }
+    return std::unique_lock<std::mutex>(*m);
 }
 
 // The stream's split-K buffer with room for `tickets` ticket words and
@@ -428,32 +445,63 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     }
     // A grid of at most half the slots with a long K leaves most SMs idle:
     // every tile is cut into S ranges of its k blocks (as many as the slots
-    // allow, at most 8, each at least 16 k blocks), the units store FP32
-    // partials, and a reduce kernel sums them in order and stores C.
+    // allow, at most 8, each at least 16 k blocks).  Single CTAs do it in a
+    // cluster of S <= 4 CTAs per tile, which add their partials up through
+    // distributed shared memory (kClusterReduce: no workspace, one kernel);
+    // otherwise the units store FP32 partials, and a reduce kernel sums them
+    // in order and stores C (kSplitReduce).
     const int cap = slots;
     const bool stats = (prm.flags & tn::kFlagStats) != 0;
-    int reduce_parts = 1;
-    if (allow_alloc && !stats && 2 * prm.num_tiles <= cap && prm.num_kb >= 32) {
+    const int long_k = g_long_k.load();
+    int reduce_parts = 1, cluster_parts = 1;
+    if (!stats && 2 * prm.num_tiles <= cap && prm.num_kb >= 32) {
         int S = cap / prm.num_tiles;
         if (S > 8) S = 8;
         if (S > prm.num_kb / 16) S = prm.num_kb / 16;
-        if (S >= 2) reduce_parts = S;
+        if (G == 1 && long_k != 1 && S >= 2 && (S <= 4 || long_k == 2 || !allow_alloc)) {
+            // clusters of Sc CTAs must fit Sc at a time into a GPC's SMs: the most
+            // Sc for which one cluster per tile is co-resident
+            for (int Sc = S < 4 ? S : 4; Sc >= 2 && cluster_parts == 1; --Sc) {
+                std::lock_guard<std::mutex> lock(g_mutex);
+                int &n = dev.cluster_slots[ki][Sc];
+                if (n == 0) {
+                    cudaLaunchConfig_t qcfg = cfg;
+                    cudaLaunchAttribute qattr[1];
+                    qattr[0].id = cudaLaunchAttributeClusterDimension;
+                    qattr[0].val.clusterDim.x = Sc;
+                    qattr[0].val.clusterDim.y = 1;
+                    qattr[0].val.clusterDim.z = 1;
+                    qcfg.attrs = qattr;
+                    qcfg.numAttrs = 1;
+                    qcfg.gridDim = dim3(Sc * (dev.sms / Sc), 1, 1);
+                    if (cudaOccupancyMaxActiveClusters(&n, kernel, &qcfg) != cudaSuccess || n <= 0) {
+                        cudaGetLastError();
+                        n = -1;
+                    }
+                }
+                if (n >= prm.num_tiles) cluster_parts = Sc;
+            }
+        }
+        if (cluster_parts == 1 && allow_alloc && long_k != 2 && S >= 2) reduce_parts = S;
     }
     // A grid of at most half the slots with a shorter K: every tile's m range
     // is cut into 2 or 4 parts (MMA N = 128 or 64).  Such a launch is bound by
     // latency, mostly the epilogue's TMEM -> shared memory -> TMA store
     // round trips, and each unit stores a half or a quarter of a tile.
     int m_parts = 1;
-    if (!W && reduce_parts == 1 && 2 * prm.num_tiles <= cap)
+    if (!W && reduce_parts == 1 && cluster_parts == 1 && 2 * prm.num_tiles <= cap)
         m_parts = tn::kMaxMParts * prm.num_tiles <= cap ? tn::kMaxMParts : 2;
     const int units0 = prm.num_tiles * reduce_parts * m_parts;
-    const int clusters = units0 < slots ? units0 : slots;
+    // (kClusterReduce: one tile per cluster of cluster_parts CTAs, never more --
+    // a CTA's ring takes the other CTAs' partials once its own MMAs are done)
+    const int clusters = cluster_parts > 1 ? prm.num_tiles : units0 < slots ? units0 : slots;
+    if (cluster_parts > 1) attr[0].val.clusterDim.x = cluster_parts;
     // A programmatic dependent of the previous kernel on the stream: the
     // kernel waits for it (griddepcontrol.wait) before touching memory.
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.numAttrs = 2;
-    cfg.gridDim = dim3(G * clusters, 1, 1);
+    cfg.gridDim = dim3(G * cluster_parts * clusters, 1, 1);
     // A last wave that fills at most half of the slots is run as twice as
     // many half-length units, so every slot finishes at about the same time:
     // each of those tiles is split into two halves of its k blocks whose
@@ -465,7 +513,11 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     prm.num_units = prm.num_tiles;
     prm.split_parts = 1;
     prm.m_part_rows = 0;
-    if (reduce_parts > 1) {
+    if (cluster_parts > 1) {
+        prm.tail_mode = tn::kClusterReduce;
+        prm.split_parts = cluster_parts;
+        prm.kb_part = (prm.num_kb + cluster_parts - 1) / cluster_parts;
+    } else if (reduce_parts > 1) {
         const size_t partial = size_t(prm.num_tiles) * reduce_parts * G * Cfg::kRowsB * Cfg::kTileMRows * sizeof(float);
         uint8_t *base = nullptr;
         size_t zeroed = 0;
@@ -512,7 +564,8 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     t_rec.quant = false;
     t_rec.G = G;
     t_rec.wide = W ? 1 : 0;
-    t_rec.grid = G * clusters;
+    t_rec.grid = G * cluster_parts * clusters;
+    t_rec.cluster = G * cluster_parts;
     t_rec.clusters = clusters;
     t_rec.slots = slots;
     t_rec.tiles = prm.num_tiles;
@@ -573,6 +626,8 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     DeviceState *dev = nullptr;
     gemm_status_t st = device_state(&dev, nullptr);
     if (st != GEMM_OK) return st;
+    // this call's launches go onto the stream together (no other host thread's in between)
+    std::unique_lock<std::mutex> stream_guard = lock_stream(*dev, stream);
 
     if (K == 0) {
         // every sum is +0; scaled scores are scale * +0 (-0 for a negative scale)
@@ -806,6 +861,7 @@ gemm_status_t run_quant(const void *x, int x_type, int64_t rows, int64_t cols, i
     DeviceState *dev = nullptr;
     gemm_status_t st = device_state(&dev, nullptr);
     if (st != GEMM_OK) return st;
+    std::unique_lock<std::mutex> stream_guard = lock_stream(*dev, stream);
     if (rows == 0 || cols == 0) {
         // no elements: amax = 0, so the dequantisation scale is 0
         cudaError_t e = cudaMemsetAsync(scale, 0, sizeof(float), stream);
@@ -943,8 +999,6 @@ void gemm_release_workspace(void)
     std::unique_lock<std::shared_mutex> workspace_guard(g_workspace_lock);
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState &d = g_devices[dev];
-    for (void *p : d.retired) cudaFree(p);
-    d.retired.clear();
     for (auto &kv : d.repack)
         if (kv.second.ptr) cudaFree(kv.second.ptr);
     d.repack.clear();
@@ -1000,6 +1054,13 @@ int gemm_debug_set_k_order(int mode)
     return 0;
 }
 
+int gemm_debug_set_long_k_mode(int mode)
+{
+    if (mode < 0 || mode > 2) return -1;
+    g_long_k.store(mode);
+    return 0;
+}
+
 int gemm_debug_set_l2_hints(int mask)
 {
     if (mask < -1 || mask > 7) return -1;
@@ -1019,7 +1080,7 @@ const char *gemm_debug_last_launch(void)
         snprintf(t_last_launch, sizeof(t_last_launch),
                  "%s: ctas_per_cluster=%d wide=%d grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d "
                  "tail_mode=%d split_parts=%d",
-                 r.name, r.G, r.wide, r.grid, r.clusters, r.slots, r.tiles, r.units,
+                 r.name, r.cluster, r.wide, r.grid, r.clusters, r.slots, r.tiles, r.units,
                  r.tail_start, r.tail_mode, r.split_parts);
     return t_last_launch;
 }
@@ -1056,6 +1117,10 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 // Device address of g_noalloc_scratch per device (host code cannot use the
 // symbol itself: on the host it names a stand-in, not device memory).
 void *g_noalloc_scratch_ptr[kMaxDevices] = {};
+
+// Held from a call's copy into the array through its GEMM launch, so that two
+// host threads' calls on one stream do not enqueue copy, copy, GEMM, GEMM.
+std::mutex g_noalloc_issue;
 
 gemm_status_t noalloc_scratch(void **out)
 {
@@ -1117,6 +1182,7 @@ extern "C" gemm_status_t gemm_f16_tn_noalloc(int64_t M, int64_t N, int64_t K, co
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *ws = static_cast<uint8_t *>(scratch);
+    std::lock_guard<std::mutex> issue_guard(g_noalloc_issue);
     const void *a_use = A, *b_use = B;
     int64_t lda_use = lda, ldb_use = ldb;
     tn::RepackJob<uint16_t> ja{static_cast<const uint16_t *>(A), lda, reinterpret_cast<uint16_t *>(ws), ldp,

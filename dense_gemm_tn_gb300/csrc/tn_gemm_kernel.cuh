@@ -104,8 +104,8 @@ struct TileCfg {
     static constexpr int kTileABytes = kAtoms * kAtomABytes;
     static constexpr int kStageBytes = kTileBBytes + kTileABytes;
     static constexpr int kSmemRing = kStages * kStageBytes;
-    // loaded[S][atoms], empty[S], accfull[2], accempty[2], drain, never
-    static constexpr int kNumBarriers = kStages * (kAtoms + 1) + 6;
+    // loaded[S][atoms], empty[S], accfull[2], accempty[2], drain, never, peers_free, received
+    static constexpr int kNumBarriers = kStages * (kAtoms + 1) + 8;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kSmemRing + kSmemEpi + kNumBarriers * 8 + 32;
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB shared memory of one CTA");
 };
@@ -123,6 +123,14 @@ constexpr int32_t kTailSplitK = 2;   // two halves of the k blocks; partial sums
 // into split_parts ranges of its k blocks; each unit stores its FP32 partial,
 // and split_reduce_kernel (launched next) sums them and stores C.
 constexpr int32_t kSplitReduce = 3;
+// The same cut made inside a cluster of single CTAs: a cluster of S =
+// split_parts (2 to 4) CTAs per tile, CTA r computing k blocks
+// [r kb_part, (r + 1) kb_part), one tile per cluster.  Of the tile's four
+// 64-column chunks of m, CTA r reduces and stores those with c % S == r: the
+// other CTAs write their FP32 partials of them into its shared memory
+// (distributed shared memory), and it adds the S partials in rank order.  No
+// workspace, no second kernel.
+constexpr int32_t kClusterReduce = 4;
 
 constexpr uint32_t kFlagTmaStore = 1u;      // C rows m < m_tma are written with TMA stores
 // Test hooks: the named thread first waits on a barrier nobody arrives on, so
@@ -153,7 +161,7 @@ __device__ int g_tn_status;
 
 enum WaitSite : int {
     kSiteEmpty = 1, kSiteLoaded = 2, kSiteAccEmpty = 3, kSiteAccFull = 4, kSiteStall = 5, kSitePeerDone = 6,
-    kSiteDrain = 7, kSiteReconcile = 8
+    kSiteDrain = 7, kSiteReconcile = 8, kSitePeersFree = 9, kSiteReceived = 10
 };
 
 struct KernelParams {
@@ -227,13 +235,14 @@ struct Unit {
     int32_t mpart;           // -1: the whole m range; else that range of m_part_rows rows (kTailMParts)
     int32_t khalf;           // -1: all k blocks; 0 / 1: that half of them (kTailSplitK)
     int32_t kpart;           // -1: all k blocks; else this range of them (kSplitReduce)
+    int32_t cpart;           // -1, or this CTA's k range of a tile reduced in the cluster (kClusterReduce)
     int32_t kb0, nkb;        // the unit's k blocks
     bool phantom;            // no such unit: loads out of bounds, computes zeros, stores nothing
 };
 
 __device__ __forceinline__ Unit unit_of(int64_t u, const KernelParams &p)
 {
-    Unit r{u, 0, 0, -1, -1, -1, 0, p.num_kb, u >= p.num_units};
+    Unit r{u, 0, 0, -1, -1, -1, -1, 0, p.num_kb, u >= p.num_units};
     if (r.phantom) return r;
     if (u >= p.tail_start) {
         const uint32_t v = static_cast<uint32_t>(u - p.tail_start), parts = static_cast<uint32_t>(p.split_parts);
@@ -309,6 +318,22 @@ struct Waiter {
         const uint64_t t0 = ptx::globaltimer();
         while (true) {
             if (ptx::mbar_try_wait(bar, parity)) return true;
+            if (*abort_flag) return false;
+            if (ptx::globaltimer() - t0 > limit) {
+                raise(site);
+                return false;
+            }
+        }
+    }
+
+    // wait() with a cluster-scope acquire (data other CTAs published with a
+    // cluster-scope release before arriving).
+    __device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity, int site) const
+    {
+        if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
+        const uint64_t t0 = ptx::globaltimer();
+        while (true) {
+            if (ptx::mbar_try_wait_cluster(bar, parity)) return true;
             if (*abort_flag) return false;
             if (ptx::globaltimer() - t0 > limit) {
                 raise(site);
@@ -533,17 +558,23 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     auto accempty_bar = [&](int b) { return bar0 + 8u * (kLoadedBars + kStages + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (kLoadedBars + kStages + 4);
     const uint32_t never_bar = bar0 + 8u * (kLoadedBars + kStages + 5);        // nothing ever arrives
+    // kClusterReduce: every other CTA of the cluster has announced that its ring
+    // is free (peers_free), and has published its partials of this CTA's columns
+    // (received)
+    const uint32_t peers_free_bar = bar0 + 8u * (kLoadedBars + kStages + 6);
+    const uint32_t received_bar = bar0 + 8u * (kLoadedBars + kStages + 7);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    constexpr uint32_t ctas = Cfg::kCtas;
-    const uint32_t rank = kGroup == 2 ? ptx::cluster_ctarank() : 0u;
-    const uint32_t pos = rank;                     // position within the pair
+    // CTAs per cluster: the pair (kGroup = 2); for single CTAs 1, or the k
+    // ranges of a tile when they are reduced in the cluster (kClusterReduce)
+    const uint32_t ctas = kGroup == 2 ? 2u : ptx::cluster_nctarank();
+    const uint32_t rank = ptx::cluster_ctarank();
+    const uint32_t pos = kGroup == 2 ? rank : 0u;  // position within the pair
     constexpr uint32_t lead = 0;                   // rank of the pair's even CTA
-    // One work slot per pair (per CTA for kGroup = 1), walking units slot,
-    // slot + nslots, ...
-    const int64_t nslots = gridDim.x / kGroup;
-    const int64_t slot0 = blockIdx.x / kGroup;
+    // One work slot per cluster, walking units slot, slot + nslots, ...
+    const int64_t nslots = gridDim.x / ctas;
+    const int64_t slot0 = blockIdx.x / ctas;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -556,6 +587,8 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         }
         ptx::mbar_init(drain_bar, 1);
         ptx::mbar_init(never_bar, 1);
+        ptx::mbar_init(peers_free_bar, ctas > 1 ? ctas - 1 : 1);
+        ptx::mbar_init(received_bar, ctas > 1 ? ctas - 1 : 1);
         *abort_flag = 0u;
         *issued_count = 0u;
         *producer_done = 0u;
@@ -572,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         ptx::tmem_relinquish_alloc_permit<kGroup>();
     }
     ptx::tc_fence_before_sync();
-    if constexpr (kGroup == 2)
+    if (kGroup == 2 || ctas > 1)
         ptx::cluster_sync();     // every CTA's barriers initialised before any remote arrive
     else
         __syncthreads();
@@ -587,8 +620,17 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     const Waiter w{abort_flag, abort_addr, rank, ctas, p.wait_limit_ns};
 
-    // The unit of step `it` of this CTA's slot (both CTAs of a pair run the same one).
-    auto slot_unit_at = [&](int64_t it) { return unit_of(slot_unit(slot0, it, nslots, p), p); };
+    // The unit of step `it` of this CTA's slot (both CTAs of a pair run the same
+    // one; the CTAs of a kClusterReduce cluster run its k ranges, by rank).
+    auto slot_unit_at = [&](int64_t it) {
+        Unit u = unit_of(slot_unit(slot0, it, nslots, p), p);
+        if (kGroup == 1 && p.tail_mode == kClusterReduce && !u.phantom) {
+            u.cpart = static_cast<int32_t>(rank);
+            u.kb0 = static_cast<int32_t>(rank) * p.kb_part;
+            u.nkb = p.kb_part;
+        }
+        return u;
+    };
     const int64_t iters = slot_iters(slot0, nslots, p);
     // m-part units cover a half or a quarter of the tile's m range
     const bool quarter_m = p.m_part_rows == kTileM / 4;
@@ -722,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued_any = false;
-            constexpr uint16_t all_mask = static_cast<uint16_t>((1u << ctas) - 1u);   // both CTAs of a pair
+            constexpr uint16_t all_mask = static_cast<uint16_t>((1u << kGroup) - 1u);   // both CTAs of a pair
             constexpr uint16_t pair_mask = all_mask;
             // m-part units: MMA N = m_part_rows
             constexpr uint32_t kIdescHalf = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 2, Kind::kFmt, Kind::kFmt);
@@ -984,6 +1026,91 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             const int32_t nw = static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB) + 32 * quarter;
             if (un.phantom) {
                 release_acc();   // nothing to store
+            } else if (un.cpart >= 0) {
+                // kClusterReduce: this CTA holds the partial sum of k range `rank` of
+                // the whole 128 x 256 tile.  Of the tile's four 64-column chunks of m,
+                // chunk c belongs to rank c % S, which adds the S partials of it in
+                // rank order and stores it.  This CTA's shared-memory ring is free
+                // once its MMAs are done; slot j of it receives the owned chunks'
+                // partials of the peer with the j-th rank other than this one (per
+                // chunk 128 rows n of 64 floats, 16-byte units swizzled by row).
+                // Only rows n < N are sent; the others are never stored.
+                const uint32_t S = ctas;
+                constexpr uint32_t kChunkBytes = Cfg::kRowsB * kEpiBoxM * 4;       // 32 KiB
+                const uint32_t slot_bytes = ((kTileM / kEpiBoxM + S - 1) / S) * kChunkBytes;
+                const uint32_t row_off = static_cast<uint32_t>(row * kEpiBoxM * 4);
+                const bool valid_n = nw + lane < p.N;
+                auto swz = [&](int c16) { return static_cast<uint32_t>((c16 ^ (row & 7)) << 4); };
+                if (warp == 2 && lane == 0) {
+                    // the ring was last written by TMA and read by the tensor cores
+                    ptx::fence_proxy_async_smem();
+                    for (uint32_t q = 0; q < S; ++q)
+                        if (q != rank) ptx::mbar_arrive_remote(ptx::mapa_shared(peers_free_bar, q));
+                }
+                bool fine = __all_sync(0xffffffffu, w.wait(peers_free_bar, 0u, kSitePeersFree));
+                if (fine) {
+                    for (uint32_t d = 1; d < S; ++d) {
+                        const uint32_t q = (rank + d) % S;
+                        const uint32_t j = rank < q ? rank : rank - 1;    // this CTA's slot in q's ring
+                        const uint32_t dst = ptx::mapa_shared(s_ring + j * slot_bytes + row_off, q);
+#pragma unroll 1
+                        for (uint32_t c = q, oc = 0; c < kTileM / kEpiBoxM; c += S, ++oc) {
+                            float v[64];
+                            load_chunk(t_row, static_cast<int>(c) * kEpiBoxM, v);
+                            if (valid_n) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    ptx::st_shared_cluster_v4(dst + oc * kChunkBytes + swz(i), v[4 * i], v[4 * i + 1],
+                                                              v[4 * i + 2], v[4 * i + 3]);
+                            }
+                        }
+                    }
+                    // every epilogue thread's stores are ordered before one
+                    // cluster-scope release per peer
+                    ptx::named_barrier_sync(1, kEpiWarps * 32);
+                    if (warp == 2 && static_cast<uint32_t>(lane) < S && static_cast<uint32_t>(lane) != rank)
+                        ptx::mbar_arrive_remote_release_cluster(ptx::mapa_shared(received_bar, lane));
+                    fine = __all_sync(0xffffffffu, w.wait_cluster(received_bar, 0u, kSiteReceived));
+                }
+                if (!fine) {
+                    release_acc();
+                    break;
+                }
+#pragma unroll 1
+                for (uint32_t c = rank, oc = 0; c < kTileM / kEpiBoxM; c += S, ++oc) {
+                    const int col = static_cast<int>(c) * kEpiBoxM;
+                    float v[64];
+                    // the S partials added in rank order
+#pragma unroll 1
+                    for (uint32_t q = 0; q < S; ++q) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            float t[32];
+                            if (q == rank) {
+                                uint32_t x[32];
+                                ptx::tmem_ld_32x32b_x32(t_row + col + 32 * h, x);
+                                ptx::tmem_ld_wait(x);
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(x[i]);
+                            } else {
+                                const uint32_t src =
+                                    s_ring + (q < rank ? q : q - 1) * slot_bytes + oc * kChunkBytes + row_off;
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const float4 f = ptx::ld_shared_v4_f32(src + swz(8 * h + i));
+                                    t[4 * i] = f.x;
+                                    t[4 * i + 1] = f.y;
+                                    t[4 * i + 2] = f.z;
+                                    t[4 * i + 3] = f.w;
+                                }
+                            }
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[32 * h + i] = q == 0 ? t[i] : v[32 * h + i] + t[i];
+                        }
+                    }
+                    if (c + S >= kTileM / kEpiBoxM) release_acc();   // this CTA's last read of its accumulator
+                    store_chunk(v, m0 + col, nw);
+                }
             } else if (un.kpart >= 0) {
                 // Split-reduce part: store this part's FP32 partial; the reduce
                 // kernel that follows sums the parts in order and stores C.  Only
@@ -1192,7 +1319,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     __syncwarp();                // .aligned barriers below need converged warps
     ptx::tc_fence_before_sync();
-    if constexpr (kGroup == 2)
+    if (kGroup == 2 || ctas > 1)
         ptx::cluster_sync();     // no CTA leaves while another may still touch its shared memory
     else
         __syncthreads();

@@ -49,13 +49,15 @@
  *     next launch.
  *   - Thread safety: every entry point may be called from several host
  *     threads, also on one stream (the legacy default stream included); the
- *     per-device state is guarded internally.  A buffer that a call has
- *     looked up stays allocated until that call's kernels are enqueued: a
- *     buffer replaced by a larger one is kept until
- *     gemm_release_workspace(), which waits for calls in progress on other
- *     threads.  On a thread's first call for a device, the library makes
- *     that device's primary context current on the thread (cudaSetDevice),
- *     so a thread that has made no CUDA call of its own can call it.
+ *     per-device state is guarded internally.  A call may enqueue several
+ *     kernels (a row copy, the GEMM, a reduce pass) that share the stream's
+ *     buffers; the calls on one stream hold a lock of that stream from their
+ *     first buffer lookup through their last launch, so two threads' calls
+ *     never interleave their kernels on it.  gemm_release_workspace() waits
+ *     for calls in progress on other threads.  On a thread's first call for
+ *     a device, the library makes that device's primary context current on
+ *     the thread (cudaSetDevice), so a thread that has made no CUDA call of
+ *     its own can call it.
  */
 #ifndef DENSE_GEMM_TN_H
 #define DENSE_GEMM_TN_H
@@ -218,6 +220,11 @@ gemm_status_t gemm_quantize_e4m3(const void *x, int x_type, int64_t rows, int64_
  * The array is shared by every call on a device and keeps the last call's
  * contents (each call overwrites all of the part it reads).  Calls that
  * overlap on the GPU -- on different streams, without ordering -- race on it.
+ * Calls on one stream do not, whatever host threads make them: each call
+ * enqueues its copy and its GEMM with no other call's launches between.
+ * The call never takes the paths that need the library's per-stream buffers
+ * (split-K partial sums in memory); small grids with a long K add up their
+ * k ranges inside a cluster of CTAs instead, which needs no buffer.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call
  * before any stream capture.
@@ -326,6 +333,17 @@ int gemm_debug_set_k_order(int mode);
  * or -1 for values outside -1 .. 7.
  */
 int gemm_debug_set_l2_hints(int mask);
+
+/*
+ * Test hook: how a grid of at most half the co-resident slots with a long K
+ * (at least 32 k blocks) is cut into k ranges.  0 (default): the library's
+ * choice; 1: always the split-reduce (FP32 partials in a per-stream buffer,
+ * summed by a second kernel); 2: wherever the tiles are single-CTA tiles,
+ * a cluster of 2 to 4 CTAs per tile that add their partials through
+ * distributed shared memory (no buffer, no second kernel).  Returns 0, or
+ * -1 for other values.
+ */
+int gemm_debug_set_long_k_mode(int mode);
 
 /* Description of the last GEMM kernel launch on the calling host thread
  * (tile shape, grid, co-resident cluster slots), for logs and tests

@@ -153,3 +153,12 @@ def test_k_order_hook_values():
     assert g.lib.gemm_debug_set_k_order(-1) == -1
     for v in (1, 2, 0):
         assert g.lib.gemm_debug_set_k_order(v) == 0
+
+
+def test_long_k_mode_hook_values():
+    assert g.lib.gemm_debug_set_long_k_mode(3) == -1
+    for v in (1, 2, 0):
+        assert g.lib.gemm_debug_set_long_k_mode(v) == 0
+    assert g.lib.gemm_debug_set_l2_hints(8) == -1
+    for v in (7, 0, -1):
+        assert g.lib.gemm_debug_set_l2_hints(v) == 0

@@ -636,3 +636,74 @@ def test_k_order_reversed_on_odd_waves(force_group, force_wide, k_order, cta_gro
     got8 = run_f8(M, N, K, qa, K, qb, K, sa, sb)
     c8, s8, _ = oracle.gemm_f8e4m3_tn_at(M, N, K, qa, K, qb, K, sa, sb, mi, ni)
     assert_tol(bf16_values(got8[ni, mi]), bf16_values(c8), s8, F8_TOL, "k order 2 e4m3")
+
+
+# ---------------------------------------------------------------- k ranges reduced in a cluster
+@pytest.fixture
+def long_k_mode():
+    import dense_gemm_tn_gb300 as g
+    yield g.gemm_debug_set_long_k_mode
+    g.gemm_debug_set_long_k_mode(0)
+
+
+@pytest.mark.parametrize("M,N,K,parts", [
+    (1024, 1024, 8192, 4),      # 32 one-CTA tiles: clusters of four k ranges
+    (4096, 512, 8192, 2),       # 64 tiles: clusters of two
+    (2000, 700, 4100, 3),       # ragged m, n, k (repacked): 8 x 6 = 48 tiles, clusters of three
+    (8192, 16, 8192, 4),        # skinny: 16 valid columns n of 128 per tile, only those exchanged
+    (300, 100, 16384, 4),       # 2 tiles: the split-reduce would take 8 ranges, a cluster 4
+])
+def test_cluster_reduce_long_k(force_group, long_k_mode, M, N, K, parts):
+    """Small grids with a long K on single CTAs, the k ranges of each tile in
+    one cluster that adds the FP32 partials through distributed shared
+    memory: +-1 inputs bit-exact against the oracle, Gaussian inputs within
+    tolerance and identical run to run, E4M3 with host and device scales."""
+    import dense_gemm_tn_gb300 as g
+    force_group(1)
+    long_k_mode(2)
+    A = synth.sign_fp16(M * K, 400 + M)
+    B = synth.sign_fp16(N * K, 401 + N)
+    got = run_f16(M, N, K, A, K, B, K)
+    rec = _launch_record()
+    if rec["slots"] == 152:
+        assert rec["tail_mode"] == 4 and rec["split_parts"] == parts and rec["ctas_per_cluster"] == parts, rec
+        assert rec["grid"] == parts * rec["tiles"], rec
+    if M * N <= 2_000_000:
+        Cref, _, _ = oracle.gemm_f16_tn(M, N, K, A, K, B, K)
+        assert np.array_equal(got, oracle.c_as_nm(Cref, M, N, M))
+    else:
+        mi, ni = sample_positions(M, N, 20000, seed=K + M)
+        c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
+        assert np.array_equal(got[ni, mi], c)
+    mi, ni = sample_positions(M, N, 20000, seed=K + N)
+    Ag = synth.gauss_fp16(M * K, 402 + M)
+    Bg = synth.gauss_fp16(N * K, 403 + N)
+    g1 = run_f16(M, N, K, Ag, K, Bg, K)
+    assert np.array_equal(g1, run_f16(M, N, K, Ag, K, Bg, K))
+    c, s, _ = oracle.gemm_f16_tn_at(M, N, K, Ag, K, Bg, K, mi, ni)
+    assert_tol(f16_values(g1[ni, mi]), f16_values(c), s, F16_TOL, "cluster reduce")
+    qa, sa = synth.gauss_e4m3(M * K, 404 + M)
+    qb, sb = synth.gauss_e4m3(N * K, 405 + N)
+    got8 = run_f8(M, N, K, qa, K, qb, K, sa, sb)
+    c8, s8, _ = oracle.gemm_f8e4m3_tn_at(M, N, K, qa, K, qb, K, sa, sb, mi, ni)
+    assert_tol(bf16_values(got8[ni, mi]), bf16_values(c8), s8, F8_TOL, "cluster reduce e4m3")
+    dA, dB = to_dev_u8(qa), to_dev_u8(qb)
+    scales = torch.tensor([sa, sb], dtype=torch.float32, device="cuda")
+    C = GuardedC(M, N, M)
+    g.gemm_f8e4m3_tn_dscale(M, N, K, dA, K, dB, K, C.ptr, M, scales.data_ptr(), scales.data_ptr() + 4)
+    g.gemm_poll_device_status()
+    assert np.array_equal(C.nm(), got8)
+
+
+def test_cluster_reduce_matches_split_reduce_on_pm1(force_group, long_k_mode):
+    """The two ways of adding up k ranges give the same bits on +-1 inputs."""
+    force_group(1)
+    M, N, K = 1024, 1024, 8192
+    A = synth.sign_fp16(M * K, 410)
+    B = synth.sign_fp16(N * K, 411)
+    long_k_mode(1)
+    a = run_f16(M, N, K, A, K, B, K)
+    assert _launch_record()["tail_mode"] in (3, 0, 1)
+    long_k_mode(2)
+    b = run_f16(M, N, K, A, K, B, K)
+    assert np.array_equal(a, b)
