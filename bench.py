@@ -405,84 +405,68 @@ def run_reference(args, w: synth.Workload, rank: int) -> None:
 BURST_REGION_MS = 1000.0     # a timed region shorter than this runs before the power cap settles
 
 
-class SpinClock:
-    """The SM clock measured on the GPU while a timed region runs: one thread
-    spins for a fixed number of its SM's clock cycles (torch.cuda._sleep) on a
-    second stream, beside the timed kernels (it needs no shared memory, so it
-    fits on an SM next to a GEMM CTA), and CUDA events time it; cycles over
-    time is the clock.  NVML's readings lag load changes of a few
-    milliseconds, which this does not."""
+class KernelClock:
+    """The SM clock the timed launches ran at, measured by the GEMM kernel
+    itself: with the library's clock probe set, the first thread of each
+    launch's first CTA adds its SM cycles (%clock64) and nanoseconds
+    (%globaltimer) from start to end to a device counter (three atomic adds
+    per launch).  NVML's readings lag load changes of a few milliseconds; a
+    kernel spinning beside the GEMM to time the clock slowed the GEMM down."""
 
-    def __init__(self, torch, dev):
-        self.torch = torch
-        self.side = torch.cuda.Stream(dev)
-        self.cycles = 0
-        self.ev = None
+    def __init__(self, torch, dev, g):
+        self.g = g
+        self.buf = torch.zeros(3, dtype=torch.int64, device=dev)
 
-    def start(self, expect_ms: float):
-        """Spin for about 80 % of a region expected to last `expect_ms` at any
-        clock of at least 1.2 GHz (so that the spin ends inside it)."""
-        torch = self.torch
-        self.cycles = int(max(expect_ms, 0.0) * 0.8 * 1.2e6)
-        if self.cycles < 200_000:          # under ~0.1 ms: too short to time
-            self.cycles = 0
-            return
-        self.ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-        with torch.cuda.stream(self.side):
-            self.ev[0].record(self.side)
-            torch.cuda._sleep(self.cycles)
-            self.ev[1].record(self.side)
+    def start(self):
+        self.buf.zero_()
+        self.g.lib.gemm_debug_set_clock_probe(self.buf.data_ptr())
+
+    def stop(self):
+        self.g.lib.gemm_debug_set_clock_probe(None)
 
     def mhz(self) -> float | None:
-        if not self.cycles:
-            return None
-        ms = self.ev[0].elapsed_time(self.ev[1])
-        return self.cycles / (ms * 1e3) if ms > 0 else None
+        cycles, ns, launches = (int(x) for x in self.buf.tolist())
+        return (cycles / ns * 1e3, launches) if ns > 0 else None
 
 
-def timed_loop(torch, dev, stream, call, sets: int, steps: int, warmup: int, sampler, dist=None, spin=None,
-               expect_ms: float | None = None):
+def timed_loop(torch, dev, stream, call, sets: int, steps: int, warmup: int, sampler, dist=None, probe=None):
     """W untimed calls, then exactly `steps` calls bracketed by a barrier and a
     device synchronisation on both sides, timed with CUDA events on the
     launching stream.  Events are recorded only before and after the loop: an
     event between two launches would end the overlap of a kernel's setup
     with the previous kernel's tail, which back-to-back calls otherwise get.
-    With `spin`, the SM clock is measured beside the loop (SpinClock); the
-    loop's length is expected from `expect_ms`, else from the warm-up's.
+    With `probe` (KernelClock), the timed launches measure their own SM clock.
     Returns (device ms, clock record of the timed region, any call failed)."""
-    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    w0.record(stream)
     for i in range(warmup):
         call(i % sets)
-    w1.record(stream)
     torch.cuda.synchronize(dev)
-    if expect_ms is None:
-        expect_ms = w0.elapsed_time(w1) / warmup * steps if warmup > 0 else 0.0
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if spin is not None:
-        spin.start(expect_ms)
+    if probe is not None:
+        probe.start()
     t0 = time.perf_counter()
     e0.record(stream)
     failed = 0
     for i in range(steps):
         failed |= call(i % sets)
     e1.record(stream)
+    if probe is not None:
+        probe.stop()
     torch.cuda.synchronize(dev)
     t1 = time.perf_counter()
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)
     clk = sampler.window(t0, t1)
-    gpu_mhz = spin.mhz() if spin is not None else None
-    if gpu_mhz is not None:
+    measured = probe.mhz() if probe is not None else None
+    if measured is not None:
         clk = dict(clk or {})
         clk["sm_mhz_nvml"] = clk.get("sm_mhz")
-        clk["sm_mhz"] = gpu_mhz
-        clk["sm_mhz_source"] = ("measured on the GPU: a one-thread spin of %d SM cycles on a second stream "
-                                "during the timed region, timed with CUDA events" % spin.cycles)
+        clk["sm_mhz"] = measured[0]
+        clk["sm_mhz_source"] = (f"measured by the timed GEMM launches themselves ({measured[1]} launches: SM cycles "
+                                "over globaltimer ns of each launch's first CTA)")
     return e0.elapsed_time(e1), clk, failed
 
 
@@ -603,7 +587,7 @@ def run_secondary(args, torch, g, dev, stream, sampler, peaks, sms) -> dict:
         raise RuntimeError(f"FP8 GEMM call failed: {g.last_error()}")
     g.gemm_poll_device_status(sh)
     total_ms, clk, failed = timed_loop(torch, dev, stream, call, sets, args.steps, args.warmup, sampler,
-                                       spin=SpinClock(torch, dev))
+                                       probe=KernelClock(torch, dev, g))
     if failed:
         raise RuntimeError(f"an FP8 GEMM call in the timed loop failed: {g.last_error()}")
     g.gemm_poll_device_status(sh)
@@ -742,7 +726,7 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
         # one C ABI call per step, its arguments bound beforehand: the loop's own
         # Python work per step stays well under a microsecond-scale GEMM's time
         total_ms, nvml_clk, failed = timed_loop(torch, dev, stream, one_call(), sets, args.steps, args.warmup,
-                                                sampler, dist, spin=SpinClock(torch, dev))
+                                                sampler, dist, probe=KernelClock(torch, dev, g))
         if failed:
             raise RuntimeError(f"a GEMM call in the timed loop failed: {g.last_error()}")
         kernel_ms = total_ms / args.steps      # one GEMM per step (after a repack where one is needed)
@@ -760,7 +744,7 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
     if args.sustained_s > 0 and roofline["bound"] == "tensor" and not pipeline:
         s_steps = max(args.steps, int(math.ceil(args.sustained_s * 1e3 / max(kernel_ms, 1e-3))))
         s_ms, s_clk, failed = timed_loop(torch, dev, stream, one_call(), sets, s_steps, 0, sampler, dist,
-                                         spin=SpinClock(torch, dev), expect_ms=s_steps * kernel_ms)
+                                         probe=KernelClock(torch, dev, g))
         if failed:
             raise RuntimeError(f"a GEMM call in the sustained loop failed: {g.last_error()}")
         g.gemm_poll_device_status(sh)

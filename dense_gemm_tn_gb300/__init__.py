@@ -45,7 +45,7 @@ EXPORTS = (
     "gemm_set_wait_limit_ns", "gemm_debug_inject_stall", "gemm_build_info",
     "gemm_f16_tn_noalloc", "gemm_debug_force_cta_group", "gemm_debug_force_wide_tiles", "gemm_debug_last_launch",
     "gemm_debug_set_raster_group", "gemm_debug_set_k_order", "gemm_debug_set_l2_hints",
-    "gemm_debug_set_long_k_mode",
+    "gemm_debug_set_long_k_mode", "gemm_debug_set_store_mode", "gemm_debug_set_clock_probe",
     "gemm_f8e4m3_tn_dscale", "gemm_quantize_e4m3", "gemm_f16_tn_softmax_stats",
 )
 
@@ -100,6 +100,10 @@ def _load() -> ctypes.CDLL:
     lib.gemm_debug_force_wide_tiles.restype = ctypes.c_int
     lib.gemm_debug_set_raster_group.argtypes = [ctypes.c_int]
     lib.gemm_debug_set_raster_group.restype = ctypes.c_int
+    lib.gemm_debug_set_clock_probe.argtypes = [ctypes.c_void_p]
+    lib.gemm_debug_set_clock_probe.restype = None
+    lib.gemm_debug_set_store_mode.argtypes = [ctypes.c_int]
+    lib.gemm_debug_set_store_mode.restype = ctypes.c_int
     lib.gemm_debug_set_long_k_mode.argtypes = [ctypes.c_int]
     lib.gemm_debug_set_long_k_mode.restype = ctypes.c_int
     lib.gemm_debug_set_l2_hints.argtypes = [ctypes.c_int]
@@ -241,6 +245,12 @@ def gemm_debug_set_raster_group(rows: int) -> None:
 def gemm_debug_set_k_order(mode: int) -> None:
     """0 the library's choice; 1 every tile walks K forward; 2 odd waves walk it backwards."""
     if _lib.gemm_debug_set_k_order(int(mode)) != 0:
+        raise ValueError("mode must be 0, 1 or 2")
+
+
+def gemm_debug_set_store_mode(mode: int) -> None:
+    """0 the library's choice; 1 TMA stores of C; 2 16-byte stores from registers."""
+    if _lib.gemm_debug_set_store_mode(int(mode)) != 0:
         raise ValueError("mode must be 0, 1 or 2")
 
 

@@ -22,6 +22,14 @@ __device__ __forceinline__ uint64_t globaltimer()
     return t;
 }
 
+// The SM's cycle counter.
+__device__ __forceinline__ uint64_t clock64()
+{
+    uint64_t c;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(c));
+    return c;
+}
+
 // ------------------------------------------------ programmatic dependent launch
 // Blocks until every grid this one depends on programmatically has completed
 // and its memory writes are visible; returns at once for an ordinary launch.
@@ -488,6 +496,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Global 16-byte store (the address is 16-byte aligned).
+__device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // Global 16-byte load that bypasses L1 (data another SM wrote in this launch).

@@ -34,6 +34,7 @@ constexpr int kGroupM = 8;                               // tile rows per raster
 // 1612 -> 1626 TFLOP/s; E4M3 3212 -> 3225.
 constexpr bool kAltKDefault = true;
 constexpr int kL2HintsDefault = 0;                       // L2 eviction hints: bits 1 A, 2 B, 4 C
+constexpr bool kDirectStoreSmallGrids = true;            // kFlagDirectStore on latency-bound small grids
 
 thread_local char t_last_error[512] = "";
 
@@ -91,6 +92,8 @@ std::atomic<int> g_force_cta_group{0};
 std::atomic<int> g_force_wide{0};       // 0: the cost estimate decides; 1: always; -1: never
 std::atomic<int> g_raster_group{0};     // tile rows per raster group; 0: kGroupM
 std::atomic<int> g_k_order{0};          // 0: the library's choice; 1: every tile forward; 2: odd waves reversed
+std::atomic<unsigned long long *> g_clock_probe{nullptr};   // gemm_debug_set_clock_probe
+std::atomic<int> g_store_mode{0};       // C stores: 0 the library's choice; 1 TMA; 2 direct 16-byte stores
 std::atomic<int> g_long_k{0};           // small grids with a long K: 0 the library's choice; 1 split-reduce; 2 cluster
 std::atomic<int> g_l2_hints{-1};        // -1: the library's choice; else bits 1 A, 2 B, 4 C (gemm_debug_set_l2_hints)
 // The last launch on this host thread, for gemm_debug_last_launch: the
@@ -552,6 +555,14 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
             prm.split_tickets = tickets;
         }
     }
+    {
+        // small grids (m-part units over the whole grid, or k ranges reduced in
+        // a cluster) store C straight from registers
+        const int sm = g_store_mode.load();
+        const bool small = (prm.tail_mode == tn::kTailMParts && prm.tail_start == 0) ||
+                           prm.tail_mode == tn::kClusterReduce;
+        if (sm == 2 || (sm == 0 && small && kDirectStoreSmallGrids)) prm.flags |= tn::kFlagDirectStore;
+    }
     if (prm.tail_mode == tn::kTailMParts) {
         prm.m_part_rows = Cfg::kTileMRows / prm.split_parts;
         // (a wide tile's parts are its halves, whose rows the A map's boxes already are)
@@ -775,6 +786,7 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         prm.flags |= (h & 1 ? tn::kFlagHintA : 0u) | (h & 2 ? tn::kFlagHintB : 0u) | (h & 4 ? tn::kFlagHintC : 0u);
     }
     prm.wait_limit_ns = g_wait_limit_ns.load();
+    prm.clock_probe = g_clock_probe.load();
 
     const ASource asrc{in_type, a_use, static_cast<uint64_t>(ka), static_cast<uint64_t>(M),
                        static_cast<uint64_t>(lda_use * esz), box_k, rows_a};
@@ -1051,6 +1063,15 @@ int gemm_debug_set_k_order(int mode)
 {
     if (mode < 0 || mode > 2) return -1;
     g_k_order.store(mode);
+    return 0;
+}
+
+void gemm_debug_set_clock_probe(unsigned long long *counters) { g_clock_probe.store(counters); }
+
+int gemm_debug_set_store_mode(int mode)
+{
+    if (mode < 0 || mode > 2) return -1;
+    g_store_mode.store(mode);
     return 0;
 }
 

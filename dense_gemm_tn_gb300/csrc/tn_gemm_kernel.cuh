@@ -154,6 +154,12 @@ constexpr uint32_t kFlagAltK = 32u;
 constexpr uint32_t kFlagHintA = 64u;
 constexpr uint32_t kFlagHintB = 128u;
 constexpr uint32_t kFlagHintC = 256u;
+// Rows m < m_tma of C are stored from registers with 16-byte global stores
+// (each epilogue thread owns a contiguous run of one column n) instead of
+// through the shared-memory staging and TMA stores: for small grids, whose
+// time is mostly latency, this takes the staging writes, the proxy fence and
+// the bulk-store wait off the end of the kernel.
+constexpr uint32_t kFlagDirectStore = 512u;
 
 // Status word of the current device; set (never cleared) by a kernel whose
 // bounded wait ran out: 4 (timeout) | site << 8.
@@ -202,6 +208,11 @@ struct KernelParams {
     int32_t stat_ctas;                  // tiles_n * CTAs per tile
     uint32_t flags;
     uint64_t wait_limit_ns;
+    // Optional (NULL: off): CTA 0's first thread adds the SM cycles and the
+    // nanoseconds from its start (after griddepcontrol.wait) to its exit to
+    // clock_probe[0] and [1], and 1 to [2]: [0] / [1] is the SM clock the
+    // launches ran at.
+    unsigned long long *clock_probe;
 };
 
 // ------------------------------------------------------------------ scheduler
@@ -617,6 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     // memory before that kernel has completed.  (The next kernel is let in by
     // the producer once it has issued its last load, below.)
     ptx::griddep_wait();
+    const bool probe_clock = p.clock_probe != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
+    const uint64_t probe_c0 = probe_clock ? ptx::clock64() : 0, probe_t0 = probe_clock ? ptx::globaltimer() : 0;
 
     const Waiter w{abort_flag, abort_addr, rank, ctas, p.wait_limit_ns};
 
@@ -920,6 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         const int row = 32 * quarter + lane;      // this thread's TMEM lane = output column within the CTA
         const bool tma_store = (p.flags & kFlagTmaStore) != 0;
         const bool hint_c = (p.flags & kFlagHintC) != 0;
+        const bool direct_c = (p.flags & kFlagDirectStore) != 0;
         const uint64_t pol_c = ptx::policy_evict_first();
         volatile uint32_t *second_flag = tmem_holder + 4;   // split-K: this CTA's half came second
         const float scale = p.scale_a_ptr ? __fmul_rn(__ldg(p.scale_a_ptr), __ldg(p.scale_b_ptr)) : p.scale;
@@ -969,7 +983,18 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             for (int j = 0; j < 32; ++j) packed[j] = Kind::pack(v[2 * j], v[2 * j + 1], scale);
         };
         auto store_packed = [&](const uint32_t (&packed)[32], int32_t mc, int32_t nw) {
-            if (tma_store && mc < p.m_tma) {
+            if (direct_c && mc < p.m_tma) {
+                // m_tma > 0: C's base and stride are 16-byte aligned, and m_tma a multiple of 8
+                const int64_t n = nw + lane;
+                if (n < p.N) {
+                    uint16_t *col = static_cast<uint16_t *>(p.c_ptr) + n * p.ldc + mc;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (mc + 8 * j + 8 <= p.m_tma)
+                            ptx::st_global_v4(col + 8 * j, packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                                              packed[4 * j + 3]);
+                }
+            } else if (tma_store && mc < p.m_tma) {
                 const uint32_t buf = s_epi + (ew * kEpiBufs + (chunk_ctr & 1u)) * kEpiBufBytes;
                 if (lane == 0) ptx::bulk_wait_group_read<kEpiBufs - 1>();   // buffer's previous store has read it
                 __syncwarp();
@@ -1327,6 +1352,11 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         __syncwarp();
         ptx::tc_fence_after_sync();
         ptx::tmem_dealloc<kGroup>(tmem_base, kTmemCols);
+    }
+    if (probe_clock) {
+        atomicAdd(&p.clock_probe[0], static_cast<unsigned long long>(ptx::clock64() - probe_c0));
+        atomicAdd(&p.clock_probe[1], static_cast<unsigned long long>(ptx::globaltimer() - probe_t0));
+        atomicAdd(&p.clock_probe[2], 1ull);
     }
 }
 

@@ -345,6 +345,27 @@ int gemm_debug_set_l2_hints(int mask);
  */
 int gemm_debug_set_long_k_mode(int mode);
 
+/*
+ * Test hook: how the kernel writes C where its base and stride allow
+ * 16-byte accesses.  0 (default): the library's choice (direct stores on
+ * small grids); 1: TMA stores through shared memory; 2: 16-byte global
+ * stores from registers.  Ragged rows are stored element by element either
+ * way.  Returns 0, or -1 for other values.
+ */
+int gemm_debug_set_store_mode(int mode);
+
+/*
+ * Measurement hook: while `counters` (a DEVICE pointer to 3 zeroed unsigned
+ * 64-bit words) is set, every GEMM kernel launched afterwards adds, from the
+ * first thread of its first CTA, the SM cycles (%clock64) and nanoseconds
+ * (%globaltimer) from its start to its end to counters[0] and counters[1],
+ * and 1 to counters[2] (three atomic adds per launch, nothing else).
+ * counters[0] / counters[1] is then the average SM clock, in GHz, that those
+ * launches ran at.  NULL turns it off (the default).  The caller owns the
+ * buffer and keeps it alive while launches that use it may run.
+ */
+void gemm_debug_set_clock_probe(unsigned long long *counters);
+
 /* Description of the last GEMM kernel launch on the calling host thread
  * (tile shape, grid, co-resident cluster slots), for logs and tests
  * (thread-local storage; "" before the first launch). */

@@ -383,11 +383,12 @@ def test_cuda_graph_capture_and_replay(force_wide, wide):
     (1, 2000, 700, 4100, 3),     # ragged m, n and k (repacked): 8 x 6 = 48 tiles, three ranges
     (2, 512, 2048, 16384, 4),    # 16 pair tiles of a long K
 ])
-def test_split_reduce_long_k(force_group, cta_group, M, N, K, parts):
+def test_split_reduce_long_k(force_group, long_k_mode, cta_group, M, N, K, parts):
     """Grids of at most half the slots with a long K: every tile is cut into k
     ranges whose FP32 partials a second kernel sums in order.  +-1 inputs are
     bit-exact, Gaussian inputs within tolerance and identical run to run."""
     force_group(cta_group)
+    long_k_mode(1)
     A = synth.sign_fp16(M * K, 95 + M)
     B = synth.sign_fp16(N * K, 96 + N)
     got = run_f16(M, N, K, A, K, B, K)
@@ -441,8 +442,9 @@ def test_split_reduce_on_wide_tiles(force_group, force_wide, M, N, K, parts):
     assert_tol(bf16_values(got8[ni, mi]), bf16_values(c), s, F8_TOL, "wide split-reduce e4m3")
 
 
-def test_split_reduce_e4m3_host_and_device_scales():
+def test_split_reduce_e4m3_host_and_device_scales(long_k_mode):
     import dense_gemm_tn_gb300 as g
+    long_k_mode(1)
     M, N, K = 1024, 1024, 8192
     qa, sa = synth.gauss_e4m3(M * K, 81)
     qb, sb = synth.gauss_e4m3(N * K, 82)
@@ -576,19 +578,31 @@ LAYOUTS = [(136, 136, 304, 0, 0, 0), (141, 137, 303, 0, 0, 0), (136, 136, 300, 1
            (130, 130, 300, 0, 3, 5)]      # lda, ldb, ldc, C offset, A offset, B offset (elements)
 
 
+@pytest.mark.parametrize("store", [1, 2])
 @pytest.mark.parametrize("cta_group,wide", [(1, -1), (2, -1), (2, 1)])
-def test_layouts_on_every_tile_shape(force_group, force_wide, cta_group, wide):
+def test_layouts_on_every_tile_shape(force_group, force_wide, cta_group, wide, store):
     """Padded, odd and unaligned leading dimensions and bases (TMA in place,
-    repacked operands, direct C stores) on each tile shape, FP16 and E4M3."""
+    repacked operands, element-wise C stores) on each tile shape, FP16 and
+    E4M3, with C written by TMA stores (store 1) or by 16-byte stores from
+    registers (store 2)."""
+    import dense_gemm_tn_gb300 as g
     force_group(cta_group)
     force_wide(wide)
+    g.gemm_debug_set_store_mode(store)
+    try:
+        _layouts_case(cta_group, wide, store)
+    finally:
+        g.gemm_debug_set_store_mode(0)
+
+
+def _layouts_case(cta_group, wide, store):
     M, N, K = 300, 700, 130
     A = synth.gauss_fp16(M * K, 31)
     B = synth.gauss_fp16(N * K, 32)
     A8, sa = synth.gauss_e4m3(M * K, 33)
     B8, sb = synth.gauss_e4m3(N * K, 34)
     for lda, ldb, ldc, c_off, a_off, b_off in LAYOUTS:
-        what = f"group {cta_group} wide {wide} ld {lda},{ldb},{ldc} offsets {c_off},{a_off},{b_off}"
+        what = f"group {cta_group} wide {wide} store {store} ld {lda},{ldb},{ldc} offsets {c_off},{a_off},{b_off}"
         check_f16_full(M, N, K, A, B, lda=lda, ldb=ldb, ldc=ldc, c_offset=c_off, a_offset=a_off, b_offset=b_off,
                        what=what)
         if cta_group == 2:
@@ -647,11 +661,12 @@ def long_k_mode():
 
 
 @pytest.mark.parametrize("M,N,K,parts", [
-    (1024, 1024, 8192, 4),      # 32 one-CTA tiles: clusters of four k ranges
-    (4096, 512, 8192, 2),       # 64 tiles: clusters of two
-    (2000, 700, 4100, 3),       # ragged m, n, k (repacked): 8 x 6 = 48 tiles, clusters of three
-    (8192, 16, 8192, 4),        # skinny: 16 valid columns n of 128 per tile, only those exchanged
-    (300, 100, 16384, 4),       # 2 tiles: the split-reduce would take 8 ranges, a cluster 4
+    (1024, 1024, 8192, (4,)),      # 32 one-CTA tiles: clusters of four k ranges
+    (4096, 512, 8192, (2,)),       # 64 tiles: clusters of two
+    (2000, 700, 4100, (2, 3)),     # ragged m, n, k (repacked): 8 x 6 = 48 tiles; clusters of three if 48 fit
+    (8192, 16, 8192, (4,)),        # skinny: 16 valid columns n of 128 per tile, only those exchanged
+    (300, 100, 16384, (4,)),       # 2 tiles: the split-reduce would take 8 ranges, a cluster 4
+    (1280, 1024, 8192, (2, 3)),    # 5 x 8 = 40 tiles: clusters of three where 40 of them fit at once
 ])
 def test_cluster_reduce_long_k(force_group, long_k_mode, M, N, K, parts):
     """Small grids with a long K on single CTAs, the k ranges of each tile in
@@ -666,8 +681,9 @@ def test_cluster_reduce_long_k(force_group, long_k_mode, M, N, K, parts):
     got = run_f16(M, N, K, A, K, B, K)
     rec = _launch_record()
     if rec["slots"] == 152:
-        assert rec["tail_mode"] == 4 and rec["split_parts"] == parts and rec["ctas_per_cluster"] == parts, rec
-        assert rec["grid"] == parts * rec["tiles"], rec
+        assert rec["tail_mode"] == 4 and rec["split_parts"] in parts, rec
+        assert rec["ctas_per_cluster"] == rec["split_parts"], rec
+        assert rec["grid"] == rec["split_parts"] * rec["tiles"], rec
     if M * N <= 2_000_000:
         Cref, _, _ = oracle.gemm_f16_tn(M, N, K, A, K, B, K)
         assert np.array_equal(got, oracle.c_as_nm(Cref, M, N, M))
@@ -707,3 +723,45 @@ def test_cluster_reduce_matches_split_reduce_on_pm1(force_group, long_k_mode):
     long_k_mode(2)
     b = run_f16(M, N, K, A, K, B, K)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("store", [1, 2])
+@pytest.mark.parametrize("M,N,K", [(8192, 8192, 256), (4100, 3000, 520), (1024, 1024, 128), (1001, 999, 8192)])
+def test_store_modes_at_scale(store, M, N, K):
+    """Both ways of writing C on the shapes the library runs as it chooses
+    (wide tiles, split-K tail, m-part units, k ranges reduced in a cluster):
+    +-1 inputs bit-exact against the oracle on sampled outputs."""
+    import dense_gemm_tn_gb300 as g
+    A = synth.sign_fp16(M * K, 500 + M)
+    B = synth.sign_fp16(N * K, 501 + N)
+    g.gemm_debug_set_store_mode(store)
+    try:
+        got = run_f16(M, N, K, A, K, B, K)
+    finally:
+        g.gemm_debug_set_store_mode(0)
+    mi, ni = sample_positions(M, N, 20000, seed=M + N + K)
+    c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
+    assert np.array_equal(got[ni, mi], c), _launch_record()
+
+
+def test_clock_probe_counts_launches_and_leaves_results_alone():
+    """The measurement hook: each launch adds its first CTA's SM cycles and
+    nanoseconds and one launch to the counters; results are unchanged."""
+    import dense_gemm_tn_gb300 as g
+    M, N, K = 2048, 2048, 1024
+    A = synth.sign_fp16(M * K, 600)
+    B = synth.sign_fp16(N * K, 601)
+    ref = run_f16(M, N, K, A, K, B, K)
+    counters = torch.zeros(3, dtype=torch.int64, device="cuda")
+    g.gemm_debug_set_clock_probe(counters.data_ptr())
+    try:
+        got = [run_f16(M, N, K, A, K, B, K) for _ in range(3)]
+    finally:
+        g.gemm_debug_set_clock_probe(None)
+    cycles, ns, launches = (int(x) for x in counters.tolist())
+    assert launches == 3 and cycles > 0 and ns > 0
+    assert 300.0 < cycles / ns * 1e3 < 2500.0, cycles / ns
+    for x in got:
+        assert np.array_equal(x, ref)
+    run_f16(M, N, K, A, K, B, K)                 # off again: the counters stay
+    assert int(counters[2].item()) == 3
