@@ -46,6 +46,7 @@ EXPORTS = (
     "gemm_f16_tn_noalloc", "gemm_debug_force_cta_group", "gemm_debug_force_wide_tiles", "gemm_debug_last_launch",
     "gemm_debug_set_raster_group", "gemm_debug_set_k_order", "gemm_debug_set_l2_hints",
     "gemm_debug_set_long_k_mode", "gemm_debug_set_store_mode", "gemm_debug_set_clock_probe",
+    "gemm_debug_set_repack_overlap",
     "gemm_f8e4m3_tn_dscale", "gemm_quantize_e4m3", "gemm_f16_tn_softmax_stats",
 )
 
@@ -100,6 +101,8 @@ def _load() -> ctypes.CDLL:
     lib.gemm_debug_force_wide_tiles.restype = ctypes.c_int
     lib.gemm_debug_set_raster_group.argtypes = [ctypes.c_int]
     lib.gemm_debug_set_raster_group.restype = ctypes.c_int
+    lib.gemm_debug_set_repack_overlap.argtypes = [ctypes.c_int]
+    lib.gemm_debug_set_repack_overlap.restype = ctypes.c_int
     lib.gemm_debug_set_clock_probe.argtypes = [ctypes.c_void_p]
     lib.gemm_debug_set_clock_probe.restype = None
     lib.gemm_debug_set_store_mode.argtypes = [ctypes.c_int]

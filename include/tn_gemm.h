@@ -36,6 +36,9 @@
  *     a multiple of 16 bytes are first copied into a library-owned, lazily
  *     grown device workspace with a padded stride, one per (device,
  *     stream), so calls on different streams may take this path at once.
+ *     For a large copied B, most of the copy runs on a second, library-owned
+ *     stream (one per stream, forked from and joined back into it with
+ *     events) beside a first GEMM over the columns already copied.
  *   - When the tiles of a launch end in a partly filled wave, each leftover
  *     tile is computed as two halves of its k range whose FP32 partial sums
  *     meet in a library-owned buffer kept per (device, stream), allocated on
@@ -365,6 +368,18 @@ int gemm_debug_set_store_mode(int mode);
  * buffer and keeps it alive while launches that use it may run.
  */
 void gemm_debug_set_clock_probe(unsigned long long *counters);
+
+/*
+ * Test hook: whether the copy of an unaligned B is split so that most of it
+ * runs beside the GEMM.  With the split, the columns n of about one wave of
+ * tiles are copied (with A) first and a first GEMM covers them, while a
+ * library-owned second stream copies the rest of B; a second GEMM covers the
+ * rest once that copy is done (an event).  0 (default): the library's
+ * choice (the rest is at least 16 MiB and spans at least two more waves'
+ * columns); 1: never; 2: wherever B is copied and more than one wave's
+ * columns exist.  Returns 0, or -1 for other values.
+ */
+int gemm_debug_set_repack_overlap(int mode);
 
 /* Description of the last GEMM kernel launch on the calling host thread
  * (tile shape, grid, co-resident cluster slots), for logs and tests

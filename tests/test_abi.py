@@ -168,3 +168,9 @@ def test_store_mode_hook_values():
     assert g.lib.gemm_debug_set_store_mode(3) == -1
     for v in (1, 2, 0):
         assert g.lib.gemm_debug_set_store_mode(v) == 0
+
+
+def test_repack_overlap_hook_values():
+    assert g.lib.gemm_debug_set_repack_overlap(3) == -1
+    for v in (1, 2, 0):
+        assert g.lib.gemm_debug_set_repack_overlap(v) == 0
