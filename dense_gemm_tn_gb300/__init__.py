@@ -251,6 +251,18 @@ def gemm_debug_set_k_order(mode: int) -> None:
         raise ValueError("mode must be 0, 1 or 2")
 
 
+def gemm_debug_set_clock_probe(counters) -> None:
+    """A device pointer (int) to 3 zeroed 64-bit words, or None: while set,
+    each GEMM launch adds its SM cycles, nanoseconds and 1 to them."""
+    _lib.gemm_debug_set_clock_probe(None if counters is None else ctypes.c_void_p(int(counters)))
+
+
+def gemm_debug_set_repack_overlap(mode: int) -> None:
+    """0 the library's choice; 1 never split B's copy; 2 split it wherever possible."""
+    if _lib.gemm_debug_set_repack_overlap(int(mode)) != 0:
+        raise ValueError("mode must be 0, 1 or 2")
+
+
 def gemm_debug_set_store_mode(mode: int) -> None:
     """0 the library's choice; 1 TMA stores of C; 2 16-byte stores from registers."""
     if _lib.gemm_debug_set_store_mode(int(mode)) != 0:
