@@ -34,10 +34,18 @@ constexpr int kGroupM = 8;                               // tile rows per raster
 // 1612 -> 1626 TFLOP/s; E4M3 3212 -> 3225.
 constexpr bool kAltKDefault = true;
 constexpr int kL2HintsDefault = 0;                       // L2 eviction hints: bits 1 A, 2 B, 4 C
-constexpr bool kDirectStoreSmallGrids = true;            // kFlagDirectStore on latency-bound small grids
-// Overlapping B's copy with a first GEMM pays once the rest of the copy is
-// this large (a copy of 16 MiB takes about 5 us of the call).
+// kFlagDirectStore on latency-bound small grids: measured on GB300 (CUDA-graph
+// replays, GPU time only) 1024 x 1024 x 128 4.19 -> 4.31 us, 512^3 6.07 ->
+// 6.16, 2048 x 1024 x 256 5.39 -> 5.79: the TMA stores stay.
+constexpr bool kDirectStoreSmallGrids = false;
+// Overlapping B's copy with a first GEMM, when the rest of the copy is this
+// large (a copy of 16 MiB takes about 5 us of the call).  Measured on GB300,
+// 3000 x 12289 x 4097 (FP16): 225.3 -> 232.5 us Gaussian, 195.2 -> 204.7 us
+// +-1: the copy's CTAs beside the first GEMM's slow that GEMM down more than
+// the copy costs on its own, so the library does not choose it
+// (kRepackOverlapDefault); gemm_debug_set_repack_overlap(2) forces it.
 constexpr int64_t kOverlapMinBytes = int64_t(16) << 20;
+constexpr bool kRepackOverlapDefault = false;
 
 thread_local char t_last_error[512] = "";
 
@@ -754,8 +762,8 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
             const int64_t rest_bytes = (N - first_cols * tile_n) * ldp * esz;
             const int mode = g_repack_overlap.load();
             const bool want = mode == 2 ? first_cols >= 1 && tiles_n > first_cols
-                                        : mode == 0 && first_cols >= 1 && tiles_n >= 3 * first_cols &&
-                                              rest_bytes >= kOverlapMinBytes;
+                                        : mode == 0 && kRepackOverlapDefault && first_cols >= 1 &&
+                                              tiles_n >= 3 * first_cols && rest_bytes >= kOverlapMinBytes;
             if (want) overlap_n1 = first_cols * tile_n;
         }
         if (overlap_n1 > 0) {

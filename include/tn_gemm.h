@@ -36,9 +36,8 @@
  *     a multiple of 16 bytes are first copied into a library-owned, lazily
  *     grown device workspace with a padded stride, one per (device,
  *     stream), so calls on different streams may take this path at once.
- *     For a large copied B, most of the copy runs on a second, library-owned
- *     stream (one per stream, forked from and joined back into it with
- *     events) beside a first GEMM over the columns already copied.
+ *     (A test hook, gemm_debug_set_repack_overlap, can instead run most of a
+ *     large B's copy on a second, library-owned stream beside a first GEMM.)
  *   - When the tiles of a launch end in a partly filled wave, each leftover
  *     tile is computed as two halves of its k range whose FP32 partial sums
  *     meet in a library-owned buffer kept per (device, stream), allocated on
@@ -350,9 +349,8 @@ int gemm_debug_set_long_k_mode(int mode);
 
 /*
  * Test hook: how the kernel writes C where its base and stride allow
- * 16-byte accesses.  0 (default): the library's choice (direct stores on
- * small grids); 1: TMA stores through shared memory; 2: 16-byte global
- * stores from registers.  Ragged rows are stored element by element either
+ * 16-byte accesses.  0 (default): the library's choice (TMA stores); 1: TMA
+ * stores through shared memory; 2: 16-byte global stores from registers.  Ragged rows are stored element by element either
  * way.  Returns 0, or -1 for other values.
  */
 int gemm_debug_set_store_mode(int mode);
@@ -375,9 +373,9 @@ void gemm_debug_set_clock_probe(unsigned long long *counters);
  * tiles are copied (with A) first and a first GEMM covers them, while a
  * library-owned second stream copies the rest of B; a second GEMM covers the
  * rest once that copy is done (an event).  0 (default): the library's
- * choice (the rest is at least 16 MiB and spans at least two more waves'
- * columns); 1: never; 2: wherever B is copied and more than one wave's
- * columns exist.  Returns 0, or -1 for other values.
+ * choice (currently never: measured slower on GB300, the copy's CTAs slow
+ * the first GEMM down); 1: never; 2: wherever B is copied and more than one
+ * wave's columns exist.  Returns 0, or -1 for other values.
  */
 int gemm_debug_set_repack_overlap(int mode);
 

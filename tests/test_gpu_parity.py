@@ -776,7 +776,7 @@ def repack_overlap():
 
 
 @pytest.mark.parametrize("M,N,K,ldb,mode", [
-    (3000, 12289, 4097, 4097, 0),    # the wide workload's shape: the library splits B's copy
+    (3000, 12289, 4097, 4097, 2),    # the wide workload's shape, split (the library does not choose it)
     (1000, 3000, 1001, 1001, 2),     # forced: two GEMMs over the columns n split at one wave's tiles
     (700, 2600, 520, 523, 2),        # K aligned, B's stride not: only B is copied
 ])
