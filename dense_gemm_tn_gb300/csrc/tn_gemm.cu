@@ -64,8 +64,9 @@ struct DeviceState {
     // per kernel, indexed [kind: f16, e4m3][1: one CTA, 2: CTA pairs, 3: CTA pairs with 256 x 512 tiles]
     bool smem_attr[2][4] = {};
     int max_clusters[2][4] = {};      // co-resident clusters of the kernel's own size (0 = not queried yet)
-    // co-resident clusters of S single CTAs (kClusterReduce), by kind and S (0 = not queried, -1 = none)
-    int cluster_slots[2][5] = {};
+    // co-resident clusters of S single CTAs or S CTA pairs (kClusterReduce), by kind, CTAs per tile and S
+    // (0 = not queried, -1 = none)
+    int cluster_slots[2][3][5] = {};
     // Split-K partial sums of the last wave, one buffer per stream (calls on
     // one stream are ordered, so they may share it): [tickets | partials].
     struct Split {
@@ -489,11 +490,12 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     }
     // A grid of at most half the slots with a long K leaves most SMs idle:
     // every tile is cut into S ranges of its k blocks (as many as the slots
-    // allow, at most 8, each at least 16 k blocks).  Single CTAs do it in a
-    // cluster of S <= 4 CTAs per tile, which add their partials up through
-    // distributed shared memory (kClusterReduce: no workspace, one kernel);
-    // otherwise the units store FP32 partials, and a reduce kernel sums them
-    // in order and stores C (kSplitReduce).
+    // allow, at most 8, each at least 16 k blocks).  Single CTAs and CTA pairs
+    // (not 256 x 512 tiles) do it in a cluster of S <= 4 CTAs or pairs per
+    // tile, which add their partials up through distributed shared memory
+    // (kClusterReduce: no workspace, one kernel); otherwise the units store
+    // FP32 partials, and a reduce kernel sums them in order and stores C
+    // (kSplitReduce).
     const int cap = slots;
     const bool stats = (prm.flags & tn::kFlagStats) != 0;
     const int long_k = g_long_k.load();
@@ -502,22 +504,22 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
         int S = cap / prm.num_tiles;
         if (S > 8) S = 8;
         if (S > prm.num_kb / 16) S = prm.num_kb / 16;
-        if (G == 1 && long_k != 1 && S >= 2 && (S <= 4 || long_k == 2 || !allow_alloc)) {
-            // clusters of Sc CTAs must fit Sc at a time into a GPC's SMs: the most
+        if (!W && long_k != 1 && S >= 2 && (S <= 4 || long_k == 2 || !allow_alloc)) {
+            // clusters of G * Sc CTAs must fit into a GPC's SMs together: the most
             // Sc for which one cluster per tile is co-resident
             for (int Sc = S < 4 ? S : 4; Sc >= 2 && cluster_parts == 1; --Sc) {
                 std::lock_guard<std::mutex> lock(g_mutex);
-                int &n = dev.cluster_slots[ki][Sc];
+                int &n = dev.cluster_slots[ki][G][Sc];
                 if (n == 0) {
                     cudaLaunchConfig_t qcfg = cfg;
                     cudaLaunchAttribute qattr[1];
                     qattr[0].id = cudaLaunchAttributeClusterDimension;
-                    qattr[0].val.clusterDim.x = Sc;
+                    qattr[0].val.clusterDim.x = G * Sc;
                     qattr[0].val.clusterDim.y = 1;
                     qattr[0].val.clusterDim.z = 1;
                     qcfg.attrs = qattr;
                     qcfg.numAttrs = 1;
-                    qcfg.gridDim = dim3(Sc * (dev.sms / Sc), 1, 1);
+                    qcfg.gridDim = dim3(G * Sc * (dev.sms / (G * Sc)), 1, 1);
                     if (cudaOccupancyMaxActiveClusters(&n, kernel, &qcfg) != cudaSuccess || n <= 0) {
                         cudaGetLastError();
                         n = -1;
@@ -539,7 +541,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     // (kClusterReduce: one tile per cluster of cluster_parts CTAs, never more --
     // a CTA's ring takes the other CTAs' partials once its own MMAs are done)
     const int clusters = cluster_parts > 1 ? prm.num_tiles : units0 < slots ? units0 : slots;
-    if (cluster_parts > 1) attr[0].val.clusterDim.x = cluster_parts;
+    if (cluster_parts > 1) attr[0].val.clusterDim.x = G * cluster_parts;
     // A programmatic dependent of the previous kernel on the stream: the
     // kernel waits for it (griddepcontrol.wait) before touching memory.
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -123,13 +123,13 @@ constexpr int32_t kTailSplitK = 2;   // two halves of the k blocks; partial sums
 // into split_parts ranges of its k blocks; each unit stores its FP32 partial,
 // and split_reduce_kernel (launched next) sums them and stores C.
 constexpr int32_t kSplitReduce = 3;
-// The same cut made inside a cluster of single CTAs: a cluster of S =
-// split_parts (2 to 4) CTAs per tile, CTA r computing k blocks
+// The same cut made inside a cluster: S = split_parts (2 to 4) single CTAs,
+// or S CTA pairs, per tile, CTA (or pair) r computing k blocks
 // [r kb_part, (r + 1) kb_part), one tile per cluster.  Of the tile's four
-// 64-column chunks of m, CTA r reduces and stores those with c % S == r: the
-// other CTAs write their FP32 partials of them into its shared memory
-// (distributed shared memory), and it adds the S partials in rank order.  No
-// workspace, no second kernel.
+// 64-column chunks of m, range r reduces and stores those with c % S == r:
+// the other ranges' CTAs write their FP32 partials of them into its shared
+// memory (distributed shared memory), and it adds the S partials in range
+// order.  No workspace, no second kernel.
 constexpr int32_t kClusterReduce = 4;
 
 constexpr uint32_t kFlagTmaStore = 1u;      // C rows m < m_tma are written with TMA stores
@@ -406,13 +406,15 @@ struct KindE4M3 {
 // producer issued every fill and each wait returns at once.
 template <int kStages, int kAtoms, int kCtas, class LoadedBar, class Contribution>
 __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar loaded_bar, Contribution contribution,
-                                                    uint32_t n_own, uint32_t count_addr, uint32_t done_addr)
+                                                    uint32_t n_own, uint32_t count_addr, uint32_t done_addr,
+                                                    uint32_t first)
 {
+    // the pair's CTAs: cluster ranks first .. first + kCtas - 1 (index q - first)
     uint32_t counts[kCtas];
     const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t q = 0; q < w.ctas; ++q) {
+    for (uint32_t q = first; q < first + kCtas; ++q) {
         if (q == w.rank) {
-            counts[q] = n_own;
+            counts[q - first] = n_own;
             continue;
         }
         bool stopped = true;
@@ -423,12 +425,12 @@ __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar l
                 break;
             }
         }
-        counts[q] = stopped ? ptx::ld_relaxed_cluster_u32(ptx::mapa_shared(count_addr, q)) : n_own;
+        counts[q - first] = stopped ? ptx::ld_relaxed_cluster_u32(ptx::mapa_shared(count_addr, q)) : n_own;
     }
     for (int s = 0; s < kStages; ++s) {
         uint32_t lo = 0xffffffffu, hi = 0;
         uint32_t passes[kCtas];
-        for (uint32_t q = 0; q < w.ctas; ++q) {
+        for (uint32_t q = 0; q < kCtas; ++q) {
             passes[q] = counts[q] / kStages + (static_cast<uint32_t>(s) < counts[q] % kStages ? 1u : 0u);
             lo = passes[q] < lo ? passes[q] : lo;
             hi = passes[q] > hi ? passes[q] : hi;
@@ -440,14 +442,14 @@ __device__ __forceinline__ void drain_cluster_loads(const Waiter &w, LoadedBar l
         }
         const uint32_t fill = (hi - 1) * kStages + s;   // index of the stage's last fill
         uint32_t sent = 0, total = 0;
-        for (uint32_t q = 0; q < w.ctas; ++q) {
+        for (uint32_t q = 0; q < kCtas; ++q) {
             const uint32_t c = contribution(q, fill);
             total += c;
             if (passes[q] == hi) sent += c;
         }
         // every atom of a fill carries the same share of its bytes, on its own barrier
         for (int t = 0; t < kAtoms; ++t) {
-            if (passes[w.rank] == hi) {
+            if (passes[w.rank - first] == hi) {
                 if (total > sent) ptx::mbar_complete_tx(loaded_bar(s, t), (total - sent) / kAtoms);
             } else {
                 ptx::mbar_arrive_expect_tx(loaded_bar(s, t), sent / kAtoms);
@@ -579,10 +581,12 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     const int lane = threadIdx.x & 31;
     // CTAs per cluster: the pair (kGroup = 2); for single CTAs 1, or the k
     // ranges of a tile when they are reduced in the cluster (kClusterReduce)
-    const uint32_t ctas = kGroup == 2 ? 2u : ptx::cluster_nctarank();
+    const uint32_t ctas = ptx::cluster_nctarank();
     const uint32_t rank = ptx::cluster_ctarank();
-    const uint32_t pos = kGroup == 2 ? rank : 0u;  // position within the pair
-    constexpr uint32_t lead = 0;                   // rank of the pair's even CTA
+    const uint32_t pos = rank % kGroup;            // position within the pair
+    const uint32_t lead = rank - pos;              // rank of the pair's even CTA
+    const uint32_t part_rank = rank / kGroup;      // the pair's (or CTA's) k range under kClusterReduce
+    const uint32_t parts = ctas / kGroup;          // k ranges per cluster (1 unless kClusterReduce)
     // One work slot per cluster, walking units slot, slot + nslots, ...
     const int64_t nslots = gridDim.x / ctas;
     const int64_t slot0 = blockIdx.x / ctas;
@@ -598,8 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         }
         ptx::mbar_init(drain_bar, 1);
         ptx::mbar_init(never_bar, 1);
-        ptx::mbar_init(peers_free_bar, ctas > 1 ? ctas - 1 : 1);
-        ptx::mbar_init(received_bar, ctas > 1 ? ctas - 1 : 1);
+        ptx::mbar_init(peers_free_bar, parts > 1 ? parts - 1 : 1);
+        ptx::mbar_init(received_bar, parts > 1 ? parts - 1 : 1);
         *abort_flag = 0u;
         *issued_count = 0u;
         *producer_done = 0u;
@@ -634,12 +638,12 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     const Waiter w{abort_flag, abort_addr, rank, ctas, p.wait_limit_ns};
 
     // The unit of step `it` of this CTA's slot (both CTAs of a pair run the same
-    // one; the CTAs of a kClusterReduce cluster run its k ranges, by rank).
+    // one; the CTAs or pairs of a kClusterReduce cluster run its k ranges).
     auto slot_unit_at = [&](int64_t it) {
         Unit u = unit_of(slot_unit(slot0, it, nslots, p), p);
-        if (kGroup == 1 && p.tail_mode == kClusterReduce && !u.phantom) {
-            u.cpart = static_cast<int32_t>(rank);
-            u.kb0 = static_cast<int32_t>(rank) * p.kb_part;
+        if (!kWide && p.tail_mode == kClusterReduce && !u.phantom) {
+            u.cpart = static_cast<int32_t>(part_rank);
+            u.kb0 = static_cast<int32_t>(part_rank) * p.kb_part;
             u.nkb = p.kb_part;
         }
         return u;
@@ -758,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                         return a_bytes(slot_unit_at(it)) + Cfg::kTileBBytes;
                     };
                     drain_cluster_loads<kStages, kAtoms, Cfg::kCtas>(w, loaded_bar, contribution, n_issued, count_addr,
-                                                                     done_addr);
+                                                                     done_addr, lead);
                 }
             } else {
                 // Let every issued load land before the CTA can exit.
@@ -777,8 +781,8 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued_any = false;
-            constexpr uint16_t all_mask = static_cast<uint16_t>((1u << kGroup) - 1u);   // both CTAs of a pair
-            constexpr uint16_t pair_mask = all_mask;
+            const uint16_t all_mask = static_cast<uint16_t>(((1u << kGroup) - 1u) << lead);   // both CTAs of the pair
+            const uint16_t pair_mask = all_mask;
             // m-part units: MMA N = m_part_rows
             constexpr uint32_t kIdescHalf = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 2, Kind::kFmt, Kind::kFmt);
             constexpr uint32_t kIdescQuarter = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 4, Kind::kFmt, Kind::kFmt);
@@ -1052,15 +1056,18 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             if (un.phantom) {
                 release_acc();   // nothing to store
             } else if (un.cpart >= 0) {
-                // kClusterReduce: this CTA holds the partial sum of k range `rank` of
-                // the whole 128 x 256 tile.  Of the tile's four 64-column chunks of m,
-                // chunk c belongs to rank c % S, which adds the S partials of it in
-                // rank order and stores it.  This CTA's shared-memory ring is free
-                // once its MMAs are done; slot j of it receives the owned chunks'
-                // partials of the peer with the j-th rank other than this one (per
-                // chunk 128 rows n of 64 floats, 16-byte units swizzled by row).
-                // Only rows n < N are sent; the others are never stored.
-                const uint32_t S = ctas;
+                // kClusterReduce: this CTA holds the partial sum of k range `me` of its
+                // 128 rows n of the tile (a CTA pair's tile has two such CTAs, one per
+                // position; the exchange runs between the CTAs of one position).  Of
+                // the tile's four 64-column chunks of m, chunk c belongs to range
+                // c % S, whose CTA adds the S partials of it in range order and stores
+                // it.  This CTA's shared-memory ring is free once its MMAs are done;
+                // slot j of it receives the owned chunks' partials of the range with
+                // the j-th index other than `me` (per chunk 128 rows n of 64 floats,
+                // 16-byte units swizzled by row).  Only rows n < N are sent; the
+                // others are never stored.
+                const uint32_t S = parts, me = part_rank;
+                auto peer = [&](uint32_t q) { return q * kGroup + pos; };   // the CTA of range q
                 constexpr uint32_t kChunkBytes = Cfg::kRowsB * kEpiBoxM * 4;       // 32 KiB
                 const uint32_t slot_bytes = ((kTileM / kEpiBoxM + S - 1) / S) * kChunkBytes;
                 const uint32_t row_off = static_cast<uint32_t>(row * kEpiBoxM * 4);
@@ -1070,14 +1077,14 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     // the ring was last written by TMA and read by the tensor cores
                     ptx::fence_proxy_async_smem();
                     for (uint32_t q = 0; q < S; ++q)
-                        if (q != rank) ptx::mbar_arrive_remote(ptx::mapa_shared(peers_free_bar, q));
+                        if (q != me) ptx::mbar_arrive_remote(ptx::mapa_shared(peers_free_bar, peer(q)));
                 }
                 bool fine = __all_sync(0xffffffffu, w.wait(peers_free_bar, 0u, kSitePeersFree));
                 if (fine) {
                     for (uint32_t d = 1; d < S; ++d) {
-                        const uint32_t q = (rank + d) % S;
-                        const uint32_t j = rank < q ? rank : rank - 1;    // this CTA's slot in q's ring
-                        const uint32_t dst = ptx::mapa_shared(s_ring + j * slot_bytes + row_off, q);
+                        const uint32_t q = (me + d) % S;
+                        const uint32_t j = me < q ? me : me - 1;    // this CTA's slot in q's ring
+                        const uint32_t dst = ptx::mapa_shared(s_ring + j * slot_bytes + row_off, peer(q));
 #pragma unroll 1
                         for (uint32_t c = q, oc = 0; c < kTileM / kEpiBoxM; c += S, ++oc) {
                             float v[64];
@@ -1093,8 +1100,8 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     // every epilogue thread's stores are ordered before one
                     // cluster-scope release per peer
                     ptx::named_barrier_sync(1, kEpiWarps * 32);
-                    if (warp == 2 && static_cast<uint32_t>(lane) < S && static_cast<uint32_t>(lane) != rank)
-                        ptx::mbar_arrive_remote_release_cluster(ptx::mapa_shared(received_bar, lane));
+                    if (warp == 2 && static_cast<uint32_t>(lane) < S && static_cast<uint32_t>(lane) != me)
+                        ptx::mbar_arrive_remote_release_cluster(ptx::mapa_shared(received_bar, peer(lane)));
                     fine = __all_sync(0xffffffffu, w.wait_cluster(received_bar, 0u, kSiteReceived));
                 }
                 if (!fine) {
@@ -1102,16 +1109,16 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     break;
                 }
 #pragma unroll 1
-                for (uint32_t c = rank, oc = 0; c < kTileM / kEpiBoxM; c += S, ++oc) {
+                for (uint32_t c = me, oc = 0; c < kTileM / kEpiBoxM; c += S, ++oc) {
                     const int col = static_cast<int>(c) * kEpiBoxM;
                     float v[64];
-                    // the S partials added in rank order
+                    // the S partials added in range order
 #pragma unroll 1
                     for (uint32_t q = 0; q < S; ++q) {
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             float t[32];
-                            if (q == rank) {
+                            if (q == me) {
                                 uint32_t x[32];
                                 ptx::tmem_ld_32x32b_x32(t_row + col + 32 * h, x);
                                 ptx::tmem_ld_wait(x);
@@ -1119,7 +1126,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                                 for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(x[i]);
                             } else {
                                 const uint32_t src =
-                                    s_ring + (q < rank ? q : q - 1) * slot_bytes + oc * kChunkBytes + row_off;
+                                    s_ring + (q < me ? q : q - 1) * slot_bytes + oc * kChunkBytes + row_off;
 #pragma unroll
                                 for (int i = 0; i < 8; ++i) {
                                     const float4 f = ptx::ld_shared_v4_f32(src + swz(8 * h + i));

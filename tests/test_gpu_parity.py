@@ -668,22 +668,28 @@ def long_k_mode():
     (300, 100, 16384, (4,)),       # 2 tiles: the split-reduce would take 8 ranges, a cluster 4
     (1280, 1024, 8192, (2, 3)),    # 5 x 8 = 40 tiles: clusters of three where 40 of them fit at once
 ])
-def test_cluster_reduce_long_k(force_group, long_k_mode, M, N, K, parts):
-    """Small grids with a long K on single CTAs, the k ranges of each tile in
-    one cluster that adds the FP32 partials through distributed shared
-    memory: +-1 inputs bit-exact against the oracle, Gaussian inputs within
-    tolerance and identical run to run, E4M3 with host and device scales."""
+@pytest.mark.parametrize("group", [1, 2])
+def test_cluster_reduce_long_k(force_group, long_k_mode, M, N, K, parts, group):
+    """Small grids with a long K, on single CTAs (group 1) or CTA pairs (group
+    2), the k ranges of each tile in one cluster that adds the FP32 partials
+    through distributed shared memory: +-1 inputs bit-exact against the
+    oracle, Gaussian inputs within tolerance and identical run to run, E4M3
+    with host and device scales."""
     import dense_gemm_tn_gb300 as g
-    force_group(1)
+    force_group(group)
     long_k_mode(2)
+    if group == 2:
+        parts = (2, 3, 4)      # as many ranges as pair clusters fit (up to 8 CTAs per cluster)
     A = synth.sign_fp16(M * K, 400 + M)
     B = synth.sign_fp16(N * K, 401 + N)
     got = run_f16(M, N, K, A, K, B, K)
     rec = _launch_record()
-    if rec["slots"] == 152:
-        assert rec["tail_mode"] == 4 and rec["split_parts"] in parts, rec
-        assert rec["ctas_per_cluster"] == rec["split_parts"], rec
-        assert rec["grid"] == rec["split_parts"] * rec["tiles"], rec
+    if rec["slots"] == 152 // group and rec["tail_mode"] == 4:
+        assert rec["split_parts"] in parts, rec
+        assert rec["ctas_per_cluster"] == group * rec["split_parts"], rec
+        assert rec["grid"] == group * rec["split_parts"] * rec["tiles"], rec
+    elif group == 1 and rec["slots"] == 152:
+        assert rec["tail_mode"] == 4, rec
     if M * N <= 2_000_000:
         Cref, _, _ = oracle.gemm_f16_tn(M, N, K, A, K, B, K)
         assert np.array_equal(got, oracle.c_as_nm(Cref, M, N, M))

@@ -16,11 +16,13 @@ pytestmark = pytest.mark.gpu
 CASES = [(1, 0, 1), (1, 0, 2), (2, 0, 1), (2, 0, 2), (2, 0, 3), (2, 1, 1), (2, 1, 2), (2, 1, 3)]
 
 
+@pytest.mark.parametrize("group", [1, 2])
 @pytest.mark.parametrize("mode", [1, 2, 3])
-def test_stalled_wait_in_a_reducing_cluster(mode):
-    """The k ranges of each tile in a cluster of four single CTAs: a stalled
-    MMA thread or producer (of cluster CTA 0 or 1) times out; the other CTAs,
-    waiting for their peers' partials, leave through the abort flag."""
+def test_stalled_wait_in_a_reducing_cluster(mode, group):
+    """The k ranges of each tile in a cluster of single CTAs or CTA pairs: a
+    stalled MMA thread or producer (of cluster CTA 0 or 1) times out; the
+    other CTAs, waiting for their peers' partials, leave through the abort
+    flag."""
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     import dense_gemm_tn_gb300 as g
@@ -29,7 +31,7 @@ def test_stalled_wait_in_a_reducing_cluster(mode):
     B = synth.gauss_fp16(N * K, 4)
     dA, dB = to_dev_u16(A), to_dev_u16(B)
     C = GuardedC(M, N, M)
-    g.gemm_debug_force_cta_group(1)
+    g.gemm_debug_force_cta_group(group)
     g.gemm_debug_set_long_k_mode(2)
     g.gemm_set_wait_limit_ns(50_000_000)
     g.gemm_debug_inject_stall(mode)
