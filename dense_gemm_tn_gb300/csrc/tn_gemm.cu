@@ -443,6 +443,71 @@ struct ASource {
     uint32_t box_k, rows;      // rows: A rows per CTA of a whole tile
 };
 
+// Co-resident slots of tn_gemm_kernel<Kind, G, W>: clusters of its own size
+// (one CTA, or a pair), queried once per device (the kernel's shared-memory
+// attribute is set first).  G * clusters_of: clusters of S pairs / CTAs.
+template <class Kind, int G, bool W>
+gemm_status_t kernel_slots(DeviceState &dev, int clusters_of, int *out)
+{
+    using Cfg = tn::TileCfg<G, W>;
+    auto kernel = tn::tn_gemm_kernel<Kind, G, W>;
+    const int ki = Kind::kF8 ? 1 : 0;
+    const int ks = W ? 3 : G;          // kernel index of the per-device caches
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!dev.smem_attr[ki][ks]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+        if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        dev.smem_attr[ki][ks] = true;
+    }
+    const int cl = G * clusters_of;
+    int &n = clusters_of == 1 ? dev.max_clusters[ki][ks] : dev.cluster_slots[ki][G][clusters_of];
+    if (n == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cl;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(tn::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(cl * (dev.sms / cl), 1, 1);
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+        if (e != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            // one slot per SM (pair) for the kernel's own size; no cluster reduce otherwise
+            n = clusters_of == 1 ? dev.sms / G : -1;
+        }
+    }
+    *out = n;
+    return GEMM_OK;
+}
+
+// The number of k ranges S (2 to 4) of a kClusterReduce launch of
+// tn_gemm_kernel<Kind, G> for num_tiles tiles of num_kb k blocks on `slots`
+// co-resident slots, or 1 for none: a grid of at most half the slots with a
+// long K, cut as the split-reduce would cut it (as many ranges as the slots
+// allow, at most 8, each at least 16 k blocks) when that is at most 4 (or
+// always, when the call may not allocate the split-reduce's buffer), with
+// one cluster of G * S CTAs per tile co-resident.
+template <class Kind, int G>
+int cluster_reduce_parts(DeviceState &dev, int64_t num_tiles, int64_t num_kb, int slots, bool allow_alloc,
+                         int long_k)
+{
+    if (long_k == 1 || 2 * num_tiles > slots || num_kb < 32) return 1;
+    int64_t S = slots / num_tiles;
+    if (S > 8) S = 8;
+    if (S > num_kb / 16) S = num_kb / 16;
+    if (S < 2 || !(S <= 4 || long_k == 2 || !allow_alloc)) return 1;
+    for (int Sc = S < 4 ? static_cast<int>(S) : 4; Sc >= 2; --Sc) {
+        int n = 0;
+        if (kernel_slots<Kind, G, false>(dev, Sc, &n) != GEMM_OK) return 1;
+        if (n >= num_tiles) return Sc;
+    }
+    return 1;
+}
+
 // Launches the persistent kernel: one CTA (or one CTA pair, a 2-CTA cluster)
 // per co-resident slot, each walking the tile raster with a stride of the
 // grid.  W: CTA pairs with 256 x 512 tiles (never with the softmax statistics
@@ -454,8 +519,6 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     static_assert(!W || G == 2, "256 x 512 tiles are CTA-pair tiles");
     using Cfg = tn::TileCfg<G, W>;
     auto kernel = tn::tn_gemm_kernel<Kind, G, W>;
-    const int ki = Kind::kF8 ? 1 : 0;
-    const int ks = W ? 3 : G;          // kernel index of the per-device caches
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -467,26 +530,10 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int slots;
+    int slots = 0;
     {
-        std::lock_guard<std::mutex> lock(g_mutex);
-        if (!dev.smem_attr[ki][ks]) {
-            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
-            if (e != cudaSuccess)
-                return fail(GEMM_ERR_CUDA, "%s: cudaFuncSetAttribute: %s", name, cudaGetErrorString(e));
-            dev.smem_attr[ki][ks] = true;
-        }
-        if (dev.max_clusters[ki][ks] == 0) {
-            int n = 0;
-            cfg.gridDim = dim3(G * (dev.sms / G), 1, 1);
-            cudaError_t e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
-            if (e != cudaSuccess || n <= 0) {
-                cudaGetLastError();
-                n = dev.sms / G;     // fall back to one slot per SM (pair)
-            }
-            dev.max_clusters[ki][ks] = n;
-        }
-        slots = dev.max_clusters[ki][ks];
+        gemm_status_t st = kernel_slots<Kind, G, W>(dev, 1, &slots);
+        if (st != GEMM_OK) return st;
     }
     // A grid of at most half the slots with a long K leaves most SMs idle:
     // every tile is cut into S ranges of its k blocks (as many as the slots
@@ -500,35 +547,12 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     const bool stats = (prm.flags & tn::kFlagStats) != 0;
     const int long_k = g_long_k.load();
     int reduce_parts = 1, cluster_parts = 1;
-    if (!stats && 2 * prm.num_tiles <= cap && prm.num_kb >= 32) {
+    if (!W && !stats) cluster_parts = cluster_reduce_parts<Kind, G>(dev, prm.num_tiles, prm.num_kb, cap, allow_alloc, long_k);
+    if (cluster_parts == 1 && !stats && allow_alloc && long_k != 2 && 2 * prm.num_tiles <= cap && prm.num_kb >= 32) {
         int S = cap / prm.num_tiles;
         if (S > 8) S = 8;
         if (S > prm.num_kb / 16) S = prm.num_kb / 16;
-        if (!W && long_k != 1 && S >= 2 && (S <= 4 || long_k == 2 || !allow_alloc)) {
-            // clusters of G * Sc CTAs must fit into a GPC's SMs together: the most
-            // Sc for which one cluster per tile is co-resident
-            for (int Sc = S < 4 ? S : 4; Sc >= 2 && cluster_parts == 1; --Sc) {
-                std::lock_guard<std::mutex> lock(g_mutex);
-                int &n = dev.cluster_slots[ki][G][Sc];
-                if (n == 0) {
-                    cudaLaunchConfig_t qcfg = cfg;
-                    cudaLaunchAttribute qattr[1];
-                    qattr[0].id = cudaLaunchAttributeClusterDimension;
-                    qattr[0].val.clusterDim.x = G * Sc;
-                    qattr[0].val.clusterDim.y = 1;
-                    qattr[0].val.clusterDim.z = 1;
-                    qcfg.attrs = qattr;
-                    qcfg.numAttrs = 1;
-                    qcfg.gridDim = dim3(G * Sc * (dev.sms / (G * Sc)), 1, 1);
-                    if (cudaOccupancyMaxActiveClusters(&n, kernel, &qcfg) != cudaSuccess || n <= 0) {
-                        cudaGetLastError();
-                        n = -1;
-                    }
-                }
-                if (n >= prm.num_tiles) cluster_parts = Sc;
-            }
-        }
-        if (cluster_parts == 1 && allow_alloc && long_k != 2 && S >= 2) reduce_parts = S;
+        if (S >= 2) reduce_parts = S;
     }
     // A grid of at most half the slots with a shorter K: every tile's m range
     // is cut into 2 or 4 parts (MMA N = 128 or 64).  Such a launch is bound by
@@ -703,6 +727,24 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     // kernel, 512^3 9.1 -> 6.0 us).
     int ctas = N > 128 ? 2 : 1;
     if (ctas == 2 && 2 * (((M + 255) / 256) * ((N + 255) / 256)) <= dev->sms / 2) ctas = 1;
+    // Small grids with a long K, their k ranges reduced in clusters: CTA pairs
+    // need two thirds of the operand bytes per MMA of single CTAs (64 against
+    // 96 bytes per SM cycle), so pairs run them where their clusters keep at
+    // least as many SMs busy.  Measured on GB300 (single CTAs -> pairs):
+    // 4096 x 512 x 8192 35.7 -> 31.7 us, 8192 x 256 x 8192 39.4 -> 35.2,
+    // 2048 x 1024 x 8192 33.0 -> 30.0; with fewer SMs busy, pairs lost
+    // (1024^2 x 8192 on 96 instead of 128 SMs: 24.4 -> 27.3).
+    if (ctas == 1 && N > 128 && !stats) {
+        const int long_k = g_long_k.load();
+        const int64_t rows = (M + tn::kTileM - 1) / tn::kTileM;
+        const int64_t t1 = rows * ((N + 127) / 128), t2 = rows * ((N + 255) / 256);
+        int s1 = 0, s2 = 0;
+        if ((st = kernel_slots<Kind, 1, false>(*dev, 1, &s1)) != GEMM_OK) return st;
+        if ((st = kernel_slots<Kind, 2, false>(*dev, 1, &s2)) != GEMM_OK) return st;
+        const int p1 = cluster_reduce_parts<Kind, 1>(*dev, t1, (K * esz + 127) / 128, s1, allow_alloc, long_k);
+        const int p2 = cluster_reduce_parts<Kind, 2>(*dev, t2, (K * esz + 255) / 256, s2, allow_alloc, long_k);
+        if (p1 > 1 && p2 > 1 && 2 * t2 * p2 >= t1 * p1) ctas = 2;
+    }
     if (const int forced = g_force_cta_group.load()) ctas = forced;
     const int cta_group = ctas >= 2 ? 2 : 1;
     const int64_t tiles_n = (N + 128 * cta_group - 1) / (128 * cta_group);

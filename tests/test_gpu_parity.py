@@ -846,3 +846,20 @@ def test_repack_overlap_graph_capture(repack_overlap):
         torch.cuda.synchronize()
         g.gemm_poll_device_status(s)
         assert torch.equal(C_graph.view(torch.int16), C_direct.view(torch.int16))
+
+
+def test_long_k_small_grid_tile_choice():
+    """Small grids with a long K: CTA pairs in k-range clusters where they keep
+    at least as many SMs busy as single CTAs would, single CTAs otherwise
+    (checked on a GB300's 152 / 76 slots); +-1 inputs bit-exact on samples."""
+    cases = [((4096, 512, 8192), 2), ((2048, 1024, 8192), 2), ((1024, 1024, 8192), 1), ((8192, 16, 8192), 1)]
+    for (M, N, K), want in cases:
+        A = synth.sign_fp16(M * K, 620 + M)
+        B = synth.sign_fp16(N * K, 621 + N)
+        got = run_f16(M, N, K, A, K, B, K)
+        rec = _launch_record()
+        if rec["slots"] in (76, 152) and rec["tail_mode"] == 4:
+            assert rec["ctas_per_cluster"] == want * rec["split_parts"], ((M, N, K), rec)
+        mi, ni = sample_positions(M, N, 10000, seed=M + N)
+        c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
+        assert np.array_equal(got[ni, mi], c), (M, N, K)
