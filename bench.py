@@ -403,6 +403,7 @@ def run_reference(args, w: synth.Workload, rank: int) -> None:
 
 # ---------------------------------------------------------------- our arm
 BURST_REGION_MS = 1000.0     # a timed region shorter than this runs before the power cap settles
+PROBE_MIN_MS = 0.05          # launches at least this long measure their own SM clock
 
 
 class KernelClock:
@@ -435,11 +436,19 @@ def timed_loop(torch, dev, stream, call, sets: int, steps: int, warmup: int, sam
     launching stream.  Events are recorded only before and after the loop: an
     event between two launches would end the overlap of a kernel's setup
     with the previous kernel's tail, which back-to-back calls otherwise get.
-    With `probe` (KernelClock), the timed launches measure their own SM clock.
+    With `probe` (KernelClock), the timed launches measure their own SM clock
+    when a launch lasts at least PROBE_MIN_MS (judged from the warm-up): its
+    atomic adds at the end of a launch of a few microseconds would delay the
+    next dependent launch.
     Returns (device ms, clock record of the timed region, any call failed)."""
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
     for i in range(warmup):
         call(i % sets)
+    w1.record(stream)
     torch.cuda.synchronize(dev)
+    if probe is not None and warmup > 0 and w0.elapsed_time(w1) / warmup < PROBE_MIN_MS:
+        probe = None
     if dist:
         dist.barrier()
     torch.cuda.synchronize(dev)

@@ -734,7 +734,7 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     // 4096 x 512 x 8192 35.7 -> 31.7 us, 8192 x 256 x 8192 39.4 -> 35.2,
     // 2048 x 1024 x 8192 33.0 -> 30.0; with fewer SMs busy, pairs lost
     // (1024^2 x 8192 on 96 instead of 128 SMs: 24.4 -> 27.3).
-    if (ctas == 1 && N > 128 && !stats) {
+    if (ctas == 1 && N > 128 && !stats && K * esz >= 32 * 256) {    // (at least 32 k blocks of a pair)
         const int long_k = g_long_k.load();
         const int64_t rows = (M + tn::kTileM - 1) / tn::kTileM;
         const int64_t t1 = rows * ((N + 127) / 128), t2 = rows * ((N + 255) / 256);
