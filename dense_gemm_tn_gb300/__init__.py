@@ -44,9 +44,8 @@ EXPORTS = (
     "gemm_poll_device_status", "gemm_release_workspace", "gemm_tile_coord",
     "gemm_set_wait_limit_ns", "gemm_debug_inject_stall", "gemm_build_info",
     "gemm_f16_tn_noalloc", "gemm_debug_force_cta_group", "gemm_debug_force_wide_tiles", "gemm_debug_last_launch",
-    "gemm_debug_set_raster_group", "gemm_debug_set_k_order", "gemm_debug_set_l2_hints",
-    "gemm_debug_set_long_k_mode", "gemm_debug_set_store_mode", "gemm_debug_set_clock_probe",
-    "gemm_debug_set_repack_overlap",
+    "gemm_debug_set_raster_group", "gemm_debug_set_k_order", "gemm_debug_set_long_k_mode",
+    "gemm_debug_set_clock_probe",
     "gemm_f8e4m3_tn_dscale", "gemm_quantize_e4m3", "gemm_f16_tn_softmax_stats",
 )
 
@@ -101,16 +100,10 @@ def _load() -> ctypes.CDLL:
     lib.gemm_debug_force_wide_tiles.restype = ctypes.c_int
     lib.gemm_debug_set_raster_group.argtypes = [ctypes.c_int]
     lib.gemm_debug_set_raster_group.restype = ctypes.c_int
-    lib.gemm_debug_set_repack_overlap.argtypes = [ctypes.c_int]
-    lib.gemm_debug_set_repack_overlap.restype = ctypes.c_int
     lib.gemm_debug_set_clock_probe.argtypes = [ctypes.c_void_p]
     lib.gemm_debug_set_clock_probe.restype = None
-    lib.gemm_debug_set_store_mode.argtypes = [ctypes.c_int]
-    lib.gemm_debug_set_store_mode.restype = ctypes.c_int
     lib.gemm_debug_set_long_k_mode.argtypes = [ctypes.c_int]
     lib.gemm_debug_set_long_k_mode.restype = ctypes.c_int
-    lib.gemm_debug_set_l2_hints.argtypes = [ctypes.c_int]
-    lib.gemm_debug_set_l2_hints.restype = ctypes.c_int
     lib.gemm_debug_set_k_order.argtypes = [ctypes.c_int]
     lib.gemm_debug_set_k_order.restype = ctypes.c_int
     lib.gemm_debug_last_launch.argtypes = []
@@ -257,28 +250,10 @@ def gemm_debug_set_clock_probe(counters) -> None:
     _lib.gemm_debug_set_clock_probe(None if counters is None else ctypes.c_void_p(int(counters)))
 
 
-def gemm_debug_set_repack_overlap(mode: int) -> None:
-    """0 the library's choice; 1 never split B's copy; 2 split it wherever possible."""
-    if _lib.gemm_debug_set_repack_overlap(int(mode)) != 0:
-        raise ValueError("mode must be 0, 1 or 2")
-
-
-def gemm_debug_set_store_mode(mode: int) -> None:
-    """0 the library's choice; 1 TMA stores of C; 2 16-byte stores from registers."""
-    if _lib.gemm_debug_set_store_mode(int(mode)) != 0:
-        raise ValueError("mode must be 0, 1 or 2")
-
-
 def gemm_debug_set_long_k_mode(mode: int) -> None:
     """0 the library's choice; 1 split-reduce (HBM partials); 2 reduce inside a cluster of single CTAs."""
     if _lib.gemm_debug_set_long_k_mode(int(mode)) != 0:
         raise ValueError("mode must be 0, 1 or 2")
-
-
-def gemm_debug_set_l2_hints(mask: int) -> None:
-    """-1 the library's choice; else bits 1 A evict_last, 2 B evict_first, 4 C evict_first."""
-    if _lib.gemm_debug_set_l2_hints(int(mask)) != 0:
-        raise ValueError("mask must be -1 .. 7")
 
 
 # ---------------------------------------------------------------- torch helpers

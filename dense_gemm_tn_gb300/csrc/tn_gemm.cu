@@ -33,19 +33,8 @@ constexpr int kGroupM = 8;                               // tile rows per raster
 // 512 tiles, FP16, under the power cap): DRAM reads 815 -> 684 MB per launch,
 // 1612 -> 1626 TFLOP/s; E4M3 3212 -> 3225.
 constexpr bool kAltKDefault = true;
-constexpr int kL2HintsDefault = 0;                       // L2 eviction hints: bits 1 A, 2 B, 4 C
-// kFlagDirectStore on latency-bound small grids: measured on GB300 (CUDA-graph
+
 // replays, GPU time only) 1024 x 1024 x 128 4.19 -> 4.31 us, 512^3 6.07 ->
-// 6.16, 2048 x 1024 x 256 5.39 -> 5.79: the TMA stores stay.
-constexpr bool kDirectStoreSmallGrids = false;
-// Overlapping B's copy with a first GEMM, when the rest of the copy is this
-// large (a copy of 16 MiB takes about 5 us of the call).  Measured on GB300,
-// 3000 x 12289 x 4097 (FP16): 225.3 -> 232.5 us Gaussian, 195.2 -> 204.7 us
-// +-1: the copy's CTAs beside the first GEMM's slow that GEMM down more than
-// the copy costs on its own, so the library does not choose it
-// (kRepackOverlapDefault); gemm_debug_set_repack_overlap(2) forces it.
-constexpr int64_t kOverlapMinBytes = int64_t(16) << 20;
-constexpr bool kRepackOverlapDefault = false;
 
 thread_local char t_last_error[512] = "";
 
@@ -61,9 +50,10 @@ gemm_status_t fail(gemm_status_t s, const char *fmt, ...)
 struct DeviceState {
     bool ready = false;
     int sms = 0, major = 0, minor = 0;
-    // per kernel, indexed [kind: f16, e4m3][1: one CTA, 2: CTA pairs, 3: CTA pairs with 256 x 512 tiles]
-    bool smem_attr[2][4] = {};
-    int max_clusters[2][4] = {};      // co-resident clusters of the kernel's own size (0 = not queried yet)
+    // per kernel, indexed [kind: f16, e4m3][1: one CTA, 2: CTA pairs, 3: CTA pairs with 256 x 512 tiles,
+    // 4 / 5: one CTA / CTA pairs in k-range clusters]
+    bool smem_attr[2][6] = {};
+    int max_clusters[2][6] = {};      // co-resident clusters of the kernel's own size (0 = not queried yet)
     // co-resident clusters of S single CTAs or S CTA pairs (kClusterReduce), by kind, CTAs per tile and S
     // (0 = not queried, -1 = none)
     int cluster_slots[2][3][5] = {};
@@ -87,15 +77,7 @@ struct DeviceState {
     // its last launch: a call is several launches (row copy, GEMM, reduce),
     // and two host threads' calls on one stream must not interleave them.
     std::unordered_map<cudaStream_t, std::unique_ptr<std::mutex>> stream_locks;
-    // A second stream per stream, with a fork and a join event, for the part
-    // of an operand copy that runs beside a GEMM (created on first need).
-    struct Side {
-        cudaStream_t stream = nullptr;
-        cudaEvent_t fork = nullptr, join = nullptr;
-    };
-    std::unordered_map<cudaStream_t, Side> side;
 };
-using SideStream = DeviceState::Side;
 
 std::mutex g_mutex;
 // Held shared by every call from its first workspace lookup through its last
@@ -113,10 +95,7 @@ std::atomic<int> g_force_wide{0};       // 0: the cost estimate decides; 1: alwa
 std::atomic<int> g_raster_group{0};     // tile rows per raster group; 0: kGroupM
 std::atomic<int> g_k_order{0};          // 0: the library's choice; 1: every tile forward; 2: odd waves reversed
 std::atomic<unsigned long long *> g_clock_probe{nullptr};   // gemm_debug_set_clock_probe
-std::atomic<int> g_repack_overlap{0};   // 0 the library's choice; 1 never; 2 wherever B is copied and tiles allow
-std::atomic<int> g_store_mode{0};       // C stores: 0 the library's choice; 1 TMA; 2 direct 16-byte stores
 std::atomic<int> g_long_k{0};           // small grids with a long K: 0 the library's choice; 1 split-reduce; 2 cluster
-std::atomic<int> g_l2_hints{-1};        // -1: the library's choice; else bits 1 A, 2 B, 4 C (gemm_debug_set_l2_hints)
 // The last launch on this host thread, for gemm_debug_last_launch: the
 // numbers are kept and formatted only when asked for (formatting every call
 // cost host time on the path of back-to-back small GEMMs).
@@ -247,27 +226,6 @@ std::unique_lock<std::mutex> lock_stream(DeviceState &d, cudaStream_t stream)
         m = slot.get();
     }
     return std::unique_lock<std::mutex>(*m);
-}
-
-// The side stream of `stream` (DeviceState::side), created on first need.
-gemm_status_t side_stream(DeviceState &d, cudaStream_t stream, SideStream **out)
-{
-    std::lock_guard<std::mutex> lock(g_mutex);
-    SideStream &sd = d.side[stream_key(stream)];
-    if (!sd.stream) {
-        cudaError_t e = cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming);
-        if (e != cudaSuccess) {
-            if (sd.join) cudaEventDestroy(sd.join);
-            if (sd.fork) cudaEventDestroy(sd.fork);
-            if (sd.stream) cudaStreamDestroy(sd.stream);
-            sd = SideStream{};
-            return fail(GEMM_ERR_CUDA, "creating a side stream: %s", cudaGetErrorString(e));
-        }
-    }
-    *out = &sd;
-    return GEMM_OK;
 }
 
 // The stream's split-K buffer with room for `tickets` ticket words and
@@ -443,16 +401,17 @@ struct ASource {
     uint32_t box_k, rows;      // rows: A rows per CTA of a whole tile
 };
 
-// Co-resident slots of tn_gemm_kernel<Kind, G, W>: clusters of its own size
-// (one CTA, or a pair), queried once per device (the kernel's shared-memory
-// attribute is set first).  G * clusters_of: clusters of S pairs / CTAs.
-template <class Kind, int G, bool W>
+// Co-resident slots of tn_gemm_kernel<Kind, G, W, C>: clusters of its own size
+// (one CTA, or a pair), or with C clusters of G * clusters_of CTAs (S pairs or
+// S single CTAs), queried once per device (the kernel's shared-memory
+// attribute is set first).
+template <class Kind, int G, bool W, bool C = false>
 gemm_status_t kernel_slots(DeviceState &dev, int clusters_of, int *out)
 {
     using Cfg = tn::TileCfg<G, W>;
-    auto kernel = tn::tn_gemm_kernel<Kind, G, W>;
+    auto kernel = tn::tn_gemm_kernel<Kind, G, W, C>;
     const int ki = Kind::kF8 ? 1 : 0;
-    const int ks = W ? 3 : G;          // kernel index of the per-device caches
+    const int ks = W ? 3 : C ? 3 + G : G;   // kernel index of the per-device caches
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!dev.smem_attr[ki][ks]) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
@@ -502,7 +461,7 @@ int cluster_reduce_parts(DeviceState &dev, int64_t num_tiles, int64_t num_kb, in
     if (S < 2 || !(S <= 4 || long_k == 2 || !allow_alloc)) return 1;
     for (int Sc = S < 4 ? static_cast<int>(S) : 4; Sc >= 2; --Sc) {
         int n = 0;
-        if (kernel_slots<Kind, G, false>(dev, Sc, &n) != GEMM_OK) return 1;
+        if (kernel_slots<Kind, G, false, true>(dev, Sc, &n) != GEMM_OK) return 1;
         if (n >= num_tiles) return Sc;
     }
     return 1;
@@ -518,7 +477,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
 {
     static_assert(!W || G == 2, "256 x 512 tiles are CTA-pair tiles");
     using Cfg = tn::TileCfg<G, W>;
-    auto kernel = tn::tn_gemm_kernel<Kind, G, W>;
+    void (*kernel)(tn::KernelParams) = tn::tn_gemm_kernel<Kind, G, W>;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -622,14 +581,6 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
             prm.split_tickets = tickets;
         }
     }
-    {
-        // small grids (m-part units over the whole grid, or k ranges reduced in
-        // a cluster) store C straight from registers
-        const int sm = g_store_mode.load();
-        const bool small = (prm.tail_mode == tn::kTailMParts && prm.tail_start == 0) ||
-                           prm.tail_mode == tn::kClusterReduce;
-        if (sm == 2 || (sm == 0 && small && kDirectStoreSmallGrids)) prm.flags |= tn::kFlagDirectStore;
-    }
     if (prm.tail_mode == tn::kTailMParts) {
         prm.m_part_rows = Cfg::kTileMRows / prm.split_parts;
         // (a wide tile's parts are its halves, whose rows the A map's boxes already are)
@@ -651,6 +602,9 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     t_rec.tail_start = prm.tail_start;
     t_rec.tail_mode = prm.tail_mode;
     t_rec.split_parts = prm.split_parts;
+    if constexpr (!W) {
+        if (cluster_parts > 1) kernel = tn::tn_gemm_kernel<Kind, G, false, true>;
+    }
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));
     if (prm.tail_mode == tn::kSplitReduce) {
@@ -780,8 +734,6 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     // measured 13 % slower on 3000 x 12289 x 4097.
     const void *a_use = A, *b_use = B;
     int64_t lda_use = lda, ldb_use = ldb, ka = K, kb = K;
-    int64_t overlap_n1 = 0;              // > 0: two GEMMs, columns n < overlap_n1 first (see below)
-    cudaEvent_t overlap_join = nullptr;
     const bool k_aligned = (K * esz) % 16 == 0;
     const bool repack_a = !k_aligned || (lda * esz) % 16 != 0 || reinterpret_cast<uintptr_t>(A) % 16 != 0;
     const bool repack_b = !k_aligned || (ldb * esz) % 16 != 0 || reinterpret_cast<uintptr_t>(B) % 16 != 0;
@@ -797,40 +749,9 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
             return st;
         using T = typename std::conditional<esz == 2, uint16_t, uint8_t>::type;
         tn::RepackJob<T> ja{static_cast<const T *>(A), lda, reinterpret_cast<T *>(ws), ldp, repack_a ? M : 0, K};
-        // B's copy overlapped with a first GEMM: the columns n of the first wave's
-        // tiles are copied (with A) before it; the rest of B on the stream's side
-        // stream, beside that GEMM (overlap_n1 > 0, see below).
-        if (repack_b && allow_alloc && !stats) {
-            const int64_t tile_n = 128 * cta_group;
-            const int64_t first_cols = (dev->sms / cta_group) / tiles_m;   // tile columns of about one wave
-            const int64_t rest_bytes = (N - first_cols * tile_n) * ldp * esz;
-            const int mode = g_repack_overlap.load();
-            const bool want = mode == 2 ? first_cols >= 1 && tiles_n > first_cols
-                                        : mode == 0 && kRepackOverlapDefault && first_cols >= 1 &&
-                                              tiles_n >= 3 * first_cols && rest_bytes >= kOverlapMinBytes;
-            if (want) overlap_n1 = first_cols * tile_n;
-        }
-        if (overlap_n1 > 0) {
-            SideStream *side = nullptr;
-            if ((st = side_stream(*dev, stream, &side)) != GEMM_OK) return st;
-            tn::RepackJob<T> jb_rest{static_cast<const T *>(B) + overlap_n1 * ldb, ldb,
-                                     reinterpret_cast<T *>(ws + bytes_a) + overlap_n1 * ldp, ldp, N - overlap_n1, K};
-            const tn::RepackJob<T> none{nullptr, ldb, nullptr, ldp, 0, K};
-            cudaError_t e = cudaEventRecord(side->fork, stream);          // after everything before on the stream
-            if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
-            if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: side stream fork: %s", name, cudaGetErrorString(e));
-            launch_repack<T>(jb_rest, none, side->stream);
-            if ((e = cudaEventRecord(side->join, side->stream)) != cudaSuccess)
-                return fail(GEMM_ERR_CUDA, "%s: side stream join: %s", name, cudaGetErrorString(e));
-            tn::RepackJob<T> jb_first{static_cast<const T *>(B), ldb, reinterpret_cast<T *>(ws + bytes_a), ldp,
-                                      overlap_n1, K};
-            launch_repack<T>(ja, jb_first, stream);
-            overlap_join = side->join;
-        } else {
-            tn::RepackJob<T> jb{static_cast<const T *>(B), ldb, reinterpret_cast<T *>(ws + bytes_a), ldp,
-                                repack_b ? N : 0, K};
-            launch_repack<T>(ja, jb, stream);       // one launch for both operands
-        }
+        tn::RepackJob<T> jb{static_cast<const T *>(B), ldb, reinterpret_cast<T *>(ws + bytes_a), ldp,
+                            repack_b ? N : 0, K};
+        launch_repack<T>(ja, jb, stream);       // one launch for both operands
         if (repack_a) {
             a_use = ws;
             lda_use = ka = ldp;
@@ -843,14 +764,6 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: repack launch: %s", name, cudaGetErrorString(e));
     }
 
-    // One GEMM launch over the columns n of C in [n0, n0 + Np): B's rows from
-    // n0 on, C's columns from n0 on.
-    auto issue = [&](int64_t n0, int64_t Np) -> gemm_status_t {
-    gemm_status_t st;
-    const int64_t tiles_n = (Np + 128 * cta_group - 1) / (128 * cta_group);
-    const void *b_p = static_cast<const uint8_t *>(b_use) + n0 * ldb_use * esz;
-    void *C_p = static_cast<uint16_t *>(C) + n0 * ldc;
-    const int64_t N = Np;
     tn::KernelParams prm;
     memset(&prm, 0, sizeof(prm));
     const CUtensorMapDataType in_type = Kind::kF8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -859,17 +772,17 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     const uint32_t rows_a = static_cast<uint32_t>(tn::kTileM / cta_group);
     if ((st = encode_2d(&prm.tmap_a, in_type, a_use, ka, M, lda_use * esz, box_k, rows_a, "A")) != GEMM_OK)
         return st;
-    if ((st = encode_2d(&prm.tmap_b, in_type, b_p, kb, N, ldb_use * esz, box_k, 128, "B")) != GEMM_OK)
+    if ((st = encode_2d(&prm.tmap_b, in_type, b_use, kb, N, ldb_use * esz, box_k, 128, "B")) != GEMM_OK)
         return st;
     // TMA stores cover rows m < M rounded down to 8 (16 bytes); the kernel
     // writes the ragged rest, or all of C when C's base or stride is unaligned.
     const int64_t m_tma = M & ~int64_t(7);
-    const bool tma_c = (ldc * 2) % 16 == 0 && reinterpret_cast<uintptr_t>(C_p) % 16 == 0 && m_tma > 0;
+    const bool tma_c = (ldc * 2) % 16 == 0 && reinterpret_cast<uintptr_t>(C) % 16 == 0 && m_tma > 0;
     if (tma_c &&
-        (st = encode_2d(&prm.tmap_c, out_type, C_p, m_tma, N, ldc * 2, tn::kEpiBoxM, tn::kEpiBoxN, "C")) != GEMM_OK)
+        (st = encode_2d(&prm.tmap_c, out_type, C, m_tma, N, ldc * 2, tn::kEpiBoxM, tn::kEpiBoxN, "C")) != GEMM_OK)
         return st;
     prm.m_tma = tma_c ? static_cast<int32_t>(m_tma) : 0;
-    prm.c_ptr = C_p;
+    prm.c_ptr = C;
     prm.ldc = ldc;
     prm.M = static_cast<int32_t>(M);
     prm.N = static_cast<int32_t>(N);
@@ -907,9 +820,6 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     {
         const int ko = g_k_order.load();
         if (ko == 2 || (ko == 0 && kAltKDefault)) prm.flags |= tn::kFlagAltK;
-        int h = g_l2_hints.load();
-        if (h < 0) h = kL2HintsDefault;
-        prm.flags |= (h & 1 ? tn::kFlagHintA : 0u) | (h & 2 ? tn::kFlagHintB : 0u) | (h & 4 ? tn::kFlagHintC : 0u);
     }
     prm.wait_limit_ns = g_wait_limit_ns.load();
     prm.clock_probe = g_clock_probe.load();
@@ -919,15 +829,6 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
     if (wide) return launch<Kind, 2, true>(name, prm, *dev, allow_alloc, asrc, stream);
     if (cta_group == 2) return launch<Kind, 2>(name, prm, *dev, allow_alloc, asrc, stream);
     return launch<Kind, 1>(name, prm, *dev, allow_alloc, asrc, stream);
-    };
-
-    if (overlap_n1 == 0) return issue(0, N);
-    // The first GEMM runs while the side stream copies the rest of B; the
-    // second waits for that copy (an event, no device-side wait).
-    if ((st = issue(0, overlap_n1)) != GEMM_OK) return st;
-    cudaError_t e = cudaStreamWaitEvent(stream, overlap_join, 0);
-    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: side stream join: %s", name, cudaGetErrorString(e));
-    return issue(overlap_n1, N - overlap_n1);
 }
 
 // Per-tensor E4M3 quantisation (quant_e4m3_kernel.cuh): the maximum-finding
@@ -1158,12 +1059,7 @@ void gemm_release_workspace(void)
     for (auto &kv : d.stats)
         if (kv.second.ptr) cudaFree(kv.second.ptr);
     d.stats.clear();
-    for (auto &kv : d.side) {
-        cudaEventDestroy(kv.second.join);
-        cudaEventDestroy(kv.second.fork);
-        cudaStreamDestroy(kv.second.stream);
-    }
-    d.side.clear();
+
 }
 
 int gemm_tile_coord(int64_t tiles_m, int64_t tiles_n, int64_t group, int64_t id, int64_t *tile_m, int64_t *tile_n)
@@ -1209,31 +1105,10 @@ int gemm_debug_set_k_order(int mode)
 
 void gemm_debug_set_clock_probe(unsigned long long *counters) { g_clock_probe.store(counters); }
 
-int gemm_debug_set_repack_overlap(int mode)
-{
-    if (mode < 0 || mode > 2) return -1;
-    g_repack_overlap.store(mode);
-    return 0;
-}
-
-int gemm_debug_set_store_mode(int mode)
-{
-    if (mode < 0 || mode > 2) return -1;
-    g_store_mode.store(mode);
-    return 0;
-}
-
 int gemm_debug_set_long_k_mode(int mode)
 {
     if (mode < 0 || mode > 2) return -1;
     g_long_k.store(mode);
-    return 0;
-}
-
-int gemm_debug_set_l2_hints(int mask)
-{
-    if (mask < -1 || mask > 7) return -1;
-    g_l2_hints.store(mask);
     return 0;
 }
 

@@ -148,18 +148,6 @@ constexpr uint32_t kFlagStats = 16u;
 // previous wave read last, which are the likeliest to be still in L2.  The
 // order of the FP32 sums changes, not their terms.
 constexpr uint32_t kFlagAltK = 32u;
-// L2 eviction priorities: A loads evict_last (the A panels of a raster group
-// are read again by the group's later waves), B loads evict_first (a wave's
-// B panels are not), C stores evict_first (C is not read back).
-constexpr uint32_t kFlagHintA = 64u;
-constexpr uint32_t kFlagHintB = 128u;
-constexpr uint32_t kFlagHintC = 256u;
-// Rows m < m_tma of C are stored from registers with 16-byte global stores
-// (each epilogue thread owns a contiguous run of one column n) instead of
-// through the shared-memory staging and TMA stores: for small grids, whose
-// time is mostly latency, this takes the staging writes, the proxy fence and
-// the bulk-store wait off the end of the kernel.
-constexpr uint32_t kFlagDirectStore = 512u;
 
 // Status word of the current device; set (never cleared) by a kernel whose
 // bounded wait ran out: 4 (timeout) | site << 8.
@@ -538,9 +526,12 @@ __device__ __forceinline__ float2 stat_warp_reduce32(const float (&x)[32], int l
 }
 
 // ------------------------------------------------------------------ kernel
-template <class Kind, int kGroup, bool kWide = false>
+// kCluster: the kClusterReduce variant (launched in clusters of S single CTAs
+// or S CTA pairs); the other variants carry none of its code.
+template <class Kind, int kGroup, bool kWide = false, bool kCluster = false>
 __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_constant__ KernelParams p)
 {
+    static_assert(!(kWide && kCluster), "256 x 512 tiles are not reduced in clusters");
     using Cfg = TileCfg<kGroup, kWide>;
     constexpr int kStages = Cfg::kStages;
     constexpr int kBlockKElems = kBlockKBytes / Kind::kElemBytes;   // K elements per atom
@@ -579,10 +570,10 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // CTAs per cluster: the pair (kGroup = 2); for single CTAs 1, or the k
-    // ranges of a tile when they are reduced in the cluster (kClusterReduce)
-    const uint32_t ctas = ptx::cluster_nctarank();
-    const uint32_t rank = ptx::cluster_ctarank();
+    // CTAs per cluster: the pair (kGroup = 2), or one CTA; kCluster: those of
+    // the k ranges of a tile reduced in the cluster (kClusterReduce)
+    const uint32_t ctas = kCluster ? ptx::cluster_nctarank() : static_cast<uint32_t>(kGroup);
+    const uint32_t rank = kGroup == 2 || kCluster ? ptx::cluster_ctarank() : 0u;
     const uint32_t pos = rank % kGroup;            // position within the pair
     const uint32_t lead = rank - pos;              // rank of the pair's even CTA
     const uint32_t part_rank = rank / kGroup;      // the pair's (or CTA's) k range under kClusterReduce
@@ -602,8 +593,10 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         }
         ptx::mbar_init(drain_bar, 1);
         ptx::mbar_init(never_bar, 1);
-        ptx::mbar_init(peers_free_bar, parts > 1 ? parts - 1 : 1);
-        ptx::mbar_init(received_bar, parts > 1 ? parts - 1 : 1);
+        if (kCluster) {
+            ptx::mbar_init(peers_free_bar, parts - 1);
+            ptx::mbar_init(received_bar, parts - 1);
+        }
         *abort_flag = 0u;
         *issued_count = 0u;
         *producer_done = 0u;
@@ -620,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         ptx::tmem_relinquish_alloc_permit<kGroup>();
     }
     ptx::tc_fence_before_sync();
-    if (kGroup == 2 || ctas > 1)
+    if constexpr (kGroup == 2 || kCluster)
         ptx::cluster_sync();     // every CTA's barriers initialised before any remote arrive
     else
         __syncthreads();
@@ -641,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     // one; the CTAs or pairs of a kClusterReduce cluster run its k ranges).
     auto slot_unit_at = [&](int64_t it) {
         Unit u = unit_of(slot_unit(slot0, it, nslots, p), p);
-        if (!kWide && p.tail_mode == kClusterReduce && !u.phantom) {
+        if (kCluster && !u.phantom) {
             u.cpart = static_cast<int32_t>(part_rank);
             u.kb0 = static_cast<int32_t>(part_rank) * p.kb_part;
             u.nkb = p.kb_part;
@@ -675,22 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             uint32_t n_issued = 0;
             bool ok = true;
             const uint32_t stall = rank == 0 ? kFlagStallProducer0 : (rank == 1 ? kFlagStallProducer1 : 0u);
-            const bool hint_a = (p.flags & kFlagHintA) != 0, hint_b = (p.flags & kFlagHintB) != 0;
-            const uint64_t pol_a = ptx::policy_evict_last(), pol_b = ptx::policy_evict_first();
-            auto load = [&](uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x, int32_t y, bool hint,
-                            uint64_t pol) {
-                if constexpr (kGroup == 2) {
-                    if (hint)
-                        ptx::tma_load_2d_pair_hint(dst, map, bar, x, y, pol);
-                    else
-                        ptx::tma_load_2d_pair(dst, map, bar, x, y);
-                } else {
-                    if (hint)
-                        ptx::tma_load_2d_hint(dst, map, bar, x, y, pol);
-                    else
-                        ptx::tma_load_2d(dst, map, bar, x, y);
-                }
-            };
+
             if (p.flags & stall) ok = w.wait(never_bar, 0u, kSiteStall);
             for (int64_t it = 0; ok && it < iters; ++it) {
                 const Unit un = unit_at(it);
@@ -723,19 +701,19 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                             if (pos == 0) ptx::mbar_arrive_expect_tx(loaded_bar(stage, t), 2 * fill / kAtoms);
                             const uint32_t lb = ptx::mapa_shared(loaded_bar(stage, t), lead);
                             const int32_t k0 = (kb * Cfg::kAtoms + t) * kBlockKElems;
-                            load(s_b + t * Cfg::kAtomBBytes, &p.tmap_b, lb, k0, nb, hint_b, pol_b);
-                            load(s_a + t * Cfg::kAtomABytes, map_a, lb, k0, m0, hint_a, pol_a);
+                            ptx::tma_load_2d_pair(s_b + t * Cfg::kAtomBBytes, &p.tmap_b, lb, k0, nb);
+                            ptx::tma_load_2d_pair(s_a + t * Cfg::kAtomABytes, map_a, lb, k0, m0);
                             if (two_halves)
-                                load(s_a + t * Cfg::kAtomABytes + Cfg::kHalfABytes, map_a, lb, k0, m0 + kTileM,
-                                     hint_a, pol_a);
+                                ptx::tma_load_2d_pair(s_a + t * Cfg::kAtomABytes + Cfg::kHalfABytes, map_a, lb, k0,
+                                                      m0 + kTileM);
                         }
                     } else {
 #pragma unroll
                         for (int t = 0; t < Cfg::kAtoms; ++t) {
                             const int32_t k0 = (kb * Cfg::kAtoms + t) * kBlockKElems;
                             ptx::mbar_arrive_expect_tx(loaded_bar(stage, t), fill / kAtoms);
-                            load(s_b + t * Cfg::kAtomBBytes, &p.tmap_b, loaded_bar(stage, t), k0, nb, hint_b, pol_b);
-                            load(s_a + t * Cfg::kAtomABytes, map_a, loaded_bar(stage, t), k0, m0, hint_a, pol_a);
+                            ptx::tma_load_2d(s_b + t * Cfg::kAtomBBytes, &p.tmap_b, loaded_bar(stage, t), k0, nb);
+                            ptx::tma_load_2d(s_a + t * Cfg::kAtomABytes, map_a, loaded_bar(stage, t), k0, m0);
                         }
                     }
                     *issued_count = ++n_issued;
@@ -942,9 +920,6 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         const int ew = warp - 2;
         const int row = 32 * quarter + lane;      // this thread's TMEM lane = output column within the CTA
         const bool tma_store = (p.flags & kFlagTmaStore) != 0;
-        const bool hint_c = (p.flags & kFlagHintC) != 0;
-        const bool direct_c = (p.flags & kFlagDirectStore) != 0;
-        const uint64_t pol_c = ptx::policy_evict_first();
         volatile uint32_t *second_flag = tmem_holder + 4;   // split-K: this CTA's half came second
         const float scale = p.scale_a_ptr ? __fmul_rn(__ldg(p.scale_a_ptr), __ldg(p.scale_b_ptr)) : p.scale;
         int acc = 0;
@@ -993,18 +968,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             for (int j = 0; j < 32; ++j) packed[j] = Kind::pack(v[2 * j], v[2 * j + 1], scale);
         };
         auto store_packed = [&](const uint32_t (&packed)[32], int32_t mc, int32_t nw) {
-            if (direct_c && mc < p.m_tma) {
-                // m_tma > 0: C's base and stride are 16-byte aligned, and m_tma a multiple of 8
-                const int64_t n = nw + lane;
-                if (n < p.N) {
-                    uint16_t *col = static_cast<uint16_t *>(p.c_ptr) + n * p.ldc + mc;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        if (mc + 8 * j + 8 <= p.m_tma)
-                            ptx::st_global_v4(col + 8 * j, packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
-                                              packed[4 * j + 3]);
-                }
-            } else if (tma_store && mc < p.m_tma) {
+            if (tma_store && mc < p.m_tma) {
                 const uint32_t buf = s_epi + (ew * kEpiBufs + (chunk_ctr & 1u)) * kEpiBufBytes;
                 if (lane == 0) ptx::bulk_wait_group_read<kEpiBufs - 1>();   // buffer's previous store has read it
                 __syncwarp();
@@ -1017,10 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    if (hint_c)                                   // clipped at m_tma and N
-                        ptx::tma_store_2d_hint(&p.tmap_c, buf, mc, nw, pol_c);
-                    else
-                        ptx::tma_store_2d(&p.tmap_c, buf, mc, nw);
+                    ptx::tma_store_2d(&p.tmap_c, buf, mc, nw);   // clipped at m_tma and N
                     ptx::bulk_commit_group();
                 }
                 ++chunk_ctr;
@@ -1061,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             const int32_t nw = static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB) + 32 * quarter;
             if (un.phantom) {
                 release_acc();   // nothing to store
-            } else if (un.cpart >= 0) {
+            } else if (kCluster && un.cpart >= 0) {
                 // kClusterReduce: this CTA holds the partial sum of k range `me` of its
                 // 128 rows n of the tile (a CTA pair's tile has two such CTAs, one per
                 // position; the exchange runs between the CTAs of one position).  Of
@@ -1132,7 +1093,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                                 for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(x[i]);
                             } else {
                                 const uint32_t src =
-                                    s_ring + (q < me ? q : q - 1) * slot_bytes + oc * kChunkBytes + row_off;
+                                    s_ring + (q - (q > me ? 1u : 0u)) * slot_bytes + oc * kChunkBytes + row_off;
 #pragma unroll
                                 for (int i = 0; i < 8; ++i) {
                                     const float4 f = ptx::ld_shared_v4_f32(src + swz(8 * h + i));
@@ -1357,7 +1318,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
 
     __syncwarp();                // .aligned barriers below need converged warps
     ptx::tc_fence_before_sync();
-    if (kGroup == 2 || ctas > 1)
+    if constexpr (kGroup == 2 || kCluster)
         ptx::cluster_sync();     // no CTA leaves while another may still touch its shared memory
     else
         __syncthreads();

@@ -36,8 +36,6 @@
  *     a multiple of 16 bytes are first copied into a library-owned, lazily
  *     grown device workspace with a padded stride, one per (device,
  *     stream), so calls on different streams may take this path at once.
- *     (A test hook, gemm_debug_set_repack_overlap, can instead run most of a
- *     large B's copy on a second, library-owned stream beside a first GEMM.)
  *   - When the tiles of a launch end in a partly filled wave, each leftover
  *     tile is computed as two halves of its k range whose FP32 partial sums
  *     meet in a library-owned buffer kept per (device, stream), allocated on
@@ -328,15 +326,6 @@ int gemm_debug_set_raster_group(int rows);
 int gemm_debug_set_k_order(int mode);
 
 /*
- * Test hook: L2 eviction priorities of the kernel's bulk copies.  -1
- * (default): the library's choice; otherwise a mask: 1 A loads evict_last
- * (later waves of a raster group read the same A panels), 2 B loads
- * evict_first, 4 C stores evict_first.  Results do not change.  Returns 0,
- * or -1 for values outside -1 .. 7.
- */
-int gemm_debug_set_l2_hints(int mask);
-
-/*
  * Test hook: how a grid of at most half the co-resident slots with a long K
  * (at least 32 k blocks) is cut into k ranges.  0 (default): the library's
  * choice; 1: always the split-reduce (FP32 partials in a per-stream buffer,
@@ -346,14 +335,6 @@ int gemm_debug_set_l2_hints(int mask);
  * -1 for other values.
  */
 int gemm_debug_set_long_k_mode(int mode);
-
-/*
- * Test hook: how the kernel writes C where its base and stride allow
- * 16-byte accesses.  0 (default): the library's choice (TMA stores); 1: TMA
- * stores through shared memory; 2: 16-byte global stores from registers.  Ragged rows are stored element by element either
- * way.  Returns 0, or -1 for other values.
- */
-int gemm_debug_set_store_mode(int mode);
 
 /*
  * Measurement hook: while `counters` (a DEVICE pointer to 3 zeroed unsigned
@@ -366,18 +347,6 @@ int gemm_debug_set_store_mode(int mode);
  * buffer and keeps it alive while launches that use it may run.
  */
 void gemm_debug_set_clock_probe(unsigned long long *counters);
-
-/*
- * Test hook: whether the copy of an unaligned B is split so that most of it
- * runs beside the GEMM.  With the split, the columns n of about one wave of
- * tiles are copied (with A) first and a first GEMM covers them, while a
- * library-owned second stream copies the rest of B; a second GEMM covers the
- * rest once that copy is done (an event).  0 (default): the library's
- * choice (currently never: measured slower on GB300, the copy's CTAs slow
- * the first GEMM down); 1: never; 2: wherever B is copied and more than one
- * wave's columns exist.  Returns 0, or -1 for other values.
- */
-int gemm_debug_set_repack_overlap(int mode);
 
 /* Description of the last GEMM kernel launch on the calling host thread
  * (tile shape, grid, co-resident cluster slots), for logs and tests

@@ -159,18 +159,5 @@ def test_long_k_mode_hook_values():
     assert g.lib.gemm_debug_set_long_k_mode(3) == -1
     for v in (1, 2, 0):
         assert g.lib.gemm_debug_set_long_k_mode(v) == 0
-    assert g.lib.gemm_debug_set_l2_hints(8) == -1
-    for v in (7, 0, -1):
-        assert g.lib.gemm_debug_set_l2_hints(v) == 0
 
 
-def test_store_mode_hook_values():
-    assert g.lib.gemm_debug_set_store_mode(3) == -1
-    for v in (1, 2, 0):
-        assert g.lib.gemm_debug_set_store_mode(v) == 0
-
-
-def test_repack_overlap_hook_values():
-    assert g.lib.gemm_debug_set_repack_overlap(3) == -1
-    for v in (1, 2, 0):
-        assert g.lib.gemm_debug_set_repack_overlap(v) == 0

@@ -578,31 +578,19 @@ LAYOUTS = [(136, 136, 304, 0, 0, 0), (141, 137, 303, 0, 0, 0), (136, 136, 300, 1
            (130, 130, 300, 0, 3, 5)]      # lda, ldb, ldc, C offset, A offset, B offset (elements)
 
 
-@pytest.mark.parametrize("store", [1, 2])
 @pytest.mark.parametrize("cta_group,wide", [(1, -1), (2, -1), (2, 1)])
-def test_layouts_on_every_tile_shape(force_group, force_wide, cta_group, wide, store):
+def test_layouts_on_every_tile_shape(force_group, force_wide, cta_group, wide):
     """Padded, odd and unaligned leading dimensions and bases (TMA in place,
-    repacked operands, element-wise C stores) on each tile shape, FP16 and
-    E4M3, with C written by TMA stores (store 1) or by 16-byte stores from
-    registers (store 2)."""
-    import dense_gemm_tn_gb300 as g
+    repacked operands, direct C stores) on each tile shape, FP16 and E4M3."""
     force_group(cta_group)
     force_wide(wide)
-    g.gemm_debug_set_store_mode(store)
-    try:
-        _layouts_case(cta_group, wide, store)
-    finally:
-        g.gemm_debug_set_store_mode(0)
-
-
-def _layouts_case(cta_group, wide, store):
     M, N, K = 300, 700, 130
     A = synth.gauss_fp16(M * K, 31)
     B = synth.gauss_fp16(N * K, 32)
     A8, sa = synth.gauss_e4m3(M * K, 33)
     B8, sb = synth.gauss_e4m3(N * K, 34)
     for lda, ldb, ldc, c_off, a_off, b_off in LAYOUTS:
-        what = f"group {cta_group} wide {wide} store {store} ld {lda},{ldb},{ldc} offsets {c_off},{a_off},{b_off}"
+        what = f"group {cta_group} wide {wide} ld {lda},{ldb},{ldc} offsets {c_off},{a_off},{b_off}"
         check_f16_full(M, N, K, A, B, lda=lda, ldb=ldb, ldc=ldc, c_offset=c_off, a_offset=a_off, b_offset=b_off,
                        what=what)
         if cta_group == 2:
@@ -731,24 +719,6 @@ def test_cluster_reduce_matches_split_reduce_on_pm1(force_group, long_k_mode):
     assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("store", [1, 2])
-@pytest.mark.parametrize("M,N,K", [(8192, 8192, 256), (4100, 3000, 520), (1024, 1024, 128), (1001, 999, 8192)])
-def test_store_modes_at_scale(store, M, N, K):
-    """Both ways of writing C on the shapes the library runs as it chooses
-    (wide tiles, split-K tail, m-part units, k ranges reduced in a cluster):
-    +-1 inputs bit-exact against the oracle on sampled outputs."""
-    import dense_gemm_tn_gb300 as g
-    A = synth.sign_fp16(M * K, 500 + M)
-    B = synth.sign_fp16(N * K, 501 + N)
-    g.gemm_debug_set_store_mode(store)
-    try:
-        got = run_f16(M, N, K, A, K, B, K)
-    finally:
-        g.gemm_debug_set_store_mode(0)
-    mi, ni = sample_positions(M, N, 20000, seed=M + N + K)
-    c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
-    assert np.array_equal(got[ni, mi], c), _launch_record()
-
 
 def test_clock_probe_counts_launches_and_leaves_results_alone():
     """The measurement hook: each launch adds its first CTA's SM cycles and
@@ -772,80 +742,6 @@ def test_clock_probe_counts_launches_and_leaves_results_alone():
     run_f16(M, N, K, A, K, B, K)                 # off again: the counters stay
     assert int(counters[2].item()) == 3
 
-
-# ---------------------------------------------------------------- copy of B overlapped with a first GEMM
-@pytest.fixture
-def repack_overlap():
-    import dense_gemm_tn_gb300 as g
-    yield g.gemm_debug_set_repack_overlap
-    g.gemm_debug_set_repack_overlap(0)
-
-
-@pytest.mark.parametrize("M,N,K,ldb,mode", [
-    (3000, 12289, 4097, 4097, 2),    # the wide workload's shape, split (the library does not choose it)
-    (1000, 3000, 1001, 1001, 2),     # forced: two GEMMs over the columns n split at one wave's tiles
-    (700, 2600, 520, 523, 2),        # K aligned, B's stride not: only B is copied
-])
-def test_repack_overlapped_with_first_gemm(repack_overlap, M, N, K, ldb, mode):
-    """B copied in two parts, the second on a side stream beside a first GEMM
-    over the columns already copied: +-1 inputs bit-exact (every output, or
-    sampled on the large shape); Gaussian inputs within tolerance, split and
-    unsplit (a tile's wave, and so its k order, can differ between the two);
-    E4M3 within its tolerance."""
-    repack_overlap(mode)
-    A = synth.sign_fp16(M * K, 700 + M)
-    B = synth.sign_fp16(N * K, 701 + N)
-    Bp = pad_rows(B, N, K, ldb, 0xFC00) if ldb != K else B
-    got = run_f16(M, N, K, A, K, Bp, ldb)
-    if M * N <= 3_000_000:
-        Cref, _, _ = oracle.gemm_f16_tn(M, N, K, A, K, B, K)
-        assert np.array_equal(got, oracle.c_as_nm(Cref, M, N, M))
-    else:
-        mi, ni = sample_positions(M, N, 30000, seed=M + 7)
-        c, _, _ = oracle.gemm_f16_tn_at(M, N, K, A, K, B, K, mi, ni)
-        assert np.array_equal(got[ni, mi], c)
-    Ag = synth.gauss_fp16(M * K, 702 + M)
-    Bg = synth.gauss_fp16(N * K, 703 + N)
-    Bgp = pad_rows(Bg, N, K, ldb, 0x7C00) if ldb != K else Bg
-    split = run_f16(M, N, K, Ag, K, Bgp, ldb)
-    repack_overlap(1)
-    whole = run_f16(M, N, K, Ag, K, Bgp, ldb)
-    repack_overlap(mode)
-    mi, ni = sample_positions(M, N, 20000, seed=K)
-    c, s, _ = oracle.gemm_f16_tn_at(M, N, K, Ag, K, Bg, K, mi, ni)
-    assert_tol(f16_values(split[ni, mi]), f16_values(c), s, F16_TOL, "split copy")
-    assert_tol(f16_values(whole[ni, mi]), f16_values(c), s, F16_TOL, "whole copy")
-    qa, sa = synth.gauss_e4m3(M * K, 704 + M)
-    qb, sb = synth.gauss_e4m3(N * K, 705 + N)
-    qbp = pad_rows(qb, N, K, ldb, 0x7F) if ldb != K else qb
-    got8 = run_f8(M, N, K, qa, K, qbp, ldb, sa, sb)
-    c8, s8, _ = oracle.gemm_f8e4m3_tn_at(M, N, K, qa, K, qb, K, sa, sb, mi, ni)
-    assert_tol(bf16_values(got8[ni, mi]), bf16_values(c8), s8, F8_TOL, "split copy e4m3")
-
-
-def test_repack_overlap_graph_capture(repack_overlap):
-    """The fork into the side stream and the join back are events, so a call
-    with the split copy can be captured into a CUDA graph after a warm-up
-    call; replays give the direct call's bits."""
-    import dense_gemm_tn_gb300 as g
-    repack_overlap(2)
-    M, N, K = 1000, 3000, 1001
-    A = synth.gauss_fp16(M * K, 710); B = synth.gauss_fp16(N * K, 711)
-    dA, dB = to_dev_u16(A), to_dev_u16(B)
-    s = torch.cuda.Stream()
-    C_direct = torch.empty((N, M), dtype=torch.float16, device="cuda")
-    C_graph = torch.empty((N, M), dtype=torch.float16, device="cuda")
-    g.gemm_f16_tn(M, N, K, dA, K, dB, K, C_direct, M, s)
-    g.gemm_poll_device_status(s)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=s):
-        g.gemm_f16_tn(M, N, K, dA, K, dB, K, C_graph, M, s)
-    for _ in range(2):
-        C_graph.fill_(float("nan"))
-        graph.replay()
-        torch.cuda.synchronize()
-        g.gemm_poll_device_status(s)
-        assert torch.equal(C_graph.view(torch.int16), C_direct.view(torch.int16))
 
 
 def test_long_k_small_grid_tile_choice():
