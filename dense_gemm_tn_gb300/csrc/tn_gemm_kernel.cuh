@@ -651,9 +651,11 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     };
     const Unit unit0 = slot_unit_at(0);      // (a phantom when the slot has no unit)
     auto unit_at = [&](int64_t it) { return it == 0 ? unit0 : slot_unit_at(it); };
+    const uint32_t flags = p.flags;
+    unsigned long long *const clock_probe = p.clock_probe;
 
     ptx::griddep_wait();
-    const bool probe_clock = p.clock_probe != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
+    const bool probe_clock = clock_probe != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
     const uint64_t probe_c0 = probe_clock ? ptx::clock64() : 0, probe_t0 = probe_clock ? ptx::globaltimer() : 0;
 
     if (warp == 0) {
@@ -669,11 +671,11 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             bool ok = true;
             const uint32_t stall = rank == 0 ? kFlagStallProducer0 : (rank == 1 ? kFlagStallProducer1 : 0u);
 
-            if (p.flags & stall) ok = w.wait(never_bar, 0u, kSiteStall);
+            if (flags & stall) ok = w.wait(never_bar, 0u, kSiteStall);
             for (int64_t it = 0; ok && it < iters; ++it) {
                 const Unit un = unit_at(it);
                 const bool cut_m = un.mpart >= 0;
-                const bool rev = (p.flags & kFlagAltK) && !un.phantom && un.tile < p.tail_start &&
+                const bool rev = (flags & kFlagAltK) && !un.phantom && un.tile < p.tail_start &&
                                  ((static_cast<uint32_t>(un.tile) / static_cast<uint32_t>(nslots)) & 1u);
                 // A rows of this CTA: one box per stage, or (a whole wide tile) one per half,
                 // the second kTileM rows further on.  A wide tile's A map has boxes of one
@@ -772,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             constexpr uint32_t kIdescQuarter = ptx::idesc_f32acc(Cfg::kTileN, kTileM / 4, Kind::kFmt, Kind::kFmt);
             // (a wide tile's m parts are its halves: MMA N = 256)
             const uint32_t idesc_part = kWide ? kIdesc : (quarter_m ? kIdescQuarter : kIdescHalf);
-            if (p.flags & kFlagStallMma) ok = w.wait(never_bar, 0u, kSiteStall);
+            if (flags & kFlagStallMma) ok = w.wait(never_bar, 0u, kSiteStall);
             if constexpr (kWide) {
                 // 256 x 512 tiles.  The epilogue hands the accumulator back one half at a
                 // time (accempty[0], then accempty[1]), each as soon as it has read that
@@ -919,7 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31 are this warp's
         const int ew = warp - 2;
         const int row = 32 * quarter + lane;      // this thread's TMEM lane = output column within the CTA
-        const bool tma_store = (p.flags & kFlagTmaStore) != 0;
+        const bool tma_store = (flags & kFlagTmaStore) != 0;
         volatile uint32_t *second_flag = tmem_holder + 4;   // split-K: this CTA's half came second
         const float scale = p.scale_a_ptr ? __fmul_rn(__ldg(p.scale_a_ptr), __ldg(p.scale_b_ptr)) : p.scale;
         int acc = 0;
@@ -1193,7 +1195,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 // (a wide tile's m parts are its 256-row halves)
                 const int n_chunks = un.mpart < 0 ? Cfg::kTileMRows / kEpiBoxM
                                                   : (kWide ? kTileM : (quarter_m ? kTileM / 4 : kTileM / 2)) / kEpiBoxM;
-                const bool stats = !Kind::kF8 && !kWide && (p.flags & kFlagStats) != 0;
+                const bool stats = !Kind::kF8 && !kWide && (flags & kFlagStats) != 0;
                 if (kWide && un.mpart < 0) {
                     // A whole wide tile, half by half: the first two chunks of the half go
                     // through the staging buffers, the last two are read into registers
@@ -1328,9 +1330,9 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         ptx::tmem_dealloc<kGroup>(tmem_base, kTmemCols);
     }
     if (probe_clock) {
-        atomicAdd(&p.clock_probe[0], static_cast<unsigned long long>(ptx::clock64() - probe_c0));
-        atomicAdd(&p.clock_probe[1], static_cast<unsigned long long>(ptx::globaltimer() - probe_t0));
-        atomicAdd(&p.clock_probe[2], 1ull);
+        atomicAdd(&clock_probe[0], static_cast<unsigned long long>(ptx::clock64() - probe_c0));
+        atomicAdd(&clock_probe[1], static_cast<unsigned long long>(ptx::globaltimer() - probe_t0));
+        atomicAdd(&clock_probe[2], 1ull);
     }
 }
 
