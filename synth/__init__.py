@@ -28,6 +28,11 @@ larger than the GPU's L2 (129 MB), so every step reads its operands from HBM:
   fp8_pipeline_8192  M=N=K=8192, N(0,1) cast to bfloat16, 2 rotating sets;
                each step quantises both operands to E4M3 on the device
                before the FP8 GEMM
+  longk_4096x512  M=4096, N=512, K=8192, N(0,1) cast to fp16, 2 rotating
+               sets: a grid of fewer tiles than half the GPU with a long K
+               (its k ranges are reduced inside clusters)
+  skinny_8192x16  M=8192, N=16, K=8192, N(0,1) cast to fp16, 2 rotating sets:
+               a decode-like product, bound by the read of A
 """
 from __future__ import annotations
 
@@ -184,6 +189,8 @@ WORKLOADS = {
         Workload("ffn_8192", 8192, 28672, 8192, "gauss", 601, 602, rotating=2),
         Workload("fp8_pipeline_8192", 8192, 8192, 8192, "bf16", 701, 702, rotating=2),
         Workload("qk_stats_1024", 1024, 1024, 128, "gauss", 201, 202, rotating=320, op="softmax_stats"),
+        Workload("longk_4096x512", 4096, 512, 8192, "gauss", 801, 802, rotating=2),
+        Workload("skinny_8192x16", 8192, 16, 8192, "gauss", 803, 804, rotating=2),
     ]
 }
 

@@ -239,6 +239,17 @@ def test_workload_ffn_8192_sampled():
     assert not np.any((got & 0x7C00) == 0x7C00), "Inf or NaN in C"
 
 
+@pytest.mark.parametrize("name", ["longk_4096x512", "skinny_8192x16"])
+def test_workload_long_k_sampled(name):
+    """The long-K benchmark workloads (k ranges reduced in clusters) against
+    the oracle on sampled outputs, within tolerance, and identical run to run."""
+    w = synth.WORKLOADS[name]
+    A, B, _, _ = synth.make_inputs(w, 0)
+    got = run_f16(w.M, w.N, w.K, A, w.K, B, w.K)
+    _sampled_f16(w, A, B, got, exact=False, count=20000)
+    assert np.array_equal(got, run_f16(w.M, w.N, w.K, A, w.K, B, w.K))
+
+
 def test_workload_e4m3_8192_sampled():
     w = synth.WORKLOADS["e4m3_8192"]
     A, B, sa, sb = synth.make_inputs(w, 0)
