@@ -204,6 +204,16 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// 2-D tiled prefetch of a box into L2 (no shared-memory destination, no
+// completion).  Elements outside the tensor are skipped.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t x, int32_t y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2-D tiled load global -> shared; completion is signalled on `bar` as
 // transaction bytes.  x is the innermost (contiguous) coordinate.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,

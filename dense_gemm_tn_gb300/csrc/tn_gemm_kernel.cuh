@@ -149,6 +149,12 @@ constexpr uint32_t kFlagStats = 16u;
 // order of the FP32 sums changes, not their terms.
 constexpr uint32_t kFlagAltK = 32u;
 
+// L2 prefetch before griddepcontrol.wait (kClusterReduce launches): units of
+// at least kPrefetchMinKb stages get their first kPrefetchAtoms 128-byte K
+// atoms prefetched.
+constexpr int kPrefetchMinKb = 16;
+constexpr int kPrefetchAtoms = 4;
+
 // Status word of the current device; set (never cleared) by a kernel whose
 // bounded wait ran out: 4 (timeout) | site << 8.
 __device__ int g_tn_status;
@@ -197,7 +203,7 @@ struct KernelParams {
     uint32_t flags;
     uint64_t wait_limit_ns;
     // Optional (NULL: off): CTA 0's first thread adds the SM cycles and the
-    // nanoseconds from its start (after griddepcontrol.wait) to its exit to
+    // nanoseconds from its start (before griddepcontrol.wait) to its exit to
     // clock_probe[0] and [1], and 1 to [2]: [0] / [1] is the SM clock the
     // launches ran at.
     unsigned long long *clock_probe;
@@ -621,13 +627,17 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     const uint32_t tmem_base = *tmem_holder;
     // The kernel is launched as a programmatic dependent of whatever precedes
     // it on the stream, so the setup above (barriers, TMEM, descriptor
-    // prefetch) overlaps the end of that kernel.  Nothing below touches global
-    // memory before that kernel has completed.  (The next kernel is let in by
-    // the producer once it has issued its last load, below.)
-    // The schedule below reads only the kernel's parameters, so it is worked out
-    // before the wait: the first reads of the parameter block then overlap the
-    // previous kernel too (measured on GB300, computing the first unit after
-    // the wait put about 0.9 us between it and the first load).
+    // prefetch) overlaps the end of that kernel.  Every thread that touches
+    // global memory first waits for that kernel to complete (griddepcontrol.wait):
+    // the producer right before its first load, the epilogue warps as they
+    // start; the MMA thread never touches global memory, and everything the
+    // other roles do comes after the producer's loads.  So the schedule, the
+    // first fill's barrier work and the code that does it (its first run)
+    // overlap the previous kernel too.  Measured on GB300: computing the first
+    // unit after a wait at the top put about 0.9 us between the wait and the
+    // first load, and the rest of the first fill's work about 0.5 us more.
+    // (The next kernel is let in by the producer once it has issued its last
+    // load, below.)
     const Waiter w{abort_flag, abort_addr, rank, ctas, p.wait_limit_ns};
 
     // The unit of step `it` of this CTA's slot (both CTAs of a pair run the same
@@ -654,7 +664,60 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     const uint32_t flags = p.flags;
     unsigned long long *const clock_probe = p.clock_probe;
 
-    ptx::griddep_wait();
+    // Where this CTA's loads of a unit go: the A map and its first row m, B's
+    // first row n, whether a whole wide tile loads A as two halves, and whether
+    // the unit walks its k blocks from the last (odd waves, kFlagAltK).
+    struct Boxes {
+        const CUtensorMap *map_a;
+        int32_t m0, nb;
+        bool two_halves, rev;
+    };
+    auto boxes_of = [&](const Unit &un) {
+        const bool cut_m = un.mpart >= 0;
+        // A rows of this CTA: one box per stage, or (a whole wide tile) one per half,
+        // the second kTileM rows further on.  A wide tile's A map has boxes of one
+        // half's rows, which are also an m part's.
+        const int32_t rows_a = kWide ? kTileM / kGroup : (cut_m ? part_rows_a : Cfg::kRowsA);
+        Boxes b;
+        b.map_a = cut_m && !kWide ? &p.tmap_a_part : &p.tmap_a;
+        b.two_halves = kWide && !cut_m;
+        b.rev = (flags & kFlagAltK) && !un.phantom && un.tile < p.tail_start &&
+                ((static_cast<uint32_t>(un.tile) / static_cast<uint32_t>(nslots)) & 1u);
+        // a phantom unit reads past the matrices: zero fill, the box's full byte count
+        b.m0 = un.phantom ? p.M
+                          : static_cast<int32_t>(un.tm * Cfg::kTileMRows + (cut_m ? un.mpart * p.m_part_rows : 0) +
+                                                 pos * rows_a);
+        b.nb = un.phantom ? p.N : static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB);
+        return b;
+    };
+
+    // The k ranges of a tile reduced in a cluster (the small grids with a long
+    // K): each CTA's work starts with a stream of its operands, and as a
+    // programmatic dependent it often waits below while the previous kernel
+    // drains.  The first kPrefetchAtoms K atoms of its boxes are prefetched into
+    // L2 before that wait.  A prefetch returns no data to the CTA, so it cannot
+    // read ahead of the previous kernel's writes: the loads after the wait read
+    // through L2, which every write reaches first.  (Measured on GB300, back to
+    // back: 8192 x 16 x 8192 27.44 -> 26.23 us, 4096 x 512 x 8192 31.02 -> 30.63
+    // us, 4096 x 256 x 4096 19.14 -> 18.77 us.  With few k blocks per unit, e.g.
+    // 2048 x 2048 x 512, prefetching made calls 2-7 % slower: the prefetches
+    // queue ahead of the loads.)
+    if (kCluster && warp == 0 && lane == 0 && !unit0.phantom && unit0.nkb >= kPrefetchMinKb) {
+        const Boxes bx = boxes_of(unit0);
+        for (int i = 0; i < kPrefetchAtoms / Cfg::kAtoms; ++i) {
+            const int kb = bx.rev ? unit0.kb0 + unit0.nkb - 1 - i : unit0.kb0 + i;
+            if (kb >= p.num_kb) continue;   // (the zero-filled end of a last k range)
+#pragma unroll
+            for (int t = 0; t < Cfg::kAtoms; ++t) {
+                const int32_t k0 = (kb * Cfg::kAtoms + t) * kBlockKElems;
+                if (k0 >= p.K) break;
+                if (bx.nb < p.N) ptx::tma_prefetch_2d(&p.tmap_b, k0, bx.nb);
+                if (bx.m0 < p.M) ptx::tma_prefetch_2d(bx.map_a, k0, bx.m0);
+                if (bx.two_halves && bx.m0 + kTileM < p.M) ptx::tma_prefetch_2d(bx.map_a, k0, bx.m0 + kTileM);
+            }
+        }
+    }
+
     const bool probe_clock = clock_probe != nullptr && blockIdx.x == 0 && threadIdx.x == 0;
     const uint64_t probe_c0 = probe_clock ? ptx::clock64() : 0, probe_t0 = probe_clock ? ptx::globaltimer() : 0;
 
@@ -674,29 +737,20 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             if (flags & stall) ok = w.wait(never_bar, 0u, kSiteStall);
             for (int64_t it = 0; ok && it < iters; ++it) {
                 const Unit un = unit_at(it);
-                const bool cut_m = un.mpart >= 0;
-                const bool rev = (flags & kFlagAltK) && !un.phantom && un.tile < p.tail_start &&
-                                 ((static_cast<uint32_t>(un.tile) / static_cast<uint32_t>(nslots)) & 1u);
-                // A rows of this CTA: one box per stage, or (a whole wide tile) one per half,
-                // the second kTileM rows further on.  A wide tile's A map has boxes of one
-                // half's rows, which are also an m part's.
-                const int32_t rows_a = kWide ? kTileM / kGroup : (cut_m ? part_rows_a : Cfg::kRowsA);
-                const bool two_halves = kWide && !cut_m;
+                const Boxes bx = boxes_of(un);
+                const bool two_halves = bx.two_halves;
                 const uint32_t fill = Cfg::kTileBBytes + a_bytes(un);
-                const CUtensorMap *map_a = cut_m && !kWide ? &p.tmap_a_part : &p.tmap_a;
-                // a phantom unit reads past the matrices: zero fill, the box's full byte count
-                const int32_t m0 = un.phantom ? p.M
-                                              : static_cast<int32_t>(un.tm * Cfg::kTileMRows +
-                                                                     (cut_m ? un.mpart * p.m_part_rows : 0) + pos * rows_a);
-                const int32_t nb = un.phantom ? p.N : static_cast<int32_t>(un.tn * Cfg::kTileN + pos * Cfg::kRowsB);
+                const CUtensorMap *map_a = bx.map_a;
+                const int32_t m0 = bx.m0, nb = bx.nb;
                 for (int i = 0; i < un.nkb; ++i) {
-                    const int kb = rev ? un.kb0 + un.nkb - 1 - i : un.kb0 + i;
+                    const int kb = bx.rev ? un.kb0 + un.nkb - 1 - i : un.kb0 + i;
                     if (!w.wait(empty_bar(stage), phase ^ 1u, kSiteEmpty)) {
                         ok = false;
                         break;
                     }
                     const uint32_t s_b = s_ring + stage * Cfg::kStageBytes;
                     const uint32_t s_a = s_b + Cfg::kTileBBytes;
+                    if (n_issued == 0) ptx::griddep_wait();   // this thread's first global access
                     if constexpr (kGroup == 2) {
 #pragma unroll
                         for (int t = 0; t < Cfg::kAtoms; ++t) {
@@ -730,7 +784,10 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
             // touches memory).  Not earlier: a dependent's CTAs that wait on SMs
             // beside this grid's for a whole launch slowed it (by 2 % for a
             // 305 us FP8 GEMM followed by the quantiser).  A single thread's
-            // signal counts for its CTA, else the CTA's exit does.
+            // signal counts for its CTA, else the CTA's exit does.  (A producer
+            // that issued no load still waits first: this thread updates the
+            // clock probe as the CTA leaves.)
+            if (n_issued == 0) ptx::griddep_wait();
             ptx::griddep_launch_dependents();
             if constexpr (kGroup == 2) {
                 // publish the final count (release: the count store is ordered before it)
@@ -923,6 +980,9 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         const int row = 32 * quarter + lane;      // this thread's TMEM lane = output column within the CTA
         const bool tma_store = (flags & kFlagTmaStore) != 0;
         volatile uint32_t *second_flag = tmem_holder + 4;   // split-K: this CTA's half came second
+        // The device scales may have been written by the previous kernel (the
+        // quantiser): these warps wait for it before their first global access.
+        ptx::griddep_wait();
         const float scale = p.scale_a_ptr ? __fmul_rn(__ldg(p.scale_a_ptr), __ldg(p.scale_b_ptr)) : p.scale;
         int acc = 0;
         uint32_t acc_phase = 0;
