@@ -587,7 +587,7 @@ def run_secondary(args, torch, g, dev, stream, sampler, peaks, sms) -> dict:
     M, N, K = w.M, w.N, w.K
     pa, pb, pc = [t.data_ptr() for t in dA], [t.data_ptr() for t in dB], C.data_ptr()
     sa, sb = [h[2] for h in host], [h[3] for h in host]
-    f_f8 = g.lib.gemm_f8e4m3_tn
+    f_f8 = g.calls.gemm_f8e4m3_tn
 
     def call(j):
         return f_f8(M, N, K, pa[j], K, pb[j], K, pc, M, sa[j], sb[j], sh)
@@ -656,9 +656,10 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
         row_sum = torch.empty(M, dtype=torch.float32, device=dev)
         rmax_p, rsum_p = row_max.data_ptr(), row_sum.data_ptr()
 
-    # the C ABI's entry points, bound once
-    f_quant, f_f8_dscale = g.lib.gemm_quantize_e4m3, g.lib.gemm_f8e4m3_tn_dscale
-    f_f8, f_stats, f_f16 = g.lib.gemm_f8e4m3_tn, g.lib.gemm_f16_tn_softmax_stats, g.lib.gemm_f16_tn
+    # the C ABI's entry points, bound once (through the CPython-API binding where
+    # it was built: a ctypes call costs about 1.5 us of host time per step)
+    f_quant, f_f8_dscale = g.calls.gemm_quantize_e4m3, g.calls.gemm_f8e4m3_tn_dscale
+    f_f8, f_stats, f_f16 = g.calls.gemm_f8e4m3_tn, g.calls.gemm_f16_tn_softmax_stats, g.calls.gemm_f16_tn
 
     def issue(j, a, b, c, mid=None):
         """One step's work on the stream: returns the status codes of its calls."""
@@ -847,7 +848,8 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
                                + (", both operands quantised to e4m3 on the device each step" if pipeline else ""),
                    "M": M, "N": N, "K": K, "accumulate": "f32",
                    "l2": l2_note(sets, (M + N) * K * esz),
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "binding": "cpython" if g.fast is not None else "ctypes"},
         "pct_of_dense_peak": 100.0 * value / world / NOMINAL_PEAK[w.dtype],
         "e2e": {"value": replica_tflops(world, flop, 1, e2e_ms), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,

@@ -14,7 +14,13 @@ The same names as the C ABI:
     gemm_poll_device_status(stream=None)
 
 A, B and C are device pointers given as ints or as CUDA torch tensors (their
-data_ptr() is passed; the tensor's shape is NOT consulted).  `stream` is an
+data_ptr() is passed; the tensor's shape is NOT consulted).
+
+Two bindings of the same C functions: `lib` (ctypes) and, where build()
+found the Python headers, `fast` (the CPython-API module _tn_fast, built from
+csrc/pyfast.c: the same names and argument order, ints for pointers, about a
+tenth of the per-call host time).  `calls` is `fast` when present, else
+`lib`; the wrappers below go through it.  `stream` is an
 int handle, a torch.cuda.Stream, or None for torch's current stream.  A
 status other than GEMM_OK raises GemmError.
 
@@ -116,6 +122,14 @@ def _load() -> ctypes.CDLL:
 _lib = _load()
 lib = _lib
 
+try:
+    # loads after _lib: it links the same library file, which the dynamic
+    # loader then shares with the ctypes binding (one device state)
+    from . import _tn_fast as fast
+except ImportError:
+    fast = None
+calls = fast if fast is not None else _lib
+
 
 def status_string(status: int) -> str:
     return _lib.gemm_status_string(int(status)).decode()
@@ -160,31 +174,31 @@ def _check(status: int) -> int:
 
 
 def gemm_f16_tn(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
-    return _check(_lib.gemm_f16_tn(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _stream(stream)))
+    return _check(calls.gemm_f16_tn(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _stream(stream)))
 
 
 def gemm_f8e4m3_tn(M, N, K, A, lda, B, ldb, C, ldc, scale_a, scale_b, stream=None) -> int:
-    return _check(_lib.gemm_f8e4m3_tn(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
-                                      float(scale_a), float(scale_b), _stream(stream)))
+    return _check(calls.gemm_f8e4m3_tn(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
+                                       float(scale_a), float(scale_b), _stream(stream)))
 
 
 def gemm_f8e4m3_tn_dscale(M, N, K, A, lda, B, ldb, C, ldc, scale_a, scale_b, stream=None) -> int:
     """gemm_f8e4m3_tn with scale_a / scale_b as device pointers (one fp32 each)."""
-    return _check(_lib.gemm_f8e4m3_tn_dscale(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
-                                             _ptr(scale_a), _ptr(scale_b), _stream(stream)))
+    return _check(calls.gemm_f8e4m3_tn_dscale(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
+                                              _ptr(scale_a), _ptr(scale_b), _stream(stream)))
 
 
 def gemm_f16_tn_softmax_stats(M, N, K, A, lda, B, ldb, C, ldc, scale, row_max, row_sum, stream=None) -> int:
     """Scaled scores C = fp16(scale * A B) with the softmax row statistics
     (row_max, row_sum: device float arrays of M)."""
-    return _check(_lib.gemm_f16_tn_softmax_stats(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, float(scale),
-                                                 _ptr(row_max), _ptr(row_sum), _stream(stream)))
+    return _check(calls.gemm_f16_tn_softmax_stats(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, float(scale),
+                                                  _ptr(row_max), _ptr(row_sum), _stream(stream)))
 
 
 def gemm_quantize_e4m3(x, x_type, rows, cols, ldx, q, ldq, scale, stream=None) -> int:
     """Per-tensor E4M3 quantisation on the device: codes into q, amax / 448 into *scale."""
-    return _check(_lib.gemm_quantize_e4m3(_ptr(x), int(x_type), rows, cols, ldx, _ptr(q), ldq, _ptr(scale),
-                                          _stream(stream)))
+    return _check(calls.gemm_quantize_e4m3(_ptr(x), int(x_type), rows, cols, ldx, _ptr(q), ldq, _ptr(scale),
+                                           _stream(stream)))
 
 
 def gemm_f16_tn_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
@@ -192,8 +206,8 @@ def gemm_f16_tn_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=None) -> int:
     memory (their own memory pool or budget, or no implicit synchronisation
     allowed): operand copies go to a fixed 32 MiB array in the library's
     device image instead of a cudaMalloc'd workspace."""
-    return _check(_lib.gemm_f16_tn_noalloc(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
-                                           _stream(stream)))
+    return _check(calls.gemm_f16_tn_noalloc(M, N, K, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc,
+                                            _stream(stream)))
 
 
 def gemm_poll_device_status(stream=None) -> int:

@@ -1,10 +1,13 @@
 """Builds libdense_gemm_tn.so in-tree with nvcc for sm_103a (no torch
-extension machinery: the library is a plain C-ABI shared object)."""
+extension machinery: the library is a plain C-ABI shared object), and the
+CPython-API binding of its compute calls (_tn_fast, gcc) where the Python
+headers are installed."""
 from __future__ import annotations
 
 import os
 import shutil
 import subprocess
+import sysconfig
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
@@ -42,3 +45,37 @@ def build(force: bool = False) -> str:
     if force or stale():
         subprocess.check_call(build_cmd())
     return LIB
+
+
+FAST_SRC = os.path.join(CSRC, "pyfast.c")
+FAST = os.path.join(PKG, "_tn_fast" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
+
+
+def fast_build_cmd() -> list[str] | None:
+    """gcc command for the CPython-API binding, or None without Python.h.  It
+    links libdense_gemm_tn.so by an $ORIGIN run path, so the process shares the
+    one copy of the library that the ctypes binding loads."""
+    inc = sysconfig.get_paths().get("include", "")
+    if not inc or not os.path.exists(os.path.join(inc, "Python.h")):
+        return None
+    cc = shutil.which("gcc") or shutil.which("cc") or "gcc"
+    return [cc, "-O2", "-std=c11", "-shared", "-fPIC", "-Wall", "-I", INCLUDE, "-I", inc, "-o", FAST, FAST_SRC,
+            "-L", PKG, "-ldense_gemm_tn", "-Wl,-rpath,$ORIGIN"]
+
+
+def fast_stale() -> bool:
+    if not os.path.exists(FAST):
+        return True
+    t = os.path.getmtime(FAST)
+    return any(os.path.getmtime(f) > t for f in (FAST_SRC, os.path.join(INCLUDE, "tn_gemm.h"), LIB))
+
+
+def build_fast(force: bool = False) -> str | None:
+    """Builds the binding after the library; returns its path, or None when the
+    Python headers are missing (the ctypes binding of the same calls remains)."""
+    cmd = fast_build_cmd()
+    if cmd is None:
+        return None
+    if force or fast_stale():
+        subprocess.check_call(cmd)
+    return FAST

@@ -161,3 +161,75 @@ def test_long_k_mode_hook_values():
         assert g.lib.gemm_debug_set_long_k_mode(v) == 0
 
 
+
+
+# ---------------------------------------------------------------- the CPython-API binding
+FAST = pytest.mark.skipif(g.fast is None, reason="the CPython-API binding was not built (no Python.h)")
+FAST_CALLS = ("gemm_f16_tn", "gemm_f16_tn_noalloc", "gemm_f8e4m3_tn", "gemm_f8e4m3_tn_dscale",
+              "gemm_f16_tn_softmax_stats", "gemm_quantize_e4m3")
+
+
+def test_fast_binding_built_where_python_headers_exist():
+    import sysconfig
+    inc = sysconfig.get_paths().get("include", "")
+    if os.path.exists(os.path.join(inc, "Python.h")):
+        assert g.fast is not None and g.calls is g.fast
+    else:
+        assert g.calls is g.lib
+
+
+@FAST
+def test_fast_binding_exports_the_compute_calls():
+    for name in FAST_CALLS:
+        assert callable(getattr(g.fast, name)), name
+        assert name in g.EXPORTS, name
+
+
+@FAST
+@pytest.mark.parametrize("bad", BAD_ARGS)
+def test_fast_binding_returns_the_c_abi_status(bad):
+    args = dict(M=8, N=8, K=4, A=0x1000, lda=4, B=0x2000, ldb=4, C=0x3000, ldc=8)
+    args.update(bad)
+    v = [args[k] for k in ("M", "N", "K", "A", "lda", "B", "ldb", "C", "ldc")]
+    assert g.fast.gemm_f16_tn(*v, None) == g.lib.gemm_f16_tn(*v, None) == g.GEMM_ERR_INVALID_ARG
+    assert g.fast.gemm_f16_tn_noalloc(*v, None) == g.lib.gemm_f16_tn_noalloc(*v, None)
+    assert g.fast.gemm_f8e4m3_tn(*v, 1.0, 1.0, None) == g.lib.gemm_f8e4m3_tn(*v, 1.0, 1.0, None)
+    assert g.fast.gemm_f8e4m3_tn_dscale(*v, 0x4000, 0x4004, None) == \
+        g.lib.gemm_f8e4m3_tn_dscale(*v, 0x4000, 0x4004, None) == g.GEMM_ERR_INVALID_ARG
+    assert g.fast.gemm_f16_tn_softmax_stats(*v, 0.5, 0x5000, 0x6000, None) == \
+        g.lib.gemm_f16_tn_softmax_stats(*v, 0.5, 0x5000, 0x6000, None) == g.GEMM_ERR_INVALID_ARG
+
+
+@FAST
+def test_fast_binding_quantiser_argument_checks():
+    # an unknown element type and a negative size fail validation in both bindings
+    for args in ((0x1000, 7, 4, 4, 4, 0x2000, 4, 0x3000, None), (0x1000, 0, -1, 4, 4, 0x2000, 4, 0x3000, None)):
+        assert g.fast.gemm_quantize_e4m3(*args) == g.lib.gemm_quantize_e4m3(*args) == g.GEMM_ERR_INVALID_ARG
+
+
+@FAST
+def test_fast_binding_empty_output_is_noop():
+    assert g.fast.gemm_f16_tn(0, 8, 4, None, 4, None, 4, None, 1, None) == g.GEMM_OK
+
+
+@FAST
+def test_fast_binding_rejects_malformed_arguments():
+    with pytest.raises(TypeError):
+        g.fast.gemm_f16_tn(8, 8, 4)
+    with pytest.raises(TypeError):
+        g.fast.gemm_f16_tn(8, 8, 4, "A", 4, 0x2000, 4, 0x3000, 8, None)
+    with pytest.raises(TypeError):
+        g.fast.gemm_f8e4m3_tn(8, 8, 4, 0x1000, 4, 0x2000, 4, 0x3000, 8, "s", 1.0, None)
+    with pytest.raises(OverflowError):
+        g.fast.gemm_f16_tn(1 << 70, 8, 4, 0x1000, 4, 0x2000, 4, 0x3000, 8, None)
+    with pytest.raises(OverflowError):
+        g.fast.gemm_quantize_e4m3(0x1000, 1 << 40, 4, 4, 4, 0x2000, 4, 0x3000, None)
+
+
+@FAST
+def test_fast_binding_shares_the_one_library_copy():
+    # the binding links libdense_gemm_tn.so by run path; the loader maps the file
+    # ctypes opened once, so both see one device state
+    with open("/proc/self/maps") as f:
+        paths = {line.split()[-1] for line in f if "libdense_gemm_tn" in line}
+    assert paths == {os.path.realpath(g.LIB_PATH)}
