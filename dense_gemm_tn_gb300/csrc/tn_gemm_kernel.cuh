@@ -1101,6 +1101,10 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 const uint32_t slot_bytes = ((kTileM / kEpiBoxM + S - 1) / S) * kChunkBytes;
                 const uint32_t row_off = static_cast<uint32_t>(row * kEpiBoxM * 4);
                 const bool valid_n = nw + lane < p.N;
+                // Whether any of this warp's 32 columns n is below N.  A warp with none
+                // (the 8192 x 16 problem: three of four) sends, adds and stores nothing,
+                // which leaves the CTA's shared-memory bandwidth to the warp that does.
+                const bool warp_rows = nw < p.N;
                 auto swz = [&](int c16) { return static_cast<uint32_t>((c16 ^ (row & 7)) << 4); };
                 if (warp == 2 && lane == 0) {
                     // the ring was last written by TMA and read by the tensor cores
@@ -1110,7 +1114,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 }
                 bool fine = __all_sync(0xffffffffu, w.wait(peers_free_bar, 0u, kSitePeersFree));
                 if (fine) {
-                    for (uint32_t d = 1; d < S; ++d) {
+                    for (uint32_t d = 1; warp_rows && d < S; ++d) {
                         const uint32_t q = (me + d) % S;
                         const uint32_t j = me < q ? me : me - 1;    // this CTA's slot in q's ring
                         const uint32_t dst = ptx::mapa_shared(s_ring + j * slot_bytes + row_off, peer(q));
@@ -1137,8 +1141,9 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                     release_acc();
                     break;
                 }
+                if (!warp_rows) release_acc();   // (the loop below is this warp's last read otherwise)
 #pragma unroll 1
-                for (uint32_t c = me, oc = 0; c < kTileM / kEpiBoxM; c += S, ++oc) {
+                for (uint32_t c = me, oc = 0; warp_rows && c < kTileM / kEpiBoxM; c += S, ++oc) {
                     const int col = static_cast<int>(c) * kEpiBoxM;
                     float v[64];
                     // the S partials added in range order

@@ -664,6 +664,7 @@ def long_k_mode():
     (4096, 512, 8192, (2,)),       # 64 tiles: clusters of two
     (2000, 700, 4100, (2, 3)),     # ragged m, n, k (repacked): 8 x 6 = 48 tiles; clusters of three if 48 fit
     (8192, 16, 8192, (4,)),        # skinny: 16 valid columns n of 128 per tile, only those exchanged
+    (4096, 40, 8192, (4,)),        # 40 columns n: one warp whole, one in part, two with none (they skip)
     (300, 100, 16384, (4,)),       # 2 tiles: the split-reduce would take 8 ranges, a cluster 4
     (1280, 1024, 8192, (2, 3)),    # 5 x 8 = 40 tiles: clusters of three where 40 of them fit at once
 ])
