@@ -165,6 +165,13 @@ __device__ __forceinline__ void st_shared_cluster_v4(uint32_t cluster_addr, floa
 }
 
 // 16-byte load from this CTA's shared memory.
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float4 ld_shared_v4_f32(uint32_t addr)
 {
     float4 v;

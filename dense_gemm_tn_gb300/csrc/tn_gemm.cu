@@ -52,8 +52,8 @@ struct DeviceState {
     int sms = 0, major = 0, minor = 0;
     // per kernel, indexed [kind: f16, e4m3][1: one CTA, 2: CTA pairs, 3: CTA pairs with 256 x 512 tiles,
     // 4 / 5: one CTA / CTA pairs in k-range clusters]
-    bool smem_attr[2][6] = {};
-    int max_clusters[2][6] = {};      // co-resident clusters of the kernel's own size (0 = not queried yet)
+    bool smem_attr[2][8] = {};
+    int max_clusters[2][8] = {};      // co-resident clusters of the kernel's own size (0 = not queried yet)
     // co-resident clusters of S single CTAs or S CTA pairs (kClusterReduce), by kind, CTAs per tile and S
     // (0 = not queried, -1 = none)
     int cluster_slots[2][3][5] = {};
@@ -401,17 +401,17 @@ struct ASource {
     uint32_t box_k, rows;      // rows: A rows per CTA of a whole tile
 };
 
-// Co-resident slots of tn_gemm_kernel<Kind, G, W, C>: clusters of its own size
-// (one CTA, or a pair), or with C clusters of G * clusters_of CTAs (S pairs or
-// S single CTAs), queried once per device (the kernel's shared-memory
+// Co-resident slots of tn_gemm_kernel<Kind, G, W, C, St>: clusters of its own
+// size (one CTA, or a pair), or with C clusters of G * clusters_of CTAs (S
+// pairs or S single CTAs), queried once per device (the kernel's shared-memory
 // attribute is set first).
-template <class Kind, int G, bool W, bool C = false>
+template <class Kind, int G, bool W, bool C = false, bool St = false>
 gemm_status_t kernel_slots(DeviceState &dev, int clusters_of, int *out)
 {
     using Cfg = tn::TileCfg<G, W>;
-    auto kernel = tn::tn_gemm_kernel<Kind, G, W, C>;
+    auto kernel = tn::tn_gemm_kernel<Kind, G, W, C, St>;
     const int ki = Kind::kF8 ? 1 : 0;
-    const int ks = W ? 3 : C ? 3 + G : G;   // kernel index of the per-device caches
+    const int ks = W ? 3 : C ? 3 + G : St ? 5 + G : G;   // kernel index of the per-device caches
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!dev.smem_attr[ki][ks]) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
@@ -504,6 +504,13 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     // (kSplitReduce).
     const int cap = slots;
     const bool stats = (prm.flags & tn::kFlagStats) != 0;
+    if constexpr (!W && !Kind::kF8) {
+        if (stats) {
+            // the statistics variant (its own shared-memory attribute, the same slots)
+            gemm_status_t st = kernel_slots<Kind, G, false, false, true>(dev, 1, &slots);
+            if (st != GEMM_OK) return st;
+        }
+    }
     const int long_k = g_long_k.load();
     int reduce_parts = 1, cluster_parts = 1;
     if (!W && !stats) cluster_parts = cluster_reduce_parts<Kind, G>(dev, prm.num_tiles, prm.num_kb, cap, allow_alloc, long_k);
@@ -604,6 +611,9 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     t_rec.split_parts = prm.split_parts;
     if constexpr (!W) {
         if (cluster_parts > 1) kernel = tn::tn_gemm_kernel<Kind, G, false, true>;
+        if constexpr (!Kind::kF8) {
+            if (stats) kernel = tn::tn_gemm_kernel<Kind, G, false, false, true>;
+        }
     }
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));

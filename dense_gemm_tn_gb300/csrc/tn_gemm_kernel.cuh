@@ -479,65 +479,39 @@ __device__ __forceinline__ void stat_merge(float &m, float &s, float m2, float s
     m = mx;
 }
 
-// Each lane holds 32 scores x[j] (one per column j; -inf where the lane has
-// no column n).  Afterwards lane l holds, for column l, the maximum over the
-// 32 lanes and the sum of exp(x - maximum).  Two passes: the maximum by five
-// halving exchanges (each lane keeps half of its columns and takes its
-// partner's values for them), a broadcast of the 32 maxima, one exp per
-// score, and the sums by the same five exchanges.
-__device__ __forceinline__ void stat_reduce32_step_max(float (&v)[32], int lane)
-{
-#pragma unroll
-    for (int step = 0; step < 5; ++step) {
-        const int o = 16 >> step;
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int j = 0; j < o; ++j) {
-            const float keep = upper ? v[j + o] : v[j];
-            const float give = upper ? v[j] : v[j + o];
-            v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, give, o));
-        }
-    }
-}
-
-__device__ __forceinline__ void stat_reduce32_step_sum(float (&v)[32], int lane)
-{
-#pragma unroll
-    for (int step = 0; step < 5; ++step) {
-        const int o = 16 >> step;
-        const bool upper = (lane & o) != 0;
-#pragma unroll
-        for (int j = 0; j < o; ++j) {
-            const float keep = upper ? v[j + o] : v[j];
-            const float give = upper ? v[j] : v[j + o];
-            v[j] = keep + __shfl_xor_sync(0xffffffffu, give, o);
-        }
-    }
-}
-
-__device__ __forceinline__ float2 stat_warp_reduce32(const float (&x)[32], int lane)
+// (max, sum of exp(x - max)) of one row's 32 scores, held by one thread: the
+// maximum by a tree of fmaxf, then the exponentials and their sum by a tree of
+// adds.  Scores of absent columns are -inf (they add 0); a row with no score
+// is (-inf, 0).
+__device__ __forceinline__ float2 stat_row32(const float (&x)[32])
 {
     float t[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) t[j] = x[j];
-    stat_reduce32_step_max(t, lane);            // t[0] = maximum of column `lane`
-    const float col_max = t[0];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const float mj = __shfl_sync(0xffffffffu, col_max, j);
-        t[j] = mj == -INFINITY ? 0.0f : exp_nonpos(x[j] - mj);
-    }
-    stat_reduce32_step_sum(t, lane);            // t[0] = sum for column `lane`
-    return make_float2(col_max, t[0]);
+    for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+    const float mx = t[0];
+    if (mx == -INFINITY) return make_float2(mx, 0.0f);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) t[j] = exp_nonpos(x[j] - mx);
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) t[j] = t[j] + t[j + w];
+    return make_float2(mx, t[0]);
 }
 
 // ------------------------------------------------------------------ kernel
 // kCluster: the kClusterReduce variant (launched in clusters of S single CTAs
-// or S CTA pairs); the other variants carry none of its code.
-template <class Kind, int kGroup, bool kWide = false, bool kCluster = false>
+// or S CTA pairs); kStats: the variant with the softmax-statistics epilogue
+// (kFlagStats).  The other variants carry none of their code.
+template <class Kind, int kGroup, bool kWide = false, bool kCluster = false, bool kStats = false>
 __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_constant__ KernelParams p)
 {
     static_assert(!(kWide && kCluster), "256 x 512 tiles are not reduced in clusters");
+    static_assert(!kStats || (!Kind::kF8 && !kWide && !kCluster), "the statistics are an FP16 epilogue of plain tiles");
     using Cfg = TileCfg<kGroup, kWide>;
     constexpr int kStages = Cfg::kStages;
     constexpr int kBlockKElems = kBlockKBytes / Kind::kElemBytes;   // K elements per atom
@@ -1260,7 +1234,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                 // (a wide tile's m parts are its 256-row halves)
                 const int n_chunks = un.mpart < 0 ? Cfg::kTileMRows / kEpiBoxM
                                                   : (kWide ? kTileM : (quarter_m ? kTileM / 4 : kTileM / 2)) / kEpiBoxM;
-                const bool stats = !Kind::kF8 && !kWide && (flags & kFlagStats) != 0;
+                const bool stats = kStats && (flags & kFlagStats) != 0;
                 if (kWide && un.mpart < 0) {
                     // A whole wide tile, half by half: the first two chunks of the half go
                     // through the staging buffers, the last two are read into registers
@@ -1302,23 +1276,52 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
                             for (int j = 0; j < 64; ++j) v[j] = __fmul_rn(v[j], p.scale);
                         }
                     }
-                    store_chunk(v, m0 + c * kEpiBoxM, nw);
+                    bool stored = false;
                     if constexpr (!Kind::kF8) {
                         if (stats) {
-                            // this warp's (max, sum) over its 32 columns n, for the chunk's 64 rows m
+                            // C's 16-bit values first: the FP32 scores are dead once staged below.
+                            uint32_t packed[32];
+                            pack_chunk(v, packed);
+                            // This warp's (max, sum) over its 32 columns n, for each of the chunk's
+                            // 64 rows m, through its two staging buffers (8 KiB): each lane (a
+                            // column n) writes its 64 scores as one row, then lane l reduces rows
+                            // l and 32 + l over the 32 columns in registers.  The 16-byte unit i
+                            // of row n sits at unit i ^ (n & 15), so neither the row writes nor
+                            // the column reads meet a bank conflict.  (Measured on GB300, the same
+                            // reduction by halving shuffle exchanges took 0.96 us per 32 rows.)
                             const bool valid = nw + lane < p.N;
+                            const uint32_t sbuf = s_epi + ew * kEpiBufs * kEpiBufBytes;
+                            if (lane == 0) ptx::bulk_wait_group_read<0>();   // earlier C stores have read both
+                            __syncwarp();
+                            constexpr uint32_t kNegInf = 0xFF800000u;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const uint32_t a = sbuf + lane * (kEpiBoxM * 4) + ((i ^ (lane & 15)) << 4);
+                                ptx::st_shared_v4(a, valid ? __float_as_uint(v[4 * i]) : kNegInf,
+                                                  valid ? __float_as_uint(v[4 * i + 1]) : kNegInf,
+                                                  valid ? __float_as_uint(v[4 * i + 2]) : kNegInf,
+                                                  valid ? __float_as_uint(v[4 * i + 3]) : kNegInf);
+                            }
+                            __syncwarp();
                             float2 *part = p.stat_parts +
                                            (static_cast<int64_t>(un.tm) * p.stat_ctas * kEpiWarps +
                                             (un.tn * kGroup + pos) * kEpiWarps + quarter) * kTileM;
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
+                                const int m = 32 * h + lane;     // this lane's row within the chunk
                                 float x[32];
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) x[j] = valid ? v[32 * h + j] : -INFINITY;
-                                part[m_in_tile + c * kEpiBoxM + 32 * h + lane] = stat_warp_reduce32(x, lane);
+                                for (int n = 0; n < 32; ++n)
+                                    x[n] = ptx::ld_shared_f32(sbuf + n * (kEpiBoxM * 4) + (((m >> 2) ^ (n & 15)) << 4) +
+                                                              (m & 3) * 4);
+                                part[m_in_tile + c * kEpiBoxM + m] = stat_row32(x);
                             }
+                            __syncwarp();   // every lane's reads are done before the C store reuses the buffers
+                            store_packed(packed, m0 + c * kEpiBoxM, nw);
+                            stored = true;
                         }
                     }
+                    if (!stored) store_chunk(v, m0 + c * kEpiBoxM, nw);
                 }
                 if constexpr (!Kind::kF8) {
                     if (stats) {
