@@ -200,6 +200,17 @@ __device__ __forceinline__ void st_release_cluster_u32(uint32_t cluster_addr, ui
     asm volatile("st.release.cluster.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
+// Atomic add at GPU scope with acquire-release order: the caller's earlier
+// writes (and, through a barrier before it, its CTA's) are visible to whoever
+// acquires the new value, and writes released before the old value are
+// visible to the caller.  Returns the old value.
+__device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long long *addr, unsigned long long v)
+{
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(addr), "l"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v)
 {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
