@@ -29,6 +29,10 @@ namespace {
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 256;   // TMA coordinates are signed 32-bit
 constexpr int kMaxDevices = 64;
 constexpr int kGroupM = 8;                               // tile rows per raster group
+// Half-m units run lean up to this many k blocks (their lean ring has two
+// stages).  Measured on GB300, back to back with inputs from HBM: 2048 x 1024
+// x 128 4.24 -> 3.74 us, x 256 4.86 -> 4.73 us, but x 512 6.01 -> 6.85 us.
+constexpr int kLeanHalfMaxKb = 4;
 // Odd waves walk K backwards (kFlagAltK).  Measured on GB300 at 8192^3 (256 x
 // 512 tiles, FP16, under the power cap): DRAM reads 815 -> 684 MB per launch,
 // 1612 -> 1626 TFLOP/s; E4M3 3212 -> 3225.
@@ -52,8 +56,8 @@ struct DeviceState {
     int sms = 0, major = 0, minor = 0;
     // per kernel, indexed [kind: f16, e4m3][1: one CTA, 2: CTA pairs, 3: CTA pairs with 256 x 512 tiles,
     // 4 / 5: one CTA / CTA pairs in k-range clusters]
-    bool smem_attr[2][8] = {};
-    int max_clusters[2][8] = {};      // co-resident clusters of the kernel's own size (0 = not queried yet)
+    bool smem_attr[2][10] = {};
+    int max_clusters[2][10] = {};     // co-resident clusters of the kernel's own size (0 = not queried yet)
     // co-resident clusters of S single CTAs or S CTA pairs (kClusterReduce), by kind, CTAs per tile and S
     // (0 = not queried, -1 = none)
     int cluster_slots[2][3][5] = {};
@@ -96,6 +100,7 @@ std::atomic<int> g_raster_group{0};     // tile rows per raster group; 0: kGroup
 std::atomic<int> g_k_order{0};          // 0: the library's choice; 1: every tile forward; 2: odd waves reversed
 std::atomic<unsigned long long *> g_clock_probe{nullptr};   // gemm_debug_set_clock_probe
 std::atomic<int> g_long_k{0};           // small grids with a long K: 0 the library's choice; 1 split-reduce; 2 cluster
+std::atomic<int> g_lean{0};             // m-part launches: 0 the library's choice; 1 never lean; 2 lean where units allow
 // The last launch on this host thread, for gemm_debug_last_launch: the
 // numbers are kept and formatted only when asked for (formatting every call
 // cost host time on the path of back-to-back small GEMMs).
@@ -103,7 +108,7 @@ struct LaunchRecord {
     const char *name = nullptr;     // nullptr: nothing launched yet
     bool quant = false;
     int G = 0, wide = 0, grid = 0, clusters = 0, slots = 0;
-    int tiles = 0, units = 0, tail_start = 0, tail_mode = 0, split_parts = 0, vec = 0, cluster = 0;
+    int tiles = 0, units = 0, tail_start = 0, tail_mode = 0, split_parts = 0, vec = 0, cluster = 0, lean = 0;
     long long qgrid = 0, qunits = 0;
 };
 thread_local LaunchRecord t_rec;
@@ -401,17 +406,17 @@ struct ASource {
     uint32_t box_k, rows;      // rows: A rows per CTA of a whole tile
 };
 
-// Co-resident slots of tn_gemm_kernel<Kind, G, W, C, St>: clusters of its own
-// size (one CTA, or a pair), or with C clusters of G * clusters_of CTAs (S
+// Co-resident slots of tn_gemm_kernel<Kind, G, W, C, St, Ln>: clusters of its
+// own size (one CTA, or a pair), or with C clusters of G * clusters_of CTAs (S
 // pairs or S single CTAs), queried once per device (the kernel's shared-memory
 // attribute is set first).
-template <class Kind, int G, bool W, bool C = false, bool St = false>
+template <class Kind, int G, bool W, bool C = false, bool St = false, int Ln = 0>
 gemm_status_t kernel_slots(DeviceState &dev, int clusters_of, int *out)
 {
-    using Cfg = tn::TileCfg<G, W>;
-    auto kernel = tn::tn_gemm_kernel<Kind, G, W, C, St>;
+    using Cfg = tn::TileCfg<G, W, Ln>;
+    auto kernel = tn::tn_gemm_kernel<Kind, G, W, C, St, Ln>;
     const int ki = Kind::kF8 ? 1 : 0;
-    const int ks = W ? 3 : C ? 3 + G : St ? 5 + G : G;   // kernel index of the per-device caches
+    const int ks = Ln == 4 ? 8 : Ln == 2 ? 9 : W ? 3 : C ? 3 + G : St ? 5 + G : G;   // kernel index of the per-device caches
     std::lock_guard<std::mutex> lock(g_mutex);
     if (!dev.smem_attr[ki][ks]) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
@@ -596,8 +601,35 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
                                          asrc.row_bytes, asrc.box_k, asrc.rows / prm.split_parts, "A part");
         if (st != GEMM_OK) return st;
     }
+    // Every unit a quarter-m (half-m) unit of a single CTA -- a grid of at
+    // most a quarter (half) of the slots' tiles with a short K: the lean
+    // configuration, two CTAs per SM, so that the launch's CTAs become
+    // resident beside the previous launch's and do their setup while it runs.
+    // Half-m units only up to kLeanHalfMaxKb k blocks (their ring has two
+    // stages).  Not with the softmax statistics: their epilogue, the longer
+    // part of such a launch, ran slower under the lean register limit and with
+    // two CTAs on an SM.
+    int lean = 0;
+    if constexpr (G == 1 && !W) {
+        const int mode = g_lean.load();
+        if (prm.tail_mode == tn::kTailMParts && prm.tail_start == 0 && !stats && mode != 1) {
+            if (prm.split_parts == 4)
+                lean = 4;
+            else if (prm.split_parts == 2 && (mode == 2 || prm.num_kb <= kLeanHalfMaxKb))
+                lean = 2;
+        }
+        if (lean) {
+            int n = 0;
+            gemm_status_t st = lean == 4 ? kernel_slots<Kind, 1, false, false, false, 4>(dev, 1, &n)
+                                         : kernel_slots<Kind, 1, false, false, false, 2>(dev, 1, &n);
+            if (st != GEMM_OK) return st;
+            cfg.dynamicSmemBytes =
+                lean == 4 ? tn::TileCfg<1, false, 4>::kSmemBytes : tn::TileCfg<1, false, 2>::kSmemBytes;
+        }
+    }
     t_rec.name = name;
     t_rec.quant = false;
+    t_rec.lean = lean;
     t_rec.G = G;
     t_rec.wide = W ? 1 : 0;
     t_rec.grid = G * cluster_parts * clusters;
@@ -614,6 +646,10 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
         if constexpr (!Kind::kF8) {
             if (stats) kernel = tn::tn_gemm_kernel<Kind, G, false, false, true>;
         }
+    }
+    if constexpr (G == 1 && !W) {
+        if (lean == 4) kernel = tn::tn_gemm_kernel<Kind, 1, false, false, false, 4>;
+        if (lean == 2) kernel = tn::tn_gemm_kernel<Kind, 1, false, false, false, 2>;
     }
     cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
     if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));
@@ -1122,6 +1158,13 @@ int gemm_debug_set_long_k_mode(int mode)
     return 0;
 }
 
+int gemm_debug_set_lean_mode(int mode)
+{
+    if (mode < 0 || mode > 2) return -1;
+    g_lean.store(mode);
+    return 0;
+}
+
 const char *gemm_debug_last_launch(void)
 {
     const LaunchRecord &r = t_rec;
@@ -1133,9 +1176,9 @@ const char *gemm_debug_last_launch(void)
     else
         snprintf(t_last_launch, sizeof(t_last_launch),
                  "%s: ctas_per_cluster=%d wide=%d grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d "
-                 "tail_mode=%d split_parts=%d",
+                 "tail_mode=%d split_parts=%d lean=%d",
                  r.name, r.cluster, r.wide, r.grid, r.clusters, r.slots, r.tiles, r.units,
-                 r.tail_start, r.tail_mode, r.split_parts);
+                 r.tail_start, r.tail_mode, r.split_parts, r.lean);
     return t_last_launch;
 }
 
@@ -1145,11 +1188,14 @@ const char *gemm_build_info(void)
     snprintf(info, sizeof(info),
              "dense_gemm_tn sm_103a: CTA-pair tile 256x256 in 2-CTA clusters, %d stages of %d B "
              "of K, %d B smem; CTA-pair tile 256x512, %d stages of %d B of K, %d B smem; 1-CTA tile 128x256, "
-             "%d stages of %d B of K, %d B smem; TMEM %u cols; raster group %d",
+             "%d stages of %d B of K, %d B smem; TMEM %u cols; lean 1-CTA quarter-m units, %d stages, %d B smem, "
+             "TMEM %u cols; half-m units, %d stages, %d B smem, TMEM %u cols; raster group %d",
              tn::TileCfg<2>::kStages, tn::TileCfg<2>::kStageKBytes, tn::TileCfg<2>::kSmemBytes,
              tn::TileCfg<2, true>::kStages, tn::TileCfg<2, true>::kStageKBytes, tn::TileCfg<2, true>::kSmemBytes,
-             tn::TileCfg<1>::kStages, tn::TileCfg<1>::kStageKBytes, tn::TileCfg<1>::kSmemBytes, tn::kTmemCols,
-             kGroupM);
+             tn::TileCfg<1>::kStages, tn::TileCfg<1>::kStageKBytes, tn::TileCfg<1>::kSmemBytes, tn::TileCfg<1>::kTmemCols,
+             tn::TileCfg<1, false, 4>::kStages, tn::TileCfg<1, false, 4>::kSmemBytes,
+             tn::TileCfg<1, false, 4>::kTmemCols, tn::TileCfg<1, false, 2>::kStages,
+             tn::TileCfg<1, false, 2>::kSmemBytes, tn::TileCfg<1, false, 2>::kTmemCols, kGroupM);
     return info;
 }
 

@@ -58,8 +58,6 @@ constexpr int kEpiBufBytes = kEpiBoxN * kEpiBoxM * 2;       // 4 KiB
 constexpr int kEpiBufs = 2;                 // per epilogue warp (ping-pong)
 constexpr int kSmemEpi = kEpiWarps * kEpiBufs * kEpiBufBytes;
 constexpr int kTileM = 256;                 // C rows m per tile = MMA N = TMEM columns per accumulator
-constexpr uint32_t kAccCols = kTileM;
-constexpr uint32_t kTmemCols = 2 * kAccCols;  // double-buffered accumulator = all 512 columns
 
 // kGroup = 1: one CTA computes a 128 (n) x 256 (m) tile with M128 MMAs.
 // kGroup = 2: a CTA pair (a cluster of two CTAs) computes a 256 (n) x 256 (m)
@@ -85,9 +83,23 @@ constexpr uint32_t kTmemCols = 2 * kAccCols;  // double-buffered accumulator = a
 // to have read that half (it hands the halves back one at a time).
 // Measured on GB300 under the power cap (8192^3 FP16), the lower L2 traffic
 // lets the SMs run at a 7-9 % higher clock for the same work per clock.
-template <int kGroup, bool kWide = false>
+//
+// kLean = 4 or 2 (single CTAs only): the configuration of launches whose units
+// are all quarter-m (or half-m) units -- a grid of few tiles with a short K,
+// each tile cut into four 64-row (two 128-row) ranges of m.  Its ring holds
+// just such a unit's A rows (three stages of 24 KiB, or two of 32 KiB), its
+// accumulators take 64 (128) TMEM columns each, and it is compiled for two
+// CTAs per SM (at most 168 registers a thread), so that a launch's CTAs all
+// become resident while the previous launch on the stream still runs and do
+// their setup in its shadow.  With one 226 KiB CTA per SM, only the CTAs that
+// found an idle SM started early; the rest entered as the previous launch's
+// CTAs left and ran their first-time code (the parameter reads, the first
+// unit's schedule) after the previous grid had completed.
+template <int kGroup, bool kWide = false, int kLean = 0>
 struct TileCfg {
     static_assert(!kWide || kGroup == 2, "256 x 512 tiles are CTA-pair tiles");
+    static_assert(kLean == 0 || (kGroup == 1 && !kWide && (kLean == 2 || kLean == 4)),
+                  "the lean configurations are single-CTA ones of half-m or quarter-m units");
     static constexpr int kCtas = kGroup;                   // CTAs per cluster
     static constexpr int kTileN = 128 * kGroup;            // C columns n per pair tile = MMA M
     static constexpr int kTileMRows = kWide ? 2 * kTileM : kTileM;   // C rows m per tile
@@ -96,10 +108,11 @@ struct TileCfg {
     static constexpr int kRowsA = kTileMRows / kGroup;      // A rows (m) per CTA and stage
     static constexpr int kAtoms = kGroup == 2 && !kWide ? 2 : 1;   // 128-byte K atoms per stage
     static constexpr int kStageKBytes = kAtoms * kBlockKBytes;
-    static constexpr int kStages = kGroup == 2 && !kWide ? 3 : 4;
+    static constexpr int kStages = kLean == 4 ? 3 : kLean == 2 ? 2 : kGroup == 2 && !kWide ? 3 : 4;
     static constexpr int kHalfABytes = kTileM / kGroup * kBlockKBytes;   // one half's A rows of one atom
+    static constexpr int kRingRowsA = kLean ? kRowsA / kLean : kRowsA;   // A rows a stage has room for
     static constexpr int kAtomBBytes = kRowsB * kBlockKBytes;
-    static constexpr int kAtomABytes = kRowsA * kBlockKBytes;
+    static constexpr int kAtomABytes = kRingRowsA * kBlockKBytes;
     static constexpr int kTileBBytes = kAtoms * kAtomBBytes;
     static constexpr int kTileABytes = kAtoms * kAtomABytes;
     static constexpr int kStageBytes = kTileBBytes + kTileABytes;
@@ -108,6 +121,12 @@ struct TileCfg {
     static constexpr int kNumBarriers = kStages * (kAtoms + 1) + 8;
     static constexpr int kSmemBytes = 1024 /* alignment slack */ + kSmemRing + kSmemEpi + kNumBarriers * 8 + 32;
     static_assert(kSmemBytes <= 232448, "exceeds the 227 KiB shared memory of one CTA");
+    // two CTAs per SM: 228 KiB of shared memory, 1 KiB of it reserved per CTA
+    static_assert(!kLean || 2 * (kSmemBytes + 1024) <= 233472, "two lean CTAs must fit one SM");
+    // TMEM columns of one accumulator (MMA N of a unit) and of the allocation
+    // (two accumulators: a unit's epilogue overlaps the next unit's MMAs)
+    static constexpr uint32_t kAccCols = kLean ? kTileM / kLean : kTileM;
+    static constexpr uint32_t kTmemCols = 2 * kAccCols;
 };
 
 // How tiles are cut into several units each (split_parts of them): the tiles
@@ -506,13 +525,20 @@ __device__ __forceinline__ float2 stat_row32(const float (&x)[32])
 // ------------------------------------------------------------------ kernel
 // kCluster: the kClusterReduce variant (launched in clusters of S single CTAs
 // or S CTA pairs); kStats: the variant with the softmax-statistics epilogue
-// (kFlagStats).  The other variants carry none of their code.
-template <class Kind, int kGroup, bool kWide = false, bool kCluster = false, bool kStats = false>
-__global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_constant__ KernelParams p)
+// (kFlagStats).  The other variants carry none of their code.  kLean = 4 or
+// 2: the two-CTAs-per-SM configuration of TileCfg, launched only when every
+// unit is a quarter-m (half-m) unit: kTailMParts with split_parts = kLean from
+// the first tile.
+template <class Kind, int kGroup, bool kWide = false, bool kCluster = false, bool kStats = false, int kLean = 0>
+__global__ void __launch_bounds__(kThreads, kLean ? 2 : 1) tn_gemm_kernel(const __grid_constant__ KernelParams p)
 {
     static_assert(!(kWide && kCluster), "256 x 512 tiles are not reduced in clusters");
     static_assert(!kStats || (!Kind::kF8 && !kWide && !kCluster), "the statistics are an FP16 epilogue of plain tiles");
-    using Cfg = TileCfg<kGroup, kWide>;
+    static_assert(!kLean || (!kCluster && !kStats), "the lean configurations are ones of plain m-part units");
+    static_assert(kMaxMParts == 4, "m parts are halves or quarters");
+    using Cfg = TileCfg<kGroup, kWide, kLean>;
+    constexpr uint32_t kAccCols = Cfg::kAccCols;
+    constexpr uint32_t kTmemCols = Cfg::kTmemCols;
     constexpr int kStages = Cfg::kStages;
     constexpr int kBlockKElems = kBlockKBytes / Kind::kElemBytes;   // K elements per atom
     constexpr uint32_t kIdesc = ptx::idesc_f32acc(Cfg::kTileN, kTileM, Kind::kFmt, Kind::kFmt);
@@ -631,6 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
     // A rows of this CTA per stage, and their bytes
     const int32_t part_rows_a = quarter_m ? Cfg::kRowsA / 4 : Cfg::kRowsA / 2;
     auto a_bytes = [&](const Unit &un) -> uint32_t {
+        if constexpr (kLean != 0) return static_cast<uint32_t>(Cfg::kTileABytes);   // (every unit an m part)
         return un.mpart < 0 ? Cfg::kTileABytes : (quarter_m ? Cfg::kTileABytes / 4 : Cfg::kTileABytes / 2);
     };
     const Unit unit0 = slot_unit_at(0);      // (a phantom when the slot has no unit)
@@ -665,20 +692,29 @@ __global__ void __launch_bounds__(kThreads, 1) tn_gemm_kernel(const __grid_const
         return b;
     };
 
-    // The k ranges of a tile reduced in a cluster (the small grids with a long
-    // K): each CTA's work starts with a stream of its operands, and as a
-    // programmatic dependent it often waits below while the previous kernel
-    // drains.  The first kPrefetchAtoms K atoms of its boxes are prefetched into
-    // L2 before that wait.  A prefetch returns no data to the CTA, so it cannot
-    // read ahead of the previous kernel's writes: the loads after the wait read
-    // through L2, which every write reaches first.  (Measured on GB300, back to
-    // back: 8192 x 16 x 8192 27.44 -> 26.23 us, 4096 x 512 x 8192 31.02 -> 30.63
-    // us, 4096 x 256 x 4096 19.14 -> 18.77 us.  With few k blocks per unit, e.g.
-    // 2048 x 2048 x 512, prefetching made calls 2-7 % slower: the prefetches
-    // queue ahead of the loads.)
-    if (kCluster && warp == 0 && lane == 0 && !unit0.phantom && unit0.nkb >= kPrefetchMinKb) {
+    // Two kinds of launch whose CTAs often wait below, as programmatic
+    // dependents, while the previous kernel drains, prefetch their first fills
+    // into L2 before that wait:
+    //  - the k ranges of a tile reduced in a cluster (the small grids with a
+    //    long K), whose work starts with a stream of its operands: the first
+    //    kPrefetchAtoms K atoms of the boxes, if the unit has kPrefetchMinKb k
+    //    blocks or more.  Measured on GB300, back to back: 8192 x 16 x 8192
+    //    27.44 -> 26.23 us, 4096 x 512 x 8192 31.02 -> 30.63 us, 4096 x 256 x
+    //    4096 19.14 -> 18.77 us.  With few k blocks per unit, e.g. 2048 x 2048
+    //    x 512, it made calls 2-7 % slower: the prefetches queue ahead of the
+    //    loads.
+    //  - the lean launches, whose CTAs become resident while the previous
+    //    launch runs: the first k block.  Back to back with inputs from HBM,
+    //    1024 x 1024 x 128 3.56 -> 3.45 us, 512^3 5.50 -> 5.36 us; four k
+    //    blocks gained no more, and with the inputs already in L2 (CUDA-graph
+    //    replays) one block costs 0.04-0.1 us and four 0.05-0.2 us.
+    // A prefetch returns no data to the CTA, so it cannot read ahead of the
+    // previous kernel's writes: the loads after the wait read through L2, which
+    // every write reaches first.
+    if ((kCluster || kLean) && warp == 0 && lane == 0 && !unit0.phantom && (kLean || unit0.nkb >= kPrefetchMinKb)) {
         const Boxes bx = boxes_of(unit0);
-        for (int i = 0; i < kPrefetchAtoms / Cfg::kAtoms; ++i) {
+        constexpr int kFills = kLean ? 1 : kPrefetchAtoms / Cfg::kAtoms;
+        for (int i = 0; i < kFills; ++i) {
             const int kb = bx.rev ? unit0.kb0 + unit0.nkb - 1 - i : unit0.kb0 + i;
             if (kb >= p.num_kb) continue;   // (the zero-filled end of a last k range)
 #pragma unroll

@@ -337,6 +337,20 @@ int gemm_debug_set_k_order(int mode);
 int gemm_debug_set_long_k_mode(int mode);
 
 /*
+ * Test hook: the configuration of launches whose units are all m-part units
+ * of single CTAs (grids of at most half the co-resident slots' tiles with a
+ * short K, each tile cut into four 64-row or two 128-row ranges of m).  The
+ * lean configuration has a ring sized for such a unit (three stages of 24 KiB
+ * for quarters, two of 32 KiB for halves), 128 or 256 TMEM columns, and runs
+ * two CTAs per SM; the full one has four stages of 48 KiB, 512 columns and
+ * one CTA per SM.  0 (default): the library's choice (lean for quarters, and
+ * for halves with few k blocks); 1: always the full one; 2: lean wherever the
+ * units are quarters or halves.  The arithmetic, and so every result, is the
+ * same.  Returns 0, or -1 for other values.
+ */
+int gemm_debug_set_lean_mode(int mode);
+
+/*
  * Measurement hook: while `counters` (a DEVICE pointer to 3 zeroed unsigned
  * 64-bit words) is set, every GEMM kernel launched afterwards adds, from the
  * first thread of its first CTA, the SM cycles (%clock64) and nanoseconds
