@@ -29,9 +29,16 @@ namespace {
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 256;   // TMA coordinates are signed 32-bit
 constexpr int kMaxDevices = 64;
 constexpr int kGroupM = 8;                               // tile rows per raster group
-// Half-m units run lean up to this many k blocks (their lean ring has two
-// stages).  Measured on GB300, back to back with inputs from HBM: 2048 x 1024
-// x 128 4.24 -> 3.74 us, x 256 4.86 -> 4.73 us, but x 512 6.01 -> 6.85 us.
+// The lean configuration (two CTAs per SM) for launches of m-part units
+// that fill more than half of the slots, up to this many k blocks: quarters
+// (a ring of three stages) and halves (two stages).  Measured on GB300, back
+// to back with inputs from HBM, full -> lean: 1024 x 1024 x 128 3.89 -> 3.40
+// us, x 512 5.64 -> 5.30, but x 1984 12.11 -> 13.44; 2048 x 1024 x 128 4.24
+// -> 3.74, x 256 4.86 -> 4.73, but x 512 6.01 -> 6.85.  Launches of at most
+// half the slots leave room for the next launch's CTAs beside them anyway,
+// and there the deeper ring of the full configuration was as fast or faster
+// (512^3 5.20 -> 5.32, 1024 x 512 x 1024 7.46 -> 7.96).
+constexpr int kLeanQuarterMaxKb = 8;
 constexpr int kLeanHalfMaxKb = 4;
 // Odd waves walk K backwards (kFlagAltK).  Measured on GB300 at 8192^3 (256 x
 // 512 tiles, FP16, under the power cap): DRAM reads 815 -> 684 MB per launch,
@@ -602,20 +609,22 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
         if (st != GEMM_OK) return st;
     }
     // Every unit a quarter-m (half-m) unit of a single CTA -- a grid of at
-    // most a quarter (half) of the slots' tiles with a short K: the lean
-    // configuration, two CTAs per SM, so that the launch's CTAs become
-    // resident beside the previous launch's and do their setup while it runs.
-    // Half-m units only up to kLeanHalfMaxKb k blocks (their ring has two
-    // stages).  Not with the softmax statistics: their epilogue, the longer
-    // part of such a launch, ran slower under the lean register limit and with
-    // two CTAs on an SM.
+    // most a quarter (half) of the slots' tiles with a short K -- and more
+    // units than half the slots, so that the next launch's CTAs would not
+    // find idle SMs: the lean configuration, two CTAs per SM, whose CTAs
+    // become resident beside the previous launch's and do their setup while
+    // it runs (up to kLeanQuarterMaxKb / kLeanHalfMaxKb k blocks).  Not with
+    // the softmax statistics: their epilogue, the longer part of such a
+    // launch, ran slower under the lean register limit and with two CTAs on
+    // an SM.
     int lean = 0;
     if constexpr (G == 1 && !W) {
         const int mode = g_lean.load();
         if (prm.tail_mode == tn::kTailMParts && prm.tail_start == 0 && !stats && mode != 1) {
-            if (prm.split_parts == 4)
+            const bool crowded = 2 * prm.num_units > slots;
+            if (prm.split_parts == 4 && (mode == 2 || (crowded && prm.num_kb <= kLeanQuarterMaxKb)))
                 lean = 4;
-            else if (prm.split_parts == 2 && (mode == 2 || prm.num_kb <= kLeanHalfMaxKb))
+            else if (prm.split_parts == 2 && (mode == 2 || (crowded && prm.num_kb <= kLeanHalfMaxKb)))
                 lean = 2;
         }
         if (lean) {

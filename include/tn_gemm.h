@@ -343,10 +343,11 @@ int gemm_debug_set_long_k_mode(int mode);
  * lean configuration has a ring sized for such a unit (three stages of 24 KiB
  * for quarters, two of 32 KiB for halves), 128 or 256 TMEM columns, and runs
  * two CTAs per SM; the full one has four stages of 48 KiB, 512 columns and
- * one CTA per SM.  0 (default): the library's choice (lean for quarters, and
- * for halves with few k blocks); 1: always the full one; 2: lean wherever the
- * units are quarters or halves.  The arithmetic, and so every result, is the
- * same.  Returns 0, or -1 for other values.
+ * one CTA per SM.  0 (default): the library's choice (lean for launches of
+ * more units than half the co-resident slots with at most 8 k blocks, 4 for
+ * halves); 1: always the full one; 2: lean wherever the units are quarters
+ * or halves.  The arithmetic, and so every result, is the same.  Returns 0,
+ * or -1 for other values.
  */
 int gemm_debug_set_lean_mode(int mode);
 

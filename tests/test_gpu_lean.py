@@ -1,12 +1,14 @@
 """The lean single-CTA configurations: launches whose units are all quarter-m
-units, or half-m units with at most 4 k blocks (grids of few tiles with a
-short K), run a variant compiled for two CTAs per SM, with a ring sized for
-such a unit (three stages for quarters, two for halves) and 128 or 256 TMEM
-columns.  Its arithmetic is the full configuration's (the same MMAs in the
-same k order), so:
+or half-m units (grids of few tiles with a short K) can run a variant compiled
+for two CTAs per SM, with a ring sized for such a unit (three stages for
+quarters, two for halves) and 128 or 256 TMEM columns.  The library picks it
+for such launches of more units than half the slots with at most 8 (halves:
+4) k blocks; gemm_debug_set_lean_mode(2) forces it wherever the units allow,
+(1) forbids it.  Its arithmetic is the full configuration's (the same MMAs in
+the same k order), so:
   - +-1 inputs give the oracle's bits on every output;
-  - Gaussian inputs give the full configuration's bits (gemm_debug_set_lean_mode(1))
-    and stay within the FP16 / FP8 tolerances of the oracle;
+  - Gaussian inputs give the full configuration's bits and stay within the
+    FP16 / FP8 tolerances of the oracle;
   - launches issued back to back, whose CTAs share SMs with the previous
     launch's, leave each output intact.
 """
@@ -38,8 +40,8 @@ def record(g):
 
 
 # (M, N, K, m parts): grids of at most a quarter (half) of the slots'
-# single-CTA tiles with fewer than 32 (at most 4) k blocks, so every tile is
-# cut into four (two) m parts
+# single-CTA tiles with fewer than 32 k blocks, so every tile is cut into four
+# (two) m parts; run lean by mode 2 whatever their unit and k block counts
 LEAN_SHAPES = [
     (1024, 1024, 128, 4),    # the QK^T block
     (512, 512, 512, 4),      # 8 k blocks through a 3-stage ring
@@ -47,7 +49,7 @@ LEAN_SHAPES = [
     (1000, 700, 136, 4),     # ragged m, n and a zero-filled last k block
     (700, 300, 40, 4),
     (64, 8, 8, 4),
-    (1024, 1024, 1984, 4),   # 31 k blocks: the ring wraps ten times
+    (1024, 1024, 1984, 4),   # 31 k blocks: the 3-stage ring wraps ten times
     (300, 1, 24, 4),         # one column n
     (2048, 1024, 128, 2),    # half-m units: 2 k blocks through a 2-stage ring
     (1024, 2048, 256, 2),
@@ -59,9 +61,12 @@ LEAN_SHAPES = [
 def test_lean_pm1_exact(g, M, N, K, parts):
     A = synth.sign_fp16(M * K, 9700 + M % 89)
     B = synth.sign_fp16(N * K, 9701 + N % 89)
-    g.gemm_debug_set_lean_mode(0)
-    got = run_f16(M, N, K, A, K, B, K)
-    rec = record(g)
+    g.gemm_debug_set_lean_mode(2)
+    try:
+        got = run_f16(M, N, K, A, K, B, K)
+        rec = record(g)
+    finally:
+        g.gemm_debug_set_lean_mode(0)
     assert rec["lean"] == parts and rec["tail_mode"] == 1 and rec["split_parts"] == parts, g.last_launch()
     Cref, _, _ = oracle.gemm_f16_tn(M, N, K, A, K, B, K)
     ref = oracle.c_as_nm(Cref, M, N, M)
@@ -72,9 +77,12 @@ def test_lean_pm1_exact(g, M, N, K, parts):
 def test_lean_gauss_equals_full_configuration(g, M, N, K, parts):
     A = synth.gauss_fp16(M * K, 9710 + K % 83)
     B = synth.gauss_fp16(N * K, 9711 + K % 83)
-    g.gemm_debug_set_lean_mode(0)
-    lean = run_f16(M, N, K, A, K, B, K)
-    assert record(g)["lean"] == parts, g.last_launch()
+    g.gemm_debug_set_lean_mode(2)
+    try:
+        lean = run_f16(M, N, K, A, K, B, K)
+        assert record(g)["lean"] == parts, g.last_launch()
+    finally:
+        g.gemm_debug_set_lean_mode(0)
     g.gemm_debug_set_lean_mode(1)
     try:
         full = run_f16(M, N, K, A, K, B, K)
@@ -92,9 +100,12 @@ def test_lean_e4m3_equals_full_configuration(g, M, N, K, parts):
     A, _ = synth.gauss_e4m3(M * K, 9720 + M % 7)
     B, _ = synth.gauss_e4m3(N * K, 9721 + N % 7)
     sa, sb = 0.5, 1.5
-    g.gemm_debug_set_lean_mode(0)
-    lean = run_f8(M, N, K, A, K, B, K, sa, sb)
-    assert record(g)["lean"] == parts, g.last_launch()
+    g.gemm_debug_set_lean_mode(2)
+    try:
+        lean = run_f8(M, N, K, A, K, B, K, sa, sb)
+        assert record(g)["lean"] == parts, g.last_launch()
+    finally:
+        g.gemm_debug_set_lean_mode(0)
     g.gemm_debug_set_lean_mode(1)
     try:
         full = run_f8(M, N, K, A, K, B, K, sa, sb)
@@ -143,15 +154,26 @@ def test_lean_back_to_back_outputs_intact(g):
         assert np.array_equal(got, ref), f"launch {i}: {np.sum(got != ref)} outputs differ"
 
 
-@pytest.mark.parametrize("M,N,K", [(2048, 1024, 512), (4096, 4096, 128), (1024, 1024, 8192)])
-def test_other_grids_keep_the_full_configuration(g, M, N, K):
-    """Half-m units with more than 4 k blocks, full grids and long-K cluster
-    launches are not lean."""
+@pytest.mark.parametrize("M,N,K,want", [
+    (1024, 1024, 128, 4),     # 128 quarter units, 2 k blocks
+    (1024, 1024, 512, 4),     # 8 k blocks
+    (2048, 1024, 128, 2),     # 128 half units
+    (2048, 1024, 256, 2),     # 4 k blocks
+    (1024, 1024, 1984, 0),    # 31 k blocks: the full ring's depth pays
+    (2048, 1024, 512, 0),     # halves with 8 k blocks
+    (512, 512, 512, 0),       # 32 units leave room beside them for the next launch
+    (1024, 512, 1024, 0),     # 64 units
+    (4096, 4096, 128, 0),     # a full grid of pair tiles
+    (1024, 1024, 8192, 0),    # k ranges reduced in clusters
+])
+def test_default_choice(g, M, N, K, want):
     A = synth.sign_fp16(M * K, 9750)
     B = synth.sign_fp16(N * K, 9751)
     g.gemm_debug_set_lean_mode(0)
-    run_f16(M, N, K, A, K, B, K)
-    assert record(g)["lean"] == 0, g.last_launch()
+    got = run_f16(M, N, K, A, K, B, K)
+    assert record(g)["lean"] == want, g.last_launch()
+    Cref, _, _ = oracle.gemm_f16_tn(M, N, K, A, K, B, K)
+    assert np.array_equal(got, oracle.c_as_nm(Cref, M, N, M))
 
 
 @pytest.mark.parametrize("M,N,K,parts", [(2048, 1024, 1024, 2), (2048, 1024, 520, 2), (1024, 1024, 1000, 4)])
