@@ -37,7 +37,8 @@ import synth  # noqa: E402
 METRIC = "TFLOP/s (2MNK/t) FP16 TN GEMM 8192³ on 1 GB300; % of dense tensor peak"
 NOMINAL_PEAK = {"f16": 2250.0, "e4m3": 4500.0}          # dense TFLOP/s per GPU
 KERNEL_NAME = {"f16": "tn_gemm_kernel<KindF16>", "e4m3": "tn_gemm_kernel<KindE4M3>"}
-KERNEL_SOURCES = ["dense_gemm_tn_gb300/csrc/tn_gemm_kernel.cuh", "dense_gemm_tn_gb300/csrc/sm103_ptx.cuh"]
+KERNEL_SOURCES = ["dense_gemm_tn_gb300/csrc/tn_gemm_kernel.cuh", "dense_gemm_tn_gb300/csrc/sm103_ptx.cuh",
+                  "dense_gemm_tn_gb300/csrc/skinny_kernel.cuh"]
 PROFILES_DIR = os.path.join(ROOT, "profiles")
 
 

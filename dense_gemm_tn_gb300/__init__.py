@@ -51,6 +51,7 @@ EXPORTS = (
     "gemm_set_wait_limit_ns", "gemm_debug_inject_stall", "gemm_build_info",
     "gemm_f16_tn_noalloc", "gemm_debug_force_cta_group", "gemm_debug_force_wide_tiles", "gemm_debug_last_launch",
     "gemm_debug_set_raster_group", "gemm_debug_set_k_order", "gemm_debug_set_long_k_mode", "gemm_debug_set_lean_mode",
+    "gemm_debug_set_skinny_mode",
     "gemm_debug_set_clock_probe",
     "gemm_f8e4m3_tn_dscale", "gemm_quantize_e4m3", "gemm_f16_tn_softmax_stats",
 )
@@ -112,6 +113,8 @@ def _load() -> ctypes.CDLL:
     lib.gemm_debug_set_long_k_mode.restype = ctypes.c_int
     lib.gemm_debug_set_lean_mode.argtypes = [ctypes.c_int]
     lib.gemm_debug_set_lean_mode.restype = ctypes.c_int
+    lib.gemm_debug_set_skinny_mode.argtypes = [ctypes.c_int]
+    lib.gemm_debug_set_skinny_mode.restype = ctypes.c_int
     lib.gemm_debug_set_k_order.argtypes = [ctypes.c_int]
     lib.gemm_debug_set_k_order.restype = ctypes.c_int
     lib.gemm_debug_last_launch.argtypes = []
@@ -269,6 +272,12 @@ def gemm_debug_set_clock_probe(counters) -> None:
 def gemm_debug_set_long_k_mode(mode: int) -> None:
     """0 the library's choice; 1 split-reduce (HBM partials); 2 reduce inside a cluster of single CTAs."""
     if _lib.gemm_debug_set_long_k_mode(int(mode)) != 0:
+        raise ValueError("mode must be 0, 1 or 2")
+
+
+def gemm_debug_set_skinny_mode(mode: int) -> None:
+    """N <= 64: 0 the library's choice; 1 never the skinny kernel; 2 always."""
+    if _lib.gemm_debug_set_skinny_mode(int(mode)) != 0:
         raise ValueError("mode must be 0, 1 or 2")
 
 

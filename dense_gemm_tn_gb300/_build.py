@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libdense_gemm_tn.so")
 SOURCES = [os.path.join(CSRC, "tn_gemm.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("tn_gemm_kernel.cuh", "sm103_ptx.cuh", "quant_e4m3_kernel.cuh", "repack_kernel.cuh",
-                                                     "aux_kernels.cuh")] + [
+                                                     "aux_kernels.cuh", "skinny_kernel.cuh")] + [
     os.path.join(INCLUDE, "tn_gemm.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -20,6 +20,7 @@
 
 #include "tn_gemm.h"
 #include "tn_gemm_kernel.cuh"
+#include "skinny_kernel.cuh"
 #include "aux_kernels.cuh"
 #include "repack_kernel.cuh"
 #include "quant_e4m3_kernel.cuh"
@@ -39,6 +40,13 @@ constexpr int kGroupM = 8;                               // tile rows per raster
 // and there the deeper ring of the full configuration was as fast or faster
 // (512^3 5.20 -> 5.32, 1024 x 512 x 1024 7.46 -> 7.96).
 constexpr int kLeanQuarterMaxKb = 8;
+// The skinny kernel (N <= 64) by default up to this many 128-byte k blocks.
+// Measured on GB300, back to back with inputs from HBM, general -> skinny:
+// 8192 x 8 x 2048 14.64 -> 10.52 us, 8192 x 16 x 512 8.61 -> 6.86, 32768 x 16
+// x 1024 16.29 -> 14.54, 4096 x 16 x 4096 12.27 -> 11.40, 1024 x 16 x 1024
+// 7.40 -> 6.53; but with 128 k blocks 8192 x 16 x 8192 26.02 -> 26.58, 8192 x
+// 64 x 8192 28.43 -> 30.23, 2048 x 16 x 8192 13.23 -> 14.25.
+constexpr int kSkinnyMaxKb = 64;
 constexpr int kLeanHalfMaxKb = 4;
 // Odd waves walk K backwards (kFlagAltK).  Measured on GB300 at 8192^3 (256 x
 // 512 tiles, FP16, under the power cap): DRAM reads 815 -> 684 MB per launch,
@@ -84,6 +92,7 @@ struct DeviceState {
     // Softmax statistics: [tickets per tile row | parts], one buffer per stream.
     std::unordered_map<cudaStream_t, Split> stats;
     int quant_blocks[3] = {};         // co-resident quantiser CTAs per SM, by input type (0 = not queried)
+    bool skinny_attr[2] = {};         // tn_skinny_kernel's shared-memory attribute set, by kind
     // One lock per stream, held by a call from its first buffer lookup through
     // its last launch: a call is several launches (row copy, GEMM, reduce),
     // and two host threads' calls on one stream must not interleave them.
@@ -108,6 +117,7 @@ std::atomic<int> g_k_order{0};          // 0: the library's choice; 1: every til
 std::atomic<unsigned long long *> g_clock_probe{nullptr};   // gemm_debug_set_clock_probe
 std::atomic<int> g_long_k{0};           // small grids with a long K: 0 the library's choice; 1 split-reduce; 2 cluster
 std::atomic<int> g_lean{0};             // m-part launches: 0 the library's choice; 1 never lean; 2 lean where units allow
+std::atomic<int> g_skinny{0};           // N <= 64: 0 the library's choice; 1 never the skinny kernel; 2 always
 // The last launch on this host thread, for gemm_debug_last_launch: the
 // numbers are kept and formatted only when asked for (formatting every call
 // cost host time on the path of back-to-back small GEMMs).
@@ -116,6 +126,7 @@ struct LaunchRecord {
     bool quant = false;
     int G = 0, wide = 0, grid = 0, clusters = 0, slots = 0;
     int tiles = 0, units = 0, tail_start = 0, tail_mode = 0, split_parts = 0, vec = 0, cluster = 0, lean = 0;
+    int skinny = 0;
     long long qgrid = 0, qunits = 0;
 };
 thread_local LaunchRecord t_rec;
@@ -639,6 +650,7 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
     t_rec.name = name;
     t_rec.quant = false;
     t_rec.lean = lean;
+    t_rec.skinny = 0;
     t_rec.G = G;
     t_rec.wide = W ? 1 : 0;
     t_rec.grid = G * cluster_parts * clusters;
@@ -680,6 +692,96 @@ gemm_status_t launch(const char *name, tn::KernelParams &prm, DeviceState &dev, 
                                prm.c_ptr, prm.ldc, prm.scale, prm.scale_a_ptr, prm.scale_b_ptr);
         if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: split reduce launch: %s", name, cudaGetErrorString(e));
     }
+    return GEMM_OK;
+}
+
+// Launches tn_skinny_kernel for N <= 64: 128-row m tiles, their k blocks cut
+// into 1, 2 or 4 ranges (each of at least 4 blocks) so that the grid fills
+// the SMs; with several ranges the partials meet in the per-stream split
+// workspace (none when the call may not allocate: then one range per tile).
+template <class Kind>
+gemm_status_t launch_skinny(const char *name, int64_t M, int64_t N, int64_t K, const void *a, int64_t ka,
+                            int64_t lda_bytes, const void *b, int64_t kb, int64_t ldb_bytes, void *C, int64_t ldc,
+                            float scale, const float *dscale_a, const float *dscale_b, DeviceState &dev,
+                            bool allow_alloc, cudaStream_t stream)
+{
+    constexpr int64_t esz = Kind::kElemBytes;
+    tn::SkinnyParams prm;
+    memset(&prm, 0, sizeof(prm));
+    const CUtensorMapDataType in_type = Kind::kF8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const uint32_t box_k = tn::kBlockKBytes / esz;
+    const int32_t n_mma = static_cast<int32_t>((N + 15) / 16 * 16);
+    gemm_status_t st;
+    if ((st = encode_2d(&prm.tmap_a, in_type, a, ka, M, lda_bytes, box_k, tn::kSkRowsM, "A")) != GEMM_OK) return st;
+    if ((st = encode_2d(&prm.tmap_b, in_type, b, kb, N, ldb_bytes, box_k, static_cast<uint32_t>(n_mma), "B")) !=
+        GEMM_OK)
+        return st;
+    const int64_t tiles_m = (M + tn::kSkRowsM - 1) / tn::kSkRowsM;
+    const int64_t num_kb = (K * esz + tn::kBlockKBytes - 1) / tn::kBlockKBytes;
+    const int slots = dev.sms;                 // one CTA per SM (about 194 KiB of shared memory each)
+    int parts = 1;
+    for (int q = tn::kSkMaxParts; q >= 2 && allow_alloc; q /= 2)
+        if (tiles_m * q <= slots && num_kb >= 4 * q) {
+            parts = q;
+            break;
+        }
+    if (tiles_m * parts > INT32_MAX) return fail(GEMM_ERR_UNSUPPORTED, "%s: too many output tiles", name);
+    prm.c_ptr = C;
+    prm.ldc = ldc;
+    prm.M = static_cast<int32_t>(M);
+    prm.N = static_cast<int32_t>(N);
+    prm.num_kb = static_cast<int32_t>(num_kb);
+    prm.n_mma = n_mma;
+    prm.tiles_m = static_cast<int32_t>(tiles_m);
+    prm.parts = parts;
+    prm.kb_part = static_cast<int32_t>((num_kb + parts - 1) / parts);
+    prm.num_units = static_cast<int32_t>(tiles_m * parts);
+    if (parts > 1) {
+        const size_t partial = size_t(tiles_m) * parts * size_t(n_mma) * tn::kSkRowsM * sizeof(float);
+        if ((st = split_workspace(dev, stream, size_t(tiles_m), partial, &prm.tickets, &prm.split_ws)) != GEMM_OK)
+            return st;
+    }
+    prm.scale = scale;
+    prm.scale_a_ptr = dscale_a;
+    prm.scale_b_ptr = dscale_b;
+    prm.flags = stall_flags(g_inject_stall.load());
+    prm.wait_limit_ns = g_wait_limit_ns.load();
+
+    auto kernel = tn::tn_skinny_kernel<Kind>;
+    const int ki = Kind::kF8 ? 1 : 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!dev.skinny_attr[ki]) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tn::kSkSmemBytes);
+            if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+            dev.skinny_attr[ki] = true;
+        }
+    }
+    const int64_t grid = prm.num_units < slots ? prm.num_units : slots;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    // a programmatic dependent of the previous kernel on the stream, like the general kernel
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(tn::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = tn::kSkSmemBytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    t_rec = LaunchRecord{};
+    t_rec.name = name;
+    t_rec.G = 1;
+    t_rec.grid = static_cast<int>(grid);
+    t_rec.cluster = 1;
+    t_rec.clusters = static_cast<int>(grid);
+    t_rec.slots = slots;
+    t_rec.tiles = prm.tiles_m;
+    t_rec.units = prm.num_units;
+    t_rec.split_parts = parts;
+    t_rec.skinny = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
+    if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: launch: %s", name, cudaGetErrorString(e));
     return GEMM_OK;
 }
 
@@ -817,6 +919,20 @@ gemm_status_t run_gemm(const char *name, int64_t M, int64_t N, int64_t K, const 
         }
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return fail(GEMM_ERR_CUDA, "%s: repack launch: %s", name, cudaGetErrorString(e));
+    }
+
+    // Few columns n: the kernel with the operands on the other MMA sides, up to
+    // kSkinnyMaxKb k blocks of 128 bytes (beyond that, with the operand stream
+    // at the DRAM roofline in both kernels, the general kernel's cluster
+    // reduce measured as fast or faster).
+    {
+        const int mode = g_skinny.load();
+        const int64_t num_kb = (K * esz + tn::kBlockKBytes - 1) / tn::kBlockKBytes;
+        // (a test hook that forces the general kernel's tile shape or k cut keeps it)
+        const bool forced = g_force_cta_group.load() != 0 || g_force_wide.load() != 0 || g_long_k.load() != 0;
+        if (!stats && N <= tn::kSkMaxN && (mode == 2 || (mode == 0 && !forced && num_kb <= kSkinnyMaxKb)))
+            return launch_skinny<Kind>(name, M, N, K, a_use, ka, lda_use * esz, b_use, kb, ldb_use * esz, C, ldc,
+                                       scale, dscale_a, dscale_b, *dev, allow_alloc, stream);
     }
 
     tn::KernelParams prm;
@@ -1167,6 +1283,13 @@ int gemm_debug_set_long_k_mode(int mode)
     return 0;
 }
 
+int gemm_debug_set_skinny_mode(int mode)
+{
+    if (mode < 0 || mode > 2) return -1;
+    g_skinny.store(mode);
+    return 0;
+}
+
 int gemm_debug_set_lean_mode(int mode)
 {
     if (mode < 0 || mode > 2) return -1;
@@ -1185,9 +1308,9 @@ const char *gemm_debug_last_launch(void)
     else
         snprintf(t_last_launch, sizeof(t_last_launch),
                  "%s: ctas_per_cluster=%d wide=%d grid=%d clusters=%d slots=%d tiles=%d units=%d tail_start=%d "
-                 "tail_mode=%d split_parts=%d lean=%d",
+                 "tail_mode=%d split_parts=%d lean=%d skinny=%d",
                  r.name, r.cluster, r.wide, r.grid, r.clusters, r.slots, r.tiles, r.units,
-                 r.tail_start, r.tail_mode, r.split_parts, r.lean);
+                 r.tail_start, r.tail_mode, r.split_parts, r.lean, r.skinny);
     return t_last_launch;
 }
 

@@ -352,6 +352,16 @@ int gemm_debug_set_long_k_mode(int mode);
 int gemm_debug_set_lean_mode(int mode);
 
 /*
+ * Test hook: problems with N <= 64 (no softmax statistics) may run a kernel
+ * with the operands on the other sides of the MMA (128 rows m of A by the N
+ * columns n), whose k ranges meet in a small per-stream workspace.  0
+ * (default): the library's choice (where K holds at most 64 blocks of 128
+ * bytes); 1: never; 2: always where N <= 64.
+ * Returns 0, or -1 for other values.
+ */
+int gemm_debug_set_skinny_mode(int mode);
+
+/*
  * Measurement hook: while `counters` (a DEVICE pointer to 3 zeroed unsigned
  * 64-bit words) is set, every GEMM kernel launched afterwards adds, from the
  * first thread of its first CTA, the SM cycles (%clock64) and nanoseconds

@@ -161,6 +161,13 @@ def test_long_k_mode_hook_values():
         assert g.lib.gemm_debug_set_long_k_mode(v) == 0
 
 
+def test_skinny_mode_hook_values():
+    assert g.lib.gemm_debug_set_skinny_mode(3) == -1
+    assert g.lib.gemm_debug_set_skinny_mode(-1) == -1
+    for v in (1, 2, 0):
+        assert g.lib.gemm_debug_set_skinny_mode(v) == 0
+
+
 def test_lean_mode_hook_values():
     assert g.lib.gemm_debug_set_lean_mode(3) == -1
     assert g.lib.gemm_debug_set_lean_mode(-1) == -1

@@ -31,8 +31,10 @@ def g():
     if not torch.cuda.is_available():
         pytest.skip("no GPU")
     import dense_gemm_tn_gb300 as g
+    g.gemm_debug_set_skinny_mode(1)      # (shapes with N <= 64 would go to the skinny kernel)
     yield g
     g.gemm_debug_set_lean_mode(0)
+    g.gemm_debug_set_skinny_mode(0)
 
 
 def record(g):
