@@ -37,6 +37,7 @@ import synth  # noqa: E402
 METRIC = "TFLOP/s (2MNK/t) FP16 TN GEMM 8192³ on 1 GB300; % of dense tensor peak"
 NOMINAL_PEAK = {"f16": 2250.0, "e4m3": 4500.0}          # dense TFLOP/s per GPU
 KERNEL_NAME = {"f16": "tn_gemm_kernel<KindF16>", "e4m3": "tn_gemm_kernel<KindE4M3>"}
+SKINNY_KERNEL_NAME = {"f16": "tn_skinny_kernel<KindF16>", "e4m3": "tn_skinny_kernel<KindE4M3>"}
 KERNEL_SOURCES = ["dense_gemm_tn_gb300/csrc/tn_gemm_kernel.cuh", "dense_gemm_tn_gb300/csrc/sm103_ptx.cuh",
                   "dense_gemm_tn_gb300/csrc/skinny_kernel.cuh"]
 PROFILES_DIR = os.path.join(ROOT, "profiles")
@@ -481,7 +482,7 @@ def timed_loop(torch, dev, stream, call, sets: int, steps: int, warmup: int, sam
 
 
 def roofline_of(w: synth.Workload, kernel_ms: float, region_ms: float, peaks: dict, clk: dict | None,
-                sms: int, stats: bool) -> dict:
+                sms: int, stats: bool, skinny: bool = False) -> dict:
     """The dominant kernel's roofline.  Below the ridge point (tensor peak over
     HBM bytes/s) the bound is HBM and `achieved` is the algorithmic bytes per
     launch (operands read once, C and any row statistics written once) over
@@ -502,7 +503,7 @@ def roofline_of(w: synth.Workload, kernel_ms: float, region_ms: float, peaks: di
     ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     intensity = flop / alg_bytes
     rf = {"intensity_flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
-          "kernel": KERNEL_NAME["e4m3" if is_f8 else "f16"], "kernel_ms": kernel_ms,
+          "kernel": (SKINNY_KERNEL_NAME if skinny else KERNEL_NAME)["e4m3" if is_f8 else "f16"], "kernel_ms": kernel_ms,
           "traffic": measured_traffic(w.name), "algorithmic_bytes": alg_bytes}
     dtype_note = " x2 (nominal fp8/bf16)" if is_f8 else " (fp16 = bf16 rate)"
     if intensity < ridge:
@@ -609,7 +610,7 @@ def run_secondary(args, torch, g, dev, stream, sampler, peaks, sms) -> dict:
                                   f"{sets} rotating input sets",
                       "l2": l2_note(sets, (M + N) * K)},
            "pct_of_dense_peak": 100.0 * value / NOMINAL_PEAK["e4m3"],
-           "roofline": roofline_of(w, kernel_ms, total_ms, peaks, clk, sms, False),
+           "roofline": roofline_of(w, kernel_ms, total_ms, peaks, clk, sms, False, "skinny=1" in g.last_launch()),
            "clocks": clk, "gpu_launches": args.steps}
     if not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_line(w, host[0], args.cpu_seconds / 2, False)
@@ -747,7 +748,9 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
 
     peaks = load_peaks()
     flop = 2.0 * M * N * K
-    roofline = roofline_of(w, kernel_ms, total_ms, peaks, clk, sms, stats)
+    # (which GEMM kernel the library ran: the last launch's record says)
+    skinny = "skinny=1" in g.last_launch()
+    roofline = roofline_of(w, kernel_ms, total_ms, peaks, clk, sms, stats, skinny)
 
     # ---- sustained: the same calls back to back for about `sustained_s`
     # seconds, long enough for the GPU to settle at its power cap
@@ -761,7 +764,7 @@ def run_ours(args, w: synth.Workload, rank: int, world: int, local_rank: int) ->
         g.gemm_poll_device_status(sh)
         s_ms = max_over_ranks([s_ms], dist, dev)[0]
         s_kernel = s_ms / s_steps
-        s_rf = roofline_of(w, s_kernel, s_ms, peaks, s_clk, sms, stats)
+        s_rf = roofline_of(w, s_kernel, s_ms, peaks, s_clk, sms, stats, skinny)
         sustained = {"steps": s_steps, "seconds": s_ms * 1e-3, "ms_per_step": s_kernel,
                      "value": replica_tflops(world, flop, s_steps, s_ms), "unit": "TFLOP/s",
                      "frac": s_rf["frac"], "peak": s_rf["peak"], "peak_kind": s_rf["peak_kind"],

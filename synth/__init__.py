@@ -33,6 +33,9 @@ larger than the GPU's L2 (129 MB), so every step reads its operands from HBM:
                (its k ranges are reduced inside clusters)
   skinny_8192x16  M=8192, N=16, K=8192, N(0,1) cast to fp16, 2 rotating sets:
                a decode-like product, bound by the read of A
+  skinny_8192x16x2048  M=8192, N=16, K=2048, N(0,1) cast to fp16, 6 rotating
+               sets: the same product with a shorter K (the kernel for few
+               columns n)
 """
 from __future__ import annotations
 
@@ -191,6 +194,7 @@ WORKLOADS = {
         Workload("qk_stats_1024", 1024, 1024, 128, "gauss", 201, 202, rotating=320, op="softmax_stats"),
         Workload("longk_4096x512", 4096, 512, 8192, "gauss", 801, 802, rotating=2),
         Workload("skinny_8192x16", 8192, 16, 8192, "gauss", 803, 804, rotating=2),
+        Workload("skinny_8192x16x2048", 8192, 16, 2048, "gauss", 805, 806, rotating=6),
     ]
 }
 

@@ -14,7 +14,7 @@ import torch
 import oracle
 import synth
 from tests.gpu_helpers import (F8_TOL, F16_TOL, GuardedC, assert_tol, bf16_values, f16_values, run_f8, run_f16,
-                               to_dev_u16)
+                               sample_positions, to_dev_u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -183,3 +183,21 @@ def test_default_choice(g, M, N, K, want):
         g.gemm_debug_set_skinny_mode(2)
     Cref, _, _ = oracle.gemm_f16_tn(M, N, K, A, K, B, K)
     assert np.array_equal(got, oracle.c_as_nm(Cref, M, N, M))
+
+
+def test_workload_skinny_8192x16x2048(g):
+    """The bench workload of the kernel, with the library's own choice, on
+    sampled outputs against the oracle, and identical run to run."""
+    w = synth.WORKLOADS["skinny_8192x16x2048"]
+    A, B, _, _ = synth.make_inputs(w, 0)
+    g.gemm_debug_set_skinny_mode(0)
+    try:
+        got = run_f16(w.M, w.N, w.K, A, w.K, B, w.K)
+        assert record(g)["skinny"] == 1, g.last_launch()
+        again = run_f16(w.M, w.N, w.K, A, w.K, B, w.K)
+    finally:
+        g.gemm_debug_set_skinny_mode(2)
+    assert np.array_equal(got, again)
+    mi, ni = sample_positions(w.M, w.N, 20000, seed=7)
+    c, s, _ = oracle.gemm_f16_tn_at(w.M, w.N, w.K, A, w.K, B, w.K, mi, ni)
+    assert_tol(f16_values(got[ni, mi]), f16_values(c), s, F16_TOL, "skinny_8192x16x2048")
