@@ -201,3 +201,30 @@ def test_workload_skinny_8192x16x2048(g):
     mi, ni = sample_positions(w.M, w.N, 20000, seed=7)
     c, s, _ = oracle.gemm_f16_tn_at(w.M, w.N, w.K, A, w.K, B, w.K, mi, ni)
     assert_tol(f16_values(got[ni, mi]), f16_values(c), s, F16_TOL, "skinny_8192x16x2048")
+
+
+def test_skinny_fp8_device_scales(g):
+    """bf16 operands quantised to E4M3 on the device, then the GEMM with the
+    scales read by the kernel (gemm_f8e4m3_tn_dscale) at N = 16: codes and
+    scales as the oracle's quantiser gives them, C within the FP8 tolerance."""
+    M, N, K = 4096, 16, 1024
+    xa = synth.gauss_bf16(M * K, 9880)
+    xb = synth.gauss_bf16(N * K, 9881)
+    da = torch.from_numpy(xa.view(np.int16)).cuda()
+    db = torch.from_numpy(xb.view(np.int16)).cuda()
+    qa = torch.zeros(M * K, dtype=torch.uint8, device="cuda")
+    qb = torch.zeros(N * K, dtype=torch.uint8, device="cuda")
+    sc = torch.zeros(2, dtype=torch.float32, device="cuda")
+    g.gemm_quantize_e4m3(da, g.GEMM_IN_BF16, M, K, K, qa, K, sc.data_ptr())
+    g.gemm_quantize_e4m3(db, g.GEMM_IN_BF16, N, K, K, qb, K, sc.data_ptr() + 4)
+    C = GuardedC(M, N, M)
+    g.gemm_f8e4m3_tn_dscale(M, N, K, qa, K, qb, K, C.ptr, M, sc.data_ptr(), sc.data_ptr() + 4)
+    g.gemm_poll_device_status(None)
+    assert record(g)["skinny"] == 1, g.last_launch()
+    ref_qa, ref_sa = oracle.quantize_e4m3(xa, "bf16", M, K)
+    ref_qb, ref_sb = oracle.quantize_e4m3(xb, "bf16", N, K)
+    assert np.array_equal(qa.cpu().numpy(), ref_qa) and np.array_equal(qb.cpu().numpy(), ref_qb)
+    scales = sc.cpu().numpy()
+    assert scales[0] == np.float32(ref_sa) and scales[1] == np.float32(ref_sb)
+    Cref, S, _ = oracle.gemm_f8e4m3_tn(M, N, K, ref_qa, K, ref_qb, K, float(scales[0]), float(scales[1]))
+    assert_tol(bf16_values(C.nm()), bf16_values(oracle.c_as_nm(Cref, M, N, M)), S, F8_TOL, "skinny dscale")
