@@ -1316,18 +1316,20 @@ const char *gemm_debug_last_launch(void)
 
 const char *gemm_build_info(void)
 {
-    static char info[512];
+    static char info[768];
     snprintf(info, sizeof(info),
              "dense_gemm_tn sm_103a: CTA-pair tile 256x256 in 2-CTA clusters, %d stages of %d B "
              "of K, %d B smem; CTA-pair tile 256x512, %d stages of %d B of K, %d B smem; 1-CTA tile 128x256, "
              "%d stages of %d B of K, %d B smem; TMEM %u cols; lean 1-CTA quarter-m units, %d stages, %d B smem, "
-             "TMEM %u cols; half-m units, %d stages, %d B smem, TMEM %u cols; raster group %d",
+             "TMEM %u cols; half-m units, %d stages, %d B smem, TMEM %u cols; N <= %d: 128-row m tiles, %d stages, "
+             "%d B smem, TMEM %u cols; raster group %d",
              tn::TileCfg<2>::kStages, tn::TileCfg<2>::kStageKBytes, tn::TileCfg<2>::kSmemBytes,
              tn::TileCfg<2, true>::kStages, tn::TileCfg<2, true>::kStageKBytes, tn::TileCfg<2, true>::kSmemBytes,
              tn::TileCfg<1>::kStages, tn::TileCfg<1>::kStageKBytes, tn::TileCfg<1>::kSmemBytes, tn::TileCfg<1>::kTmemCols,
              tn::TileCfg<1, false, 4>::kStages, tn::TileCfg<1, false, 4>::kSmemBytes,
              tn::TileCfg<1, false, 4>::kTmemCols, tn::TileCfg<1, false, 2>::kStages,
-             tn::TileCfg<1, false, 2>::kSmemBytes, tn::TileCfg<1, false, 2>::kTmemCols, kGroupM);
+             tn::TileCfg<1, false, 2>::kSmemBytes, tn::TileCfg<1, false, 2>::kTmemCols, tn::kSkMaxN, tn::kSkStages,
+             tn::kSkSmemBytes, tn::kSkTmemCols, kGroupM);
     return info;
 }
 

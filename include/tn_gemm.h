@@ -41,7 +41,10 @@
  *     meet in a library-owned buffer kept per (device, stream), allocated on
  *     first need (about 0.5 MiB per leftover tile).  The sum is taken in a
  *     fixed way, so results do not depend on timing.  cudaStreamPerThread
- *     counts as one stream per host thread.
+ *     counts as one stream per host thread.  Problems with at most 64
+ *     columns n and a short K run a kernel of their own whose k ranges meet
+ *     in the same buffer (at most 128 KiB per 128 rows m), also in a fixed
+ *     order.
  *   - CUDA graphs: once a call has run on a stream (the first call may
  *     allocate that stream's buffers and set kernel attributes), later calls
  *     with the same sizes on that stream enqueue kernel launches only and can
