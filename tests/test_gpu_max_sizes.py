@@ -266,3 +266,33 @@ def test_softmax_stats_scores_beyond_2_31_elements():
     err = np.abs(got_sum - sm_ref) / sm_ref
     assert np.all(err <= rel), f"row_sum rel error {err.max()} > {rel[np.argmax(err)]}"
     check_tail(C, N * M)
+
+
+@pytest.mark.parametrize("pad", [0, 1])
+def test_skinny_kernel_a_beyond_2_31_elements(pad):
+    """The kernel for few columns (forced) on A of 270000 x 8192 (2.2e9
+    elements) with lda = K or K + 1: rows m on both sides of element 2^31,
+    2110 tiles walked by 152 CTAs in turn."""
+    import dense_gemm_tn_gb300 as g
+    M, N, K = 270000, 16, 8192
+    lda = K + pad
+    tall = TallSigns(M, K, 841)
+    dA = tall.device(lda)
+    B = synth.sign_fp16(N * K, 843)
+    C = big_output(N, M)
+    g.gemm_debug_set_skinny_mode(2)
+    try:
+        g.gemm_f16_tn(M, N, K, dA, lda, to_dev_u16(B), K, C, M, None)
+        g.gemm_poll_device_status()
+        assert "skinny=1" in g.last_launch(), g.last_launch()
+    finally:
+        g.gemm_debug_set_skinny_mode(0)
+    del dA
+    wrap = (1 << 31) // lda
+    ms = picks(48, M, 844, [0, 1, wrap - 1, wrap, wrap + 1, (1 << 32) // (2 * lda), 269951, 269952, M - 2, M - 1])
+    got = C[: N * M].view(N, M)[:, torch.from_numpy(ms).cuda()].cpu().numpy().view(np.uint16).T    # (S, N)
+    ref, _, _ = oracle.gemm_f16_tn(ms.size, N, K, tall.host_rows(ms).reshape(-1), K, B, K)
+    ref = oracle.c_as_nm(ref, ms.size, N, ms.size).T                                                 # (S, N)
+    bad = np.flatnonzero((got != ref).any(axis=1))
+    assert bad.size == 0, f"rows {ms[bad][:8]} differ"
+    check_tail(C, N * M)
