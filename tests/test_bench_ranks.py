@@ -99,3 +99,30 @@ def test_kernel_hash_ignores_comments_only():
     assert bench.code_of(src.replace("// one", "// uno")) == bench.code_of(src)
     assert bench.code_of(src.replace("a = 1", "a = 2")) != bench.code_of(src)
     assert bench.code_of("char c = '\\\\'; // x") == "char c = '\\\\';"
+
+
+def test_roofline_bound_peak_and_kernel_name():
+    """The roofline object: HBM-bound below the ridge point (algorithmic bytes
+    over the launch time against the copy bandwidth), tensor-bound above it
+    against the burst peak for a region under a second and the sustained one
+    beyond; the kernel named is the one the library ran."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    peaks = {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "src": "test"}
+    sq = synth.WORKLOADS["sq_8192"]
+    rf = bench.roofline_of(sq, 0.6, 12.0, peaks, {"sm_mhz": 1700.0}, 152, False)
+    assert rf["bound"] == "tensor" and rf["peak_kind"] == "burst" and rf["peak"] == 1900.0
+    assert abs(rf["achieved"] - 2.0 * 8192 ** 3 / 0.6e-3 / 1e12) < 1e-6
+    assert rf["kernel"] == "tn_gemm_kernel<KindF16>"
+    rf = bench.roofline_of(sq, 0.6, 2000.0, peaks, None, 152, False)
+    assert rf["peak_kind"] == "sustained" and rf["peak"] == 1700.0
+    e4 = synth.WORKLOADS["e4m3_8192"]
+    rf = bench.roofline_of(e4, 0.3, 12.0, peaks, None, 152, False)
+    assert rf["peak"] == 3800.0 and rf["kernel"] == "tn_gemm_kernel<KindE4M3>"
+    sk = synth.WORKLOADS["skinny_8192x16x2048"]
+    rf = bench.roofline_of(sk, 0.01, 20.0, peaks, None, 152, False, True)
+    alg = (8192 * 2048 + 16 * 2048) * 2 + 2 * 8192 * 16
+    assert rf["bound"] == "hbm" and rf["algorithmic_bytes"] == alg
+    assert abs(rf["achieved"] - alg / 0.01e-3 / 1e9) < 1e-6 and rf["peak"] == 6800.0
+    assert rf["kernel"] == "tn_skinny_kernel<KindF16>"
