@@ -366,8 +366,9 @@ int gemm_debug_set_skinny_mode(int mode);
 
 /*
  * Measurement hook: while `counters` (a DEVICE pointer to 3 zeroed unsigned
- * 64-bit words) is set, every GEMM kernel launched afterwards adds, from the
- * first thread of its first CTA, the SM cycles (%clock64) and nanoseconds
+ * 64-bit words) is set, every launch of the general GEMM kernel (not the
+ * kernel for at most 64 columns) afterwards adds, from the first thread of
+ * its first CTA, the SM cycles (%clock64) and nanoseconds
  * (%globaltimer) from its start to its end to counters[0] and counters[1],
  * and 1 to counters[2] (three atomic adds per launch, nothing else).
  * counters[0] / counters[1] is then the average SM clock, in GHz, that those
